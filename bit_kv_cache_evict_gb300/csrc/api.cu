@@ -1,0 +1,257 @@
+// api.cu -- the liboscar C ABI (include/oscar.h): argument checks, the
+// workspace plan, the host page-table layout and kernel launches.
+#include <cstdio>
+#include <cstring>
+#include <vector>
+
+#include "oscar_common.cuh"
+
+namespace oscar {
+
+
+
+constexpr int kPagesPerSplit = 8;  // history pages per split-K work item
+
+static thread_local int g_last_cuda_error = 0;
+
+static oscar_status cuda_fail(cudaError_t e) {
+    g_last_cuda_error = (int)e;
+    return OSCAR_ERR_CUDA;
+}
+
+static bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+static size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// shape check shared by all calls: INVALID_ARG for impossible values,
+// UNSUPPORTED for valid shapes this build has no kernels for
+static oscar_status check_shape(const oscar_shape* s) {
+    if (!s) return OSCAR_ERR_INVALID_ARG;
+    if (s->head_dim <= 0 || s->quant_group <= 0 || s->page_size <= 0 || s->sink < 0 || s->recent < 0 ||
+        s->num_q_heads <= 0 || s->num_kv_heads <= 0 || s->num_q_heads % s->num_kv_heads != 0 ||
+        s->head_dim % s->quant_group != 0)
+        return OSCAR_ERR_INVALID_ARG;
+    const int G = s->num_q_heads / s->num_kv_heads;
+    if (s->head_dim != kD || s->quant_group != kGroup || s->page_size != kPage) return OSCAR_ERR_UNSUPPORTED;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return OSCAR_ERR_UNSUPPORTED;
+    if (s->sink + s->recent > 4096) return OSCAR_ERR_UNSUPPORTED;
+    return OSCAR_OK;
+}
+
+struct WsLayout {
+    size_t counter, item_start, qfrag, qsum, part, bf_part, total;
+    int NT, pps, part_stride, max_items;
+};
+
+static WsLayout ws_layout(const oscar_shape* s, int batch, int max_pages) {
+    WsLayout w{};
+    const int G = s->num_q_heads / s->num_kv_heads, hk = s->num_kv_heads;
+    w.NT = (G + 3) / 4;
+    w.pps = kPagesPerSplit;
+    w.part_stride = (int)round_up((size_t)G * (kD + 2), 4);
+    w.max_items = batch * hk * ((max_pages + w.pps - 1) / w.pps);
+    size_t off = 0;
+    w.counter = off;
+    off += 256;
+    w.item_start = off;
+    off = round_up(off + (size_t)(batch + 1) * 4, 256);
+    w.qfrag = off;
+    off = round_up(off + (size_t)batch * hk * w.NT * 8 * 32 * 2 * 4, 256);
+    w.qsum = off;
+    off = round_up(off + (size_t)batch * hk * w.NT * 4 * 4 * 4, 256);
+    w.part = off;
+    off = round_up(off + (size_t)w.max_items * w.part_stride * 4, 256);
+    w.bf_part = off;
+    off = round_up(off + (size_t)batch * hk * w.part_stride * 4, 256);
+    w.total = off;
+    return w;
+}
+
+// ------------------------------------------------------------------
+// page-table layout (host)
+// ------------------------------------------------------------------
+static uint64_t splitmix64(uint64_t& state) {
+    uint64_t z = (state += 0x9E3779B97F4A7C15ull);
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+}  // namespace oscar
+
+using namespace oscar;
+
+extern "C" {
+
+size_t oscar_block_bytes(const oscar_shape* shape) {
+    if (check_shape(shape) != OSCAR_OK) return 0;
+    return (size_t)kBlock;
+}
+
+const char* oscar_status_string(oscar_status st) {
+    switch (st) {
+        case OSCAR_OK: return "ok";
+        case OSCAR_ERR_INVALID_ARG: return "invalid argument";
+        case OSCAR_ERR_UNSUPPORTED: return "unsupported shape";
+        case OSCAR_ERR_OUT_OF_PAGES: return "out of pages";
+        case OSCAR_ERR_WORKSPACE: return "workspace too small";
+        case OSCAR_ERR_CUDA: return "CUDA error";
+    }
+    return "unknown status";
+}
+
+int oscar_last_cuda_error(void) { return g_last_cuda_error; }
+
+oscar_status oscar_pool_layout(const oscar_shape* shape, int32_t batch, const int32_t* hist_capacity,
+                               const int32_t* prefix_group, int32_t shared_hist_tokens, uint64_t perm_seed,
+                               int32_t max_pages, int32_t* page_table, int32_t* num_pages_out,
+                               uint64_t* pool_bytes_out) {
+    const oscar_status sst = check_shape(shape);
+    if (sst != OSCAR_OK) return sst;
+    if (batch < 0 || max_pages <= 0 || (batch > 0 && (!hist_capacity || !page_table)))
+        return OSCAR_ERR_INVALID_ARG;
+    const int P = shape->page_size;
+    if (shared_hist_tokens < 0 || shared_hist_tokens % P != 0) return OSCAR_ERR_INVALID_ARG;
+    const int n_shared = shared_hist_tokens / P;
+    for (int b = 0; b < batch; ++b) {
+        if (hist_capacity[b] < 0) return OSCAR_ERR_INVALID_ARG;
+        if (((int64_t)hist_capacity[b] + P - 1) / P > max_pages) return OSCAR_ERR_OUT_OF_PAGES;
+        if (prefix_group && prefix_group[b] >= 0 && hist_capacity[b] < shared_hist_tokens)
+            return OSCAR_ERR_INVALID_ARG;
+    }
+    // page ids in allocation order: shared runs first (one per group, in
+    // order of first appearance), then private pages sequence by sequence
+    std::vector<int32_t> table((size_t)batch * max_pages, -1);
+    std::vector<int> group_owner;  // owner sequence of each group id seen
+    std::vector<int32_t> group_ids;
+    int64_t next = 0;
+    for (int b = 0; b < batch; ++b) {
+        if (!prefix_group || prefix_group[b] < 0) continue;
+        int owner = -1;
+        for (size_t i = 0; i < group_ids.size(); ++i)
+            if (group_ids[i] == prefix_group[b]) owner = group_owner[i];
+        int32_t* row = &table[(size_t)b * max_pages];
+        if (owner < 0) {
+            group_ids.push_back(prefix_group[b]);
+            group_owner.push_back(b);
+            for (int pg = 0; pg < n_shared; ++pg) row[pg] = (int32_t)next++;
+        } else {
+            const int32_t* orow = &table[(size_t)owner * max_pages];
+            for (int pg = 0; pg < n_shared; ++pg) row[pg] = orow[pg];
+        }
+    }
+    for (int b = 0; b < batch; ++b) {
+        const int need = (hist_capacity[b] + P - 1) / P;
+        const int first = (prefix_group && prefix_group[b] >= 0) ? n_shared : 0;
+        int32_t* row = &table[(size_t)b * max_pages];
+        for (int pg = first; pg < need; ++pg) row[pg] = (int32_t)next++;
+    }
+    if (next > INT32_MAX) return OSCAR_ERR_INVALID_ARG;
+    if (perm_seed != 0 && next > 1) {
+        std::vector<int32_t> perm((size_t)next);
+        for (int64_t i = 0; i < next; ++i) perm[(size_t)i] = (int32_t)i;
+        uint64_t state = perm_seed;
+        for (int64_t i = next - 1; i >= 1; --i) {
+            const int64_t j = (int64_t)(splitmix64(state) % (uint64_t)(i + 1));
+            std::swap(perm[(size_t)i], perm[(size_t)j]);
+        }
+        for (auto& v : table)
+            if (v >= 0) v = perm[(size_t)v];
+    }
+    if (batch > 0) std::memcpy(page_table, table.data(), table.size() * sizeof(int32_t));
+    if (num_pages_out) *num_pages_out = (int32_t)next;
+    if (pool_bytes_out) *pool_bytes_out = (uint64_t)next * (uint64_t)shape->num_kv_heads * (uint64_t)kBlock;
+    return OSCAR_OK;
+}
+
+oscar_status oscar_evict_quantize(const oscar_shape* shape, int32_t n_tok, const void* src_kv,
+                                  int32_t src_rows, const int32_t* src_row, const int32_t* dst_seq,
+                                  const int32_t* dst_pos, const void* new_kv, const float* U,
+                                  const float* clip, uint8_t* pool, const int32_t* page_table,
+                                  int32_t batch, int32_t max_pages, int32_t num_pages,
+                                  int32_t* dev_status, void* stream) {
+    const oscar_status sst = check_shape(shape);
+    if (sst != OSCAR_OK) return sst;
+    if (n_tok < 0 || src_rows < 0 || batch < 0 || max_pages <= 0 || num_pages < 0) return OSCAR_ERR_INVALID_ARG;
+    if (n_tok == 0) return OSCAR_OK;
+    if (!src_kv || !dst_seq || !dst_pos || !U || !clip || !pool || !page_table) return OSCAR_ERR_INVALID_ARG;
+    if (!aligned(src_kv, 8) || (new_kv && !aligned(new_kv, 8)) || !aligned(U, 16) || !aligned(pool, 16) ||
+        !aligned(clip, 4) || !aligned(dev_status, 4))
+        return OSCAR_ERR_INVALID_ARG;
+    if (!src_row && src_rows < n_tok) return OSCAR_ERR_INVALID_ARG;
+    if ((int64_t)n_tok * shape->num_kv_heads * 2 > INT32_MAX) return OSCAR_ERR_INVALID_ARG;
+    EvictParams p{};
+    p.src_kv = static_cast<const __nv_bfloat16*>(src_kv);
+    p.src_row = src_row;
+    p.dst_seq = dst_seq;
+    p.dst_pos = dst_pos;
+    p.new_kv = static_cast<const __nv_bfloat16*>(new_kv);
+    p.U = U;
+    p.clip = clip;
+    p.pool = pool;
+    p.page_table = page_table;
+    p.status = dev_status;
+    p.n_tok = n_tok;
+    p.hk = shape->num_kv_heads;
+    p.src_rows = src_rows;
+    p.batch = batch;
+    p.max_pages = max_pages;
+    p.num_pages = num_pages;
+    const cudaError_t e = launch_evict(p, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? OSCAR_OK : cuda_fail(e);
+}
+
+oscar_status oscar_decode_attn(const oscar_shape* shape, int32_t batch, const void* q, const void* bf16_kv,
+                               const int32_t* bf16_len, const uint8_t* pool, const int32_t* page_table,
+                               int32_t max_pages, int32_t num_pages, const int32_t* hist_len, const float* U,
+                               float sm_scale, float* out, void* workspace, size_t* ws_bytes,
+                               int32_t* dev_status, void* stream) {
+    const oscar_status sst = check_shape(shape);
+    if (sst != OSCAR_OK) return sst;
+    if (batch < 0 || max_pages <= 0 || num_pages < 0 || !ws_bytes) return OSCAR_ERR_INVALID_ARG;
+    const WsLayout w = ws_layout(shape, batch, max_pages);
+    if (!workspace) {
+        *ws_bytes = w.total;
+        return OSCAR_OK;
+    }
+    if (*ws_bytes < w.total) return OSCAR_ERR_WORKSPACE;
+    if (batch == 0) return OSCAR_OK;
+    if (!q || !bf16_kv || !bf16_len || !hist_len || !U || !out || !page_table) return OSCAR_ERR_INVALID_ARG;
+    if (num_pages > 0 && !pool) return OSCAR_ERR_INVALID_ARG;
+    if (!aligned(q, 8) || !aligned(bf16_kv, 8) || !aligned(U, 16) || !aligned(pool, 16) || !aligned(out, 16) ||
+        !aligned(workspace, 16) || !aligned(dev_status, 4))
+        return OSCAR_ERR_INVALID_ARG;
+    if (!(sm_scale == sm_scale) || (double)w.max_items * w.part_stride > 4.0e9) return OSCAR_ERR_INVALID_ARG;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    DecodeParams p{};
+    p.q = static_cast<const __nv_bfloat16*>(q);
+    p.bf16_kv = static_cast<const __nv_bfloat16*>(bf16_kv);
+    p.bf16_len = bf16_len;
+    p.pool = pool;
+    p.page_table = page_table;
+    p.hist_len = hist_len;
+    p.U = U;
+    p.out = out;
+    p.status = dev_status;
+    p.counter = reinterpret_cast<int32_t*>(ws + w.counter);
+    p.item_start = reinterpret_cast<int32_t*>(ws + w.item_start);
+    p.qfrag = reinterpret_cast<uint32_t*>(ws + w.qfrag);
+    p.qsum = reinterpret_cast<float*>(ws + w.qsum);
+    p.part = reinterpret_cast<float*>(ws + w.part);
+    p.bf_part = reinterpret_cast<float*>(ws + w.bf_part);
+    p.B = batch;
+    p.hq = shape->num_q_heads;
+    p.hk = shape->num_kv_heads;
+    p.G = shape->num_q_heads / shape->num_kv_heads;
+    p.NT = w.NT;
+    p.nslot = shape->sink + shape->recent;
+    p.max_pages = max_pages;
+    p.num_pages = num_pages;
+    p.pps = w.pps;
+    p.part_stride = w.part_stride;
+    p.qscale = sm_scale * kLog2e;
+    const cudaError_t e = launch_decode(p, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? OSCAR_OK : cuda_fail(e);
+}
+
+}  // extern "C"

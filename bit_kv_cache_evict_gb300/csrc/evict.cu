@@ -1,0 +1,200 @@
+// evict.cu -- fused rotate + clip + quantise + pack of evicted tokens into
+// the paged INT2 history (the eviction kernel of the serving pipeline in
+// "卓绝TurboQuant：Together AI把2-bit KV Cache推向实在行状", figure
+// "从离线校准到在线推理的 pipeline"; rotation R = U.Hadamard.bit-reversal
+// from section "OSCAR 把旋转瞄准 attention").
+//
+// One warp per (token, KV head, K|V) vector.  Lane l owns Hadamard indices
+// j = 4l..4l+3.  y = x.U is accumulated with error-free transformations
+// (FMA-based exact products, TwoSum accumulation: the "Dot2" scheme of
+// Ogita, Rump and Oishi, "Accurate sum and dot product", 2005), the fast
+// Walsh-Hadamard transform runs on the (hi, lo) float pairs, and the group
+// statistics and code decisions run in fp64, so the result follows a
+// float64 evaluation of the method.  Stored position p = bitrev7(j) =
+// 32*bitrev2(i) + bitrev5(l) for value i of lane l: each lane holds one
+// element of every group, and group reductions are warp reductions.
+#include "oscar_common.cuh"
+
+namespace oscar {
+
+
+struct df {  // unevaluated sum hi + lo
+    float hi, lo;
+};
+
+__device__ __forceinline__ df two_sum(float a, float b) {
+    float s = __fadd_rn(a, b);
+    float bp = __fsub_rn(s, a);
+    float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
+    return {s, e};
+}
+
+__device__ __forceinline__ df fast_two_sum(float a, float b) {  // |a| >= |b|
+    float s = __fadd_rn(a, b);
+    return {s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+
+__device__ __forceinline__ df df_add(df a, df b) {
+    df s = two_sum(a.hi, b.hi);
+    float e = __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo));
+    return fast_two_sum(s.hi, e);
+}
+
+__device__ __forceinline__ df df_neg(df a) { return {-a.hi, -a.lo}; }
+
+__global__ void __launch_bounds__(128) evict_kernel(EvictParams p) {
+    const int lane = threadIdx.x & 31;
+    const int vec = blockIdx.x * 4 + (threadIdx.x >> 5);
+    if (vec >= p.n_tok * p.hk * 2) return;
+    const int i = vec / (p.hk * 2);
+    const int kv = (vec >> 1) % p.hk;
+    const int which = vec & 1;
+
+    const long row = p.src_row ? (long)__ldg(p.src_row + i) : (long)i;
+    if (row < 0 || row >= p.src_rows) {
+        if (lane == 0) report(p.status, OSCAR_STATUS_BAD_POS);
+        return;
+    }
+    const size_t xoff = ((size_t)row * p.hk * 2 + (size_t)kv * 2 + which) * kD + 4 * lane;
+    const uint2 xr = *reinterpret_cast<const uint2*>(p.src_kv + xoff);
+    float x[4] = {bf16_lo(xr.x), bf16_hi(xr.x), bf16_lo(xr.y), bf16_hi(xr.y)};
+    if (p.new_kv) {  // fused ring append: this lane read its four elements already
+        const size_t noff = ((size_t)i * p.hk * 2 + (size_t)kv * 2 + which) * kD + 4 * lane;
+        *reinterpret_cast<uint2*>(const_cast<__nv_bfloat16*>(p.src_kv) + xoff) =
+            *reinterpret_cast<const uint2*>(p.new_kv + noff);
+    }
+
+    // ---- y = x . U, compensated --------------------------------------------
+    const float* Um = p.U + ((size_t)kv * 2 + which) * kD * kD;
+    float s[4] = {0.f, 0.f, 0.f, 0.f}, c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+    for (int a = 0; a < kD; ++a) {
+        const float xa = __shfl_sync(kFull, x[a & 3], a >> 2);
+        const float4 u = __ldg(reinterpret_cast<const float4*>(Um + (size_t)a * kD + 4 * lane));
+        const float uu[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float pr = __fmul_rn(xa, uu[k]);
+            const float pe = __fmaf_rn(xa, uu[k], -pr);  // exact product error
+            const df t = two_sum(s[k], pr);
+            s[k] = t.hi;
+            c[k] = __fadd_rn(c[k], __fadd_rn(pe, t.lo));
+        }
+    }
+    df y[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) y[k] = two_sum(s[k], c[k]);
+
+    // ---- Walsh-Hadamard transform (unnormalised), Sylvester order ------------
+    // in-lane stages (distance 1, 2)
+    {
+        df t0 = df_add(y[0], y[1]), t1 = df_add(y[0], df_neg(y[1]));
+        df t2 = df_add(y[2], y[3]), t3 = df_add(y[2], df_neg(y[3]));
+        y[0] = df_add(t0, t2);
+        y[2] = df_add(t0, df_neg(t2));
+        y[1] = df_add(t1, t3);
+        y[3] = df_add(t1, df_neg(t3));
+    }
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {  // distance 4*m: partner lane l ^ m
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            df o{__shfl_xor_sync(kFull, y[k].hi, m), __shfl_xor_sync(kFull, y[k].lo, m)};
+            y[k] = upper ? df_add(o, df_neg(y[k])) : df_add(y[k], o);
+        }
+    }
+
+    // ---- per-group clip / scale / zero / codes in fp64 -----------------------
+    // value k of this lane: stored position 32*bitrev2(k) + bitrev5(lane)
+    const double cr = (double)__ldg(p.clip + kv * 2 + which);
+    double yd[4], amax[4], lo[4], hi[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        yd[k] = ((double)y[k].hi + (double)y[k].lo) * kInvSqrtD;
+        amax[k] = fabs(yd[k]);
+    }
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) amax[k] = fmax(amax[k], __shfl_xor_sync(kFull, amax[k], m));
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const double t = cr * amax[k];
+        yd[k] = fmin(fmax(yd[k], -t), t);
+        lo[k] = hi[k] = yd[k];
+    }
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            lo[k] = fmin(lo[k], __shfl_xor_sync(kFull, lo[k], m));
+            hi[k] = fmax(hi[k], __shfl_xor_sync(kFull, hi[k], m));
+        }
+    unsigned short sb[4], zb[4];
+    uint32_t byte_part[4];
+    const int r5 = bitrev5(lane);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        sb[k] = f64_to_f16_bits((hi[k] - lo[k]) / 3.0);
+        zb[k] = f64_to_f16_bits(lo[k]);
+        const double sd = (double)__half2float(__ushort_as_half(sb[k]));
+        const double zd = (double)__half2float(__ushort_as_half(zb[k]));
+        int code = 0;
+        if (sd != 0.0) {
+            double r = rint((yd[k] - zd) / sd);
+            r = fmin(fmax(r, 0.0), 3.0);
+            code = (int)r;
+        }
+        // position within its byte = r5 & 3
+        byte_part[k] = (uint32_t)code << (2 * (r5 & 3));
+    }
+    // OR the four codes of a byte: they sit in lanes l, l^8, l^16, l^24
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        byte_part[k] |= __shfl_xor_sync(kFull, byte_part[k], 8);
+        byte_part[k] |= __shfl_xor_sync(kFull, byte_part[k], 16);
+    }
+
+    // ---- store ---------------------------------------------------------------
+    const int seq = __ldg(p.dst_seq + i);
+    const int pos = __ldg(p.dst_pos + i);
+    if (pos < 0 || pos >= p.max_pages * kPage || seq < 0 || seq >= p.batch) {
+        if (lane == 0) report(p.status, OSCAR_STATUS_BAD_POS);
+        return;
+    }
+    const int page = __ldg(p.page_table + (size_t)seq * p.max_pages + pos / kPage);
+    if (page < 0 || page >= p.num_pages) {
+        if (lane == 0) report(p.status, OSCAR_STATUS_BAD_PAGE);
+        return;
+    }
+    const int slot = pos % kPage;
+    uint8_t* blk = p.pool + ((size_t)page * p.hk + kv) * kBlock;
+    if (lane < 8) {
+        const int j8 = r5 >> 2;  // byte index within each group's 8 bytes
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int j = 8 * bitrev2(k) + j8;
+            const uint8_t b = (uint8_t)byte_part[k];
+            if (which == 0) blk[kKCodes + slot * (kD / 4) + j] = b;
+            else blk[kVCodes + j * kPage + slot] = b;
+        }
+    }
+    if (lane == 0) {
+        // group of value k is bitrev2(k); scale/zero words in group order
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) w[bitrev2(k)] = (uint32_t)sb[k] | ((uint32_t)zb[k] << 16);
+        *reinterpret_cast<uint4*>(blk + (which == 0 ? kKScale : kVScale) + slot * 16) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+cudaError_t launch_evict(const EvictParams& p, cudaStream_t st) {
+    const int vecs = p.n_tok * p.hk * 2;
+    if (vecs == 0) return cudaSuccess;
+    evict_kernel<<<(vecs + 3) / 4, 128, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace oscar

@@ -1,0 +1,186 @@
+// oscar_common.cuh -- device helpers shared by the liboscar kernels
+// (sm_103a).  Library-internal.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/oscar.h"
+
+namespace oscar {
+
+constexpr int kD = 128;           // head_dim
+constexpr int kGroup = 32;        // quantisation group
+constexpr int kNumGroups = kD / kGroup;
+constexpr int kPage = 64;         // tokens per page
+constexpr int kBlock = OSCAR_BLOCK_BYTES;
+constexpr int kKCodes = 0;        // byte offsets inside a (page, kv) block
+constexpr int kVCodes = 2048;
+constexpr int kKScale = 4096;
+constexpr int kVScale = 5120;
+constexpr float kLog2e = 1.4426950408889634f;
+// 1/sqrt(128) in double
+constexpr double kInvSqrtD = 0.088388347648318440550105545263;
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// bit reversal of the low 5 / 2 bits
+__device__ __forceinline__ int bitrev5(int v) { return (int)(__brev((unsigned)v) >> 27); }
+__device__ __forceinline__ int bitrev2(int v) { return ((v & 1) << 1) | ((v >> 1) & 1); }
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ float half_lo(uint32_t w) {
+    return __half2float(__ushort_as_half((unsigned short)(w & 0xffffu)));
+}
+__device__ __forceinline__ float half_hi(uint32_t w) {
+    return __half2float(__ushort_as_half((unsigned short)(w >> 16)));
+}
+
+// binary16 from binary64, one rounding (round to nearest even)
+__device__ __forceinline__ unsigned short f64_to_f16_bits(double x) {
+    unsigned short h;
+    asm("cvt.rn.f16.f64 %0, %1;" : "=h"(h) : "d"(x));
+    return h;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// (x & mask) | bits in one LOP3
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t x, uint32_t mask, uint32_t bits) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(x), "r"(mask), "r"(bits));
+    return r;
+}
+
+// Two 2-bit codes at bits 4-5 and 20-21 of x -> bf16x2 (8 + c_lo, 8 + c_hi):
+// bf16 0x4100 is 8.0 with 7 mantissa bits, so code c placed in mantissa
+// bits 4-5 reads as 8 + c exactly.
+__device__ __forceinline__ uint32_t codes_to_bf16x2(uint32_t x) {
+    return lop3_and_or(x, 0x00300030u, 0x41004100u);
+}
+
+__device__ __forceinline__ uint32_t rotr(uint32_t x, uint32_t n) { return __funnelshift_r(x, x, n); }
+
+// D += A(16x16 bf16, row) * B(16x8 bf16, col), fp32 accumulate
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// bf16x2 with lo -> bits 0-15, hi -> bits 16-31, round to nearest even
+__device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// ------------------------------------------------------------------
+// mbarrier + bulk async copy (TMA, non-tensor), all waits bounded
+// ------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for phase `parity` of the barrier, giving up after max_iter polls
+// (each try_wait itself suspends for a hardware-defined time).  Returns
+// false on timeout; callers then report and skip instead of hanging.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int max_iter) {
+    for (int i = 0; i < max_iter; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+__device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst_smem)),
+        "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void report(int32_t* status, int32_t bits) {
+    if (status) atomicOr(status, bits);
+}
+
+
+// ------------------------------------------------------------------
+// launch parameters (host <-> kernels)
+// ------------------------------------------------------------------
+struct EvictParams {
+    const __nv_bfloat16* src_kv;
+    const int32_t* src_row;
+    const int32_t* dst_seq;
+    const int32_t* dst_pos;
+    const __nv_bfloat16* new_kv;
+    const float* U;
+    const float* clip;
+    uint8_t* pool;
+    const int32_t* page_table;
+    int32_t* status;
+    int n_tok, hk, src_rows, batch, max_pages, num_pages;
+};
+
+struct DecodeParams {
+    const __nv_bfloat16* q;
+    const __nv_bfloat16* bf16_kv;
+    const int32_t* bf16_len;
+    const uint8_t* pool;
+    const int32_t* page_table;
+    const int32_t* hist_len;
+    const float* U;
+    float* out;
+    int32_t* status;
+    // workspace sections
+    int32_t* counter;     // [1]
+    int32_t* item_start;  // [B + 1]
+    uint32_t* qfrag;      // [B*Hk][NT][8][32][2]
+    float* qsum;          // [B*Hk][NT*4][4]
+    float* part;          // [max_items][part_stride]
+    float* bf_part;       // [B*Hk][part_stride]
+    int B, hq, hk, G, NT, nslot, max_pages, num_pages, pps, part_stride;
+    float qscale;  // sm_scale * log2(e)
+};
+
+cudaError_t launch_evict(const EvictParams& p, cudaStream_t st);
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st);
+
+}  // namespace oscar

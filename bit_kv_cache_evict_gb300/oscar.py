@@ -1,0 +1,171 @@
+"""Thin ctypes binding of liboscar (include/oscar.h), same call names.
+
+Argument marshalling only: every step of the hot path runs in the CUDA
+kernels of liboscar.so.  There is no CPU fallback: if the library is missing
+or cannot be loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import numpy as np
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "liboscar.so")
+HEADER = os.path.join(os.path.dirname(PKG), "include", "oscar.h")
+
+OSCAR_OK, OSCAR_ERR_INVALID_ARG, OSCAR_ERR_UNSUPPORTED, OSCAR_ERR_OUT_OF_PAGES, OSCAR_ERR_WORKSPACE, \
+    OSCAR_ERR_CUDA = range(6)
+OSCAR_STATUS_BAD_PAGE, OSCAR_STATUS_BAD_POS, OSCAR_STATUS_TIMEOUT = 1, 2, 4
+BLOCK_BYTES = 6144
+
+
+class OscarError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn}: {msg} (status {status})")
+        self.status = status
+
+
+class oscar_shape(ctypes.Structure):
+    _fields_ = [("head_dim", ctypes.c_int32), ("quant_group", ctypes.c_int32), ("sink", ctypes.c_int32),
+                ("recent", ctypes.c_int32), ("page_size", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32)]
+
+
+def make_shape(num_q_heads: int, num_kv_heads: int, head_dim: int = 128, quant_group: int = 32, sink: int = 64,
+               recent: int = 256, page_size: int = 64) -> oscar_shape:
+    return oscar_shape(head_dim, quant_group, sink, recent, page_size, num_q_heads, num_kv_heads)
+
+
+_LIB = None
+_P = ctypes.c_void_p
+
+
+def lib() -> ctypes.CDLL:
+    """Load liboscar.so (built in-tree by ``build.build()``); raise if absent."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"liboscar.so not built ({LIB_PATH}); run bit_kv_cache_evict_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        S = ctypes.POINTER(oscar_shape)
+        L.oscar_block_bytes.restype = ctypes.c_size_t
+        L.oscar_block_bytes.argtypes = [S]
+        L.oscar_status_string.restype = ctypes.c_char_p
+        L.oscar_status_string.argtypes = [ctypes.c_int]
+        L.oscar_last_cuda_error.restype = ctypes.c_int
+        L.oscar_pool_layout.restype = ctypes.c_int
+        L.oscar_pool_layout.argtypes = [S, ctypes.c_int32, _P, _P, ctypes.c_int32, ctypes.c_uint64, ctypes.c_int32,
+                                        _P, _P, _P]
+        L.oscar_evict_quantize.restype = ctypes.c_int
+        L.oscar_evict_quantize.argtypes = [S, ctypes.c_int32, _P, ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P, _P,
+                                           ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, _P]
+        L.oscar_decode_attn.restype = ctypes.c_int
+        L.oscar_decode_attn.argtypes = [S, ctypes.c_int32, _P, _P, _P, _P, _P, ctypes.c_int32, ctypes.c_int32, _P,
+                                        _P, ctypes.c_float, _P, _P, ctypes.POINTER(ctypes.c_size_t), _P, _P]
+        _LIB = L
+    return _LIB
+
+
+def declared_functions() -> list[str]:
+    """Entry points declared in include/oscar.h."""
+    with open(HEADER) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:[\w\s\*]+?)\b(oscar_\w+)\s*\(", text, re.M)))
+
+
+def _check(fn: str, st: int) -> None:
+    if st != OSCAR_OK:
+        msg = lib().oscar_status_string(st).decode()
+        if st == OSCAR_ERR_CUDA:
+            msg += f" (cudaError {lib().oscar_last_cuda_error()})"
+        raise OscarError(fn, st, msg)
+
+
+def _dptr(t, what: str, dtype=None, align: int = 1):
+    """Device pointer of a CUDA tensor (None -> NULL)."""
+    if t is None:
+        return None
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{what}: expected a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{what}: expected {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{what}: must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def block_bytes(shape: oscar_shape) -> int:
+    return int(lib().oscar_block_bytes(ctypes.byref(shape)))
+
+
+def oscar_pool_layout(shape: oscar_shape, hist_capacity, prefix_group=None, shared_hist_tokens: int = 0,
+                      perm_seed: int = 0, max_pages: int | None = None):
+    """Host page-table layout.  Returns (page_table int32 [B][max_pages],
+    num_pages, pool_bytes)."""
+    cap = np.ascontiguousarray(hist_capacity, np.int32)
+    B = cap.shape[0]
+    if max_pages is None:
+        max_pages = max(1, int((int(cap.max(initial=0)) + shape.page_size - 1) // shape.page_size))
+    pg = None if prefix_group is None else np.ascontiguousarray(prefix_group, np.int32)
+    table = np.zeros((B, max_pages), np.int32)
+    n = ctypes.c_int32(0)
+    nbytes = ctypes.c_uint64(0)
+    st = lib().oscar_pool_layout(ctypes.byref(shape), B, cap.ctypes.data_as(_P),
+                                 None if pg is None else pg.ctypes.data_as(_P), shared_hist_tokens,
+                                 ctypes.c_uint64(perm_seed), max_pages, table.ctypes.data_as(_P), ctypes.byref(n),
+                                 ctypes.byref(nbytes))
+    _check("oscar_pool_layout", st)
+    return table, int(n.value), int(nbytes.value)
+
+
+def oscar_evict_quantize(shape: oscar_shape, src_kv, dst_seq, dst_pos, U, clip, pool, page_table, batch: int,
+                         max_pages: int, num_pages: int, src_row=None, new_kv=None, dev_status=None,
+                         stream=None) -> None:
+    """Fused rotate/clip/quantise/pack of dst_seq.numel() token rows into the
+    pool (see include/oscar.h).  src_kv: bf16 [rows][Hk][2][d]."""
+    import torch
+    n_tok = int(dst_seq.numel())
+    st = lib().oscar_evict_quantize(
+        ctypes.byref(shape), n_tok, _dptr(src_kv, "src_kv", torch.bfloat16), int(src_kv.shape[0]),
+        _dptr(src_row, "src_row", torch.int32), _dptr(dst_seq, "dst_seq", torch.int32),
+        _dptr(dst_pos, "dst_pos", torch.int32), _dptr(new_kv, "new_kv", torch.bfloat16),
+        _dptr(U, "U", torch.float32), _dptr(clip, "clip", torch.float32), _dptr(pool, "pool", torch.uint8),
+        _dptr(page_table, "page_table", torch.int32), batch, max_pages, num_pages,
+        _dptr(dev_status, "dev_status", torch.int32), _stream_ptr(stream))
+    _check("oscar_evict_quantize", st)
+
+
+def oscar_decode_workspace_bytes(shape: oscar_shape, batch: int, max_pages: int) -> int:
+    ws = ctypes.c_size_t(0)
+    st = lib().oscar_decode_attn(ctypes.byref(shape), batch, None, None, None, None, None, max_pages, 0, None,
+                                 None, ctypes.c_float(1.0), None, None, ctypes.byref(ws), None, None)
+    _check("oscar_decode_attn", st)
+    return int(ws.value)
+
+
+def oscar_decode_attn(shape: oscar_shape, q, bf16_kv, bf16_len, pool, page_table, max_pages: int, num_pages: int,
+                      hist_len, U, sm_scale: float, out, workspace, dev_status=None, stream=None) -> None:
+    """Decode attention over sink + INT2 history + recent (see
+    include/oscar.h).  ``workspace``: CUDA uint8 tensor of at least
+    oscar_decode_workspace_bytes(shape, batch, max_pages) bytes."""
+    import torch
+    B = int(q.shape[0])
+    ws = ctypes.c_size_t(int(workspace.numel()))
+    st = lib().oscar_decode_attn(
+        ctypes.byref(shape), B, _dptr(q, "q", torch.bfloat16), _dptr(bf16_kv, "bf16_kv", torch.bfloat16),
+        _dptr(bf16_len, "bf16_len", torch.int32), _dptr(pool, "pool", torch.uint8),
+        _dptr(page_table, "page_table", torch.int32), max_pages, num_pages, _dptr(hist_len, "hist_len", torch.int32),
+        _dptr(U, "U", torch.float32), ctypes.c_float(sm_scale), _dptr(out, "out", torch.float32),
+        _dptr(workspace, "workspace", torch.uint8), ctypes.byref(ws), _dptr(dev_status, "dev_status", torch.int32),
+        _stream_ptr(stream))
+    _check("oscar_decode_attn", st)

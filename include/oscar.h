@@ -1,0 +1,209 @@
+/*
+ * oscar.h -- C ABI of liboscar, the GB300 (sm_103a) hot path of OSCAR's
+ * 2-bit KV-cache serving scheme.
+ *
+ * The method, as the pages describe it:
+ *   [NEWS] "卓绝TurboQuant：Together AI把2-bit KV Cache推向实在行状"
+ *          (www.sanyangsrq.com news article on OSCAR)
+ *          sec. B "OSCAR 把旋转瞄准 attention": the rotation
+ *                 R = U . Hadamard . bit-reversal, U per layer and KV head,
+ *                 separately for K and V;
+ *          sec. C figure "从离线校准到在线推理的 pipeline" and the text
+ *                 under it: three-segment token pool (BF16 sink of 64 |
+ *                 INT2 history | BF16 recent window of 256); the oldest
+ *                 recent token is rotated, clipped, quantised and packed by
+ *                 one fused kernel and moved into the history; four 2-bit
+ *                 codes per byte; decode runs an INT2 kernel (unpack,
+ *                 scale/zero dequantisation, float accumulation) and a BF16
+ *                 kernel for sink/recent, merged by online softmax;
+ *                 compatible with paged KV and prefix caching.
+ *   [TALK] ml-summit.org speaker page, "Beyond the Paper: Engineering 2-Bit
+ *          KV Cache for Real-World Deployment": mixed-precision data in a
+ *          paged KV cache.
+ *
+ * Conventions for every call
+ *   - Device pointers are caller-owned (allocate them with any allocator);
+ *     the library never allocates, frees or keeps device memory, and keeps
+ *     no state between calls except a per-device cache of kernel
+ *     attributes.
+ *   - Device calls are asynchronous on the given stream (a cudaStream_t
+ *     passed as void*; NULL = the legacy default stream).  They validate
+ *     their host-visible arguments first and return an error before any
+ *     launch; after launching they return OSCAR_ERR_CUDA if the launch
+ *     failed (oscar_last_cuda_error() then holds the cudaError_t value).
+ *   - Kernels never trap.  Out-of-range page ids or positions found on the
+ *     device are skipped (a skipped history page contributes nothing) and
+ *     reported by OR-ing bits into *dev_status when dev_status (a device
+ *     int32) is not NULL: OSCAR_STATUS_BAD_PAGE, OSCAR_STATUS_BAD_POS.
+ *   - Only head_dim 128, quant_group 32, page_size 64 and query-per-KV-head
+ *     groups G = Hq/Hk in {1, 2, 4, 8} are supported; other shapes return
+ *     OSCAR_ERR_UNSUPPORTED.
+ *
+ * Data layouts (row-major, little-endian)
+ *   K/V token rows   bf16 [rows][Hk][2][d]           (index 0 = K, 1 = V)
+ *   BF16 segments    bf16 [B][sink+recent][Hk][2][d] per layer; slots
+ *                    [0, bf16_len[b]) are the valid sink + recent tokens
+ *                    (their order does not matter to attention)
+ *   U                fp32 [Hk][2][d][d]  (U_K, U_V); a row vector x is
+ *                    rotated as y = x . U . H . P
+ *   clip             fp32 [Hk][2]        clip ratio c in (0, 1]
+ *   q                bf16 [B][Hq][d];  query head h reads KV head h / G
+ *   out              fp32 [B][Hq][d]
+ *   page_table       int32 [B][max_pages]: history position pos of sequence
+ *                    b lives in page page_table[b*max_pages + pos/64],
+ *                    slot pos % 64
+ *   pool             num_pages * Hk blocks of OSCAR_BLOCK_BYTES (6144 B);
+ *                    block (page, kv) starts at (page*Hk + kv) * 6144 and
+ *                    holds 64 token slots t:
+ *       [0, 2048)     K codes, token-major: byte t*32 + j
+ *       [2048, 4096)  V codes, byte-plane-major: byte 2048 + j*64 + t
+ *       [4096, 5120)  K scale/zero: at 4096 + t*16 + k*4, fp16 s then fp16 z
+ *       [5120, 6144)  V scale/zero: at 5120 + t*16 + k*4
+ *                    Code byte j holds stored positions 4j..4j+3, position
+ *                    4j+i in bits 2i..2i+1; group k is stored positions
+ *                    32k..32k+31; stored position p holds Hadamard output
+ *                    bitrev7(p) (the bit-reversal of R, folded into
+ *                    addressing); value = s*code + z in the rotated domain.
+ */
+#ifndef OSCAR_H
+#define OSCAR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    OSCAR_OK = 0,
+    OSCAR_ERR_INVALID_ARG = 1,  /* bad pointer, size, alignment or value */
+    OSCAR_ERR_UNSUPPORTED = 2,  /* valid but unsupported shape */
+    OSCAR_ERR_OUT_OF_PAGES = 3, /* a sequence needs more pages than max_pages */
+    OSCAR_ERR_WORKSPACE = 4,    /* workspace smaller than oscar_decode_attn needs */
+    OSCAR_ERR_CUDA = 5          /* a CUDA launch or query failed */
+} oscar_status;
+
+/* Device-side report bits (see dev_status). */
+#define OSCAR_STATUS_BAD_PAGE 1 /* a page id outside [0, num_pages) */
+#define OSCAR_STATUS_BAD_POS 2  /* a position, row or sequence index out of range */
+#define OSCAR_STATUS_TIMEOUT 4  /* a bounded wait for a page copy gave up */
+
+#define OSCAR_BLOCK_BYTES 6144  /* bytes per (page, KV head) block, d=128, g=32, page 64 */
+
+typedef struct {
+    int32_t head_dim;     /* d = 128 */
+    int32_t quant_group;  /* g = 32 elements per fp16 scale/zero */
+    int32_t sink;         /* BF16 sink tokens (64) */
+    int32_t recent;       /* BF16 recent-window tokens (256) */
+    int32_t page_size;    /* tokens per history page (64) */
+    int32_t num_q_heads;  /* Hq */
+    int32_t num_kv_heads; /* Hk; Hq % Hk == 0 */
+} oscar_shape;
+
+/* Bytes of one (page, KV head) block for this shape, 0 if unsupported. */
+size_t oscar_block_bytes(const oscar_shape* shape);
+
+/* Human-readable name of a status code (static string). */
+const char* oscar_status_string(oscar_status st);
+
+/* cudaError_t of the last call that returned OSCAR_ERR_CUDA on this thread. */
+int oscar_last_cuda_error(void);
+
+/*
+ * oscar_pool_layout -- paged-block allocation for the INT2 history
+ * ([NEWS] sec. C: paged KV and radix-prefix-cache compatibility;
+ * [TALK]: mixed-precision data in a paged KV cache).  Host only.
+ *
+ *   hist_capacity[batch]  (host) history tokens each sequence may hold.
+ *   prefix_group[batch]   (host, nullable) sequences with the same group
+ *                         id >= 0 share their first shared_hist_tokens/64
+ *                         history pages (one physical copy, read-only by
+ *                         convention); -1 = no sharing.
+ *   shared_hist_tokens    multiple of 64, <= hist_capacity of every sharer.
+ *   perm_seed             0: pages are numbered in allocation order; else
+ *                         page L of that order becomes pi[L], pi a
+ *                         Fisher-Yates shuffle of 0..N-1 driven by
+ *                         SplitMix64 started at perm_seed (for i = N-1 down
+ *                         to 1: j = next() mod (i+1), swap pi[i], pi[j]).
+ *   Allocation order: the shared pages of each prefix group in order of
+ *   first appearance, then each sequence's private pages in order.
+ *   page_table[batch*max_pages] (host, out): page ids, -1 where unused.
+ *   num_pages_out, pool_bytes_out (host, out, nullable): pages allocated and
+ *   pool bytes (num_pages * Hk * block bytes).
+ * Errors: INVALID_ARG for bad sizes/pointers/prefix settings, OUT_OF_PAGES
+ * if a sequence needs more than max_pages pages.
+ */
+oscar_status oscar_pool_layout(const oscar_shape* shape, int32_t batch, const int32_t* hist_capacity,
+                               const int32_t* prefix_group, int32_t shared_hist_tokens, uint64_t perm_seed,
+                               int32_t max_pages, int32_t* page_table, int32_t* num_pages_out,
+                               uint64_t* pool_bytes_out);
+
+/*
+ * oscar_evict_quantize -- the fused eviction kernel ([NEWS] sec. C): for
+ * each of n_tok tokens and each KV head, rotate the K and V vectors by
+ * R = U . H . P ([NEWS] sec. B), clip each group of 32 stored positions to
+ * +-c*max|y|, quantise to 2-bit codes with fp16 scale s = (max-min)/3 and
+ * zero z = min (codes from the stored fp16 s, z, round half to even,
+ * clamped to 0..3; all codes 0 when s == 0), pack four codes per byte and
+ * write codes and s/z into the pool slot of history position dst_pos[i] of
+ * sequence dst_seq[i].
+ *
+ *   src_kv   (device) bf16 token rows [src_rows][Hk][2][d]; token i reads
+ *            row src_row[i] (device int32, nullable: row i).
+ *   new_kv   (device, nullable) bf16 [n_tok][Hk][2][d]: when given, row
+ *            src_row[i] is overwritten with new_kv[i] after it was read (the
+ *            ring-buffer append of a decode step fused into the eviction).
+ *            Rows must then be distinct.
+ *   dst_seq, dst_pos (device int32 [n_tok]); page_table (device int32
+ *            [batch][max_pages]); num_pages = pool extent.  Rows, sequences,
+ *            positions and page ids are bounds-checked on the device; a
+ *            token with a bad index is skipped and reported in dev_status.
+ *   U, clip  (device fp32) as in the layouts above.
+ * The arithmetic keeps y = x.U.H accurate to ~2^-44 relative (compensated
+ * fp32 products and sums, group statistics and code decisions in fp64), so
+ * codes and fp16 s/z match a float64 evaluation except for values within
+ * ~1e-13 of a rounding boundary.
+ */
+oscar_status oscar_evict_quantize(const oscar_shape* shape, int32_t n_tok, const void* src_kv,
+                                  int32_t src_rows, const int32_t* src_row, const int32_t* dst_seq,
+                                  const int32_t* dst_pos, const void* new_kv, const float* U,
+                                  const float* clip, uint8_t* pool, const int32_t* page_table,
+                                  int32_t batch, int32_t max_pages, int32_t num_pages,
+                                  int32_t* dev_status, void* stream);
+
+/*
+ * oscar_decode_attn -- one decode step of attention for every (sequence,
+ * query head) over sink + INT2 history + recent window ([NEWS] sec. C):
+ *   out[b,h] = softmax_t(sm_scale * q . k_t) . V
+ * over the valid BF16 slots and the hist_len[b] history tokens, whose keys
+ * and values are the dequantised stored vectors mapped back by R^T.  The
+ * INT2 segment is attended in the rotated domain (q' = q . R_K; output
+ * mapped back by R_V^T); segments and split-K partials are merged by their
+ * log-sum-exp.  An empty context gives a zero output.
+ *
+ *   q        (device) bf16 [B][Hq][d]       bf16_kv (device) see layouts
+ *   bf16_len (device int32 [B], each in [0, sink+recent])
+ *   pool, page_table (device), max_pages, num_pages (pool extent)
+ *   hist_len (device int32 [B]) history tokens at positions [0, hist_len)
+ *   U        (device fp32 [Hk][2][d][d]) same matrices as the eviction
+ *   out      (device fp32 [B][Hq][d])
+ *   workspace, *ws_bytes: caller-owned device scratch, 16-byte aligned.
+ *            With workspace == NULL the call only stores the required size
+ *            in *ws_bytes (it depends on shape, batch and max_pages) and
+ *            launches nothing; with a smaller *ws_bytes it returns
+ *            OSCAR_ERR_WORKSPACE.  The workspace holds the rotated queries,
+ *            the work plan and the split-K partials of this call; calls that
+ *            share a workspace must be ordered on one stream.
+ */
+oscar_status oscar_decode_attn(const oscar_shape* shape, int32_t batch, const void* q, const void* bf16_kv,
+                               const int32_t* bf16_len, const uint8_t* pool, const int32_t* page_table,
+                               int32_t max_pages, int32_t num_pages, const int32_t* hist_len, const float* U,
+                               float sm_scale, float* out, void* workspace, size_t* ws_bytes,
+                               int32_t* dev_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OSCAR_H */

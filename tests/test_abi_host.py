@@ -1,0 +1,96 @@
+"""CPU tests of the C-ABI library: it loads, exports every declared entry
+point, and its host-only logic (page-table layout, argument checks) matches
+the oracle / the header's contract.  No compute call needs a GPU here."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle
+from bit_kv_cache_evict_gb300 import build as B
+from bit_kv_cache_evict_gb300 import oscar as O
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return O.lib()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = O.declared_functions()
+    assert {"oscar_pool_layout", "oscar_evict_quantize", "oscar_decode_attn"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_block_bytes_and_status_strings(lib):
+    assert O.block_bytes(O.make_shape(32, 8)) == 6144
+    assert O.block_bytes(O.make_shape(32, 8, quant_group=64)) == 0       # unsupported
+    for st in range(6):
+        assert lib.oscar_status_string(st)
+
+
+CASES = [
+    (np.array([64, 1, 0, 130, 640]), None, 0, 0),
+    (np.array([64, 1, 0, 130, 640]), None, 0, 77),
+    (np.array([300, 200, 500, 256]), np.array([0, -1, 0, 0]), 128, 0),
+    (np.array([300, 200, 500, 256, 700, 1000]), np.array([1, -1, 1, 1, 2, 2]), 256, 5),
+    (np.random.default_rng(0).integers(0, 5000, 64), None, 0, 1003),
+]
+
+
+@pytest.mark.parametrize("cap,grp,shared,seed", CASES)
+def test_pool_layout_matches_oracle(lib, orc, cap, grp, shared, seed):
+    sh = O.make_shape(32, 8)
+    mp = int(max(1, (cap.max() + 63) // 64)) + 1
+    t, n, nb = O.oscar_pool_layout(sh, cap, grp, shared, seed, mp)
+    rc, t2, n2, nb2 = orc.pool_layout(oracle.Shape(128, 32, 64, 256, 64, 32, 8), cap, grp, shared, seed, mp)
+    assert rc == 0
+    assert np.array_equal(t, t2) and n == n2 and nb == nb2
+
+
+def test_pool_layout_errors(lib):
+    sh = O.make_shape(32, 8)
+    with pytest.raises(O.OscarError) as e:
+        O.oscar_pool_layout(sh, np.array([65 * 64]), max_pages=64)
+    assert e.value.status == O.OSCAR_ERR_OUT_OF_PAGES
+    with pytest.raises(O.OscarError) as e:
+        O.oscar_pool_layout(sh, np.array([300, 300]), np.array([0, 0]), 100, 0, 8)
+    assert e.value.status == O.OSCAR_ERR_INVALID_ARG
+    with pytest.raises(O.OscarError) as e:
+        O.oscar_pool_layout(O.make_shape(24, 8), np.array([10]), max_pages=4)     # G = 3
+    assert e.value.status == O.OSCAR_ERR_UNSUPPORTED
+
+
+def test_argument_checks_before_launch(lib):
+    """Host-side validation returns before touching the GPU (NULL / bad sizes)."""
+    sh = O.make_shape(32, 8)
+    ws = ctypes.c_size_t(0)
+    # workspace query needs no device
+    assert lib.oscar_decode_attn(ctypes.byref(sh), 4, None, None, None, None, None, 10, 0, None, None,
+                                 ctypes.c_float(1.0), None, None, ctypes.byref(ws), None, None) == O.OSCAR_OK
+    assert ws.value > 0
+    small = ctypes.c_size_t(ws.value - 1)
+    fake = ctypes.c_void_p(256)
+    assert lib.oscar_decode_attn(ctypes.byref(sh), 4, fake, fake, fake, fake, fake, 10, 1, fake, fake,
+                                 ctypes.c_float(1.0), fake, fake, ctypes.byref(small), None,
+                                 None) == O.OSCAR_ERR_WORKSPACE
+    assert lib.oscar_decode_attn(ctypes.byref(sh), 4, None, None, None, None, None, 0, 0, None, None,
+                                 ctypes.c_float(1.0), None, fake, ctypes.byref(ws), None,
+                                 None) == O.OSCAR_ERR_INVALID_ARG       # max_pages = 0
+    assert lib.oscar_decode_attn(ctypes.byref(sh), 4, None, None, None, None, None, 10, 0, None, None,
+                                 ctypes.c_float(1.0), None, fake, ctypes.byref(ws), None,
+                                 None) == O.OSCAR_ERR_INVALID_ARG       # NULL q
+    mis = ctypes.c_void_p(258)
+    assert lib.oscar_decode_attn(ctypes.byref(sh), 4, mis, fake, fake, fake, fake, 10, 1, fake, fake,
+                                 ctypes.c_float(1.0), fake, fake, ctypes.byref(ws), None,
+                                 None) == O.OSCAR_ERR_INVALID_ARG       # misaligned q
+    # eviction: n_tok = 0 is a no-op; NULL pointers are rejected
+    assert lib.oscar_evict_quantize(ctypes.byref(sh), 0, None, 0, None, None, None, None, None, None, None, None,
+                                    1, 1, 1, None, None) == O.OSCAR_OK
+    assert lib.oscar_evict_quantize(ctypes.byref(sh), 3, None, 3, None, None, None, None, None, None, None, None,
+                                    1, 1, 1, None, None) == O.OSCAR_ERR_INVALID_ARG
+    bad = O.make_shape(32, 8, head_dim=96)
+    assert lib.oscar_evict_quantize(ctypes.byref(bad), 3, fake, 3, None, fake, fake, None, fake, fake, fake, fake,
+                                    1, 1, 1, None, None) == O.OSCAR_ERR_UNSUPPORTED
