@@ -1,0 +1,527 @@
+#!/usr/bin/env python3
+"""Benchmark of the OSCAR decode hot path on GB300 (one JSON line on rank 0).
+
+A step is one full decode step of the workload: for every layer, the fused
+eviction of the oldest recent token of every sequence into the INT2 history
+(with the ring append of the new token) followed by decode attention over
+sink + INT2 history + recent window.  The state advances every step
+(history +1 token per sequence and layer).  Inputs are synthetic, seeded,
+and already resident in HBM when the timed region starts; every layer has
+its own pool (far larger than the 129 MB L2), so no L2 flush is needed.
+
+  python bench.py [--gpus N --steps K --warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the float64 CPU oracle arm
+
+Multi-GPU (torchrun): every rank runs its own replica of the workload (the
+sequences are independent); no collective is on the data path, and timing
+takes the max over ranks ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from bit_kv_cache_evict_gb300 import synth as S  # noqa: E402
+
+METRIC = "decode context-tokens/s attended"
+UNIT = "tokens/s"
+HIST_BYTES_PER_TOKEN_HEAD = 96      # 2 x 32 B codes + 2 x 4 x (fp16 s, fp16 z)
+BF16_BYTES_PER_TOKEN_HEAD = 2 * 128 * 2
+DEFAULT_WORKLOAD = "qwen3_8b_36l"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["oscar", "reference"], default="oscar")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(S.WORKLOADS))
+    ap.add_argument("--layers", type=int, default=None, help="override the layer count (testing)")
+    ap.add_argument("--cpu-tokens", type=int, default=60000,
+                    help="history tokens in the oracle's bounded sample")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing
+# ---------------------------------------------------------------------------
+
+def dist_info():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def dist_init(world: int, backend: str):
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend)
+
+
+def reduce_max(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
+                                          "-lms", "100", "-i", str(self.gpu)], stdout=self.file,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.count(",") >= 8]
+        self.file.close()
+        os.unlink(self.file.name)
+        sm, smax, power, reasons = [], None, [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1].split()[0]))
+                smax = float(r[2].split()[0])
+                power.append(float(r[3].split()[0]))
+            except (ValueError, IndexError):
+                continue
+            for name, v in zip(names, r[5:9]):
+                if "Active" in v and "Not" not in v:
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": ["no samples"]}
+        # samples under load: power within 35% of the peak seen
+        pmax = max(power) if power else 0
+        loaded = [s for s, p in zip(sm, power) if p >= 0.65 * pmax] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": pmax}
+
+
+# ---------------------------------------------------------------------------
+# workload state on the GPU
+# ---------------------------------------------------------------------------
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return {"hbm_gbs": float(pk["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+class GpuState:
+    """Pools, BF16 segments, queries and per-step metadata for every layer."""
+
+    def __init__(self, w: S.Workload, layers: int, steps_total: int, rank: int):
+        import torch
+        from bit_kv_cache_evict_gb300 import oscar as O
+        self.O, self.torch = O, torch
+        self.w, self.L = w, layers
+        dev = torch.device("cuda")
+        self.dev = dev
+        B, Hq, Hk, d = w.batch, w.hq, w.hk, S.D
+        self.shape = O.make_shape(Hq, Hk)
+        ctx = S.context_lengths(w)
+        self.ctx0 = ctx
+        hist0 = np.maximum(ctx - S.NSLOT, 0).astype(np.int64)
+        self.hist0 = hist0
+        cap = hist0 + steps_total + 1
+        self.max_pages = int((cap.max() + S.PAGE - 1) // S.PAGE)
+        grp = None
+        if w.prefix_seqs:
+            grp = np.full(B, -1, np.int32)
+            grp[: w.prefix_seqs] = 0
+        perm_seed = (w.seed * 7919 + 1) if w.shuffled else 0
+        table, self.num_pages, self.pool_bytes = O.oscar_pool_layout(self.shape, cap, grp, w.shared_hist_tokens,
+                                                                     perm_seed, self.max_pages)
+        self.table = torch.from_numpy(table).to(dev)
+        self.B, self.Hq, self.Hk = B, Hq, Hk
+        # per-step metadata (device): eviction target position, ring row,
+        # history length after the step
+        steps = np.arange(steps_total, dtype=np.int64)[:, None]
+        self.hist_before = torch.from_numpy((hist0[None, :] + steps).astype(np.int32)).to(dev)
+        self.hist_after = torch.from_numpy((hist0[None, :] + steps + 1).astype(np.int32)).to(dev)
+        rows = np.arange(B)[None, :] * S.NSLOT + S.SINK + (steps % S.RECENT)
+        self.src_row = torch.from_numpy(rows.astype(np.int32)).to(dev)
+        self.seqs = torch.arange(B, dtype=torch.int32, device=dev)
+        self.bf16_len = torch.full((B,), S.NSLOT, dtype=torch.int32, device=dev)
+        self.sm_scale = 1.0 / math.sqrt(d)
+        self.ws = torch.empty(O.oscar_decode_workspace_bytes(self.shape, B, self.max_pages), dtype=torch.uint8,
+                              device=dev)
+        self.layers = []
+        gen = torch.Generator(device=dev)
+        for layer in range(layers):
+            gen.manual_seed(w.seed * 100003 + 1009 * layer + 7 * rank)
+            U = torch.from_numpy(S.rotation_U(w, layer).astype(np.float32)).to(dev)
+            clip = torch.from_numpy(S.clip_ratios(w).astype(np.float32)).to(dev)
+            prof = torch.from_numpy(S.channel_profile(w, layer).astype(np.float32)).to(dev)
+            pool = torch.empty(self.pool_bytes, dtype=torch.uint8, device=dev)
+            self._fill_history(pool, U, clip, prof, gen, hist0, grp)
+            kv = S.kv_tokens_torch(w, B * S.NSLOT, gen, prof, dev).view(B, S.NSLOT, Hk, 2, d).contiguous()
+            q = torch.randn((B, Hq, d), generator=gen, device=dev).to(torch.bfloat16)
+            new_kv = S.kv_tokens_torch(w, B, gen, prof, dev).contiguous()
+            out = torch.empty((B, Hq, d), dtype=torch.float32, device=dev)
+            self.layers.append(dict(U=U, clip=clip, pool=pool, kv=kv, q=q, new_kv=new_kv, out=out))
+        torch.cuda.synchronize()
+
+    def _fill_history(self, pool, U, clip, prof, gen, hist0, grp):
+        """Bulk-evict each sequence's initial history (shared prefix pages
+        once, by the first sharer) in chunks."""
+        torch = self.torch
+        seqs, poss = [], []
+        for b in range(self.B):
+            start = 0
+            if grp is not None and grp[b] >= 0 and b != int(np.argmax(grp == grp[b])):
+                start = self.w.shared_hist_tokens
+            n = int(hist0[b]) - start
+            if n > 0:
+                seqs.append(np.full(n, b, np.int32))
+                poss.append(np.arange(start, start + n, dtype=np.int32))
+        if not seqs:
+            return
+        seq = np.concatenate(seqs)
+        pos = np.concatenate(poss)
+        chunk = 1 << 19
+        for i in range(0, seq.size, chunk):
+            n = min(chunk, seq.size - i)
+            toks = S.kv_tokens_torch(self.w, n, gen, prof, self.dev).contiguous()
+            self.O.oscar_evict_quantize(self.shape, toks, torch.from_numpy(seq[i:i + n]).to(self.dev),
+                                        torch.from_numpy(pos[i:i + n]).to(self.dev), U, clip, pool, self.table,
+                                        self.B, self.max_pages, self.num_pages)
+
+    def layer_step(self, layer: int, s: int, int2_events=None):
+        O = self.O
+        st = self.layers[layer]
+        O.oscar_evict_quantize(self.shape, st["kv"].view(self.B * S.NSLOT, self.Hk, 2, S.D), self.seqs,
+                               self.hist_before[s], st["U"], st["clip"], st["pool"], self.table, self.B,
+                               self.max_pages, self.num_pages, src_row=self.src_row[s], new_kv=st["new_kv"])
+        if int2_events is not None:
+            O.oscar_time_next_int2(*int2_events)
+        O.oscar_decode_attn(self.shape, st["q"], st["kv"], self.bf16_len, st["pool"], self.table, self.max_pages,
+                            self.num_pages, self.hist_after[s], st["U"], self.sm_scale, st["out"], self.ws)
+
+    # algorithmic bytes (per layer) of the step with index s
+    def hist_tokens_after(self, s: int) -> int:
+        return int((self.hist0 + s + 1).sum())
+
+    def attended_tokens(self, s: int) -> int:
+        return self.hist_tokens_after(s) + self.B * S.NSLOT
+
+    def step_bytes(self, s: int) -> float:
+        hist = self.hist_tokens_after(s) * self.Hk * HIST_BYTES_PER_TOKEN_HEAD
+        bf16 = self.B * S.NSLOT * self.Hk * BF16_BYTES_PER_TOKEN_HEAD
+        qo = self.B * self.Hq * S.D * (2 + 4)
+        evict = self.B * self.Hk * 2 * (S.D * 2 * 2 + 48)    # read old + write new row, write codes + s/z
+        return float(hist + bf16 + qo + evict)
+
+
+# ---------------------------------------------------------------------------
+# oracle (float64 CPU) on a bounded sample of the workload
+# ---------------------------------------------------------------------------
+
+class OracleSample:
+    """The first sequences of layer 0 whose history totals about
+    ``budget`` tokens, with their history written by the oracle's own
+    eviction; one timed step = evict one token per sampled sequence + decode
+    all their heads."""
+
+    def __init__(self, w: S.Workload, budget: int):
+        import oracle
+        self.orc = oracle.get()
+        ctx = S.context_lengths(w)
+        hist = np.maximum(ctx - S.NSLOT, 0)
+        n = 1
+        while n < w.batch and hist[:n].sum() < budget:
+            n += 1
+        self.n = n
+        self.ctx = ctx[:n]
+        self.hist = hist[:n].astype(np.int32)
+        self.shape = oracle.Shape(S.D, S.GROUP, S.SINK, S.RECENT, S.PAGE, w.hq, w.hk)
+        rng = S.rng_for(w, 11)
+        prof = S.channel_profile(w)
+        cap = self.hist + 64
+        self.max_pages = int((cap.max() + 63) // 64)
+        rc, self.table, npages, nbytes = self.orc.pool_layout(self.shape, cap, max_pages=self.max_pages)
+        self.pool = np.zeros(nbytes, np.uint8)
+        self.U = S.rotation_U(w).astype(np.float32).astype(np.float64)
+        self.clip = S.clip_ratios(w)
+        for b in range(n):
+            h = int(self.hist[b])
+            toks = S.kv_tokens(w, h, rng, prof)
+            self.orc.evict(self.shape, toks, np.full(h, b, np.int32), np.arange(h, dtype=np.int32), self.U,
+                           self.clip, self.pool, self.table, self.max_pages)
+        self.kv = S.kv_tokens(w, n * S.NSLOT, rng, prof).reshape(n, S.NSLOT, w.hk, 2, S.D)
+        self.new = S.kv_tokens(w, n, rng, prof)
+        self.q = S.queries(w, rng, n)
+        self.bf16_len = np.full(n, S.NSLOT, np.int32)
+        self.threads = self.orc.num_threads()
+
+    def step(self):
+        rows = (np.arange(self.n) * S.NSLOT + S.SINK).astype(np.int32)
+        flat = self.kv.reshape(self.n * S.NSLOT, -1, 2, S.D)
+        pool = self.pool.copy()   # keep the sample's state fixed across steps
+        self.orc.evict(self.shape, flat, np.arange(self.n, dtype=np.int32), self.hist, self.U, self.clip, pool,
+                       self.table, self.max_pages, src_row=rows)
+        self.orc.decode(self.shape, self.q, self.kv, self.bf16_len, pool, self.table, self.max_pages,
+                        self.hist + 1, self.U, 1.0 / math.sqrt(S.D))
+        return int((self.hist + 1).sum() + self.n * S.NSLOT)
+
+    def time(self, steps: int, warmup: int = 0):
+        for _ in range(warmup):
+            self.step()
+        t0 = time.perf_counter()
+        toks = 0
+        for _ in range(steps):
+            toks += self.step()
+        dt = time.perf_counter() - t0
+        return toks / dt, dt
+
+    def describe(self) -> str:
+        return (f"layer 0 of the workload: sequences 0..{self.n - 1} (history {int(self.hist.sum())} tokens, "
+                f"{self.shape.num_q_heads} query / {self.shape.num_kv_heads} KV heads), one eviction per "
+                f"sequence + decode of all heads per step, float64")
+
+
+def cpu_info() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part", "processor\t: 0")) and ":" in line:
+                    if "model name" in line.lower():
+                        return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+
+def run_reference(args, rank: int, world: int) -> None:
+    if rank != 0:
+        return
+    w = S.WORKLOADS[args.workload]
+    samp = OracleSample(w, args.cpu_tokens)
+    tps, dt = samp.time(args.steps, args.warmup)
+    ms = dt / args.steps * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tps, "unit": UNIT, "n_gpus": 0, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w, args.layers or w.layers),
+        "cpu_baseline": {"value": tps, "unit": UNIT, "cores": samp.threads, "kind": "oracle",
+                         "sample": samp.describe(), "cpu": cpu_info()},
+        "e2e": {"value": tps, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w: S.Workload, layers: int) -> dict:
+    ctx = {"fixed": f"{w.ctx_lo}", "uniform": f"uniform[{w.ctx_lo},{w.ctx_hi}]",
+           "loguniform": f"loguniform[{w.ctx_lo},{w.ctx_hi}]"}[w.ctx_kind]
+    cfg = {"workload": w.name, "batch_per_gpu": w.batch, "layers": layers, "q_heads": w.hq, "kv_heads": w.hk,
+           "head_dim": S.D, "context": ctx, "sink": S.SINK, "recent": S.RECENT, "quant_group": S.GROUP,
+           "page": S.PAGE, "page_table": "shuffled" if w.shuffled else "contiguous",
+           "kv_values": w.dist, "l2": "inputs larger than L2 (a distinct pool per layer)",
+           "parallelism": "replicas (independent sequences per GPU)"}
+    if w.prefix_seqs:
+        cfg["prefix_sharing"] = f"{w.prefix_seqs} sequences share a {w.prefix_tokens}-token prefix"
+    return cfg
+
+
+def run_oscar(args, rank: int, world: int, local: int) -> None:
+    import torch
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    from bit_kv_cache_evict_gb300 import build as Bld
+    Bld.build()
+    w = S.WORKLOADS[args.workload]
+    L = args.layers or w.layers
+    K, W = args.steps, args.warmup
+    e2e_steps = 0 if args.no_e2e else K
+    total_steps = W + K + e2e_steps
+    t0 = time.time()
+    st = GpuState(w, L, total_steps, rank)
+    setup_s = time.time() - t0
+    stream = torch.cuda.current_stream()
+
+    for s in range(W):
+        for layer in range(L):
+            st.layer_step(layer, s)
+    torch.cuda.synchronize()
+    barrier(world)
+
+    # int2-kernel events: one pair per launch in the timed region
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K * L)]
+    for a, b in evs:   # materialise the events
+        a.record(stream)
+        b.record(stream)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for k in range(K):
+        s = W + k
+        for layer in range(L):
+            st.layer_step(layer, s, evs[k * L + layer])
+    stop.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(world)
+    t_ms = start.elapsed_time(stop)
+    int2_ms = [a.elapsed_time(b) for a, b in evs]
+
+    t_ms_max = reduce_max(t_ms, world, dev)
+    ms_per_step = t_ms_max / K
+    att = sum(st.attended_tokens(W + k) for k in range(K)) * L
+    att_all = reduce_sum(float(att), world, dev)
+    value = att_all / (t_ms_max / 1e3)
+    step_bytes = sum(st.step_bytes(W + k) for k in range(K)) * L / K
+    hist_bytes = [st.hist_tokens_after(W + k) * st.Hk * HIST_BYTES_PER_TOKEN_HEAD for k in range(K)]
+    int2_avg_ms = statistics.mean(int2_ms)
+    int2_bytes = statistics.mean(hist_bytes)
+    peaks = load_peaks()
+    achieved = int2_bytes / (int2_avg_ms * 1e-3) / 1e9
+
+    # end to end through the C ABI from pinned host buffers: per layer, copy
+    # the step's query and new token in, run the step, copy the output out
+    e2e = None
+    if e2e_steps:
+        hq = [torch.empty_like(l["q"], device="cpu").pin_memory() for l in st.layers]
+        hn = [torch.empty_like(l["new_kv"], device="cpu").pin_memory() for l in st.layers]
+        ho = [torch.empty_like(l["out"], device="cpu").pin_memory() for l in st.layers]
+        for layer in range(L):
+            hq[layer].copy_(st.layers[layer]["q"])
+            hn[layer].copy_(st.layers[layer]["new_kv"])
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for k in range(e2e_steps):
+            s = W + K + k
+            for layer in range(L):
+                lay = st.layers[layer]
+                lay["q"].copy_(hq[layer], non_blocking=True)
+                lay["new_kv"].copy_(hn[layer], non_blocking=True)
+                st.layer_step(layer, s)
+                ho[layer].copy_(lay["out"], non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = reduce_max(e0.elapsed_time(e1), world, dev)
+        e_att = reduce_sum(float(sum(st.attended_tokens(W + K + k) for k in range(e2e_steps)) * L), world, dev)
+        h2d = L * (st.layers[0]["q"].numel() * 2 + st.layers[0]["new_kv"].numel() * 2)
+        d2h = L * st.layers[0]["out"].numel() * 4
+        e2e = {"value": e_att / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e_ms / e2e_steps}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        samp = OracleSample(w, args.cpu_tokens)
+        tps, dt = samp.time(1, 0)
+        cpu = {"value": tps, "unit": UNIT, "cores": samp.threads, "kind": "oracle", "sample": samp.describe(),
+               "seconds": dt, "cpu": cpu_info()}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+            "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "int2 codes x bf16 hi/lo on tensor cores, fp32 accumulate", "data": "synthetic",
+            "config": config_of(w, L),
+            "decode_tokens_per_s": world * w.batch * K / (t_ms_max / 1e3),
+            "step_algorithmic_gbs": step_bytes / (ms_per_step * 1e-3) / 1e9,
+            "roofline": {"kernel": "int2_kernel (split-K INT2 history attention)", "bound": "hbm",
+                         "achieved": achieved, "peak": peaks["hbm_gbs"], "peak_source": peaks["source"],
+                         "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                         "bytes_per_launch": int2_bytes, "launch_ms": int2_avg_ms,
+                         "share_of_step": sum(int2_ms) / t_ms},
+            "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": K * L * 5,
+            "clocks": clk, "setup_s": setup_s,
+        }
+        print(json.dumps(line), flush=True)
+    barrier(world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_info()
+    if args.gpus != world and world > 1:
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    run_oscar(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

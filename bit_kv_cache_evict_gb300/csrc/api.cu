@@ -13,6 +13,7 @@ namespace oscar {
 constexpr int kPagesPerSplit = 8;  // history pages per split-K work item
 
 static thread_local int g_last_cuda_error = 0;
+static thread_local cudaEvent_t g_int2_ev_start = nullptr, g_int2_ev_stop = nullptr;
 
 static oscar_status cuda_fail(cudaError_t e) {
     g_last_cuda_error = (int)e;
@@ -101,6 +102,11 @@ const char* oscar_status_string(oscar_status st) {
 }
 
 int oscar_last_cuda_error(void) { return g_last_cuda_error; }
+
+void oscar_time_next_int2(void* ev_start, void* ev_stop) {
+    g_int2_ev_start = static_cast<cudaEvent_t>(ev_start);
+    g_int2_ev_stop = static_cast<cudaEvent_t>(ev_stop);
+}
 
 oscar_status oscar_pool_layout(const oscar_shape* shape, int32_t batch, const int32_t* hist_capacity,
                                const int32_t* prefix_group, int32_t shared_hist_tokens, uint64_t perm_seed,
@@ -250,7 +256,10 @@ oscar_status oscar_decode_attn(const oscar_shape* shape, int32_t batch, const vo
     p.pps = w.pps;
     p.part_stride = w.part_stride;
     p.qscale = sm_scale * kLog2e;
-    const cudaError_t e = launch_decode(p, static_cast<cudaStream_t>(stream));
+    cudaEvent_t ev0 = g_int2_ev_start, ev1 = g_int2_ev_stop;
+    g_int2_ev_start = g_int2_ev_stop = nullptr;
+    if (!ev0 || !ev1) ev0 = ev1 = nullptr;
+    const cudaError_t e = launch_decode(p, static_cast<cudaStream_t>(stream), ev0, ev1);
     return e == cudaSuccess ? OSCAR_OK : cuda_fail(e);
 }
 

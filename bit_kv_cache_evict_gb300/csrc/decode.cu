@@ -720,7 +720,8 @@ static cudaError_t launch_int2(const DecodeParams& p, cudaStream_t st, int sms, 
     return cudaGetLastError();
 }
 
-cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st) {
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st, cudaEvent_t ev_int2_start,
+                          cudaEvent_t ev_int2_stop) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -732,8 +733,10 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st) {
     const int prep_warps = p.B * p.hk * p.NT * 4;
     prep_kernel<<<(prep_warps + 3) / 4 + 1, 128, 0, st>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (ev_int2_start && (e = cudaEventRecord(ev_int2_start, st)) != cudaSuccess) return e;
     e = (p.NT == 1) ? launch_int2<1>(p, st, at.sms, at.set1) : launch_int2<2>(p, st, at.sms, at.set2);
     if (e != cudaSuccess) return e;
+    if (ev_int2_stop && (e = cudaEventRecord(ev_int2_stop, st)) != cudaSuccess) return e;
     bf16_kernel<<<p.B * p.hk, 128, 0, st>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (!at.setm) {

@@ -181,6 +181,7 @@ struct DecodeParams {
 };
 
 cudaError_t launch_evict(const EvictParams& p, cudaStream_t st);
-cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st);
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st, cudaEvent_t ev_int2_start,
+                          cudaEvent_t ev_int2_stop);
 
 }  // namespace oscar

@@ -65,6 +65,8 @@ def lib() -> ctypes.CDLL:
         L.oscar_decode_attn.restype = ctypes.c_int
         L.oscar_decode_attn.argtypes = [S, ctypes.c_int32, _P, _P, _P, _P, _P, ctypes.c_int32, ctypes.c_int32, _P,
                                         _P, ctypes.c_float, _P, _P, ctypes.POINTER(ctypes.c_size_t), _P, _P]
+        L.oscar_time_next_int2.restype = None
+        L.oscar_time_next_int2.argtypes = [_P, _P]
         _LIB = L
     return _LIB
 
@@ -143,6 +145,13 @@ def oscar_evict_quantize(shape: oscar_shape, src_kv, dst_seq, dst_pos, U, clip, 
         _dptr(page_table, "page_table", torch.int32), batch, max_pages, num_pages,
         _dptr(dev_status, "dev_status", torch.int32), _stream_ptr(stream))
     _check("oscar_evict_quantize", st)
+
+
+def oscar_time_next_int2(ev_start, ev_stop) -> None:
+    """Measurement hook: the next oscar_decode_attn on this thread records the
+    two (already recorded once, timing-enabled) torch.cuda.Event objects
+    around its INT2 split-K kernel."""
+    lib().oscar_time_next_int2(ctypes.c_void_p(ev_start.cuda_event), ctypes.c_void_p(ev_stop.cuda_event))
 
 
 def oscar_decode_workspace_bytes(shape: oscar_shape, batch: int, max_pages: int) -> int:

@@ -202,6 +202,17 @@ oscar_status oscar_decode_attn(const oscar_shape* shape, int32_t batch, const vo
                                float sm_scale, float* out, void* workspace, size_t* ws_bytes,
                                int32_t* dev_status, void* stream);
 
+/*
+ * oscar_time_next_int2 -- measurement hook (no counterpart on the pages).
+ * When ev_start and ev_stop are both non-NULL cudaEvent_t handles (passed as
+ * void*), the next oscar_decode_attn call made by this host thread records
+ * ev_start on its stream immediately before launching the INT2 split-K
+ * kernel and ev_stop immediately after it; the hook then clears itself.
+ * A benchmark uses it to time that kernel alone with CUDA events; it adds
+ * two event records to the stream and changes nothing else.
+ */
+void oscar_time_next_int2(void* ev_start, void* ev_stop);
+
 #ifdef __cplusplus
 }
 #endif

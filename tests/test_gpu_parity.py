@@ -147,8 +147,9 @@ def test_bad_indices_are_skipped_and_reported(orc):
     table = H.i32_t(np.array([[0, 5]], np.int32))            # page 5 does not exist (num_pages = 1)
     pool = torch.zeros(6144, dtype=torch.uint8, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    O.oscar_evict_quantize(sh, toks, H.i32_t([0, 1, 0, 0]), H.i32_t([3, 3, 200, 70]), U, clip, pool, table,
-                           batch=1, max_pages=2, num_pages=1, src_row=H.i32_t([0, 1, 2, 9]), dev_status=status)
+    # tokens: ok | bad sequence | bad position | page id 5 >= num_pages | bad source row
+    O.oscar_evict_quantize(sh, toks, H.i32_t([0, 1, 0, 0, 0]), H.i32_t([3, 3, 200, 70, 4]), U, clip, pool, table,
+                           batch=1, max_pages=2, num_pages=1, src_row=H.i32_t([0, 1, 2, 3, 9]), dev_status=status)
     torch.cuda.synchronize()
     st = int(status.item())
     assert st & O.OSCAR_STATUS_BAD_POS and st & O.OSCAR_STATUS_BAD_PAGE
