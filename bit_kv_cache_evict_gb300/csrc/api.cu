@@ -15,6 +15,8 @@ constexpr int kPagesPerSplit = 8;  // history pages per split-K work item
 static thread_local int g_last_cuda_error = 0;
 static thread_local cudaEvent_t g_int2_ev_start = nullptr, g_int2_ev_stop = nullptr;
 
+void set_last_cuda_error(int e) { g_last_cuda_error = e; }
+
 static oscar_status cuda_fail(cudaError_t e) {
     g_last_cuda_error = (int)e;
     return OSCAR_ERR_CUDA;

@@ -65,6 +65,9 @@ def lib() -> ctypes.CDLL:
         L.oscar_decode_attn.restype = ctypes.c_int
         L.oscar_decode_attn.argtypes = [S, ctypes.c_int32, _P, _P, _P, _P, _P, ctypes.c_int32, ctypes.c_int32, _P,
                                         _P, ctypes.c_float, _P, _P, ctypes.POINTER(ctypes.c_size_t), _P, _P]
+        L.oscar_decode_attn_noalloc.restype = ctypes.c_int
+        L.oscar_decode_attn_noalloc.argtypes = [S, ctypes.c_int32, _P, _P, _P, _P, _P, ctypes.c_int32,
+                                                ctypes.c_int32, _P, _P, ctypes.c_float, _P, _P, _P]
         L.oscar_time_next_int2.restype = None
         L.oscar_time_next_int2.argtypes = [_P, _P]
         _LIB = L
@@ -178,3 +181,23 @@ def oscar_decode_attn(shape: oscar_shape, q, bf16_kv, bf16_len, pool, page_table
         _dptr(workspace, "workspace", torch.uint8), ctypes.byref(ws), _dptr(dev_status, "dev_status", torch.int32),
         _stream_ptr(stream))
     _check("oscar_decode_attn", st)
+
+
+NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def oscar_decode_attn_noalloc(shape: oscar_shape, q, bf16_kv, bf16_len, pool, page_table, max_pages: int,
+                              num_pages: int, hist_len, U, sm_scale: float, out, dev_status=None,
+                              stream=None) -> None:
+    """oscar_decode_attn for callers that cannot allocate device memory: the
+    scratch is the library's fixed 64 MiB device array (see include/oscar.h
+    for the limits, the first-call set-up and why overlapping calls race)."""
+    import torch
+    B = int(q.shape[0])
+    st = lib().oscar_decode_attn_noalloc(
+        ctypes.byref(shape), B, _dptr(q, "q", torch.bfloat16), _dptr(bf16_kv, "bf16_kv", torch.bfloat16),
+        _dptr(bf16_len, "bf16_len", torch.int32), _dptr(pool, "pool", torch.uint8),
+        _dptr(page_table, "page_table", torch.int32), max_pages, num_pages, _dptr(hist_len, "hist_len", torch.int32),
+        _dptr(U, "U", torch.float32), ctypes.c_float(sm_scale), _dptr(out, "out", torch.float32),
+        _dptr(dev_status, "dev_status", torch.int32), _stream_ptr(stream))
+    _check("oscar_decode_attn_noalloc", st)

@@ -213,6 +213,37 @@ oscar_status oscar_decode_attn(const oscar_shape* shape, int32_t batch, const vo
  */
 void oscar_time_next_int2(void* ev_start, void* ev_stop);
 
+/* Size of the fixed device scratch array used by oscar_decode_attn_noalloc. */
+#define OSCAR_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20) /* 64 MiB */
+
+/*
+ * oscar_decode_attn_noalloc -- oscar_decode_attn without a caller workspace.
+ * The pages have no counterpart for this call: it exists for callers that
+ * cannot allocate device memory (for instance code running inside a runtime
+ * that owns all device memory and hands none out, or a plugin that may only
+ * touch the buffers it is given).  Arguments and results are those of
+ * oscar_decode_attn minus workspace/ws_bytes; the caller still owns every
+ * input and output.  The scratch lives in a fixed 64 MiB array
+ * (OSCAR_NOALLOC_SCRATCH_BYTES) in the library's device code, held by every
+ * GPU that loads that code until the process exits; the call itself
+ * allocates nothing.
+ *   - A request needing more scratch than that (large batch x max_pages)
+ *     returns OSCAR_ERR_WORKSPACE before any launch; use oscar_decode_attn
+ *     with a workspace instead.  oscar_decode_attn with workspace == NULL
+ *     reports the size a request needs.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents;
+ *     each call rebuilds what it reads, but calls that may overlap on the GPU
+ *     (different streams, or different host threads) race on it: order them.
+ */
+oscar_status oscar_decode_attn_noalloc(const oscar_shape* shape, int32_t batch, const void* q, const void* bf16_kv,
+                                       const int32_t* bf16_len, const uint8_t* pool, const int32_t* page_table,
+                                       int32_t max_pages, int32_t num_pages, const int32_t* hist_len,
+                                       const float* U, float sm_scale, float* out, int32_t* dev_status,
+                                       void* stream);
+
 #ifdef __cplusplus
 }
 #endif
