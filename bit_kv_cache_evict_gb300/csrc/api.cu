@@ -10,7 +10,15 @@ namespace oscar {
 
 
 
-constexpr int kPagesPerSplit = 8;  // history pages per split-K work item
+// History pages per split-K work item: about 8192 items for the largest
+// request the table allows, between 4 and 64 pages.
+static int pages_per_split(int batch, int hk, int max_pages) {
+    const int64_t cap = (int64_t)batch * hk * max_pages;
+    int64_t pps = (cap + 8191) / 8192;
+    if (pps < 4) pps = 4;
+    if (pps > 64) pps = 64;
+    return (int)pps;
+}
 
 static thread_local int g_last_cuda_error = 0;
 static thread_local cudaEvent_t g_int2_ev_start = nullptr, g_int2_ev_stop = nullptr;
@@ -37,7 +45,7 @@ static oscar_status check_shape(const oscar_shape* s) {
     const int G = s->num_q_heads / s->num_kv_heads;
     if (s->head_dim != kD || s->quant_group != kGroup || s->page_size != kPage) return OSCAR_ERR_UNSUPPORTED;
     if (G != 1 && G != 2 && G != 4 && G != 8) return OSCAR_ERR_UNSUPPORTED;
-    if (s->sink + s->recent > 4096) return OSCAR_ERR_UNSUPPORTED;
+    if (s->sink + s->recent > 320) return OSCAR_ERR_UNSUPPORTED;
     return OSCAR_OK;
 }
 
@@ -50,7 +58,7 @@ static WsLayout ws_layout(const oscar_shape* s, int batch, int max_pages) {
     WsLayout w{};
     const int G = s->num_q_heads / s->num_kv_heads, hk = s->num_kv_heads;
     w.NT = (G + 3) / 4;
-    w.pps = kPagesPerSplit;
+    w.pps = pages_per_split(batch, hk, max_pages);
     w.part_stride = (int)round_up((size_t)G * (kD + 2), 4);
     w.max_items = batch * hk * ((max_pages + w.pps - 1) / w.pps);
     size_t off = 0;
@@ -226,7 +234,7 @@ oscar_status oscar_decode_attn(const oscar_shape* shape, int32_t batch, const vo
     if (batch == 0) return OSCAR_OK;
     if (!q || !bf16_kv || !bf16_len || !hist_len || !U || !out || !page_table) return OSCAR_ERR_INVALID_ARG;
     if (num_pages > 0 && !pool) return OSCAR_ERR_INVALID_ARG;
-    if (!aligned(q, 8) || !aligned(bf16_kv, 8) || !aligned(U, 16) || !aligned(pool, 16) || !aligned(out, 16) ||
+    if (!aligned(q, 8) || !aligned(bf16_kv, 16) || !aligned(U, 16) || !aligned(pool, 16) || !aligned(out, 16) ||
         !aligned(workspace, 16) || !aligned(dev_status, 4))
         return OSCAR_ERR_INVALID_ARG;
     if (!(sm_scale == sm_scale) || (double)w.max_items * w.part_stride > 4.0e9) return OSCAR_ERR_INVALID_ARG;
@@ -258,6 +266,10 @@ oscar_status oscar_decode_attn(const oscar_shape* shape, int32_t batch, const vo
     p.pps = w.pps;
     p.part_stride = w.part_stride;
     p.qscale = sm_scale * kLog2e;
+    for (int i = 0; i < 8; ++i) {
+        const int P = 2 * i;
+        p.code_mul[i] = P < 4 ? (1u << (4 - P)) : (P > 4 ? (1u << (36 - P)) : 1u);
+    }
     cudaEvent_t ev0 = g_int2_ev_start, ev1 = g_int2_ev_stop;
     g_int2_ev_start = g_int2_ev_stop = nullptr;
     if (!ev0 || !ev1) ev0 = ev1 = nullptr;

@@ -37,14 +37,22 @@ namespace oscar {
 // ---------------------------------------------------------------------------
 // prep: rotated query fragments + split-K plan
 // ---------------------------------------------------------------------------
-// One warp per (b, kv, nt, hh): head h = kv*G + 4*nt + hh (hh >= G: zero
-// padding columns).  The last block builds the plan.
-__global__ void __launch_bounds__(128) prep_kernel(DecodeParams p) {
-    __shared__ float qs[4][kD];
+// Block (kv, chunk of kPrepSeqs sequences): U_K of that KV head is staged in
+// shared memory once; warp w then handles (b, nt, hh) units: head
+// h = kv*G + 4*nt + hh (hh >= G: zero padding columns).  Block (last x,
+// y = 0) builds the plan.
+constexpr int kPrepSeqs = 2;
+constexpr int kPrepThreads = 256;
+constexpr int kPrepSmem = kD * kD * 4 + (kPrepThreads / 32) * kD * 4;
+
+__global__ void __launch_bounds__(kPrepThreads) prep_kernel(DecodeParams p) {
+    extern __shared__ __align__(16) float psm[];
+    float* Us = psm;                       // [a][k] = U_K[a][k]
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float* qs = psm + kD * kD + warp * kD;
 
     if (blockIdx.x == gridDim.x - 1) {  // plan
-        if (warp != 0) return;
+        if (blockIdx.y != 0 || warp != 0) return;
         int running = 0;
         if (lane == 0) {
             p.item_start[0] = 0;
@@ -74,99 +82,134 @@ __global__ void __launch_bounds__(128) prep_kernel(DecodeParams p) {
         return;
     }
 
-    const int wid = blockIdx.x * 4 + warp;  // = ((b*Hk + kv)*NT + nt)*4 + hh
-    if (wid >= p.B * p.hk * p.NT * 4) return;
-    const int hh = wid & 3;
-    const int nt = (wid >> 2) % p.NT;
-    const int bk = (wid >> 2) / p.NT;
-    const int b = bk / p.hk, kv = bk % p.hk;
-    const int hl = 4 * nt + hh;  // head within the KV group
-    uint32_t* frag = p.qfrag + ((size_t)bk * p.NT + nt) * 8 * 32 * 2;
-    float* qsum = p.qsum + ((size_t)bk * p.NT * 4 + hl) * 4;
+    const int kv = blockIdx.y;
+    const int b0 = blockIdx.x * kPrepSeqs;
+    const int nseq = min(kPrepSeqs, p.B - b0);
+    {
+        const float4* src = reinterpret_cast<const float4*>(p.U + ((size_t)kv * 2 + 0) * kD * kD);
+        float4* dst = reinterpret_cast<float4*>(Us);
+        for (int i = threadIdx.x; i < kD * kD / 4; i += kPrepThreads) dst[i] = __ldg(src + i);
+    }
+    __syncthreads();
 
-    if (hl >= p.G) {  // padding column pair: zeros
+    const int units = nseq * p.NT * 4;
+    for (int u = warp; u < units; u += kPrepThreads / 32) {
+        const int hh = u & 3;
+        const int nt = (u >> 2) % p.NT;
+        const int b = b0 + (u >> 2) / p.NT;
+        const int bk = b * p.hk + kv;
+        const int hl = 4 * nt + hh;  // head within the KV group
+        uint32_t* frag = p.qfrag + ((size_t)bk * p.NT + nt) * 8 * 32 * 2;
+        float* qsum = p.qsum + ((size_t)bk * p.NT * 4 + hl) * 4;
         const int ks = lane >> 2, tq = lane & 3;
+        if (hl >= p.G) {  // padding column pair: zeros
 #pragma unroll
-        for (int par = 0; par < 2; ++par) {
-            const int L = (2 * hh + par) * 4 + tq;
-            *reinterpret_cast<uint2*>(frag + ((size_t)ks * 32 + L) * 2) = make_uint2(0u, 0u);
+            for (int par = 0; par < 2; ++par) {
+                const int L = (2 * hh + par) * 4 + tq;
+                *reinterpret_cast<uint2*>(frag + ((size_t)ks * 32 + L) * 2) = make_uint2(0u, 0u);
+            }
+            if (lane < 4) qsum[lane] = 0.f;
+            continue;
         }
-        if (lane < 4) qsum[lane] = 0.f;
-        return;
-    }
-    const int h = kv * p.G + hl;
-    const uint2 qr = *reinterpret_cast<const uint2*>(p.q + ((size_t)b * p.hq + h) * kD + 4 * lane);
-    const float x[4] = {bf16_lo(qr.x), bf16_hi(qr.x), bf16_lo(qr.y), bf16_hi(qr.y)};
-    const float* Uk = p.U + ((size_t)kv * 2 + 0) * kD * kD;
-    float y[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-    for (int a = 0; a < kD; ++a) {
-        const float xa = __shfl_sync(kFull, x[a & 3], a >> 2);
-        const float4 u = __ldg(reinterpret_cast<const float4*>(Uk + (size_t)a * kD + 4 * lane));
-        y[0] = fmaf(xa, u.x, y[0]);
-        y[1] = fmaf(xa, u.y, y[1]);
-        y[2] = fmaf(xa, u.z, y[2]);
-        y[3] = fmaf(xa, u.w, y[3]);
-    }
-    {  // Hadamard, in-lane stages
-        const float t0 = y[0] + y[1], t1 = y[0] - y[1], t2 = y[2] + y[3], t3 = y[2] - y[3];
-        y[0] = t0 + t2;
-        y[2] = t0 - t2;
-        y[1] = t1 + t3;
-        y[3] = t1 - t3;
-    }
+        const int h = kv * p.G + hl;
+        const uint2 qr = *reinterpret_cast<const uint2*>(p.q + ((size_t)b * p.hq + h) * kD + 4 * lane);
+        const float x[4] = {bf16_lo(qr.x), bf16_hi(qr.x), bf16_lo(qr.y), bf16_hi(qr.y)};
+        float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+        for (int a4 = 0; a4 < kD; a4 += 4) {
 #pragma unroll
-    for (int m = 1; m < 32; m <<= 1) {
-        const bool upper = (lane & m) != 0;
+            for (int i = 0; i < 4; ++i) {
+                const float xa = __shfl_sync(kFull, x[i], a4 >> 2);
+                const float4 uu = *reinterpret_cast<const float4*>(Us + (size_t)(a4 + i) * kD + 4 * lane);
+                y[0] = fmaf(xa, uu.x, y[0]);
+                y[1] = fmaf(xa, uu.y, y[1]);
+                y[2] = fmaf(xa, uu.z, y[2]);
+                y[3] = fmaf(xa, uu.w, y[3]);
+            }
+        }
+        {  // Hadamard, in-lane stages
+            const float t0 = y[0] + y[1], t1 = y[0] - y[1], t2 = y[2] + y[3], t3 = y[2] - y[3];
+            y[0] = t0 + t2;
+            y[2] = t0 - t2;
+            y[1] = t1 + t3;
+            y[3] = t1 - t3;
+        }
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1) {
+            const bool upper = (lane & m) != 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float o = __shfl_xor_sync(kFull, y[k], m);
+                y[k] = upper ? o - y[k] : y[k] + o;
+            }
+        }
+        const float scale = (float)kInvSqrtD * p.qscale;
+        const int r5 = bitrev5(lane);
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) qs[32 * bitrev2(k) + r5] = y[k] * scale;  // stored order
+        __syncwarp();
+
+        // group sums of the split values (exactly what the MMA multiplies)
+        float gs = 0.f;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const float o = __shfl_xor_sync(kFull, y[k], m);
-            y[k] = upper ? o - y[k] : y[k] + o;
+            const float v = qs[4 * lane + k];
+            const float hi = __bfloat162float(__float2bfloat16_rn(v));
+            const float lo = __bfloat162float(__float2bfloat16_rn(v - hi));
+            gs += hi + lo;
         }
-    }
-    const float scale = (float)kInvSqrtD * p.qscale;
-    const int r5 = bitrev5(lane);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) qs[warp][32 * bitrev2(k) + r5] = y[k] * scale;  // stored order
-    __syncwarp();
+        for (int m = 1; m < 8; m <<= 1) gs += __shfl_xor_sync(kFull, gs, m);
+        if ((lane & 7) == 0) qsum[lane >> 3] = gs;
 
-    // group sums of the split values (exactly what the MMA multiplies)
-    float gs = 0.f;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const float v = qs[warp][4 * lane + k];
-        const float hi = __bfloat162float(__float2bfloat16_rn(v));
-        const float lo = __bfloat162float(__float2bfloat16_rn(v - hi));
-        gs += hi + lo;
+        // fragments: lane -> (ks, tq), k-step ks = (group g = ks/2, half h = ks%2)
+        // covers in-group indices 8tq + 4h + {0,2} (b0) and + {1,3} (b1), the
+        // four codes of bytes 4(2tq+h)..4(2tq+h)+3 of group g's slot; column
+        // 2hh = hi, 2hh+1 = lo
+        const int base = 32 * (ks >> 1) + 8 * tq + 4 * (ks & 1);
+        const float v0 = qs[base], v1 = qs[base + 2];
+        const float v2 = qs[base + 1], v3 = qs[base + 3];
+        const uint32_t h01 = pack_bf16x2_rn(v0, v1), h23 = pack_bf16x2_rn(v2, v3);
+        const uint32_t l01 = pack_bf16x2_rn(v0 - bf16_lo(h01), v1 - bf16_hi(h01));
+        const uint32_t l23 = pack_bf16x2_rn(v2 - bf16_lo(h23), v3 - bf16_hi(h23));
+        *reinterpret_cast<uint2*>(frag + ((size_t)ks * 32 + (2 * hh) * 4 + tq) * 2) = make_uint2(h01, h23);
+        *reinterpret_cast<uint2*>(frag + ((size_t)ks * 32 + (2 * hh + 1) * 4 + tq) * 2) = make_uint2(l01, l23);
     }
-#pragma unroll
-    for (int m = 1; m < 8; m <<= 1) gs += __shfl_xor_sync(kFull, gs, m);
-    if ((lane & 7) == 0) qsum[lane >> 3] = gs;
-
-    // fragments: lane -> (ks, tq); b0 = (q'[16ks+tq], q'[16ks+8+tq]),
-    // b1 = (q'[16ks+4+tq], q'[16ks+12+tq]); column 2hh = hi, 2hh+1 = lo
-    const int ks = lane >> 2, tq = lane & 3;
-    const float v0 = qs[warp][16 * ks + tq], v1 = qs[warp][16 * ks + 8 + tq];
-    const float v2 = qs[warp][16 * ks + 4 + tq], v3 = qs[warp][16 * ks + 12 + tq];
-    const uint32_t h01 = pack_bf16x2_rn(v0, v1), h23 = pack_bf16x2_rn(v2, v3);
-    const uint32_t l01 = pack_bf16x2_rn(v0 - bf16_lo(h01), v1 - bf16_hi(h01));
-    const uint32_t l23 = pack_bf16x2_rn(v2 - bf16_lo(h23), v3 - bf16_hi(h23));
-    *reinterpret_cast<uint2*>(frag + ((size_t)ks * 32 + (2 * hh) * 4 + tq) * 2) = make_uint2(h01, h23);
-    *reinterpret_cast<uint2*>(frag + ((size_t)ks * 32 + (2 * hh + 1) * 4 + tq) * 2) = make_uint2(l01, l23);
 }
 
 // ---------------------------------------------------------------------------
 // INT2 split-K decode
 // ---------------------------------------------------------------------------
-constexpr int kStages = 3;
+// Block = 4 consumer warps + 1 producer warp.  The producer takes split-K
+// items from a global counter and streams their 6 KB page blocks into a
+// ring of shared-memory stages with bulk async copies (one copy per page,
+// completion on a "full" mbarrier); consumer warp w attends over the 16
+// tokens [16w, 16w+16) of every page, and releases the stage on an "empty"
+// mbarrier.  At the last page of an item the four warps merge their
+// partial softmax states in shared memory and write one partial per item.
+// Every wait is bounded; on a timeout the block reports
+// OSCAR_STATUS_TIMEOUT, lets its copies land and exits.
+constexpr int kStages = 4;
 constexpr int kWaitPolls = 1 << 22;
+constexpr int kConsumerWarps = 4;
+constexpr int kInt2Threads = (kConsumerWarps + 1) * 32;
+constexpr int kFlagFirst = 1, kFlagLast = 2;
+
+struct StageInfo {
+    int item, b, kv, valid, flags, pad0, pad1, pad2;
+};
 
 template <int NT>
 struct Int2Smem {
-    static constexpr int kStageBytes = kStages * kBlock;
-    static constexpr int kScaleBytes = kPage * 4 * 16;  // per token: sK, zzK, sV, zzV (float4 each)
-    static constexpr int kPBytes = NT * 4 * kPage * 4;
-    static constexpr int kWarpBytes = kStageBytes + kScaleBytes + kPBytes + 64;
+    static constexpr int G4 = NT * 4;  // head columns (padded to 4 per n-tile)
+    static constexpr int kStage = 0;
+    static constexpr int kInfo = kStage + kStages * kBlock;
+    static constexpr int kBars = kInfo + kStages * (int)sizeof(StageInfo);
+    static constexpr int kScale = kBars + 2 * kStages * 8 + 16;            // [warp][64] float4, see consumer
+    static constexpr int kP = kScale + kConsumerWarps * 2 * 2 * 16 * 16;    // [warp][G4][16] float
+    static constexpr int kMerge = kP + kConsumerWarps * G4 * 16 * 4;        // [warp][G4][kD + 2] float
+    static constexpr int kBytes = kMerge + kConsumerWarps * G4 * (kD + 2) * 4;
 };
 
 __device__ __forceinline__ int find_seq(const int32_t* item_start, int B, int item) {
@@ -179,192 +222,251 @@ __device__ __forceinline__ int find_seq(const int32_t* item_start, int B, int it
     return lo;
 }
 
+
 template <int NT>
-__global__ void __launch_bounds__(128, 2) int2_kernel(DecodeParams p) {
+__global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(DecodeParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     using SM = Int2Smem<NT>;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int gID = lane >> 2, tq = lane & 3;
-    uint8_t* wsm = smem + warp * SM::kWarpBytes;
-    uint8_t* stage_buf = wsm;
-    float4* sc4 = reinterpret_cast<float4*>(wsm + SM::kStageBytes);
-    float* pbuf = reinterpret_cast<float*>(wsm + SM::kStageBytes + SM::kScaleBytes);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(wsm + SM::kStageBytes + SM::kScaleBytes + SM::kPBytes);
-    int* stage_valid = reinterpret_cast<int*>(bars + kStages);
+    uint8_t* stages = smem + SM::kStage;
+    StageInfo* info = reinterpret_cast<StageInfo*>(smem + SM::kInfo);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::kBars);
+    uint64_t* empty = full + kStages;
+    uint64_t* merge_bar = empty + kStages;  // consumer-warp rendezvous at item ends
 
-    if (lane == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
+        }
+        mbar_init(merge_bar, kConsumerWarps);
         fence_mbar_init();
     }
-    __syncwarp();
+    __syncthreads();
 
-    const int total = __ldg(p.item_start + p.B);
-    // lane-dependent rotations for the K operand: codes at bits 2tq / 16+2tq
-    // and 8+2tq / 24+2tq move to bits 4-5 / 20-21
-    const uint32_t rotA = (uint32_t)(2 * tq + 28) & 31u, rotB = (uint32_t)(4 + 2 * tq);
-    const bool lo_lane = (gID & 1) != 0;  // PV B-operand column parity: hi / lo
-    uint32_t issued = 0, consumed = 0;    // page-stream counters (stage = n % kStages)
-
-    for (;;) {
-        int item = 0;
-        if (lane == 0) item = atomicAdd(p.counter, 1);
-        item = __shfl_sync(kFull, item, 0);
-        if (item >= total) break;
-        const int b = find_seq(p.item_start, p.B, item);
-        const int s0 = __ldg(p.item_start + b);
-        const int splits = (__ldg(p.item_start + b + 1) - s0) / p.hk;
-        const int local = item - s0;
-        const int kv = local / splits, split = local % splits;
-        const int hist = min(max(__ldg(p.hist_len + b), 0), p.max_pages * kPage);
-        const int npg_seq = (hist + kPage - 1) / kPage;
-        const int pg0 = split * p.pps;
-        const int npg = min(p.pps, npg_seq - pg0);
-        const int bk = b * p.hk + kv;
-
-        // rotated-query fragments and group sums for this (b, kv)
-        uint32_t qf[NT][8][2];
-        float4 qsv[NT];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const uint32_t* fr = p.qfrag + ((size_t)bk * NT + nt) * 8 * 32 * 2;
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint2 v = *reinterpret_cast<const uint2*>(fr + ((size_t)ks * 32 + lane) * 2);
-                qf[nt][ks][0] = v.x;
-                qf[nt][ks][1] = v.y;
+    if (warp == kConsumerWarps) {
+        // ------------------------------ producer ------------------------------
+        const int total = __ldg(p.item_start + p.B);
+        uint32_t n = 0;      // pages issued so far (stage = n % kStages)
+        bool ok = true;
+        for (;;) {
+            int item = 0;
+            if (lane == 0) item = atomicAdd(p.counter, 1);
+            item = __shfl_sync(kFull, item, 0);
+            const bool last_item = item >= total;
+            int b = 0, kv = 0, pg0 = 0, npg = 1, hist = 0;
+            if (!last_item) {
+                b = find_seq(p.item_start, p.B, item);
+                const int s0 = __ldg(p.item_start + b);
+                const int splits = (__ldg(p.item_start + b + 1) - s0) / p.hk;
+                kv = (item - s0) / splits;
+                const int split = (item - s0) % splits;
+                hist = min(max(__ldg(p.hist_len + b), 0), p.max_pages * kPage);
+                pg0 = split * p.pps;
+                npg = min(p.pps, (hist + kPage - 1) / kPage - pg0);
             }
-            qsv[nt] = *reinterpret_cast<const float4*>(p.qsum + ((size_t)bk * NT * 4 + 4 * nt + tq) * 4);
-        }
-
-        float m_run[NT], l_run[NT], zacc[NT][4], acc_o[NT][8][4];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            m_run[nt] = -INFINITY;
-            l_run[nt] = 0.f;
-#pragma unroll
-            for (int g = 0; g < 4; ++g) zacc[nt][g] = 0.f;
-#pragma unroll
-            for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc_o[nt][mt][e] = 0.f;
-        }
-
-        auto issue = [&](int pi_local) {  // lane 0 only
-            const int st = issued % kStages;
-            const int pi = pg0 + pi_local;
-            const int pid = __ldg(p.page_table + (size_t)b * p.max_pages + pi);
-            if (pid < 0 || pid >= p.num_pages) {
-                report(p.status, OSCAR_STATUS_BAD_PAGE);
-                stage_valid[st] = 0;
-                mbar_arrive(&bars[st]);
-            } else {
-                stage_valid[st] = min(kPage, hist - pi * kPage);
-                mbar_arrive_expect_tx(&bars[st], kBlock);
-                bulk_g2s(stage_buf + st * kBlock, p.pool + ((size_t)pid * p.hk + kv) * kBlock, kBlock, &bars[st]);
-            }
-            ++issued;
-        };
-        if (lane == 0)
-            for (int i = 0; i < min(kStages, npg); ++i) issue(i);
-        issued = __shfl_sync(kFull, issued, 0);
-        __syncwarp();
-
-        bool failed = false;
-        for (int pl = 0; pl < npg; ++pl) {
-            const int st = consumed % kStages;
-            const uint32_t parity = (consumed / kStages) & 1u;
-            const bool ok = __all_sync(kFull, mbar_wait_bounded(&bars[st], parity, kWaitPolls));
-            if (!ok) {
-                failed = true;
-                break;
-            }
-            ++consumed;
-            const uint8_t* blk = stage_buf + st * kBlock;
-            const int valid = stage_valid[st];
-
-            // -- scales: fp16 (s, z) -> fp32 (s, z - 8 s); zero for masked slots
-#pragma unroll
-            for (int tt = 0; tt < 2; ++tt) {
-                const int t = lane + 32 * tt;
-                const uint4 kw = *reinterpret_cast<const uint4*>(blk + kKScale + t * 16);
-                const uint4 vw = *reinterpret_cast<const uint4*>(blk + kVScale + t * 16);
-                const bool on = t < valid;
-                const uint32_t kk[4] = {kw.x, kw.y, kw.z, kw.w}, vv[4] = {vw.x, vw.y, vw.z, vw.w};
-                float ks_[4], kz_[4], vs_[4], vz_[4];
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    const float sk = half_lo(kk[g]), zk = half_hi(kk[g]);
-                    const float sv = half_lo(vv[g]), zv = half_hi(vv[g]);
-                    ks_[g] = on ? sk : 0.f;
-                    kz_[g] = on ? fmaf(-8.f, sk, zk) : 0.f;
-                    vs_[g] = on ? sv : 0.f;
-                    vz_[g] = on ? fmaf(-8.f, sv, zv) : 0.f;
-                }
-                sc4[t * 4 + 0] = make_float4(ks_[0], ks_[1], ks_[2], ks_[3]);
-                sc4[t * 4 + 1] = make_float4(kz_[0], kz_[1], kz_[2], kz_[3]);
-                sc4[t * 4 + 2] = make_float4(vs_[0], vs_[1], vs_[2], vs_[3]);
-                sc4[t * 4 + 3] = make_float4(vz_[0], vz_[1], vz_[2], vz_[3]);
-            }
-            __syncwarp();
-
-            // -- logits: rows = tokens (2gID, 2gID+1 of each 16-token tile)
-            float sv[4][NT][2];
-#pragma unroll
-            for (int tile = 0; tile < 4; ++tile) {
-                const int tA = tile * 16 + 2 * gID;
-                const uint4* kr = reinterpret_cast<const uint4*>(blk + kKCodes + tA * 32);
-                const uint4 ka0 = kr[0], ka1 = kr[1], kb0 = kr[2], kb1 = kr[3];
-                const uint32_t wa[8] = {ka0.x, ka0.y, ka0.z, ka0.w, ka1.x, ka1.y, ka1.z, ka1.w};
-                const uint32_t wb[8] = {kb0.x, kb0.y, kb0.z, kb0.w, kb1.x, kb1.y, kb1.z, kb1.w};
-                float acc[4][NT][4];
-#pragma unroll
-                for (int g = 0; g < 4; ++g)
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) acc[g][nt][e] = 0.f;
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t a0 = codes_to_bf16x2(rotr(wa[ks], rotA));
-                    const uint32_t a1 = codes_to_bf16x2(rotr(wb[ks], rotA));
-                    const uint32_t a2 = codes_to_bf16x2(rotr(wa[ks], rotB));
-                    const uint32_t a3 = codes_to_bf16x2(rotr(wb[ks], rotB));
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-                        mma_bf16_16816(acc[ks >> 1][nt], a0, a1, a2, a3, qf[nt][ks][0], qf[nt][ks][1]);
-                }
-                const float4 sA = sc4[tA * 4 + 0], zA = sc4[tA * 4 + 1];
-                const float4 sB = sc4[(tA + 1) * 4 + 0], zB = sc4[(tA + 1) * 4 + 1];
-                const float sa[4] = {sA.x, sA.y, sA.z, sA.w}, za[4] = {zA.x, zA.y, zA.z, zA.w};
-                const float sb[4] = {sB.x, sB.y, sB.z, sB.w}, zb[4] = {zB.x, zB.y, zB.z, zB.w};
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const float qg[4] = {qsv[nt].x, qsv[nt].y, qsv[nt].z, qsv[nt].w};
-                    float la = 0.f, lb = 0.f;
-#pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        la = fmaf(sa[g], acc[g][nt][0] + acc[g][nt][1], la);
-                        la = fmaf(za[g], qg[g], la);
-                        lb = fmaf(sb[g], acc[g][nt][2] + acc[g][nt][3], lb);
-                        lb = fmaf(zb[g], qg[g], lb);
+            for (int c = 0; c < npg; c += 32) {
+                // page ids of the next 32 pages, one per lane
+                int pid = -1;
+                if (!last_item && c + lane < npg) pid = __ldg(p.page_table + (size_t)b * p.max_pages + pg0 + c + lane);
+                const int cnt = last_item ? 1 : min(32, npg - c);
+                for (int i = 0; i < cnt; ++i) {
+                    const int pi = __shfl_sync(kFull, pid, i);
+                    const uint32_t s = n % kStages;
+                    if (n >= (uint32_t)kStages) {
+                        const bool w = mbar_wait_bounded(&empty[s], ((n / kStages) - 1) & 1u, kWaitPolls);
+                        ok = __all_sync(kFull, w);
+                        if (!ok) break;
                     }
-                    sv[tile][nt][0] = (tA < valid) ? la : -INFINITY;
-                    sv[tile][nt][1] = (tA + 1 < valid) ? lb : -INFINITY;
+                    if (lane == 0) {
+                        StageInfo& si = info[s];
+                        if (last_item) {
+                            si.item = -1;
+                            mbar_arrive(&full[s]);
+                        } else {
+                            const int pl = c + i;
+                            si.item = item;
+                            si.b = b;
+                            si.kv = kv;
+                            si.flags = (pl == 0 ? kFlagFirst : 0) | (pl == npg - 1 ? kFlagLast : 0);
+                            if (pi < 0 || pi >= p.num_pages) {
+                                report(p.status, OSCAR_STATUS_BAD_PAGE);
+                                si.valid = 0;
+                                mbar_arrive(&full[s]);
+                            } else {
+                                si.valid = min(kPage, hist - (pg0 + pl) * kPage);
+                                mbar_arrive_expect_tx(&full[s], kBlock);
+                                bulk_g2s(stages + s * kBlock, p.pool + ((size_t)pi * p.hk + kv) * kBlock, kBlock,
+                                         &full[s]);
+                            }
+                        }
+                    }
+                    __syncwarp();
+                    ++n;
                 }
+                if (!ok) break;
             }
+            if (!ok || last_item) break;
+        }
+        if (!ok) {
+            if (lane == 0) report(p.status, OSCAR_STATUS_TIMEOUT);
+            // let issued copies land before the block can exit
+            const uint32_t first = n > (uint32_t)kStages ? n - kStages : 0;
+            for (uint32_t k = first; k < n; ++k)
+                (void)mbar_wait_bounded(&full[k % kStages], (k / kStages) & 1u, kWaitPolls);
+        }
+        return;
+    }
 
-            // -- online softmax (base 2): page max per head, rescale, p
+    // ------------------------------- consumers ---------------------------------
+    const int gID = lane >> 2, tq = lane & 3;
+    const int tb = 16 * warp;  // this warp's token tile inside each page
+    float4* scS = reinterpret_cast<float4*>(smem + SM::kScale) + warp * 64;   // [K|V][s|zz][16]
+    float* pbuf = reinterpret_cast<float*>(smem + SM::kP) + warp * SM::G4 * 16;
+    float* mrg = reinterpret_cast<float*>(smem + SM::kMerge);
+    const float2 take_lo = (gID & 1) ? make_float2(1.f, 1.f) : make_float2(0.f, 0.f);  // PV column: hi / lo
+    const CodeMul cm = code_mul_regs(p.code_mul);
+
+    uint32_t merge_phase = 0;
+    // bounded rendezvous of the four consumer warps (an mbarrier, so that a
+    // warp that gave up on a page cannot leave the others waiting forever)
+    auto consumer_sync = [&]() -> bool {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(merge_bar);
+        const bool w = mbar_wait_bounded(merge_bar, merge_phase & 1u, kWaitPolls);
+        ++merge_phase;
+        return __all_sync(kFull, w);
+    };
+
+    uint32_t qf[NT][8][2];
+    float4 qsv[NT];
+    float m_run[NT], l_run[NT], zacc[NT][4], acc_o[NT][8][4];
+
+    for (uint32_t n = 0;; ++n) {
+        const uint32_t s = n % kStages;
+        const bool w = mbar_wait_bounded(&full[s], (n / kStages) & 1u, kWaitPolls);
+        if (!__all_sync(kFull, w)) {
+            if (lane == 0) report(p.status, OSCAR_STATUS_TIMEOUT);
+            return;
+        }
+        const StageInfo si = info[s];
+        if (si.item < 0) break;
+        const uint8_t* blk = stages + s * kBlock;
+
+        if (si.flags & kFlagFirst) {
+            const int bk = si.b * p.hk + si.kv;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                float mx = -INFINITY;
+                const uint32_t* fr = p.qfrag + ((size_t)bk * NT + nt) * 8 * 32 * 2;
 #pragma unroll
-                for (int tile = 0; tile < 4; ++tile) mx = fmaxf(mx, fmaxf(sv[tile][nt][0], sv[tile][nt][1]));
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint2 v = *reinterpret_cast<const uint2*>(fr + ((size_t)ks * 32 + lane) * 2);
+                    qf[nt][ks][0] = v.x;
+                    qf[nt][ks][1] = v.y;
+                }
+                qsv[nt] = *reinterpret_cast<const float4*>(p.qsum + ((size_t)bk * NT * 4 + 4 * nt + tq) * 4);
+                m_run[nt] = -INFINITY;
+                l_run[nt] = 0.f;
+#pragma unroll
+                for (int g = 0; g < 4; ++g) zacc[nt][g] = 0.f;
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc_o[nt][mt][e] = 0.f;
+            }
+        }
+
+        // -- scales of this tile: fp16 (s, z) -> fp32 (s, z - 8 s); zero when masked
+        {
+            const int t = lane & 15, which = lane >> 4;
+            const uint4 raw = *reinterpret_cast<const uint4*>(blk + (which ? kVScale : kKScale) + (tb + t) * 16);
+            const bool on = tb + t < si.valid;
+            const uint32_t r[4] = {raw.x, raw.y, raw.z, raw.w};
+            float sv[4], zz[4];
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const float sg = half_lo(r[g]);
+                sv[g] = on ? sg : 0.f;
+                zz[g] = on ? fmaf(-8.f, sg, half_hi(r[g])) : 0.f;
+            }
+            // K: s at [t], zz at [16 + t]; V: zz at [48 + t], s transposed to
+            // [32 + g*4 ..] as floats [g][pv_slot(t)]
+            if (which == 0) scS[t] = make_float4(sv[0], sv[1], sv[2], sv[3]);
+            scS[which * 32 + 16 + t] = make_float4(zz[0], zz[1], zz[2], zz[3]);
+            if (which == 1) {
+                float* vs = reinterpret_cast<float*>(scS + 32);
+#pragma unroll
+                for (int g = 0; g < 4; ++g) vs[g * 16 + pv_slot(t)] = sv[g];
+            }
+        }
+        __syncwarp();
+
+        // -- logits: A rows gID / gID+8 = tokens tb+gID / tb+gID+8; k-step
+        //    (g, h) takes slot g of words 2tq+h of each token
+        float la[NT], lb[NT];
+        {
+            const uint2 x = *reinterpret_cast<const uint2*>(blk + kKCodes + (tb + gID) * 32 + 8 * tq);
+            const uint2 y = *reinterpret_cast<const uint2*>(blk + kKCodes + (tb + gID + 8) * 32 + 8 * tq);
+            const uint32_t wa[2] = {x.x, x.y}, wb[2] = {y.x, y.y};
+            float acc[4][NT][4];
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc[g][nt][e] = 0.f;
+            const uint32_t wa8[2] = {wa[0] >> 8, wa[1] >> 8}, wb8[2] = {wb[0] >> 8, wb[1] >> 8};
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+                // half-major order: the four groups' accumulation chains interleave
+                const int h = it >> 2, g = it & 3, ks = 2 * g + h;
+                uint32_t a0, a1, a2, a3;
+                switch (g) {  // compile-time after unrolling
+                    case 0: a0 = unpack_pair<0>(wa[h], cm); a1 = unpack_pair<0>(wb[h], cm);
+                            a2 = unpack_pair<0>(wa8[h], cm); a3 = unpack_pair<0>(wb8[h], cm); break;
+                    case 1: a0 = unpack_pair<2>(wa[h], cm); a1 = unpack_pair<2>(wb[h], cm);
+                            a2 = unpack_pair<2>(wa8[h], cm); a3 = unpack_pair<2>(wb8[h], cm); break;
+                    case 2: a0 = unpack_pair<4>(wa[h], cm); a1 = unpack_pair<4>(wb[h], cm);
+                            a2 = unpack_pair<4>(wa8[h], cm); a3 = unpack_pair<4>(wb8[h], cm); break;
+                    default: a0 = unpack_pair<6>(wa[h], cm); a1 = unpack_pair<6>(wb[h], cm);
+                             a2 = unpack_pair<6>(wa8[h], cm); a3 = unpack_pair<6>(wb8[h], cm); break;
+                }
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                    mma_bf16_16816(acc[g][nt], a0, a1, a2, a3, qf[nt][ks][0], qf[nt][ks][1]);
+            }
+            const float4 sA = scS[gID], sB = scS[gID + 8], zA = scS[16 + gID], zB = scS[16 + gID + 8];
+            const float sa[4] = {sA.x, sA.y, sA.z, sA.w}, za[4] = {zA.x, zA.y, zA.z, zA.w};
+            const float sb[4] = {sB.x, sB.y, sB.z, sB.w}, zb[4] = {zB.x, zB.y, zB.z, zB.w};
+            const bool va = tb + gID < si.valid, vb = tb + gID + 8 < si.valid;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const float qg[4] = {qsv[nt].x, qsv[nt].y, qsv[nt].z, qsv[nt].w};
+                float xa = 0.f, xb = 0.f;
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    xa = fmaf(sa[g], acc[g][nt][0] + acc[g][nt][1], xa);
+                    xa = fmaf(za[g], qg[g], xa);
+                    xb = fmaf(sb[g], acc[g][nt][2] + acc[g][nt][3], xb);
+                    xb = fmaf(zb[g], qg[g], xb);
+                }
+                la[nt] = va ? xa : -INFINITY;
+                lb[nt] = vb ? xb : -INFINITY;
+            }
+        }
+
+        // -- online softmax (base 2) for this warp's tokens
+        {
+            const float4 vzA = scS[48 + gID], vzB = scS[48 + gID + 8];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                float mx = fmaxf(la[nt], lb[nt]);
                 mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
                 mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
                 mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
                 const float m_new = fmaxf(m_run[nt], mx);
-                if (m_new > m_run[nt]) {  // uniform across the lanes of head tq
-                    const float alpha = ex2(m_run[nt] - m_new);
+                if (__any_sync(kFull, m_new > m_run[nt])) {  // warp-uniform rescale
+                    const float alpha = (m_new > m_run[nt]) ? ex2(m_run[nt] - m_new) : 1.f;
                     l_run[nt] *= alpha;
 #pragma unroll
                     for (int g = 0; g < 4; ++g) zacc[nt][g] *= alpha;
@@ -374,275 +476,377 @@ __global__ void __launch_bounds__(128, 2) int2_kernel(DecodeParams p) {
                         for (int e = 0; e < 4; ++e) acc_o[nt][mt][e] *= alpha;
                     m_run[nt] = m_new;
                 }
-                // all tokens masked so far: subtract 0 so p = ex2(-inf) = 0
                 const float m_sub = (m_new == -INFINITY) ? 0.f : m_new;
-#pragma unroll
-                for (int tile = 0; tile < 4; ++tile) {
-                    const int tA = tile * 16 + 2 * gID;
-                    const float pa = ex2(sv[tile][nt][0] - m_sub);
-                    const float pb = ex2(sv[tile][nt][1] - m_sub);
-                    l_run[nt] += pa + pb;
-                    const float4 vzA = sc4[tA * 4 + 3], vzB = sc4[(tA + 1) * 4 + 3];
-                    zacc[nt][0] = fmaf(pa, vzA.x, fmaf(pb, vzB.x, zacc[nt][0]));
-                    zacc[nt][1] = fmaf(pa, vzA.y, fmaf(pb, vzB.y, zacc[nt][1]));
-                    zacc[nt][2] = fmaf(pa, vzA.z, fmaf(pb, vzB.z, zacc[nt][2]));
-                    zacc[nt][3] = fmaf(pa, vzA.w, fmaf(pb, vzB.w, zacc[nt][3]));
-                    *reinterpret_cast<float2*>(pbuf + (nt * 4 + tq) * kPage + tA) = make_float2(pa, pb);
-                }
+                const float pa = ex2(la[nt] - m_sub), pb = ex2(lb[nt] - m_sub);
+                l_run[nt] += pa + pb;
+                zacc[nt][0] = fmaf(pa, vzA.x, fmaf(pb, vzB.x, zacc[nt][0]));
+                zacc[nt][1] = fmaf(pa, vzA.y, fmaf(pb, vzB.y, zacc[nt][1]));
+                zacc[nt][2] = fmaf(pa, vzA.z, fmaf(pb, vzB.z, zacc[nt][2]));
+                zacc[nt][3] = fmaf(pa, vzA.w, fmaf(pb, vzB.w, zacc[nt][3]));
+                pbuf[(nt * 4 + tq) * 16 + pv_slot(gID)] = pa;
+                pbuf[(nt * 4 + tq) * 16 + pv_slot(gID + 8)] = pb;
             }
-            __syncwarp();
-
-            // -- values: rows = dims, columns = heads (hi, lo), k = tokens
-#pragma unroll
-            for (int tile = 0; tile < 4; ++tile) {
-                const int t0 = tile * 16 + 4 * tq;
-                float4 pp[NT];
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-                    pp[nt] = *reinterpret_cast<const float4*>(pbuf + (nt * 4 + (gID >> 1)) * kPage + t0);
-                const float4 s0 = sc4[(t0 + 0) * 4 + 2], s1 = sc4[(t0 + 1) * 4 + 2];
-                const float4 s2 = sc4[(t0 + 2) * 4 + 2], s3 = sc4[(t0 + 3) * 4 + 2];
-                const float sv0[4] = {s0.x, s0.y, s0.z, s0.w}, sv1[4] = {s1.x, s1.y, s1.z, s1.w};
-                const float sv2[4] = {s2.x, s2.y, s2.z, s2.w}, sv3[4] = {s3.x, s3.y, s3.z, s3.w};
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    const uint32_t wv =
-                        *reinterpret_cast<const uint32_t*>(blk + kVCodes + (8 * g + gID) * kPage + t0);
-                    uint32_t bb0[NT], bb1[NT];
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        const float w0 = pp[nt].x * sv0[g], w1 = pp[nt].y * sv1[g];
-                        const float w2 = pp[nt].z * sv2[g], w3 = pp[nt].w * sv3[g];
-                        // hi lanes: bf16 truncation; lo lanes: rounded remainder
-                        const uint32_t u0 = __float_as_uint(w0), u1 = __float_as_uint(w1);
-                        const uint32_t u2 = __float_as_uint(w2), u3 = __float_as_uint(w3);
-                        const uint32_t hi02 = __byte_perm(u0, u2, 0x7632), hi13 = __byte_perm(u1, u3, 0x7632);
-                        const uint32_t lo02 = pack_bf16x2_rn(w0 - __uint_as_float(u0 & 0xffff0000u),
-                                                             w2 - __uint_as_float(u2 & 0xffff0000u));
-                        const uint32_t lo13 = pack_bf16x2_rn(w1 - __uint_as_float(u1 & 0xffff0000u),
-                                                             w3 - __uint_as_float(u3 & 0xffff0000u));
-                        bb0[nt] = lo_lane ? lo02 : hi02;
-                        bb1[nt] = lo_lane ? lo13 : hi13;
-                    }
-#pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        const uint32_t sa0 = (uint32_t)(4 * half + 28) & 31u;      // slot 2half, bytes 0/2
-                        const uint32_t sa1 = (uint32_t)(4 * half + 30) & 31u;      // slot 2half+1
-                        const uint32_t a0 = codes_to_bf16x2(rotr(wv, sa0));
-                        const uint32_t a1 = codes_to_bf16x2(rotr(wv, sa1));
-                        const uint32_t a2 = codes_to_bf16x2(rotr(wv, (uint32_t)(4 + 4 * half)));
-                        const uint32_t a3 = codes_to_bf16x2(rotr(wv, (uint32_t)(6 + 4 * half)));
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt)
-                            mma_bf16_16816(acc_o[nt][2 * g + half], a0, a1, a2, a3, bb0[nt], bb1[nt]);
-                    }
-                }
-            }
-            __syncwarp();
-            if (lane == 0 && pl + kStages < npg) issue(pl + kStages);
-            issued = __shfl_sync(kFull, issued, 0);
-            __syncwarp();
         }
-        if (failed) {
-            if (lane == 0) report(p.status, OSCAR_STATUS_TIMEOUT);
-            // let copies still in flight land before the block can exit
-            while (consumed < issued) {
-                const int st = consumed % kStages;
-                (void)mbar_wait_bounded(&bars[st], (consumed / kStages) & 1u, kWaitPolls);
-                ++consumed;
-            }
-            return;
-        }
+        __syncwarp();
 
-        // -- partial (unnormalised o', base-2 max m, sum l) of this item
-        float* part = p.part + (size_t)item * p.part_stride;
+        // -- values: A rows = dims (m-tile (g, half): in-group index 16 half + row,
+        //    code plane 16 half + row, slot g), k = tokens (4tq, 4tq+2 | 4tq+1,
+        //    4tq+3), columns = heads (hi, lo)
+        {
+            float4 pp[NT];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            float l = l_run[nt];
-            l += __shfl_xor_sync(kFull, l, 4);
-            l += __shfl_xor_sync(kFull, l, 8);
-            l += __shfl_xor_sync(kFull, l, 16);
-            float z[4];
+            for (int nt = 0; nt < NT; ++nt)
+                pp[nt] = *reinterpret_cast<const float4*>(pbuf + (nt * 4 + (gID >> 1)) * 16 + 4 * tq);
+            // (p, s) of tokens (4tq, 4tq+2) and (4tq+1, 4tq+3) as adjacent pairs
+            const float* vs = reinterpret_cast<const float*>(scS + 32);
+            const uint8_t* vrow = blk + kVCodes + tb + 4 * tq;
+            const uint32_t pw[4] = {*reinterpret_cast<const uint32_t*>(vrow + gID * kPage),
+                                    *reinterpret_cast<const uint32_t*>(vrow + (8 + gID) * kPage),
+                                    *reinterpret_cast<const uint32_t*>(vrow + (16 + gID) * kPage),
+                                    *reinterpret_cast<const uint32_t*>(vrow + (24 + gID) * kPage)};
+            const uint32_t pw8[4] = {pw[0] >> 8, pw[1] >> 8, pw[2] >> 8, pw[3] >> 8};
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
-                z[g] = zacc[nt][g];
-                z[g] += __shfl_xor_sync(kFull, z[g], 4);
-                z[g] += __shfl_xor_sync(kFull, z[g], 8);
-                z[g] += __shfl_xor_sync(kFull, z[g], 16);
-            }
-            const int hl = 4 * nt + tq;
-            if (hl < p.G) {
-                float* o = part + (size_t)hl * kD;
+                const float4 sg = *reinterpret_cast<const float4*>(vs + g * 16 + 4 * tq);
+                uint32_t bb0[NT], bb1[NT];
 #pragma unroll
-                for (int g = 0; g < 4; ++g)
-                    *reinterpret_cast<float4*>(o + 32 * g + 4 * gID) = make_float4(
-                        acc_o[nt][2 * g][0] + acc_o[nt][2 * g][1] + z[g],
-                        acc_o[nt][2 * g][2] + acc_o[nt][2 * g][3] + z[g],
-                        acc_o[nt][2 * g + 1][0] + acc_o[nt][2 * g + 1][1] + z[g],
-                        acc_o[nt][2 * g + 1][2] + acc_o[nt][2 * g + 1][3] + z[g]);
-                if (gID == 0) {
-                    part[(size_t)p.G * kD + hl] = m_run[nt];
-                    part[(size_t)p.G * kD + p.G + hl] = l;
+                for (int nt = 0; nt < NT; ++nt) {
+                    bb0[nt] = split_w_pair(make_float2(pp[nt].x, pp[nt].y), make_float2(sg.x, sg.y), take_lo);
+                    bb1[nt] = split_w_pair(make_float2(pp[nt].z, pp[nt].w), make_float2(sg.z, sg.w), take_lo);
+                }
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const uint32_t r0 = pw[2 * half], r1 = pw[2 * half + 1];
+                    const uint32_t r08 = pw8[2 * half], r18 = pw8[2 * half + 1];
+                    uint32_t a0, a1, a2, a3;
+                    switch (g) {
+                        case 0: a0 = unpack_pair<0>(r0, cm); a1 = unpack_pair<0>(r1, cm);
+                                a2 = unpack_pair<0>(r08, cm); a3 = unpack_pair<0>(r18, cm); break;
+                        case 1: a0 = unpack_pair<2>(r0, cm); a1 = unpack_pair<2>(r1, cm);
+                                a2 = unpack_pair<2>(r08, cm); a3 = unpack_pair<2>(r18, cm); break;
+                        case 2: a0 = unpack_pair<4>(r0, cm); a1 = unpack_pair<4>(r1, cm);
+                                a2 = unpack_pair<4>(r08, cm); a3 = unpack_pair<4>(r18, cm); break;
+                        default: a0 = unpack_pair<6>(r0, cm); a1 = unpack_pair<6>(r1, cm);
+                                 a2 = unpack_pair<6>(r08, cm); a3 = unpack_pair<6>(r18, cm); break;
+                    }
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                        mma_bf16_16816(acc_o[nt][2 * g + half], a0, a1, a2, a3, bb0[nt], bb1[nt]);
                 }
             }
         }
+        __syncwarp();
+
+        if (si.flags & kFlagLast) {
+            // this warp's partial state -> shared memory
+            float* mw = mrg + (size_t)warp * SM::G4 * (kD + 2);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                float l = l_run[nt];
+                l += __shfl_xor_sync(kFull, l, 4);
+                l += __shfl_xor_sync(kFull, l, 8);
+                l += __shfl_xor_sync(kFull, l, 16);
+                float z[4];
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    z[g] = zacc[nt][g];
+                    z[g] += __shfl_xor_sync(kFull, z[g], 4);
+                    z[g] += __shfl_xor_sync(kFull, z[g], 8);
+                    z[g] += __shfl_xor_sync(kFull, z[g], 16);
+                }
+                float* o = mw + (size_t)(4 * nt + tq) * (kD + 2);
+#pragma unroll
+                for (int g = 0; g < 4; ++g)
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        o[32 * g + 16 * half + gID] = acc_o[nt][2 * g + half][0] + acc_o[nt][2 * g + half][1] + z[g];
+                        o[32 * g + 16 * half + 8 + gID] =
+                            acc_o[nt][2 * g + half][2] + acc_o[nt][2 * g + half][3] + z[g];
+                    }
+                if (gID == 0) {
+                    o[kD] = m_run[nt];
+                    o[kD + 1] = l;
+                }
+            }
+            if (!consumer_sync()) {
+                if (lane == 0) report(p.status, OSCAR_STATUS_TIMEOUT);
+                return;
+            }
+            // merge the four warps: thread -> dimension, all heads
+            float* part = p.part + (size_t)si.item * p.part_stride;
+            const int d = threadIdx.x;  // 0..127
+            for (int hl = 0; hl < p.G; ++hl) {
+                float M = -INFINITY;
+#pragma unroll
+                for (int ww = 0; ww < kConsumerWarps; ++ww)
+                    M = fmaxf(M, mrg[((size_t)ww * SM::G4 + hl) * (kD + 2) + kD]);
+                float acc = 0.f, L = 0.f;
+                if (M != -INFINITY) {
+#pragma unroll
+                    for (int ww = 0; ww < kConsumerWarps; ++ww) {
+                        const float* src = mrg + ((size_t)ww * SM::G4 + hl) * (kD + 2);
+                        const float sc = ex2(src[kD] - M);
+                        acc = fmaf(sc, src[d], acc);
+                        L = fmaf(sc, src[kD + 1], L);
+                    }
+                }
+                part[(size_t)hl * kD + d] = acc;
+                if (d == 0) {
+                    part[(size_t)p.G * kD + hl] = M;
+                    part[(size_t)p.G * kD + p.G + hl] = L;
+                }
+            }
+            if (!consumer_sync()) {
+                if (lane == 0) report(p.status, OSCAR_STATUS_TIMEOUT);
+                return;
+            }
+        }
+        if (lane == 0) mbar_arrive(&empty[s]);
     }
 }
 
 // ---------------------------------------------------------------------------
 // BF16 sink + recent segment
 // ---------------------------------------------------------------------------
-// One block (4 warps) per (b, kv); warp w takes slots w, w+4, ...; lane l
-// owns dims 4l..4l+3.  Logits in base 2 (q scaled by sm_scale*log2 e).
-struct Bf16Red {
-    float m[4][8], l[4][8];
-    float o[4][8][kD];
-};
+// One block per (b, kv), 128 threads.  The segment's K|V rows (512 B per
+// token) are staged in 32-token chunks into shared memory with cp.async,
+// double buffered, so that two chunks of loads are in flight per block.
+// Per chunk: logits by four threads per token (32 dims each), online
+// softmax statistics by one warp per head, values by one thread per
+// dimension.  Logits in base 2 (q scaled by sm_scale * log2 e).
+constexpr int kBfThreads = 128;
+constexpr int kBfChunk = 32;
+constexpr int kBfPitch = 528;                  // bytes per staged token row (512 + 16)
+constexpr int kBfQPitch = 4 * 36;              // floats per staged query row (4 quarters of 32 + 4 pad)
+constexpr int kBfSmem = 2 * kBfChunk * kBfPitch + 8 * kBfQPitch * 4 + 8 * kBfChunk * 4 + 8 * 4 * 4;
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 template <int G>
-__device__ void bf16_segment(const DecodeParams& p, int b, int kv, Bf16Red& red) {
-    auto& red_m = red.m;
-    auto& red_l = red.l;
-    auto& red_o = red.o;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    float qv[G][4], m[G], l[G], o[G][4];
-#pragma unroll
-    for (int hh = 0; hh < G; ++hh) {
-        const uint2 qr = *reinterpret_cast<const uint2*>(p.q + ((size_t)b * p.hq + kv * G + hh) * kD + 4 * lane);
-        qv[hh][0] = bf16_lo(qr.x) * p.qscale;
-        qv[hh][1] = bf16_hi(qr.x) * p.qscale;
-        qv[hh][2] = bf16_lo(qr.y) * p.qscale;
-        qv[hh][3] = bf16_hi(qr.y) * p.qscale;
-        m[hh] = -INFINITY;
-        l[hh] = 0.f;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) o[hh][e] = 0.f;
-    }
+__device__ void bf16_segment(const DecodeParams& p, int b, int kv, uint8_t* sm) {
+    uint8_t* buf = sm;                                                  // [2][kBfChunk][kBfPitch]
+    float* qsh = reinterpret_cast<float*>(sm + 2 * kBfChunk * kBfPitch);   // [G][kBfQPitch]
+    float* pw = qsh + 8 * kBfQPitch;                                   // [G][kBfChunk] weights
+    float* st = pw + 8 * kBfChunk;                                     // [G][4]: m, l, alpha
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n = min(max(__ldg(p.bf16_len + b), 0), p.nslot);
-    for (int t = warp; t < n; t += 4) {
-        const __nv_bfloat16* row = p.bf16_kv + (((size_t)b * p.nslot + t) * p.hk + kv) * 2 * kD;
-        const uint2 kr = *reinterpret_cast<const uint2*>(row + 4 * lane);
-        const uint2 vr = *reinterpret_cast<const uint2*>(row + kD + 4 * lane);
-        const float k4[4] = {bf16_lo(kr.x), bf16_hi(kr.x), bf16_lo(kr.y), bf16_hi(kr.y)};
-        const float v4[4] = {bf16_lo(vr.x), bf16_hi(vr.x), bf16_lo(vr.y), bf16_hi(vr.y)};
-        float s[G];
-#pragma unroll
-        for (int hh = 0; hh < G; ++hh) {
-            float d = qv[hh][0] * k4[0];
-            d = fmaf(qv[hh][1], k4[1], d);
-            d = fmaf(qv[hh][2], k4[2], d);
-            d = fmaf(qv[hh][3], k4[3], d);
-            s[hh] = d;
+    const int nch = (n + kBfChunk - 1) / kBfChunk;
+    const size_t row_elems = (size_t)p.hk * 2 * kD;
+    const __nv_bfloat16* base = p.bf16_kv + ((size_t)b * p.nslot * p.hk + kv) * 2 * kD;
+
+    auto stage = [&](int c) {  // copy chunk c (its valid rows only)
+        uint8_t* dst = buf + (c & 1) * kBfChunk * kBfPitch;
+        const int t0 = c * kBfChunk, cnt = min(kBfChunk, n - t0);
+        for (int i = tid; i < cnt * 32; i += kBfThreads) {
+            const int r = i >> 5, k = i & 31;
+            cp_async16(dst + r * kBfPitch + 16 * k,
+                       reinterpret_cast<const uint8_t*>(base + (size_t)(t0 + r) * row_elems) + 16 * k);
         }
-#pragma unroll
-        for (int mm = 16; mm > 0; mm >>= 1)
-#pragma unroll
-            for (int hh = 0; hh < G; ++hh) s[hh] += __shfl_xor_sync(kFull, s[hh], mm);
-#pragma unroll
-        for (int hh = 0; hh < G; ++hh) {
-            const float mn = fmaxf(m[hh], s[hh]);
-            const float alpha = ex2(m[hh] - mn);
-            const float pr = ex2(s[hh] - mn);
-            l[hh] = l[hh] * alpha + pr;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) o[hh][e] = fmaf(pr, v4[e], o[hh][e] * alpha);
-            m[hh] = mn;
-        }
+        cp_async_commit();
+    };
+    if (nch > 0) stage(0);
+    for (int i = tid; i < G * kD; i += kBfThreads) {
+        const int h = i / kD, d = i % kD;
+        qsh[h * kBfQPitch + (d >> 5) * 36 + (d & 31)] =
+            __bfloat162float(p.q[((size_t)b * p.hq + kv * G + h) * kD + d]) * p.qscale;
     }
-#pragma unroll
-    for (int hh = 0; hh < G; ++hh) {
-        if (lane == 0) {
-            red_m[warp][hh] = m[hh];
-            red_l[warp][hh] = l[hh];
-        }
-        *reinterpret_cast<float4*>(&red_o[warp][hh][4 * lane]) = make_float4(o[hh][0], o[hh][1], o[hh][2], o[hh][3]);
+    if (tid < G) {
+        st[tid * 4 + 0] = -INFINITY;
+        st[tid * 4 + 1] = 0.f;
     }
-    __syncthreads();
-    // merge the four warps: warp w handles heads w, w+4
+    float o[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) o[h] = 0.f;
+
+    for (int c = 0; c < nch; ++c) {
+        if (c + 1 < nch) {
+            stage(c + 1);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();
+        const uint8_t* cb = buf + (c & 1) * kBfChunk * kBfPitch;
+        const int cnt = min(kBfChunk, n - c * kBfChunk);
+        {  // logits: token t = tid / 4, quarter = tid % 4 (32 dims)
+            const int t = tid >> 2, qr = tid & 3;
+            float acc[G];
+#pragma unroll
+            for (int h = 0; h < G; ++h) acc[h] = 0.f;
+            const uint4* kr = reinterpret_cast<const uint4*>(cb + t * kBfPitch + qr * 64);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint4 w = kr[j];
+                const float k8[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
+                                     bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    const float4 qa = *reinterpret_cast<const float4*>(qsh + h * kBfQPitch + qr * 36 + 8 * j);
+                    const float4 qb = *reinterpret_cast<const float4*>(qsh + h * kBfQPitch + qr * 36 + 8 * j + 4);
+                    acc[h] = fmaf(qa.x, k8[0], acc[h]);
+                    acc[h] = fmaf(qa.y, k8[1], acc[h]);
+                    acc[h] = fmaf(qa.z, k8[2], acc[h]);
+                    acc[h] = fmaf(qa.w, k8[3], acc[h]);
+                    acc[h] = fmaf(qb.x, k8[4], acc[h]);
+                    acc[h] = fmaf(qb.y, k8[5], acc[h]);
+                    acc[h] = fmaf(qb.z, k8[6], acc[h]);
+                    acc[h] = fmaf(qb.w, k8[7], acc[h]);
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                acc[h] += __shfl_xor_sync(kFull, acc[h], 1);
+                acc[h] += __shfl_xor_sync(kFull, acc[h], 2);
+                if (qr == 0) pw[h * kBfChunk + t] = (t < cnt) ? acc[h] : -INFINITY;
+            }
+        }
+        __syncthreads();
+        // softmax statistics: warp w handles heads w, w + 4
+        for (int h = warp; h < G; h += 4) {
+            const float x = pw[h * kBfChunk + lane];
+            float mx = x;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+            const float m_old = st[h * 4 + 0];
+            const float m_new = fmaxf(m_old, mx);
+            const float alpha = (m_old == -INFINITY) ? 0.f : ex2(m_old - m_new);
+            const float w = (x == -INFINITY) ? 0.f : ex2(x - m_new);
+            float sum = w;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
+            pw[h * kBfChunk + lane] = w;
+            __syncwarp();
+            if (lane == 0) {
+                st[h * 4 + 0] = m_new;
+                st[h * 4 + 1] = st[h * 4 + 1] * alpha + sum;
+                st[h * 4 + 2] = alpha;
+            }
+        }
+        __syncthreads();
+        {  // values: thread = dimension
+            const int d = tid;
+            float acc[G];
+#pragma unroll
+            for (int h = 0; h < G; ++h) acc[h] = 0.f;
+            const uint8_t* vcol = cb + 256 + 2 * d;
+            // weights of masked / absent tokens are 0 and their rows are not read
+            const int cnt4 = cnt & ~3;
+            for (int t = 0; t < cnt4; t += 4) {
+                float v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    v[u] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(vcol + (t + u) * kBfPitch));
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    const float4 w = *reinterpret_cast<const float4*>(pw + h * kBfChunk + t);
+                    acc[h] = fmaf(w.x, v[0], acc[h]);
+                    acc[h] = fmaf(w.y, v[1], acc[h]);
+                    acc[h] = fmaf(w.z, v[2], acc[h]);
+                    acc[h] = fmaf(w.w, v[3], acc[h]);
+                }
+            }
+            for (int t = cnt4; t < cnt; ++t) {
+                const float v = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(vcol + t * kBfPitch));
+#pragma unroll
+                for (int h = 0; h < G; ++h) acc[h] = fmaf(pw[h * kBfChunk + t], v, acc[h]);
+            }
+#pragma unroll
+            for (int h = 0; h < G; ++h) o[h] = fmaf(o[h], st[h * 4 + 2], acc[h]);
+        }
+        __syncthreads();
+    }
     float* part = p.bf_part + (size_t)(b * p.hk + kv) * p.part_stride;
-    for (int hh = warp; hh < G; hh += 4) {
-        float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < 4; ++w) M = fmaxf(M, red_m[w][hh]);
-        float L = 0.f, oo[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            const float sc = (red_l[w][hh] > 0.f) ? ex2(red_m[w][hh] - M) : 0.f;
-            L += sc * red_l[w][hh];
-            const float4 v = *reinterpret_cast<const float4*>(&red_o[w][hh][4 * lane]);
-            oo[0] += sc * v.x;
-            oo[1] += sc * v.y;
-            oo[2] += sc * v.z;
-            oo[3] += sc * v.w;
-        }
-        *reinterpret_cast<float4*>(part + (size_t)hh * kD + 4 * lane) = make_float4(oo[0], oo[1], oo[2], oo[3]);
-        if (lane == 0) {
-            part[(size_t)G * kD + hh] = M;
-            part[(size_t)G * kD + G + hh] = L;
+    for (int h = 0; h < G; ++h) {
+        part[(size_t)h * kD + tid] = o[h];
+        if (tid == 0) {
+            part[(size_t)G * kD + h] = st[h * 4 + 0];
+            part[(size_t)G * kD + G + h] = st[h * 4 + 1];
         }
     }
 }
 
-__global__ void __launch_bounds__(128) bf16_kernel(DecodeParams p) {
-    __shared__ __align__(16) Bf16Red red;
+__global__ void __launch_bounds__(kBfThreads) bf16_kernel(DecodeParams p) {
+    extern __shared__ __align__(16) uint8_t bsm[];
     const int b = blockIdx.x / p.hk, kv = blockIdx.x % p.hk;
     switch (p.G) {
-        case 1: bf16_segment<1>(p, b, kv, red); break;
-        case 2: bf16_segment<2>(p, b, kv, red); break;
-        case 4: bf16_segment<4>(p, b, kv, red); break;
-        default: bf16_segment<8>(p, b, kv, red); break;
+        case 1: bf16_segment<1>(p, b, kv, bsm); break;
+        case 2: bf16_segment<2>(p, b, kv, bsm); break;
+        case 4: bf16_segment<4>(p, b, kv, bsm); break;
+        default: bf16_segment<8>(p, b, kv, bsm); break;
     }
 }
 
 // ---------------------------------------------------------------------------
 // merge: INT2 splits -> un-rotate -> merge with the BF16 partial
 // ---------------------------------------------------------------------------
-constexpr int kMergeSeqs = 4;     // sequences per block
-constexpr int kUPitch = kD + 1;   // padded row pitch of U_V in shared memory
-constexpr int kMergeSmem = (kD * kUPitch + kMergeSeqs * 8 * kD + kMergeSeqs * 8 * 4) * 4;
+// One warp per output row (b, head), eight rows per block, block y = KV
+// head.  U_V is copied row-major into shared memory with cp.async while the
+// warps merge their split-K partials; the un-rotation o = w . U_V^T then
+// reads U_V in a lane-rotated order (lane l takes index (j + l) mod 128 at
+// step j) so that every shared-memory access is conflict-free.
+constexpr int kMergeRows = 8;
+constexpr int kMergeThreads = 32 * kMergeRows;
+constexpr int kMergeSmem = (kD * kD + kMergeRows * kD) * 4;
 
-__global__ void __launch_bounds__(256) merge_kernel(DecodeParams p) {
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(DecodeParams p) {
     extern __shared__ __align__(16) float msm[];
-    float* Us = msm;                                   // [d][kUPitch]: U_V[a][j]
-    float* Wr = msm + kD * kUPitch;                    // [rows][d]: normalised o'.P.H (Hadamard domain)
-    float* st = Wr + kMergeSeqs * 8 * kD;              // [rows][4]: M_i2, L_i2, m_bf, l_bf
+    float* Us = msm;                  // [a][j] = U_V[a][j]
+    float* Wr = msm + kD * kD;        // [warp][j]: normalised o'.P.H (Hadamard domain)
     const int kv = blockIdx.y;
-    const int b0 = blockIdx.x * kMergeSeqs;
-    const int nseq = min(kMergeSeqs, p.B - b0);
-    const int rows = nseq * p.G;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-
-    const float* Uv = p.U + ((size_t)kv * 2 + 1) * kD * kD;
-    for (int i = threadIdx.x; i < kD * kD / 4; i += blockDim.x) {
-        const float4 u = __ldg(reinterpret_cast<const float4*>(Uv) + i);
-        const int a = (4 * i) / kD, j = (4 * i) % kD;
-        Us[a * kUPitch + j] = u.x;
-        Us[a * kUPitch + j + 1] = u.y;
-        Us[a * kUPitch + j + 2] = u.z;
-        Us[a * kUPitch + j + 3] = u.w;
+    {
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(p.U + ((size_t)kv * 2 + 1) * kD * kD);
+        uint8_t* dst = reinterpret_cast<uint8_t*>(Us);
+        for (int i = threadIdx.x; i < kD * kD / 4; i += kMergeThreads)
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst + 16 * i)), "l"(src + 16 * i)
+                         : "memory");
+        asm volatile("cp.async.commit_group;" ::: "memory");
     }
-    const int r5 = bitrev5(lane);
-    for (int r = warp; r < rows; r += 8) {
-        const int b = b0 + r / p.G, hh = r % p.G;
+    const int r = blockIdx.x * kMergeRows + warp;
+    const bool active = r < p.B * p.G;
+    const int b = active ? r / p.G : 0, hh = active ? r % p.G : 0;
+    float M = -INFINITY, L = 0.f;
+    if (active) {
         const int s0 = __ldg(p.item_start + b);
         const int splits = (__ldg(p.item_start + b + 1) - s0) / p.hk;
         const int first = s0 + kv * splits;
-        // lane handles Hadamard indices j = 4 lane + k, stored at bitrev7(j)
-        float M = -INFINITY;
+        const int r5 = bitrev5(lane);
+        // lane handles Hadamard indices j = 4 lane + k, stored at bitrev7(j);
+        // split statistics are read lane-parallel, then the partial vectors
+        // are accumulated with independent loads
         for (int s = lane; s < splits; s += 32)
             M = fmaxf(M, p.part[(size_t)(first + s) * p.part_stride + (size_t)p.G * kD + hh]);
 #pragma unroll
         for (int mm = 16; mm > 0; mm >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, mm));
-        float L = 0.f, y[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int s = 0; s < splits; ++s) {
-            const float* pt = p.part + (size_t)(first + s) * p.part_stride;
-            const float ls = pt[(size_t)p.G * kD + p.G + hh];
-            if (!(ls > 0.f)) continue;
-            const float sc = ex2(pt[(size_t)p.G * kD + hh] - M);
-            L += sc * ls;
+        float y[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int s0b = 0; s0b < splits; s0b += 32) {
+            float sc = 0.f;
+            const int sl = s0b + lane;
+            if (sl < splits) {
+                const float* pt = p.part + (size_t)(first + sl) * p.part_stride + (size_t)p.G * kD;
+                const float ls = pt[p.G + hh];
+                if (ls > 0.f) {
+                    sc = ex2(pt[hh] - M);
+                    L += sc * ls;
+                }
+            }
+            const int cnt = min(32, splits - s0b);
+#pragma unroll 4
+            for (int i = 0; i < cnt; ++i) {
+                const float w = __shfl_sync(kFull, sc, i);
+                const float* o = p.part + (size_t)(first + s0b + i) * p.part_stride + (size_t)hh * kD;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) y[k] = fmaf(sc, pt[(size_t)hh * kD + 32 * bitrev2(k) + r5], y[k]);
+                for (int k = 0; k < 4; ++k) y[k] = fmaf(w, o[32 * bitrev2(k) + r5], y[k]);
+            }
         }
+#pragma unroll
+        for (int mm = 16; mm > 0; mm >>= 1) L += __shfl_xor_sync(kFull, L, mm);
         const float inv = (L > 0.f) ? 1.f / L : 0.f;
 #pragma unroll
         for (int k = 0; k < 4; ++k) y[k] *= inv;
@@ -662,33 +866,35 @@ __global__ void __launch_bounds__(256) merge_kernel(DecodeParams p) {
                 y[k] = upper ? o - y[k] : y[k] + o;
             }
         }
-        *reinterpret_cast<float4*>(Wr + (size_t)r * kD + 4 * lane) =
+        *reinterpret_cast<float4*>(Wr + (size_t)warp * kD + 4 * lane) =
             make_float4(y[0] * (float)kInvSqrtD, y[1] * (float)kInvSqrtD, y[2] * (float)kInvSqrtD,
                         y[3] * (float)kInvSqrtD);
-        if (lane == 0) {
-            const float* bp = p.bf_part + (size_t)(b * p.hk + kv) * p.part_stride;
-            st[r * 4 + 0] = M;
-            st[r * 4 + 1] = L;
-            st[r * 4 + 2] = bp[(size_t)p.G * kD + hh];
-            st[r * 4 + 3] = bp[(size_t)p.G * kD + p.G + hh];
-        }
     }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
     __syncthreads();
-    for (int idx = threadIdx.x; idx < rows * kD; idx += blockDim.x) {
-        const int r = idx / kD, a = idx % kD;
-        const int b = b0 + r / p.G, hh = r % p.G;
-        const float* w = Wr + (size_t)r * kD;
-        const float* u = Us + a * kUPitch;
-        float acc = 0.f;
+    if (!active) return;
+    // o[a] = sum_j w[j] U_V[a][j] for a = lane + 32 c
+    const float* w = Wr + (size_t)warp * kD;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 8
-        for (int j = 0; j < kD; ++j) acc = fmaf(w[j], u[j], acc);
-        const float Mi = st[r * 4 + 0], Li = st[r * 4 + 1], mb = st[r * 4 + 2], lb = st[r * 4 + 3];
-        const float Mx = fmaxf(Li > 0.f ? Mi : -INFINITY, lb > 0.f ? mb : -INFINITY);
-        const float wi = (Li > 0.f) ? ex2(Mi - Mx) * Li : 0.f;
-        const float wb = (lb > 0.f) ? ex2(mb - Mx) : 0.f;
-        const float den = wi + wb * lb;
-        const float ob = p.bf_part[(size_t)(b * p.hk + kv) * p.part_stride + (size_t)hh * kD + a];
-        p.out[((size_t)b * p.hq + kv * p.G + hh) * kD + a] = (den > 0.f) ? (wi * acc + wb * ob) / den : 0.f;
+    for (int j = 0; j < kD; ++j) {
+        const int jj = (j + lane) & (kD - 1);
+        const float wj = w[jj];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[c] = fmaf(wj, Us[(lane + 32 * c) * kD + jj], acc[c]);
+    }
+    const float* bp = p.bf_part + (size_t)(b * p.hk + kv) * p.part_stride;
+    const float mb = bp[(size_t)p.G * kD + hh], lb = bp[(size_t)p.G * kD + p.G + hh];
+    const float Mx = fmaxf(L > 0.f ? M : -INFINITY, lb > 0.f ? mb : -INFINITY);
+    const float wi = (L > 0.f) ? ex2(M - Mx) * L : 0.f;
+    const float wb = (lb > 0.f) ? ex2(mb - Mx) : 0.f;
+    const float den = wi + wb * lb;
+    const float inv = (den > 0.f) ? 1.f / den : 0.f;
+    float* o = p.out + ((size_t)b * p.hq + kv * p.G + hh) * kD;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const int a2 = lane + 32 * c;
+        o[a2] = (wi * acc[c] + wb * bp[(size_t)hh * kD + a2]) * inv;
     }
 }
 
@@ -697,7 +903,7 @@ __global__ void __launch_bounds__(256) merge_kernel(DecodeParams p) {
 // ---------------------------------------------------------------------------
 struct Int2Attr {
     int sms = 0;
-    bool set1 = false, set2 = false, setm = false;
+    bool set1 = false, set2 = false, setm = false, setp = false, setb = false;
 };
 
 static Int2Attr& attr_for_device(int dev) {
@@ -707,16 +913,17 @@ static Int2Attr& attr_for_device(int dev) {
 
 template <int NT>
 static cudaError_t launch_int2(const DecodeParams& p, cudaStream_t st, int sms, bool& attr_set) {
-    const int smem = 4 * Int2Smem<NT>::kWarpBytes;
+    const int smem = Int2Smem<NT>::kBytes;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(int2_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
+    const int per_sm = (NT == 1) ? 3 : 2;
     const int max_items = p.B * p.hk * ((p.max_pages + p.pps - 1) / p.pps);
-    int blocks = min(2 * sms, (max_items + 3) / 4);
+    int blocks = min(per_sm * sms, max_items);
     if (blocks < 1) blocks = 1;
-    int2_kernel<NT><<<blocks, 128, smem, st>>>(p);
+    int2_kernel<NT><<<blocks, kInt2Threads, smem, st>>>(p);
     return cudaGetLastError();
 }
 
@@ -730,22 +937,32 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st, cudaEvent_t ev
         e = cudaDeviceGetAttribute(&at.sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
     }
-    const int prep_warps = p.B * p.hk * p.NT * 4;
-    prep_kernel<<<(prep_warps + 3) / 4 + 1, 128, 0, st>>>(p);
+    if (!at.setp) {
+        e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
+        if (e != cudaSuccess) return e;
+        at.setp = true;
+    }
+    dim3 pg((p.B + kPrepSeqs - 1) / kPrepSeqs + 1, p.hk);
+    prep_kernel<<<pg, kPrepThreads, kPrepSmem, st>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (ev_int2_start && (e = cudaEventRecord(ev_int2_start, st)) != cudaSuccess) return e;
     e = (p.NT == 1) ? launch_int2<1>(p, st, at.sms, at.set1) : launch_int2<2>(p, st, at.sms, at.set2);
     if (e != cudaSuccess) return e;
     if (ev_int2_stop && (e = cudaEventRecord(ev_int2_stop, st)) != cudaSuccess) return e;
-    bf16_kernel<<<p.B * p.hk, 128, 0, st>>>(p);
+    if (!at.setb) {
+        e = cudaFuncSetAttribute(bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kBfSmem);
+        if (e != cudaSuccess) return e;
+        at.setb = true;
+    }
+    bf16_kernel<<<p.B * p.hk, kBfThreads, kBfSmem, st>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (!at.setm) {
         e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMergeSmem);
         if (e != cudaSuccess) return e;
         at.setm = true;
     }
-    dim3 mg((p.B + kMergeSeqs - 1) / kMergeSeqs, p.hk);
-    merge_kernel<<<mg, 256, kMergeSmem, st>>>(p);
+    dim3 mg((p.B * p.G + kMergeRows - 1) / kMergeRows, p.hk);
+    merge_kernel<<<mg, kMergeThreads, kMergeSmem, st>>>(p);
     return cudaGetLastError();
 }
 

@@ -4,15 +4,16 @@
 // "从离线校准到在线推理的 pipeline"; rotation R = U.Hadamard.bit-reversal
 // from section "OSCAR 把旋转瞄准 attention").
 //
-// One warp per (token, KV head, K|V) vector.  Lane l owns Hadamard indices
-// j = 4l..4l+3.  y = x.U is accumulated with error-free transformations
+// One block of four warps per (token, KV head, K|V) vector; lane l owns
+// Hadamard indices j = 4l..4l+3.  y = x.U is accumulated with error-free transformations
 // (FMA-based exact products, TwoSum accumulation: the "Dot2" scheme of
 // Ogita, Rump and Oishi, "Accurate sum and dot product", 2005), the fast
 // Walsh-Hadamard transform runs on the (hi, lo) float pairs, and the group
 // statistics and code decisions run in fp64, so the result follows a
 // float64 evaluation of the method.  Stored position p = bitrev7(j) =
 // 32*bitrev2(i) + bitrev5(l) for value i of lane l: each lane holds one
-// element of every group, and group reductions are warp reductions.
+// element of every group (group reductions are warp reductions), and the
+// four codes of one code byte (in-group index bitrev5(l) of groups 0..3).
 #include "oscar_common.cuh"
 
 namespace oscar {
@@ -42,34 +43,33 @@ __device__ __forceinline__ df df_add(df a, df b) {
 
 __device__ __forceinline__ df df_neg(df a) { return {-a.hi, -a.lo}; }
 
+// Block = one (token, KV head, K|V) vector; warp w accumulates the terms
+// a in [32w, 32w + 32) of y = x . U, warp 0 adds the four partial sums
+// exactly and finishes the vector.
 __global__ void __launch_bounds__(128) evict_kernel(EvictParams p) {
-    const int lane = threadIdx.x & 31;
-    const int vec = blockIdx.x * 4 + (threadIdx.x >> 5);
-    if (vec >= p.n_tok * p.hk * 2) return;
+    __shared__ df part[4][kD];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int vec = blockIdx.x;
     const int i = vec / (p.hk * 2);
     const int kv = (vec >> 1) % p.hk;
     const int which = vec & 1;
 
     const long row = p.src_row ? (long)__ldg(p.src_row + i) : (long)i;
     if (row < 0 || row >= p.src_rows) {
-        if (lane == 0) report(p.status, OSCAR_STATUS_BAD_POS);
+        if (threadIdx.x == 0) report(p.status, OSCAR_STATUS_BAD_POS);
         return;
     }
     const size_t xoff = ((size_t)row * p.hk * 2 + (size_t)kv * 2 + which) * kD + 4 * lane;
     const uint2 xr = *reinterpret_cast<const uint2*>(p.src_kv + xoff);
     float x[4] = {bf16_lo(xr.x), bf16_hi(xr.x), bf16_lo(xr.y), bf16_hi(xr.y)};
-    if (p.new_kv) {  // fused ring append: this lane read its four elements already
-        const size_t noff = ((size_t)i * p.hk * 2 + (size_t)kv * 2 + which) * kD + 4 * lane;
-        *reinterpret_cast<uint2*>(const_cast<__nv_bfloat16*>(p.src_kv) + xoff) =
-            *reinterpret_cast<const uint2*>(p.new_kv + noff);
-    }
 
-    // ---- y = x . U, compensated --------------------------------------------
+    // ---- partial y = x . U over this warp's 32 terms, compensated -------------
     const float* Um = p.U + ((size_t)kv * 2 + which) * kD * kD;
     float s[4] = {0.f, 0.f, 0.f, 0.f}, c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
-    for (int a = 0; a < kD; ++a) {
-        const float xa = __shfl_sync(kFull, x[a & 3], a >> 2);
+    for (int aa = 0; aa < 32; ++aa) {
+        const int a = 32 * warp + aa;
+        const float xa = __shfl_sync(kFull, x[aa & 3], a >> 2);
         const float4 u = __ldg(reinterpret_cast<const float4*>(Um + (size_t)a * kD + 4 * lane));
         const float uu[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -81,9 +81,22 @@ __global__ void __launch_bounds__(128) evict_kernel(EvictParams p) {
             c[k] = __fadd_rn(c[k], __fadd_rn(pe, t.lo));
         }
     }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) part[warp][4 * lane + k] = two_sum(s[k], c[k]);
+    __syncthreads();  // all warps have read the source row and written partials
+    if (warp != 0) return;
+    if (p.new_kv) {  // fused ring append: overwrite the row just read
+        const size_t noff = ((size_t)i * p.hk * 2 + (size_t)kv * 2 + which) * kD + 4 * lane;
+        *reinterpret_cast<uint2*>(const_cast<__nv_bfloat16*>(p.src_kv) + xoff) =
+            *reinterpret_cast<const uint2*>(p.new_kv + noff);
+    }
     df y[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) y[k] = two_sum(s[k], c[k]);
+    for (int k = 0; k < 4; ++k) {
+        y[k] = part[0][4 * lane + k];
+#pragma unroll
+        for (int w = 1; w < 4; ++w) y[k] = df_add(y[k], part[w][4 * lane + k]);
+    }
 
     // ---- Walsh-Hadamard transform (unnormalised), Sylvester order ------------
     // in-lane stages (distance 1, 2)
@@ -132,8 +145,10 @@ __global__ void __launch_bounds__(128) evict_kernel(EvictParams p) {
             hi[k] = fmax(hi[k], __shfl_xor_sync(kFull, hi[k], m));
         }
     unsigned short sb[4], zb[4];
-    uint32_t byte_part[4];
-    const int r5 = bitrev5(lane);
+    // value k of this lane is in-group index bitrev5(lane) of group bitrev2(k):
+    // all four codes of code byte j = bitrev5(lane) are this lane's, group k in
+    // bits 2k..2k+1
+    uint32_t byte = 0;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         sb[k] = f64_to_f16_bits((hi[k] - lo[k]) / 3.0);
@@ -146,14 +161,7 @@ __global__ void __launch_bounds__(128) evict_kernel(EvictParams p) {
             r = fmin(fmax(r, 0.0), 3.0);
             code = (int)r;
         }
-        // position within its byte = r5 & 3
-        byte_part[k] = (uint32_t)code << (2 * (r5 & 3));
-    }
-    // OR the four codes of a byte: they sit in lanes l, l^8, l^16, l^24
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        byte_part[k] |= __shfl_xor_sync(kFull, byte_part[k], 8);
-        byte_part[k] |= __shfl_xor_sync(kFull, byte_part[k], 16);
+        byte |= (uint32_t)code << (2 * bitrev2(k));
     }
 
     // ---- store ---------------------------------------------------------------
@@ -170,16 +178,9 @@ __global__ void __launch_bounds__(128) evict_kernel(EvictParams p) {
     }
     const int slot = pos % kPage;
     uint8_t* blk = p.pool + ((size_t)page * p.hk + kv) * kBlock;
-    if (lane < 8) {
-        const int j8 = r5 >> 2;  // byte index within each group's 8 bytes
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int j = 8 * bitrev2(k) + j8;
-            const uint8_t b = (uint8_t)byte_part[k];
-            if (which == 0) blk[kKCodes + slot * (kD / 4) + j] = b;
-            else blk[kVCodes + j * kPage + slot] = b;
-        }
-    }
+    const int j = bitrev5(lane);
+    if (which == 0) blk[kKCodes + slot * (kD / 4) + j] = (uint8_t)byte;
+    else blk[kVCodes + j * kPage + slot] = (uint8_t)byte;
     if (lane == 0) {
         // group of value k is bitrev2(k); scale/zero words in group order
         uint32_t w[4];
@@ -193,7 +194,7 @@ __global__ void __launch_bounds__(128) evict_kernel(EvictParams p) {
 cudaError_t launch_evict(const EvictParams& p, cudaStream_t st) {
     const int vecs = p.n_tok * p.hk * 2;
     if (vecs == 0) return cudaSuccess;
-    evict_kernel<<<(vecs + 3) / 4, 128, 0, st>>>(p);
+    evict_kernel<<<vecs, 128, 0, st>>>(p);
     return cudaGetLastError();
 }
 

@@ -67,24 +67,104 @@ __device__ __forceinline__ uint32_t codes_to_bf16x2(uint32_t x) {
     return lop3_and_or(x, 0x00300030u, 0x41004100u);
 }
 
-__device__ __forceinline__ uint32_t rotr(uint32_t x, uint32_t n) { return __funnelshift_r(x, x, n); }
-
-// D += A(16x16 bf16, row) * B(16x8 bf16, col), fp32 accumulate
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                               uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
 // bf16x2 with lo -> bits 0-15, hi -> bits 16-31, round to nearest even
 __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
 }
+
+__device__ __forceinline__ uint32_t rotr(uint32_t x, uint32_t n) { return __funnelshift_r(x, x, n); }
+
+// Multipliers that move a code pair to bits 4-5 / 20-21 with an integer
+// multiply-add: x16 (from bits 0-1), x4 (bits 2-3), high word of x 2^30
+// (bits 6-7).  Held in registers made opaque by a warp shuffle, so the
+// compiler keeps them as multiply-adds (FMA pipe) instead of shifts (ALU
+// pipe) or per-use constant loads.
+struct CodeMul {
+    uint32_t m16, m4, mh30;
+};
+
+__device__ __forceinline__ CodeMul code_mul_regs(const uint32_t* mul_param) {
+    CodeMul c;
+    c.m16 = __shfl_sync(kFull, mul_param[0], 0);
+    c.m4 = __shfl_sync(kFull, mul_param[1], 0);
+    c.mh30 = __shfl_sync(kFull, mul_param[3], 0);
+    return c;
+}
+
+// Codes at bits (P, P+16) of x, P in {0, 2, 4, 6} -> bf16x2 (8 + c_lo,
+// 8 + c_hi): one logic op (mask) and, unless P == 4, one integer
+// multiply-add that moves the pair to bits 4-5 / 20-21 and adds the bf16
+// exponent bits of 8.0.  Codes in bytes 1 and 3 are first shifted down by 8.
+template <int P>
+__device__ __forceinline__ uint32_t unpack_pair(uint32_t x, const CodeMul& m) {
+    constexpr uint32_t kMask = 0x00030003u << P;
+    if constexpr (P == 4) {
+        return lop3_and_or(x, kMask, 0x41004100u);
+    } else {
+        const uint32_t v = x & kMask;
+        uint32_t r;
+        if constexpr (P == 0)
+            asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(r) : "r"(v), "r"(m.m16), "r"(0x41004100u));
+        else if constexpr (P == 2)
+            asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(r) : "r"(v), "r"(m.m4), "r"(0x41004100u));
+        else
+            asm("mad.hi.u32 %0, %1, %2, %3;" : "=r"(r) : "r"(v), "r"(m.mh30), "r"(0x41004100u));
+        return r;
+    }
+}
+
+// ---- packed fp32x2 arithmetic (two lanes of fp32 per instruction) --------
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    float2 r;
+    asm("{.reg .b64 A, B, C; mov.b64 A, {%2, %3}; mov.b64 B, {%4, %5}; mul.rn.f32x2 C, A, B; mov.b64 {%0, %1}, C;}"
+        : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+    float2 r;
+    asm("{.reg .b64 A, B, C; mov.b64 A, {%2, %3}; mov.b64 B, {%4, %5}; sub.rn.f32x2 C, A, B; mov.b64 {%0, %1}, C;}"
+        : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    float2 r;
+    asm("{.reg .b64 A, B, C, D; mov.b64 A, {%2, %3}; mov.b64 B, {%4, %5}; mov.b64 C, {%6, %7}; "
+        "fma.rn.f32x2 D, A, B, C; mov.b64 {%0, %1}, D;}"
+        : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return r;
+}
+
+// B-operand register of two products w = p * s, split into bf16 hi + lo:
+// hi = w with its low 16 bits cleared (exact in bf16), w - hi exact in fp32.
+// Returns the hi parts (take_lo = 0) or the rounded w - hi (take_lo = 1),
+// chosen arithmetically so that hi and lo lanes run the same instructions.
+// (hi is taken by masking, not by the rounding-based Veltkamp split: the
+// packed c - (c - w) form is exposed to algebraic simplification.)
+__device__ __forceinline__ uint32_t split_w_pair(float2 p, float2 s, float2 take_lo) {
+    const float2 w = mul2(p, s);
+    const float2 hi = make_float2(__uint_as_float(__float_as_uint(w.x) & 0xffff0000u),
+                                  __uint_as_float(__float_as_uint(w.y) & 0xffff0000u));
+    const float2 e = fma2(make_float2(-2.0f, -2.0f), hi, w);  // w - 2 hi, exact
+    const float2 x = fma2(take_lo, e, hi);                     // hi or w - hi
+    return pack_bf16x2_rn(x.x, x.y);
+}
+
+// Token order inside the shared probability / V-scale rows of a 16-token
+// tile: bits 0 and 1 swapped, so tokens (4a, 4a+2) and (4a+1, 4a+3) are
+// adjacent pairs (the two token pairs of a PV B-operand register).
+__device__ __forceinline__ int pv_slot(int t) { return (t & ~3) | ((t & 1) << 1) | ((t >> 1) & 1); }
+
+// D += A(16x16 bf16, row) * B(16x8 bf16, col), fp32 accumulate
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 
 // ------------------------------------------------------------------
 // mbarrier + bulk async copy (TMA, non-tensor), all waits bounded
@@ -178,6 +258,11 @@ struct DecodeParams {
     float* bf_part;       // [B*Hk][part_stride]
     int B, hq, hk, G, NT, nslot, max_pages, num_pages, pps, part_stride;
     float qscale;  // sm_scale * log2(e)
+    // multipliers that move a code pair from bits (P, P+16) to (4, 20):
+    // index P/2; 2^(4-P) for P < 4 (low product), 2^(36-P) for P > 4 (high
+    // product).  Passed at run time so the compiler keeps them as integer
+    // multiply-adds (FMA pipe) instead of turning them into shifts.
+    uint32_t code_mul[8];
 };
 
 cudaError_t launch_evict(const EvictParams& p, cudaStream_t st);

@@ -59,11 +59,12 @@
  *       [2048, 4096)  V codes, byte-plane-major: byte 2048 + j*64 + t
  *       [4096, 5120)  K scale/zero: at 4096 + t*16 + k*4, fp16 s then fp16 z
  *       [5120, 6144)  V scale/zero: at 5120 + t*16 + k*4
- *                    Code byte j holds stored positions 4j..4j+3, position
- *                    4j+i in bits 2i..2i+1; group k is stored positions
- *                    32k..32k+31; stored position p holds Hadamard output
- *                    bitrev7(p) (the bit-reversal of R, folded into
- *                    addressing); value = s*code + z in the rotated domain.
+ *                    Group k is stored positions 32k..32k+31; code byte j
+ *                    (j = 0..31) holds in-group index j of each group: stored
+ *                    position 32i + j in bits 2i..2i+1 (i = 0..3); stored
+ *                    position p holds Hadamard output bitrev7(p) (the
+ *                    bit-reversal of R, folded into addressing); value =
+ *                    s*code + z in the rotated domain.
  */
 #ifndef OSCAR_H
 #define OSCAR_H
@@ -182,7 +183,8 @@ oscar_status oscar_evict_quantize(const oscar_shape* shape, int32_t n_tok, const
  * mapped back by R_V^T); segments and split-K partials are merged by their
  * log-sum-exp.  An empty context gives a zero output.
  *
- *   q        (device) bf16 [B][Hq][d]       bf16_kv (device) see layouts
+ *   q        (device) bf16 [B][Hq][d], 8-byte aligned
+ *   bf16_kv  (device) see layouts, 16-byte aligned
  *   bf16_len (device int32 [B], each in [0, sink+recent])
  *   pool, page_table (device), max_pages, num_pages (pool extent)
  *   hist_len (device int32 [B]) history tokens at positions [0, hist_len)

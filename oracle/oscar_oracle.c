@@ -28,8 +28,11 @@
  * symmetric clip to +-c*max|y| per group; asymmetric fp16 scale/zero with
  * zero = clipped minimum and scale = (max-min)/3; codes from the stored
  * fp16 scale/zero with round-half-even; all-zero codes when the fp16 scale
- * is 0; four codes per byte, position 4j+i in bits 2i..2i+1 of byte j;
- * attention with the softmax scale given by the caller.
+ * is 0; four codes per byte, byte j holding stored positions j, j + d/4,
+ * j + 2d/4, j + 3d/4 in bits 0-1, 2-3, 4-5, 6-7 (the pages fix only "four
+ * codes per byte"; with d = 128 and g = 32 a byte then holds in-group index
+ * j of each of the four groups); attention with the softmax scale given by
+ * the caller.
  *
  * Parity pins for every function here live in tests/test_oracle_pins.py.
  */
@@ -250,8 +253,9 @@ void oracle_dequantize_vec(int d, int g, const uint8_t* codes, const uint16_t* s
 /*                         little-endian                               */
 /*   next P*(d/g)*4 bytes  V (s,z), same arrangement                   */
 /* where t = token slot in the page, j = code byte (stored positions   */
-/* 4j..4j+3), k = group.  History position pos of sequence b lives in  */
-/* page page_table[b*max_pages + pos/P], slot pos%P.                   */
+/* j + i*d/4 in bits 2i..2i+1, i = 0..3), k = group.  History position */
+/* pos of sequence b lives in page page_table[b*max_pages + pos/P],    */
+/* slot pos%P.                                                         */
 /* ------------------------------------------------------------------ */
 
 size_t oracle_block_bytes(int d, int g, int P) {
@@ -274,7 +278,9 @@ static void pool_write(uint8_t* block, int d, int g, int P, int slot, int which,
     size_t codes_bytes = (size_t)P * nbytes;
     size_t sz_bytes = (size_t)P * ng * 4;
     for (int j = 0; j < nbytes; ++j) {
-        uint8_t byte = oracle_pack4(codes + 4 * j);
+        uint8_t four[4];
+        for (int i = 0; i < 4; ++i) four[i] = codes[j + i * nbytes];
+        uint8_t byte = oracle_pack4(four);
         if (which == 0) block[(size_t)slot * nbytes + j] = byte;
         else block[codes_bytes + (size_t)j * P + slot] = byte;
     }
@@ -295,7 +301,9 @@ static void pool_read(const uint8_t* block, int d, int g, int P, int slot, int w
     for (int j = 0; j < nbytes; ++j) {
         uint8_t byte = (which == 0) ? block[(size_t)slot * nbytes + j]
                                     : block[codes_bytes + (size_t)j * P + slot];
-        oracle_unpack4(byte, codes + 4 * j);
+        uint8_t four[4];
+        oracle_unpack4(byte, four);
+        for (int i = 0; i < 4; ++i) codes[j + i * nbytes] = four[i];
     }
     const uint8_t* sz = block + 2 * codes_bytes + (size_t)which * sz_bytes;
     for (int k = 0; k < ng; ++k) {

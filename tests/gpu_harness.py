@@ -93,7 +93,7 @@ def read_vec(pool, table, b, pos, kv, which, Hk):
         byts = blk[t * 32:(t + 1) * 32]
     else:
         byts = blk[2048 + np.arange(32) * 64 + t]
-    codes = ((byts[:, None] >> np.array([0, 2, 4, 6], np.uint8)[None, :]) & 3).reshape(-1)
+    codes = ((byts[None, :] >> np.array([0, 2, 4, 6], np.uint8)[:, None]) & 3).reshape(-1)  # byte j: j + 32 i
     sz = blk[4096 + which * 1024 + t * 16: 4096 + which * 1024 + (t + 1) * 16].view(np.uint16)
     return codes, sz[0::2].copy(), sz[1::2].copy()
 

@@ -322,8 +322,9 @@ def numpy_read_pool(pool, table, b, n, kv, Hk, d=128, g=32, P=64):
         blk = pool[(page * Hk + kv) * bb:(page * Hk + kv + 1) * bb]
         kb = blk[t * (d // 4):(t + 1) * (d // 4)]
         vb = blk[P * d // 4 + np.arange(d // 4) * P + t]
-        kc = ((kb[:, None] >> shifts[None, :]) & 3).reshape(-1).astype(np.float64)
-        vc = ((vb[:, None] >> shifts[None, :]) & 3).reshape(-1).astype(np.float64)
+        # byte j holds positions j + i*d/4 in bits 2i..2i+1
+        kc = ((kb[None, :] >> shifts[:, None]) & 3).reshape(-1).astype(np.float64)
+        vc = ((vb[None, :] >> shifts[:, None]) & 3).reshape(-1).astype(np.float64)
         ksz = blk[2 * P * d // 4 + t * ng * 4: 2 * P * d // 4 + (t + 1) * ng * 4].view(np.float16).astype(np.float64)
         vo = 2 * P * d // 4 + P * ng * 4
         vsz = blk[vo + t * ng * 4: vo + (t + 1) * ng * 4].view(np.float16).astype(np.float64)

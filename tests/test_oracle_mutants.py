@@ -29,6 +29,8 @@ MUTANTS = [
     ("clip ignored", "double t = clip * amax;", "double t = amax;"),
     ("pack order reversed", "return (uint8_t)((c[0] & 3u) | ((c[1] & 3u) << 2) | ((c[2] & 3u) << 4) | ((c[3] & 3u) << 6));",
      "return (uint8_t)((c[3] & 3u) | ((c[2] & 3u) << 2) | ((c[1] & 3u) << 4) | ((c[0] & 3u) << 6));"),
+    ("consecutive positions share a byte", "for (int i = 0; i < 4; ++i) four[i] = codes[j + i * nbytes];",
+     "for (int i = 0; i < 4; ++i) four[i] = codes[4 * j + i];"),
     ("V stored token-major", "else block[codes_bytes + (size_t)j * P + slot] = byte;",
      "else block[codes_bytes + (size_t)slot * nbytes + j] = byte;"),
     ("V scale/zero written over K's", "    uint8_t* sz = block + 2 * codes_bytes + (size_t)which * sz_bytes;",
