@@ -266,10 +266,9 @@ oscar_status oscar_decode_attn(const oscar_shape* shape, int32_t batch, const vo
     p.pps = w.pps;
     p.part_stride = w.part_stride;
     p.qscale = sm_scale * kLog2e;
-    for (int i = 0; i < 8; ++i) {
-        const int P = 2 * i;
-        p.code_mul[i] = P < 4 ? (1u << (4 - P)) : (P > 4 ? (1u << (36 - P)) : 1u);
-    }
+    for (int i = 0; i < 8; ++i) p.code_mul[i] = 0;
+    p.code_mul[1] = 4u;          // code pair bits 0-1 -> 2-3
+    p.code_mul[3] = 1u << 30;    // bits 6-7 -> 4-5 (high word of the product)
     cudaEvent_t ev0 = g_int2_ev_start, ev1 = g_int2_ev_stop;
     g_int2_ev_start = g_int2_ev_stop = nullptr;
     if (!ev0 || !ev1) ev0 = ev1 = nullptr;

@@ -197,7 +197,7 @@ constexpr int kInt2Threads = (kConsumerWarps + 1) * 32;
 constexpr int kFlagFirst = 1, kFlagLast = 2;
 
 struct StageInfo {
-    int item, b, kv, valid, flags, pad0, pad1, pad2;
+    int item, b, kv, valid_flags;  // valid tokens in bits 0-7, flags above
 };
 
 template <int NT>
@@ -288,13 +288,13 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
                             si.item = item;
                             si.b = b;
                             si.kv = kv;
-                            si.flags = (pl == 0 ? kFlagFirst : 0) | (pl == npg - 1 ? kFlagLast : 0);
+                            const int flags = (pl == 0 ? kFlagFirst : 0) | (pl == npg - 1 ? kFlagLast : 0);
                             if (pi < 0 || pi >= p.num_pages) {
                                 report(p.status, OSCAR_STATUS_BAD_PAGE);
-                                si.valid = 0;
+                                si.valid_flags = flags << 8;
                                 mbar_arrive(&full[s]);
                             } else {
-                                si.valid = min(kPage, hist - (pg0 + pl) * kPage);
+                                si.valid_flags = min(kPage, hist - (pg0 + pl) * kPage) | (flags << 8);
                                 mbar_arrive_expect_tx(&full[s], kBlock);
                                 bulk_g2s(stages + s * kBlock, p.pool + ((size_t)pi * p.hk + kv) * kBlock, kBlock,
                                          &full[s]);
@@ -349,8 +349,11 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
             if (lane == 0) report(p.status, OSCAR_STATUS_TIMEOUT);
             return;
         }
-        const StageInfo si = info[s];
-        if (si.item < 0) break;
+        const int4 sraw = *reinterpret_cast<const int4*>(&info[s]);
+        if (sraw.x < 0) break;
+        struct {
+            int item, b, kv, valid, flags;
+        } si{sraw.x, sraw.y, sraw.z, sraw.w & 0xff, sraw.w >> 8};
         const uint8_t* blk = stages + s * kBlock;
 
         if (si.flags & kFlagFirst) {
@@ -376,18 +379,21 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
             }
         }
 
-        // -- scales of this tile: fp16 (s, z) -> fp32 (s, z - 8 s); zero when masked
+        // -- scales of this tile: fp16 (s, z) -> fp32 (s, z - M_g s); zero when masked
+        const bool full_tile = tb + 16 <= si.valid;  // warp-uniform
         {
             const int t = lane & 15, which = lane >> 4;
             const uint4 raw = *reinterpret_cast<const uint4*>(blk + (which ? kVScale : kKScale) + (tb + t) * 16);
-            const bool on = tb + t < si.valid;
             const uint32_t r[4] = {raw.x, raw.y, raw.z, raw.w};
             float sv[4], zz[4];
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                const float sg = half_lo(r[g]);
-                sv[g] = on ? sg : 0.f;
-                zz[g] = on ? fmaf(-8.f, sg, half_hi(r[g])) : 0.f;
+            for (int g = 0; g < 4; ++g) {  // z - M_g s with the group's code offset M_g
+                sv[g] = half_lo(r[g]);
+                zz[g] = fmaf(which ? -v_magic(g) : -k_magic(g), sv[g], half_hi(r[g]));
+            }
+            if (!full_tile && tb + t >= si.valid) {
+#pragma unroll
+                for (int g = 0; g < 4; ++g) sv[g] = zz[g] = 0.f;
             }
             // K: s at [t], zz at [16 + t]; V: zz at [48 + t], s transposed to
             // [32 + g*4 ..] as floats [g][pv_slot(t)]
@@ -422,14 +428,14 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
                 const int h = it >> 2, g = it & 3, ks = 2 * g + h;
                 uint32_t a0, a1, a2, a3;
                 switch (g) {  // compile-time after unrolling
-                    case 0: a0 = unpack_pair<0>(wa[h], cm); a1 = unpack_pair<0>(wb[h], cm);
-                            a2 = unpack_pair<0>(wa8[h], cm); a3 = unpack_pair<0>(wb8[h], cm); break;
-                    case 1: a0 = unpack_pair<2>(wa[h], cm); a1 = unpack_pair<2>(wb[h], cm);
-                            a2 = unpack_pair<2>(wa8[h], cm); a3 = unpack_pair<2>(wb8[h], cm); break;
-                    case 2: a0 = unpack_pair<4>(wa[h], cm); a1 = unpack_pair<4>(wb[h], cm);
-                            a2 = unpack_pair<4>(wa8[h], cm); a3 = unpack_pair<4>(wb8[h], cm); break;
-                    default: a0 = unpack_pair<6>(wa[h], cm); a1 = unpack_pair<6>(wb[h], cm);
-                             a2 = unpack_pair<6>(wa8[h], cm); a3 = unpack_pair<6>(wb8[h], cm); break;
+                    case 0: a0 = unpack_pair<0, 0>(wa[h], cm); a1 = unpack_pair<0, 0>(wb[h], cm);
+                            a2 = unpack_pair<0, 0>(wa8[h], cm); a3 = unpack_pair<0, 0>(wb8[h], cm); break;
+                    case 1: a0 = unpack_pair<2, 2>(wa[h], cm); a1 = unpack_pair<2, 2>(wb[h], cm);
+                            a2 = unpack_pair<2, 2>(wa8[h], cm); a3 = unpack_pair<2, 2>(wb8[h], cm); break;
+                    case 2: a0 = unpack_pair<4, 4>(wa[h], cm); a1 = unpack_pair<4, 4>(wb[h], cm);
+                            a2 = unpack_pair<4, 4>(wa8[h], cm); a3 = unpack_pair<4, 4>(wb8[h], cm); break;
+                    default: a0 = unpack_pair<6, 4>(wa[h], cm); a1 = unpack_pair<6, 4>(wb[h], cm);
+                             a2 = unpack_pair<6, 4>(wa8[h], cm); a3 = unpack_pair<6, 4>(wb8[h], cm); break;
                 }
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
@@ -450,8 +456,8 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
                     xb = fmaf(sb[g], acc[g][nt][2] + acc[g][nt][3], xb);
                     xb = fmaf(zb[g], qg[g], xb);
                 }
-                la[nt] = va ? xa : -INFINITY;
-                lb[nt] = vb ? xb : -INFINITY;
+                la[nt] = (full_tile || va) ? xa : -INFINITY;
+                lb[nt] = (full_tile || vb) ? xb : -INFINITY;
             }
         }
 
@@ -520,14 +526,14 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
                     const uint32_t r08 = pw8[2 * half], r18 = pw8[2 * half + 1];
                     uint32_t a0, a1, a2, a3;
                     switch (g) {
-                        case 0: a0 = unpack_pair<0>(r0, cm); a1 = unpack_pair<0>(r1, cm);
-                                a2 = unpack_pair<0>(r08, cm); a3 = unpack_pair<0>(r18, cm); break;
-                        case 1: a0 = unpack_pair<2>(r0, cm); a1 = unpack_pair<2>(r1, cm);
-                                a2 = unpack_pair<2>(r08, cm); a3 = unpack_pair<2>(r18, cm); break;
-                        case 2: a0 = unpack_pair<4>(r0, cm); a1 = unpack_pair<4>(r1, cm);
-                                a2 = unpack_pair<4>(r08, cm); a3 = unpack_pair<4>(r18, cm); break;
-                        default: a0 = unpack_pair<6>(r0, cm); a1 = unpack_pair<6>(r1, cm);
-                                 a2 = unpack_pair<6>(r08, cm); a3 = unpack_pair<6>(r18, cm); break;
+                        case 0: a0 = unpack_pair<0, 2>(r0, cm); a1 = unpack_pair<0, 2>(r1, cm);
+                                a2 = unpack_pair<0, 2>(r08, cm); a3 = unpack_pair<0, 2>(r18, cm); break;
+                        case 1: a0 = unpack_pair<2, 2>(r0, cm); a1 = unpack_pair<2, 2>(r1, cm);
+                                a2 = unpack_pair<2, 2>(r08, cm); a3 = unpack_pair<2, 2>(r18, cm); break;
+                        case 2: a0 = unpack_pair<4, 4>(r0, cm); a1 = unpack_pair<4, 4>(r1, cm);
+                                a2 = unpack_pair<4, 4>(r08, cm); a3 = unpack_pair<4, 4>(r18, cm); break;
+                        default: a0 = unpack_pair<6, 4>(r0, cm); a1 = unpack_pair<6, 4>(r1, cm);
+                                 a2 = unpack_pair<6, 4>(r08, cm); a3 = unpack_pair<6, 4>(r18, cm); break;
                     }
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt)

@@ -76,44 +76,54 @@ __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
 
 __device__ __forceinline__ uint32_t rotr(uint32_t x, uint32_t n) { return __funnelshift_r(x, x, n); }
 
-// Multipliers that move a code pair to bits 4-5 / 20-21 with an integer
-// multiply-add: x16 (from bits 0-1), x4 (bits 2-3), high word of x 2^30
-// (bits 6-7).  Held in registers made opaque by a warp shuffle, so the
-// compiler keeps them as multiply-adds (FMA pipe) instead of shifts (ALU
-// pipe) or per-use constant loads.
+// Code pairs -> bf16x2 MMA operands.  A code pair sits at bits (P, P+16) of
+// a 32-bit word (P = 2 * group in bytes 0/2; bytes 1/3 are first shifted
+// down by 8).  Placed in bf16 mantissa bits T..T+1 under the exponent of
+// M = 2^(7-T), a code c reads as the exact value M + c, so a group whose
+// codes already sit at T = P in {0, 2, 4} needs a single logic op; the
+// offset M is removed afterwards with the zero point (z - M s).  Pairs at
+// P = 6 are moved to T = 4 by the high word of a multiply by 2^30, and
+// pairs at P = 0 to T = 2 by a multiply by 4.  K may use M = 128 (its
+// accumulator restarts every 16 tokens) while V keeps M <= 32 (its
+// accumulators run over a whole split).  The multipliers are held in
+// registers made opaque by a warp shuffle, so the compiler keeps them as
+// integer multiply-adds (FMA pipe) instead of shifts or constant loads.
 struct CodeMul {
-    uint32_t m16, m4, mh30;
+    uint32_t m4, mh30;
 };
 
 __device__ __forceinline__ CodeMul code_mul_regs(const uint32_t* mul_param) {
     CodeMul c;
-    c.m16 = __shfl_sync(kFull, mul_param[0], 0);
     c.m4 = __shfl_sync(kFull, mul_param[1], 0);
     c.mh30 = __shfl_sync(kFull, mul_param[3], 0);
     return c;
 }
 
-// Codes at bits (P, P+16) of x, P in {0, 2, 4, 6} -> bf16x2 (8 + c_lo,
-// 8 + c_hi): one logic op (mask) and, unless P == 4, one integer
-// multiply-add that moves the pair to bits 4-5 / 20-21 and adds the bf16
-// exponent bits of 8.0.  Codes in bytes 1 and 3 are first shifted down by 8.
-template <int P>
+// bf16 exponent bits of M = 2^(7-T) in both halves
+template <int T>
+struct Magic {
+    static constexpr uint32_t bits = T == 0 ? 0x43004300u : (T == 2 ? 0x42004200u : 0x41004100u);
+};
+
+// pair at bits (P, P+16) -> bf16x2 (M + c_lo, M + c_hi), M = 2^(7-T)
+template <int P, int T>
 __device__ __forceinline__ uint32_t unpack_pair(uint32_t x, const CodeMul& m) {
     constexpr uint32_t kMask = 0x00030003u << P;
-    if constexpr (P == 4) {
-        return lop3_and_or(x, kMask, 0x41004100u);
+    uint32_t r;
+    if constexpr (P == T) {
+        r = lop3_and_or(x, kMask, Magic<T>::bits);
+    } else if constexpr (P == 0 && T == 2) {
+        asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(r) : "r"(x & kMask), "r"(m.m4), "r"(Magic<T>::bits));
     } else {
-        const uint32_t v = x & kMask;
-        uint32_t r;
-        if constexpr (P == 0)
-            asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(r) : "r"(v), "r"(m.m16), "r"(0x41004100u));
-        else if constexpr (P == 2)
-            asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(r) : "r"(v), "r"(m.m4), "r"(0x41004100u));
-        else
-            asm("mad.hi.u32 %0, %1, %2, %3;" : "=r"(r) : "r"(v), "r"(m.mh30), "r"(0x41004100u));
-        return r;
+        static_assert(P == 6 && T == 4, "unsupported code move");
+        asm("mad.hi.u32 %0, %1, %2, %3;" : "=r"(r) : "r"(x & kMask), "r"(m.mh30), "r"(Magic<T>::bits));
     }
+    return r;
 }
+
+// offsets M per group: K (accumulator restarted per tile) and V
+__device__ __forceinline__ constexpr float k_magic(int g) { return g == 0 ? 128.f : (g == 1 ? 32.f : 8.f); }
+__device__ __forceinline__ constexpr float v_magic(int g) { return g <= 1 ? 32.f : 8.f; }
 
 // ---- packed fp32x2 arithmetic (two lanes of fp32 per instruction) --------
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
