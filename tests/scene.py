@@ -31,18 +31,25 @@ class Scene:
 
 def make_scene(w: S.Workload, ctx: np.ndarray | None = None, hq: int | None = None, hk: int | None = None,
                extra_capacity: int = 64, perm_seed: int = 0, prefix_group=None, shared_hist_tokens: int = 0,
-               orc: oracle.Oracle | None = None, quant_group: int = S.GROUP) -> Scene:
+               orc: oracle.Oracle | None = None, quant_group: int = S.GROUP, only_kv: int | None = None) -> Scene:
     """Build a decode state: sink = first 64 tokens, recent ring = last 256,
-    history = the rest (quantised by the oracle)."""
+    history = the rest (quantised by the oracle).  With only_kv, the draws
+    are those of the full head layout, but only KV head only_kv (and its G
+    query heads) is kept: a one-KV-head scene of that unit."""
     orc = orc or oracle.get()
     hq = hq or w.hq
     hk = hk or w.hk
     ctx = S.context_lengths(w) if ctx is None else np.asarray(ctx, np.int32)
     B = ctx.shape[0]
-    shape = oracle.Shape(S.D, quant_group, S.SINK, S.RECENT, S.PAGE, hq, hk)
     wl = dataclasses.replace(w, hq=hq, hk=hk, batch=B)
     rng = S.rng_for(wl, 7)
     prof = S.channel_profile(wl)
+    G = hq // hk
+    keep = slice(None) if only_kv is None else slice(only_kv, only_kv + 1)
+    keep_q = slice(None) if only_kv is None else slice(only_kv * G, (only_kv + 1) * G)
+    if only_kv is not None:
+        hq, hk = G, 1
+    shape = oracle.Shape(S.D, quant_group, S.SINK, S.RECENT, S.PAGE, hq, hk)
     hist = np.maximum(ctx - S.NSLOT, 0).astype(np.int32)
     bf16_len = np.minimum(ctx, S.NSLOT).astype(np.int32)
     cap = hist + extra_capacity
@@ -51,13 +58,14 @@ def make_scene(w: S.Workload, ctx: np.ndarray | None = None, hq: int | None = No
                                                 max_pages)
     assert rc == 0, rc
     pool = np.zeros(max(nbytes, 16), np.uint8)
-    U = S.rotation_U(wl).astype(np.float32)
+    U = S.rotation_U(wl).astype(np.float32)[keep]
     clip = S.clip_ratios(wl)
     bf16_kv = np.zeros((B, S.NSLOT, hk, 2, S.D), np.uint16)
+    clip_keep = clip[keep]
     ring_head = np.zeros(B, np.int32)
     prefix_toks = {}
     for b in range(B):
-        toks = S.kv_tokens(wl, int(ctx[b]), rng, prof)
+        toks = S.kv_tokens(wl, int(ctx[b]), rng, prof)[:, keep]
         if prefix_group is not None and prefix_group[b] >= 0:
             # sharers see identical sink + shared-history tokens
             n_pre = S.SINK + shared_hist_tokens
@@ -81,12 +89,13 @@ def make_scene(w: S.Workload, ctx: np.ndarray | None = None, hq: int | None = No
                         pos = pos[pos >= shared_hist_tokens]
                 if pos.size:
                     orc.evict(shape, toks[S.SINK:S.SINK + h], np.full(pos.size, b, np.int32), pos,
-                              U.astype(np.float64), clip, pool, table, max_pages,
+                              U.astype(np.float64), clip_keep, pool, table, max_pages,
                               src_row=pos)
-    q = S.queries(wl, rng, B)
-    new_kv = S.kv_tokens(wl, B, rng, prof)
-    return Scene(shape, hist, bf16_len, ring_head, q, bf16_kv, pool, table, max_pages, U.astype(np.float64),
-                 U, clip, new_kv, 1.0 / np.sqrt(S.D))
+    q = S.queries(wl, rng, B)[:, keep_q]
+    new_kv = S.kv_tokens(wl, B, rng, prof)[:, keep]
+    return Scene(shape, hist, bf16_len, ring_head, np.ascontiguousarray(q), bf16_kv, pool, table, max_pages,
+                 U.astype(np.float64), np.ascontiguousarray(U), clip[keep], np.ascontiguousarray(new_kv),
+                 1.0 / np.sqrt(S.D))
 
 
 def oracle_step(orc: oracle.Oracle, sc: Scene):
