@@ -52,6 +52,8 @@ def parse_args():
     ap.add_argument("--layers", type=int, default=None, help="override the layer count (testing)")
     ap.add_argument("--cpu-tokens", type=int, default=60000,
                     help="history tokens in the oracle's bounded sample")
+    ap.add_argument("--cpu-steps", type=int, default=12,
+                    help="oracle steps timed for cpu_baseline (about 10 s of host work)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -96,6 +98,22 @@ def barrier(world: int):
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
+
+
+def aggregate(t_ms: float, units: float, world: int, device=None):
+    """Whole-job throughput of a weak-scaling replica run: the slowest
+    rank's time (max over ranks) and the units all ranks processed (sum).
+    Returns (value in units/s, max time in ms)."""
+    t_max = reduce_max(t_ms, world, device)
+    total = reduce_sum(float(units), world, device)
+    return total / (t_max / 1e3), t_max
+
+
+def reference_budget(args) -> int:
+    """History tokens of the oracle's sample per reference-arm step: about
+    six million attended tokens over the whole --steps/--warmup run (a few
+    minutes on the host cores), at most --cpu-tokens, at least 8000."""
+    return int(min(args.cpu_tokens, max(8000, 6e6 / max(1, args.steps + args.warmup))))
 
 
 # ---------------------------------------------------------------------------
@@ -364,7 +382,7 @@ def run_reference(args, rank: int, world: int) -> None:
     if rank != 0:
         return
     w = S.WORKLOADS[args.workload]
-    samp = OracleSample(w, args.cpu_tokens)
+    samp = OracleSample(w, reference_budget(args))
     tps, dt = samp.time(args.steps, args.warmup)
     ms = dt / args.steps * 1e3
     line = {
@@ -438,11 +456,9 @@ def run_oscar(args, rank: int, world: int, local: int) -> None:
     t_ms = start.elapsed_time(stop)
     int2_ms = [a.elapsed_time(b) for a, b in evs]
 
-    t_ms_max = reduce_max(t_ms, world, dev)
-    ms_per_step = t_ms_max / K
     att = sum(st.attended_tokens(W + k) for k in range(K)) * L
-    att_all = reduce_sum(float(att), world, dev)
-    value = att_all / (t_ms_max / 1e3)
+    value, t_ms_max = aggregate(t_ms, att, world, dev)
+    ms_per_step = t_ms_max / K
     step_bytes = sum(st.step_bytes(W + k) for k in range(K)) * L / K
     hist_bytes = [st.hist_tokens_after(W + k) * st.Hk * HIST_BYTES_PER_TOKEN_HEAD for k in range(K)]
     int2_avg_ms = statistics.mean(int2_ms)
@@ -474,19 +490,19 @@ def run_oscar(args, rank: int, world: int, local: int) -> None:
                 ho[layer].copy_(lay["out"], non_blocking=True)
         e1.record(stream)
         torch.cuda.synchronize()
-        e_ms = reduce_max(e0.elapsed_time(e1), world, dev)
-        e_att = reduce_sum(float(sum(st.attended_tokens(W + K + k) for k in range(e2e_steps)) * L), world, dev)
+        e_att = sum(st.attended_tokens(W + K + k) for k in range(e2e_steps)) * L
+        e_value, e_ms = aggregate(e0.elapsed_time(e1), e_att, world, dev)
         h2d = L * (st.layers[0]["q"].numel() * 2 + st.layers[0]["new_kv"].numel() * 2)
         d2h = L * st.layers[0]["out"].numel() * 4
-        e2e = {"value": e_att / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+        e2e = {"value": e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e_ms / e2e_steps}
 
     cpu = None
     if rank == 0 and not args.no_cpu:
         samp = OracleSample(w, args.cpu_tokens)
-        tps, dt = samp.time(1, 0)
-        cpu = {"value": tps, "unit": UNIT, "cores": samp.threads, "kind": "oracle", "sample": samp.describe(),
-               "seconds": dt, "cpu": cpu_info()}
+        tps, dt = samp.time(args.cpu_steps, 0)
+        cpu = {"value": tps, "unit": UNIT, "cores": samp.threads, "kind": "oracle",
+               "sample": f"{args.cpu_steps} steps of " + samp.describe(), "seconds": dt, "cpu": cpu_info()}
 
     if rank == 0:
         line = {
