@@ -41,6 +41,34 @@ HIST_BYTES_PER_TOKEN_HEAD = 96      # 2 x 32 B codes + 2 x 4 x (fp16 s, fp16 z)
 BF16_BYTES_PER_TOKEN_HEAD = 2 * 128 * 2
 DEFAULT_WORKLOAD = "qwen3_8b_36l"
 
+# DRAM traffic of int2_kernel from one ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum of one launch; the capture's summary and command are
+# in profiles/int2_kernel_qwen3_8b_1layer.md), with the algorithmic bytes of
+# the captured launch.  Reported, scaled to the bench's mean launch by the
+# units processed, only while the kernel source is the one captured.
+INT2_TRAFFIC_CAPTURE = {
+    "workload": "qwen3_8b_36l",
+    "source_sha256_16": "06329dd8b3d11df1",     # csrc/decode.cu + csrc/oscar_common.cuh
+    "traffic_bytes": 913.93e6 + 12.18e6,
+    "algorithmic_bytes": 911.11e6,
+}
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("decode.cu", "oscar_common.cuh"):
+        with open(os.path.join(ROOT, "bit_kv_cache_evict_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def int2_traffic(workload: str, int2_bytes: float):
+    cap = INT2_TRAFFIC_CAPTURE
+    if workload != cap["workload"] or kernel_source_hash() != cap["source_sha256_16"]:
+        return None
+    return int2_bytes * cap["traffic_bytes"] / cap["algorithmic_bytes"]
+
 
 def parse_args():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
@@ -286,6 +314,21 @@ class GpuState:
     def attended_tokens(self, s: int) -> int:
         return self.hist_tokens_after(s) + self.B * S.NSLOT
 
+    def bits_per_element(self, s: int) -> dict:
+        """Stored bits per K/V element after step s: the INT2 history alone,
+        and over every token of every sequence (BF16 sink + recent included),
+        with shared prefix pages counted per sequence and once."""
+        hist = self.hist0 + s + 1
+        elems = float((hist + S.NSLOT).sum()) * 2 * S.D
+        hist_bits = float(hist.sum()) * HIST_BYTES_PER_TOKEN_HEAD * 8
+        bf16_bits = float(self.B * S.NSLOT) * BF16_BYTES_PER_TOKEN_HEAD * 8
+        out = {"int2_history": HIST_BYTES_PER_TOKEN_HEAD * 8 / (2 * S.D),
+               "all_tokens": (hist_bits + bf16_bits) / elems}
+        if self.w.prefix_seqs:
+            dup = (self.w.prefix_seqs - 1) * self.w.shared_hist_tokens * HIST_BYTES_PER_TOKEN_HEAD * 8
+            out["all_tokens_shared_pages_once"] = (hist_bits - dup + bf16_bits) / elems
+        return out
+
     def step_bytes(self, s: int) -> float:
         hist = self.hist_tokens_after(s) * self.Hk * HIST_BYTES_PER_TOKEN_HEAD
         bf16 = self.B * S.NSLOT * self.Hk * BF16_BYTES_PER_TOKEN_HEAD
@@ -511,10 +554,12 @@ def run_oscar(args, rank: int, world: int, local: int) -> None:
             "dtype": "int2 codes x bf16 hi/lo on tensor cores, fp32 accumulate", "data": "synthetic",
             "config": config_of(w, L),
             "decode_tokens_per_s": world * w.batch * K / (t_ms_max / 1e3),
+            "bits_per_element": st.bits_per_element(W + K - 1),
             "step_algorithmic_gbs": step_bytes / (ms_per_step * 1e-3) / 1e9,
             "roofline": {"kernel": "int2_kernel (split-K INT2 history attention)", "bound": "hbm",
                          "achieved": achieved, "peak": peaks["hbm_gbs"], "peak_source": peaks["source"],
-                         "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                         "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                         "traffic": int2_traffic(w.name, int2_bytes),
                          "bytes_per_launch": int2_bytes, "launch_ms": int2_avg_ms,
                          "share_of_step": sum(int2_ms) / t_ms},
             "cpu_baseline": cpu, "e2e": e2e,
