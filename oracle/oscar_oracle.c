@@ -13,7 +13,7 @@
  * Sources (page title, then section):
  *   [NEWS]  "卓绝TurboQuant：Together AI把2-bit KV Cache推向实在行状"
  *           (www.sanyangsrq.com news article on OSCAR; the text is a
- *           synonym-spun copy, decoded where quoted below).
+ *           synonym-spun copy of a Chinese write-up).
  *           sec. A = "不是更会'压缩向量'，而是运转保护 attention"
  *           sec. B = "OSCAR 把旋转瞄准 attention" (rotation formula)
  *           sec. C = figure "从离线校准到在线推理的 pipeline" and the
@@ -29,8 +29,8 @@
  * zero = clipped minimum and scale = (max-min)/3; codes from the stored
  * fp16 scale/zero with round-half-even; all-zero codes when the fp16 scale
  * is 0; four codes per byte, byte j holding stored positions j, j + d/4,
- * j + 2d/4, j + 3d/4 in bits 0-1, 2-3, 4-5, 6-7 (the pages fix only "four
- * codes per byte"; with d = 128 and g = 32 a byte then holds in-group index
+ * j + 2d/4, j + 3d/4 in bits 0-1, 2-3, 4-5, 6-7 (the pages fix only that
+ * four codes share a byte; with d = 128 and g = 32 a byte then holds in-group index
  * j of each of the four groups); attention with the softmax scale given by
  * the caller.
  *
@@ -171,8 +171,8 @@ double oracle_f64_from_bf16(uint16_t b) {
     return (double)f;
 }
 
-/* Four 2-bit codes per byte ([NEWS] sec. C, "every four 2-bit values are
- * packed into one byte"); code i in bits 2i..2i+1. */
+/* Four 2-bit codes share one byte ([NEWS] sec. C, the storage note under
+ * the pipeline figure); code i in bits 2i..2i+1. */
 uint8_t oracle_pack4(const uint8_t* c) {
     return (uint8_t)((c[0] & 3u) | ((c[1] & 3u) << 2) | ((c[2] & 3u) << 4) | ((c[3] & 3u) << 6));
 }
