@@ -183,18 +183,23 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(DecodeParams p) {
 // ---------------------------------------------------------------------------
 // Block = 4 consumer warps + 1 producer warp.  The producer takes split-K
 // items from a global counter and streams their 6 KB page blocks into a
-// ring of shared-memory stages with bulk async copies (one copy per page,
-// completion on a "full" mbarrier); consumer warp w attends over the 16
-// tokens [16w, 16w+16) of every page, and releases the stage on an "empty"
-// mbarrier.  At the last page of an item the four warps merge their
-// partial softmax states in shared memory and write one partial per item.
-// Every wait is bounded; on a timeout the block reports
-// OSCAR_STATUS_TIMEOUT, lets its copies land and exits.
-constexpr int kStages = 4;
-constexpr int kWaitPolls = 1 << 22;
+// ring of 8 shared-memory stages with bulk async copies (completion on a
+// "full" mbarrier).  Ring slot n goes to consumer warp n % 4, so each warp
+// owns two stages and attends over whole 64-token pages: the pages of an
+// item are dealt round-robin to the four warps (an item's slot count is
+// padded to a multiple of four with empty slots, so that every warp sees
+// every item).  Per page a warp converts the page's scales, computes the
+// logits of its four 16-token tiles, updates its softmax state once, and
+// runs the P.V products; it then releases the stage on an "empty"
+// mbarrier.  At an item's end the four warps merge their partial states in
+// shared memory and write one partial per item.  Every wait is bounded; on a
+// timeout the block reports OSCAR_STATUS_TIMEOUT, lets its copies land and
+// exits.
 constexpr int kConsumerWarps = 4;
+constexpr int kStages = 2 * kConsumerWarps;
+constexpr int kWaitPolls = 1 << 22;
 constexpr int kInt2Threads = (kConsumerWarps + 1) * 32;
-constexpr int kFlagFirst = 1, kFlagLast = 2;
+constexpr int kFlagFirst = 1, kFlagLast = 2, kFlagPad = 4;
 
 struct StageInfo {
     int item, b, kv, valid_flags;  // valid tokens in bits 0-7, flags above
@@ -203,13 +208,19 @@ struct StageInfo {
 template <int NT>
 struct Int2Smem {
     static constexpr int G4 = NT * 4;  // head columns (padded to 4 per n-tile)
+    // per-warp scratch: K s [64] float4 | K z-M s [64] float4 | V z-M s [64]
+    // float4 | V s [4][64] float (token order pv_slot within 16-token tiles)
+    // | P [G4][64] float (same token order).  Reused at an item's end for
+    // the warp's (o', m, l) state [G4][kD + 2].
+    static constexpr int kWKs = 0, kWKz = 1024, kWVz = 2048, kWVs = 3072, kWP = 4096;
+    static constexpr int kWarpBytes0 = kWP + G4 * 64 * 4;
+    static constexpr int kMergeBytes = G4 * (kD + 2) * 4;
+    static constexpr int kWarpBytes = kWarpBytes0 > kMergeBytes ? kWarpBytes0 : kMergeBytes;
     static constexpr int kStage = 0;
     static constexpr int kInfo = kStage + kStages * kBlock;
     static constexpr int kBars = kInfo + kStages * (int)sizeof(StageInfo);
-    static constexpr int kScale = kBars + 2 * kStages * 8 + 16;            // [warp][64] float4, see consumer
-    static constexpr int kP = kScale + kConsumerWarps * 2 * 2 * 16 * 16;    // [warp][G4][16] float
-    static constexpr int kMerge = kP + kConsumerWarps * G4 * 16 * 4;        // [warp][G4][kD + 2] float
-    static constexpr int kBytes = kMerge + kConsumerWarps * G4 * (kD + 2) * 4;
+    static constexpr int kWarp = kBars + (2 * kStages + 2) * 8;
+    static constexpr int kBytes = kWarp + kConsumerWarps * kWarpBytes;
 };
 
 __device__ __forceinline__ int find_seq(const int32_t* item_start, int B, int item) {
@@ -222,6 +233,29 @@ __device__ __forceinline__ int find_seq(const int32_t* item_start, int B, int it
     return lo;
 }
 
+// A-operand registers of one K k-step (group g, word half h) from the
+// token-row words of rows gID and gID + 8 (w*) and their >> 8 copies (w*8).
+template <int G>
+__device__ __forceinline__ void k_operands(uint32_t wa, uint32_t wb, uint32_t wa8, uint32_t wb8, const CodeMul& cm,
+                                           uint32_t& a0, uint32_t& a1, uint32_t& a2, uint32_t& a3) {
+    constexpr int P = 2 * G, T = (G == 3) ? 4 : 2 * G;
+    a0 = unpack_pair<P, T>(wa, cm);
+    a1 = unpack_pair<P, T>(wb, cm);
+    a2 = unpack_pair<P, T>(wa8, cm);
+    a3 = unpack_pair<P, T>(wb8, cm);
+}
+
+// A-operand registers of one V m-tile half (group g): plane words r0, r1 and
+// their >> 8 copies.
+template <int G>
+__device__ __forceinline__ void v_operands(uint32_t r0, uint32_t r1, uint32_t r08, uint32_t r18, const CodeMul& cm,
+                                           uint32_t& a0, uint32_t& a1, uint32_t& a2, uint32_t& a3) {
+    constexpr int P = 2 * G, T = (G == 0) ? 2 : ((G == 3) ? 4 : 2 * G);
+    a0 = unpack_pair<P, T>(r0, cm);
+    a1 = unpack_pair<P, T>(r1, cm);
+    a2 = unpack_pair<P, T>(r08, cm);
+    a3 = unpack_pair<P, T>(r18, cm);
+}
 
 template <int NT>
 __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(DecodeParams p) {
@@ -237,7 +271,7 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kConsumerWarps);
+            mbar_init(&empty[s], 1);
         }
         mbar_init(merge_bar, kConsumerWarps);
         fence_mbar_init();
@@ -247,66 +281,68 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
     if (warp == kConsumerWarps) {
         // ------------------------------ producer ------------------------------
         const int total = __ldg(p.item_start + p.B);
-        uint32_t n = 0;      // pages issued so far (stage = n % kStages)
+        uint32_t n = 0;      // slots issued so far (stage n % kStages, warp n % 4)
         bool ok = true;
+        // one slot: wait for the stage, then publish its info (and copy)
+        auto post = [&](int item, int b, int kv, int pid, int valid, int flags) -> bool {
+            const uint32_t s = n % kStages;
+            if (n >= (uint32_t)kStages) {
+                const bool w = mbar_wait_bounded(&empty[s], ((n / kStages) - 1) & 1u, kWaitPolls);
+                if (!__all_sync(kFull, w)) return false;
+            }
+            if (lane == 0) {
+                StageInfo& si = info[s];
+                si.item = item;
+                si.b = b;
+                si.kv = kv;
+                if (item >= 0 && !(flags & kFlagPad) && (pid < 0 || pid >= p.num_pages)) {
+                    report(p.status, OSCAR_STATUS_BAD_PAGE);
+                    flags |= kFlagPad;
+                }
+                si.valid_flags = valid | (flags << 8);
+                if (item < 0 || (flags & kFlagPad)) {
+                    mbar_arrive(&full[s]);
+                } else {
+                    mbar_arrive_expect_tx(&full[s], kBlock);
+                    bulk_g2s(stages + s * kBlock, p.pool + ((size_t)pid * p.hk + kv) * kBlock, kBlock, &full[s]);
+                }
+            }
+            __syncwarp();
+            ++n;
+            return true;
+        };
         for (;;) {
             int item = 0;
             if (lane == 0) item = atomicAdd(p.counter, 1);
             item = __shfl_sync(kFull, item, 0);
-            const bool last_item = item >= total;
-            int b = 0, kv = 0, pg0 = 0, npg = 1, hist = 0;
-            if (!last_item) {
-                b = find_seq(p.item_start, p.B, item);
-                const int s0 = __ldg(p.item_start + b);
-                const int splits = (__ldg(p.item_start + b + 1) - s0) / p.hk;
-                kv = (item - s0) / splits;
-                const int split = (item - s0) % splits;
-                hist = min(max(__ldg(p.hist_len + b), 0), p.max_pages * kPage);
-                pg0 = split * p.pps;
-                npg = min(p.pps, (hist + kPage - 1) / kPage - pg0);
+            if (item >= total) {  // one end marker per consumer warp
+                for (int i = 0; i < kConsumerWarps && ok; ++i) ok = post(-1, 0, 0, 0, 0, 0);
+                break;
             }
-            for (int c = 0; c < npg; c += 32) {
-                // page ids of the next 32 pages, one per lane
+            const int b = find_seq(p.item_start, p.B, item);
+            const int s0 = __ldg(p.item_start + b);
+            const int splits = (__ldg(p.item_start + b + 1) - s0) / p.hk;
+            const int kv = (item - s0) / splits;
+            const int split = (item - s0) % splits;
+            const int hist = min(max(__ldg(p.hist_len + b), 0), p.max_pages * kPage);
+            const int pg0 = split * p.pps;
+            const int npg = min(p.pps, (hist + kPage - 1) / kPage - pg0);
+            const int nslots = (npg + kConsumerWarps - 1) / kConsumerWarps * kConsumerWarps;
+            for (int c = 0; c < nslots && ok; c += 32) {
+                // page ids of the next 32 slots, one per lane
                 int pid = -1;
-                if (!last_item && c + lane < npg) pid = __ldg(p.page_table + (size_t)b * p.max_pages + pg0 + c + lane);
-                const int cnt = last_item ? 1 : min(32, npg - c);
-                for (int i = 0; i < cnt; ++i) {
+                if (c + lane < npg) pid = __ldg(p.page_table + (size_t)b * p.max_pages + pg0 + c + lane);
+                const int cnt = min(32, nslots - c);
+                for (int i = 0; i < cnt && ok; ++i) {
+                    const int pl = c + i;
                     const int pi = __shfl_sync(kFull, pid, i);
-                    const uint32_t s = n % kStages;
-                    if (n >= (uint32_t)kStages) {
-                        const bool w = mbar_wait_bounded(&empty[s], ((n / kStages) - 1) & 1u, kWaitPolls);
-                        ok = __all_sync(kFull, w);
-                        if (!ok) break;
-                    }
-                    if (lane == 0) {
-                        StageInfo& si = info[s];
-                        if (last_item) {
-                            si.item = -1;
-                            mbar_arrive(&full[s]);
-                        } else {
-                            const int pl = c + i;
-                            si.item = item;
-                            si.b = b;
-                            si.kv = kv;
-                            const int flags = (pl == 0 ? kFlagFirst : 0) | (pl == npg - 1 ? kFlagLast : 0);
-                            if (pi < 0 || pi >= p.num_pages) {
-                                report(p.status, OSCAR_STATUS_BAD_PAGE);
-                                si.valid_flags = flags << 8;
-                                mbar_arrive(&full[s]);
-                            } else {
-                                si.valid_flags = min(kPage, hist - (pg0 + pl) * kPage) | (flags << 8);
-                                mbar_arrive_expect_tx(&full[s], kBlock);
-                                bulk_g2s(stages + s * kBlock, p.pool + ((size_t)pi * p.hk + kv) * kBlock, kBlock,
-                                         &full[s]);
-                            }
-                        }
-                    }
-                    __syncwarp();
-                    ++n;
+                    const int flags = (pl < kConsumerWarps ? kFlagFirst : 0) |
+                                      (pl >= nslots - kConsumerWarps ? kFlagLast : 0) | (pl >= npg ? kFlagPad : 0);
+                    const int valid = pl < npg ? min(kPage, hist - (pg0 + pl) * kPage) : 0;
+                    ok = post(item, b, kv, pi, valid, flags);
                 }
-                if (!ok) break;
             }
-            if (!ok || last_item) break;
+            if (!ok) break;
         }
         if (!ok) {
             if (lane == 0) report(p.status, OSCAR_STATUS_TIMEOUT);
@@ -320,10 +356,12 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
 
     // ------------------------------- consumers ---------------------------------
     const int gID = lane >> 2, tq = lane & 3;
-    const int tb = 16 * warp;  // this warp's token tile inside each page
-    float4* scS = reinterpret_cast<float4*>(smem + SM::kScale) + warp * 64;   // [K|V][s|zz][16]
-    float* pbuf = reinterpret_cast<float*>(smem + SM::kP) + warp * SM::G4 * 16;
-    float* mrg = reinterpret_cast<float*>(smem + SM::kMerge);
+    uint8_t* wbuf = smem + SM::kWarp + warp * SM::kWarpBytes;
+    float4* ksS = reinterpret_cast<float4*>(wbuf + SM::kWKs);   // [64] K s
+    float4* kzS = reinterpret_cast<float4*>(wbuf + SM::kWKz);   // [64] K z - M s
+    float4* vzS = reinterpret_cast<float4*>(wbuf + SM::kWVz);   // [64] V z - M s
+    float* vsS = reinterpret_cast<float*>(wbuf + SM::kWVs);     // [4][64] V s
+    float* pS = reinterpret_cast<float*>(wbuf + SM::kWP);       // [G4][64] P
     const float2 take_lo = (gID & 1) ? make_float2(1.f, 1.f) : make_float2(0.f, 0.f);  // PV column: hi / lo
     const CodeMul cm = code_mul_regs(p.code_mul);
 
@@ -342,7 +380,7 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
     float4 qsv[NT];
     float m_run[NT], l_run[NT], zacc[NT][4], acc_o[NT][8][4];
 
-    for (uint32_t n = 0;; ++n) {
+    for (uint32_t n = warp;; n += kConsumerWarps) {
         const uint32_t s = n % kStages;
         const bool w = mbar_wait_bounded(&full[s], (n / kStages) & 1u, kWaitPolls);
         if (!__all_sync(kFull, w)) {
@@ -351,13 +389,11 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
         }
         const int4 sraw = *reinterpret_cast<const int4*>(&info[s]);
         if (sraw.x < 0) break;
-        struct {
-            int item, b, kv, valid, flags;
-        } si{sraw.x, sraw.y, sraw.z, sraw.w & 0xff, sraw.w >> 8};
+        const int item = sraw.x, flags = sraw.w >> 8, valid = sraw.w & 0xff;
         const uint8_t* blk = stages + s * kBlock;
 
-        if (si.flags & kFlagFirst) {
-            const int bk = si.b * p.hk + si.kv;
+        if (flags & kFlagFirst) {
+            const int bk = sraw.y * p.hk + sraw.z;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 const uint32_t* fr = p.qfrag + ((size_t)bk * NT + nt) * 8 * 32 * 2;
@@ -379,94 +415,105 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
             }
         }
 
-        // -- scales of this tile: fp16 (s, z) -> fp32 (s, z - M_g s); zero when masked
-        const bool full_tile = tb + 16 <= si.valid;  // warp-uniform
-        {
-            const int t = lane & 15, which = lane >> 4;
-            const uint4 raw = *reinterpret_cast<const uint4*>(blk + (which ? kVScale : kKScale) + (tb + t) * 16);
-            const uint32_t r[4] = {raw.x, raw.y, raw.z, raw.w};
-            float sv[4], zz[4];
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {  // z - M_g s with the group's code offset M_g
-                sv[g] = half_lo(r[g]);
-                zz[g] = fmaf(which ? -v_magic(g) : -k_magic(g), sv[g], half_hi(r[g]));
-            }
-            if (!full_tile && tb + t >= si.valid) {
-#pragma unroll
-                for (int g = 0; g < 4; ++g) sv[g] = zz[g] = 0.f;
-            }
-            // K: s at [t], zz at [16 + t]; V: zz at [48 + t], s transposed to
-            // [32 + g*4 ..] as floats [g][pv_slot(t)]
-            if (which == 0) scS[t] = make_float4(sv[0], sv[1], sv[2], sv[3]);
-            scS[which * 32 + 16 + t] = make_float4(zz[0], zz[1], zz[2], zz[3]);
-            if (which == 1) {
-                float* vs = reinterpret_cast<float*>(scS + 32);
-#pragma unroll
-                for (int g = 0; g < 4; ++g) vs[g * 16 + pv_slot(t)] = sv[g];
-            }
-        }
-        __syncwarp();
+        if (!(flags & kFlagPad)) {
+            const int ntile = (valid + 15) >> 4;  // warp-uniform, 1..4
 
-        // -- logits: A rows gID / gID+8 = tokens tb+gID / tb+gID+8; k-step
-        //    (g, h) takes slot g of words 2tq+h of each token
-        float la[NT], lb[NT];
-        {
-            const uint2 x = *reinterpret_cast<const uint2*>(blk + kKCodes + (tb + gID) * 32 + 8 * tq);
-            const uint2 y = *reinterpret_cast<const uint2*>(blk + kKCodes + (tb + gID + 8) * 32 + 8 * tq);
-            const uint32_t wa[2] = {x.x, x.y}, wb[2] = {y.x, y.y};
-            float acc[4][NT][4];
+            // -- scales of the page: fp16 (s, z) -> fp32 (s, z - M_g s); rows
+            //    past the valid tokens are zero
 #pragma unroll
-            for (int g = 0; g < 4; ++g)
+            for (int it = 0; it < 4; ++it) {
+                const int which = it >> 1, t = lane + 32 * (it & 1);
+                if (t < 16 * ntile) {
+                    float sv[4], zz[4];
+                    if (t < valid) {
+                        const uint4 raw =
+                            *reinterpret_cast<const uint4*>(blk + (which ? kVScale : kKScale) + t * 16);
+                        const uint32_t r[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
+                        for (int g = 0; g < 4; ++g) {  // z - M_g s with the group's code offset M_g
+                            sv[g] = half_lo(r[g]);
+                            zz[g] = fmaf(which ? -v_magic(g) : -k_magic(g), sv[g], half_hi(r[g]));
+                        }
+                    } else {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) acc[g][nt][e] = 0.f;
-            const uint32_t wa8[2] = {wa[0] >> 8, wa[1] >> 8}, wb8[2] = {wb[0] >> 8, wb[1] >> 8};
+                        for (int g = 0; g < 4; ++g) sv[g] = zz[g] = 0.f;
+                    }
+                    if (which == 0) {
+                        ksS[t] = make_float4(sv[0], sv[1], sv[2], sv[3]);
+                        kzS[t] = make_float4(zz[0], zz[1], zz[2], zz[3]);
+                    } else {
+                        vzS[t] = make_float4(zz[0], zz[1], zz[2], zz[3]);
+                        const int ts = (t & ~15) | pv_slot(t & 15);
 #pragma unroll
-            for (int it = 0; it < 8; ++it) {
-                // half-major order: the four groups' accumulation chains interleave
-                const int h = it >> 2, g = it & 3, ks = 2 * g + h;
-                uint32_t a0, a1, a2, a3;
-                switch (g) {  // compile-time after unrolling
-                    case 0: a0 = unpack_pair<0, 0>(wa[h], cm); a1 = unpack_pair<0, 0>(wb[h], cm);
-                            a2 = unpack_pair<0, 0>(wa8[h], cm); a3 = unpack_pair<0, 0>(wb8[h], cm); break;
-                    case 1: a0 = unpack_pair<2, 2>(wa[h], cm); a1 = unpack_pair<2, 2>(wb[h], cm);
-                            a2 = unpack_pair<2, 2>(wa8[h], cm); a3 = unpack_pair<2, 2>(wb8[h], cm); break;
-                    case 2: a0 = unpack_pair<4, 4>(wa[h], cm); a1 = unpack_pair<4, 4>(wb[h], cm);
-                            a2 = unpack_pair<4, 4>(wa8[h], cm); a3 = unpack_pair<4, 4>(wb8[h], cm); break;
-                    default: a0 = unpack_pair<6, 4>(wa[h], cm); a1 = unpack_pair<6, 4>(wb[h], cm);
-                             a2 = unpack_pair<6, 4>(wa8[h], cm); a3 = unpack_pair<6, 4>(wb8[h], cm); break;
+                        for (int g = 0; g < 4; ++g) vsS[g * 64 + ts] = sv[g];
+                    }
                 }
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-                    mma_bf16_16816(acc[g][nt], a0, a1, a2, a3, qf[nt][ks][0], qf[nt][ks][1]);
             }
-            const float4 sA = scS[gID], sB = scS[gID + 8], zA = scS[16 + gID], zB = scS[16 + gID + 8];
-            const float sa[4] = {sA.x, sA.y, sA.z, sA.w}, za[4] = {zA.x, zA.y, zA.z, zA.w};
-            const float sb[4] = {sB.x, sB.y, sB.z, sB.w}, zb[4] = {zB.x, zB.y, zB.z, zB.w};
-            const bool va = tb + gID < si.valid, vb = tb + gID + 8 < si.valid;
+            __syncwarp();
+
+            // -- logits of the page's tiles: A rows gID / gID+8 = tokens
+            //    16m+gID / 16m+gID+8; k-step (g, h) takes slot g of words
+            //    2tq+h of each token
+            float la[4][NT], lb[4][NT];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) la[m][nt] = lb[m][nt] = -INFINITY;
+                if (m < ntile) {
+                    const int ta = 16 * m + gID;
+                    const uint2 x = *reinterpret_cast<const uint2*>(blk + kKCodes + ta * 32 + 8 * tq);
+                    const uint2 y = *reinterpret_cast<const uint2*>(blk + kKCodes + (ta + 8) * 32 + 8 * tq);
+                    const uint32_t wa[2] = {x.x, x.y}, wb[2] = {y.x, y.y};
+                    const uint32_t wa8[2] = {wa[0] >> 8, wa[1] >> 8}, wb8[2] = {wb[0] >> 8, wb[1] >> 8};
+                    float acc[4][NT][4];
+#pragma unroll
+                    for (int g = 0; g < 4; ++g)
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) acc[g][nt][e] = 0.f;
+#pragma unroll
+                    for (int it = 0; it < 8; ++it) {
+                        // half-major order: the four groups' accumulation chains interleave
+                        const int h = it >> 2, g = it & 3, ks = 2 * g + h;
+                        uint32_t a0, a1, a2, a3;
+                        switch (g) {  // compile-time after unrolling
+                            case 0: k_operands<0>(wa[h], wb[h], wa8[h], wb8[h], cm, a0, a1, a2, a3); break;
+                            case 1: k_operands<1>(wa[h], wb[h], wa8[h], wb8[h], cm, a0, a1, a2, a3); break;
+                            case 2: k_operands<2>(wa[h], wb[h], wa8[h], wb8[h], cm, a0, a1, a2, a3); break;
+                            default: k_operands<3>(wa[h], wb[h], wa8[h], wb8[h], cm, a0, a1, a2, a3); break;
+                        }
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+                            mma_bf16_16816(acc[g][nt], a0, a1, a2, a3, qf[nt][ks][0], qf[nt][ks][1]);
+                    }
+                    const float4 sA = ksS[ta], sB = ksS[ta + 8], zA = kzS[ta], zB = kzS[ta + 8];
+                    const float sa[4] = {sA.x, sA.y, sA.z, sA.w}, za[4] = {zA.x, zA.y, zA.z, zA.w};
+                    const float sb[4] = {sB.x, sB.y, sB.z, sB.w}, zb[4] = {zB.x, zB.y, zB.z, zB.w};
+                    const bool va = ta < valid, vb = ta + 8 < valid;
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const float qg[4] = {qsv[nt].x, qsv[nt].y, qsv[nt].z, qsv[nt].w};
+                        float xa = 0.f, xb = 0.f;
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) {
+                            xa = fmaf(sa[g], acc[g][nt][0] + acc[g][nt][1], xa);
+                            xa = fmaf(za[g], qg[g], xa);
+                            xb = fmaf(sb[g], acc[g][nt][2] + acc[g][nt][3], xb);
+                            xb = fmaf(zb[g], qg[g], xb);
+                        }
+                        la[m][nt] = va ? xa : -INFINITY;
+                        lb[m][nt] = vb ? xb : -INFINITY;
+                    }
+                }
+            }
+
+            // -- online softmax (base 2), once per page
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                const float qg[4] = {qsv[nt].x, qsv[nt].y, qsv[nt].z, qsv[nt].w};
-                float xa = 0.f, xb = 0.f;
+                float mx = fmaxf(la[0][nt], lb[0][nt]);
 #pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    xa = fmaf(sa[g], acc[g][nt][0] + acc[g][nt][1], xa);
-                    xa = fmaf(za[g], qg[g], xa);
-                    xb = fmaf(sb[g], acc[g][nt][2] + acc[g][nt][3], xb);
-                    xb = fmaf(zb[g], qg[g], xb);
-                }
-                la[nt] = (full_tile || va) ? xa : -INFINITY;
-                lb[nt] = (full_tile || vb) ? xb : -INFINITY;
-            }
-        }
-
-        // -- online softmax (base 2) for this warp's tokens
-        {
-            const float4 vzA = scS[48 + gID], vzB = scS[48 + gID + 8];
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                float mx = fmaxf(la[nt], lb[nt]);
+                for (int m = 1; m < 4; ++m) mx = fmaxf(mx, fmaxf(la[m][nt], lb[m][nt]));
                 mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
                 mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
                 mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
@@ -483,69 +530,74 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
                     m_run[nt] = m_new;
                 }
                 const float m_sub = (m_new == -INFINITY) ? 0.f : m_new;
-                const float pa = ex2(la[nt] - m_sub), pb = ex2(lb[nt] - m_sub);
-                l_run[nt] += pa + pb;
-                zacc[nt][0] = fmaf(pa, vzA.x, fmaf(pb, vzB.x, zacc[nt][0]));
-                zacc[nt][1] = fmaf(pa, vzA.y, fmaf(pb, vzB.y, zacc[nt][1]));
-                zacc[nt][2] = fmaf(pa, vzA.z, fmaf(pb, vzB.z, zacc[nt][2]));
-                zacc[nt][3] = fmaf(pa, vzA.w, fmaf(pb, vzB.w, zacc[nt][3]));
-                pbuf[(nt * 4 + tq) * 16 + pv_slot(gID)] = pa;
-                pbuf[(nt * 4 + tq) * 16 + pv_slot(gID + 8)] = pb;
-            }
-        }
-        __syncwarp();
-
-        // -- values: A rows = dims (m-tile (g, half): in-group index 16 half + row,
-        //    code plane 16 half + row, slot g), k = tokens (4tq, 4tq+2 | 4tq+1,
-        //    4tq+3), columns = heads (hi, lo)
-        {
-            float4 pp[NT];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-                pp[nt] = *reinterpret_cast<const float4*>(pbuf + (nt * 4 + (gID >> 1)) * 16 + 4 * tq);
-            // (p, s) of tokens (4tq, 4tq+2) and (4tq+1, 4tq+3) as adjacent pairs
-            const float* vs = reinterpret_cast<const float*>(scS + 32);
-            const uint8_t* vrow = blk + kVCodes + tb + 4 * tq;
-            const uint32_t pw[4] = {*reinterpret_cast<const uint32_t*>(vrow + gID * kPage),
-                                    *reinterpret_cast<const uint32_t*>(vrow + (8 + gID) * kPage),
-                                    *reinterpret_cast<const uint32_t*>(vrow + (16 + gID) * kPage),
-                                    *reinterpret_cast<const uint32_t*>(vrow + (24 + gID) * kPage)};
-            const uint32_t pw8[4] = {pw[0] >> 8, pw[1] >> 8, pw[2] >> 8, pw[3] >> 8};
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                const float4 sg = *reinterpret_cast<const float4*>(vs + g * 16 + 4 * tq);
-                uint32_t bb0[NT], bb1[NT];
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    bb0[nt] = split_w_pair(make_float2(pp[nt].x, pp[nt].y), make_float2(sg.x, sg.y), take_lo);
-                    bb1[nt] = split_w_pair(make_float2(pp[nt].z, pp[nt].w), make_float2(sg.z, sg.w), take_lo);
-                }
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    const uint32_t r0 = pw[2 * half], r1 = pw[2 * half + 1];
-                    const uint32_t r08 = pw8[2 * half], r18 = pw8[2 * half + 1];
-                    uint32_t a0, a1, a2, a3;
-                    switch (g) {
-                        case 0: a0 = unpack_pair<0, 2>(r0, cm); a1 = unpack_pair<0, 2>(r1, cm);
-                                a2 = unpack_pair<0, 2>(r08, cm); a3 = unpack_pair<0, 2>(r18, cm); break;
-                        case 1: a0 = unpack_pair<2, 2>(r0, cm); a1 = unpack_pair<2, 2>(r1, cm);
-                                a2 = unpack_pair<2, 2>(r08, cm); a3 = unpack_pair<2, 2>(r18, cm); break;
-                        case 2: a0 = unpack_pair<4, 4>(r0, cm); a1 = unpack_pair<4, 4>(r1, cm);
-                                a2 = unpack_pair<4, 4>(r08, cm); a3 = unpack_pair<4, 4>(r18, cm); break;
-                        default: a0 = unpack_pair<6, 4>(r0, cm); a1 = unpack_pair<6, 4>(r1, cm);
-                                 a2 = unpack_pair<6, 4>(r08, cm); a3 = unpack_pair<6, 4>(r18, cm); break;
+                for (int m = 0; m < 4; ++m) {
+                    if (m < ntile) {
+                        const int ta = 16 * m + gID;
+                        const float pa = ex2(la[m][nt] - m_sub), pb = ex2(lb[m][nt] - m_sub);
+                        l_run[nt] += pa + pb;
+                        const float4 vzA = vzS[ta], vzB = vzS[ta + 8];
+                        zacc[nt][0] = fmaf(pa, vzA.x, fmaf(pb, vzB.x, zacc[nt][0]));
+                        zacc[nt][1] = fmaf(pa, vzA.y, fmaf(pb, vzB.y, zacc[nt][1]));
+                        zacc[nt][2] = fmaf(pa, vzA.z, fmaf(pb, vzB.z, zacc[nt][2]));
+                        zacc[nt][3] = fmaf(pa, vzA.w, fmaf(pb, vzB.w, zacc[nt][3]));
+                        pS[(nt * 4 + tq) * 64 + 16 * m + pv_slot(gID)] = pa;
+                        pS[(nt * 4 + tq) * 64 + 16 * m + pv_slot(gID + 8)] = pb;
                     }
+                }
+            }
+            __syncwarp();
+
+            // -- values: A rows = dims (m-tile (g, half): in-group index 16 half +
+            //    row, code plane 16 half + row, slot g), k = the 16 tokens of
+            //    tile m (4tq, 4tq+2 | 4tq+1, 4tq+3), columns = heads (hi, lo)
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                if (m < ntile) {
+                    float4 pp[NT];
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt)
-                        mma_bf16_16816(acc_o[nt][2 * g + half], a0, a1, a2, a3, bb0[nt], bb1[nt]);
+                        pp[nt] = *reinterpret_cast<const float4*>(pS + (nt * 4 + (gID >> 1)) * 64 + 16 * m + 4 * tq);
+                    const uint8_t* vrow = blk + kVCodes + 16 * m + 4 * tq;
+                    const uint32_t pw[4] = {*reinterpret_cast<const uint32_t*>(vrow + gID * kPage),
+                                            *reinterpret_cast<const uint32_t*>(vrow + (8 + gID) * kPage),
+                                            *reinterpret_cast<const uint32_t*>(vrow + (16 + gID) * kPage),
+                                            *reinterpret_cast<const uint32_t*>(vrow + (24 + gID) * kPage)};
+                    const uint32_t pw8[4] = {pw[0] >> 8, pw[1] >> 8, pw[2] >> 8, pw[3] >> 8};
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        const float4 sg = *reinterpret_cast<const float4*>(vsS + g * 64 + 16 * m + 4 * tq);
+                        uint32_t bb0[NT], bb1[NT];
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            bb0[nt] = split_w_pair(make_float2(pp[nt].x, pp[nt].y), make_float2(sg.x, sg.y), take_lo);
+                            bb1[nt] = split_w_pair(make_float2(pp[nt].z, pp[nt].w), make_float2(sg.z, sg.w), take_lo);
+                        }
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            const uint32_t r0 = pw[2 * half], r1 = pw[2 * half + 1];
+                            const uint32_t r08 = pw8[2 * half], r18 = pw8[2 * half + 1];
+                            uint32_t a0, a1, a2, a3;
+                            switch (g) {
+                                case 0: v_operands<0>(r0, r1, r08, r18, cm, a0, a1, a2, a3); break;
+                                case 1: v_operands<1>(r0, r1, r08, r18, cm, a0, a1, a2, a3); break;
+                                case 2: v_operands<2>(r0, r1, r08, r18, cm, a0, a1, a2, a3); break;
+                                default: v_operands<3>(r0, r1, r08, r18, cm, a0, a1, a2, a3); break;
+                            }
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt)
+                                mma_bf16_16816(acc_o[nt][2 * g + half], a0, a1, a2, a3, bb0[nt], bb1[nt]);
+                        }
+                    }
                 }
             }
         }
         __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
 
-        if (si.flags & kFlagLast) {
-            // this warp's partial state -> shared memory
-            float* mw = mrg + (size_t)warp * SM::G4 * (kD + 2);
+        if (flags & kFlagLast) {
+            // this warp's partial state -> its scratch (no longer needed)
+            float* mw = reinterpret_cast<float*>(wbuf);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 float l = l_run[nt];
@@ -579,18 +631,19 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
                 return;
             }
             // merge the four warps: thread -> dimension, all heads
-            float* part = p.part + (size_t)si.item * p.part_stride;
+            float* part = p.part + (size_t)item * p.part_stride;
             const int d = threadIdx.x;  // 0..127
             for (int hl = 0; hl < p.G; ++hl) {
                 float M = -INFINITY;
 #pragma unroll
                 for (int ww = 0; ww < kConsumerWarps; ++ww)
-                    M = fmaxf(M, mrg[((size_t)ww * SM::G4 + hl) * (kD + 2) + kD]);
+                    M = fmaxf(M, reinterpret_cast<const float*>(smem + SM::kWarp + ww * SM::kWarpBytes)[hl * (kD + 2) + kD]);
                 float acc = 0.f, L = 0.f;
                 if (M != -INFINITY) {
 #pragma unroll
                     for (int ww = 0; ww < kConsumerWarps; ++ww) {
-                        const float* src = mrg + ((size_t)ww * SM::G4 + hl) * (kD + 2);
+                        const float* src =
+                            reinterpret_cast<const float*>(smem + SM::kWarp + ww * SM::kWarpBytes) + hl * (kD + 2);
                         const float sc = ex2(src[kD] - M);
                         acc = fmaf(sc, src[d], acc);
                         L = fmaf(sc, src[kD + 1], L);
@@ -607,7 +660,6 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
                 return;
             }
         }
-        if (lane == 0) mbar_arrive(&empty[s]);
     }
 }
 
