@@ -49,6 +49,8 @@ static oscar_status check_shape(const oscar_shape* s) {
     return OSCAR_OK;
 }
 
+static int bf16_items(const oscar_shape* s) { return (s->sink + s->recent + 63) / 64; }
+
 struct WsLayout {
     size_t counter, item_start, qfrag, qsum, part, bf_part, total;
     int NT, pps, part_stride, max_items;
@@ -73,7 +75,7 @@ static WsLayout ws_layout(const oscar_shape* s, int batch, int max_pages) {
     w.part = off;
     off = round_up(off + (size_t)w.max_items * w.part_stride * 4, 256);
     w.bf_part = off;
-    off = round_up(off + (size_t)batch * hk * w.part_stride * 4, 256);
+    off = round_up(off + (size_t)batch * hk * bf16_items(s) * w.part_stride * 4, 256);
     w.total = off;
     return w;
 }
@@ -261,6 +263,7 @@ oscar_status oscar_decode_attn(const oscar_shape* shape, int32_t batch, const vo
     p.G = shape->num_q_heads / shape->num_kv_heads;
     p.NT = w.NT;
     p.nslot = shape->sink + shape->recent;
+    p.bf_items = bf16_items(shape);
     p.max_pages = max_pages;
     p.num_pages = num_pages;
     p.pps = w.pps;

@@ -666,177 +666,211 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
 // ---------------------------------------------------------------------------
 // BF16 sink + recent segment
 // ---------------------------------------------------------------------------
-// One block per (b, kv), 128 threads.  The segment's K|V rows (512 B per
-// token) are staged in 32-token chunks into shared memory with cp.async,
-// double buffered, so that two chunks of loads are in flight per block.
-// Per chunk: logits by four threads per token (32 dims each), online
-// softmax statistics by one warp per head, values by one thread per
-// dimension.  Logits in base 2 (q scaled by sm_scale * log2 e).
-constexpr int kBfThreads = 128;
-constexpr int kBfChunk = 32;
-constexpr int kBfPitch = 528;                  // bytes per staged token row (512 + 16)
-constexpr int kBfQPitch = 4 * 36;              // floats per staged query row (4 quarters of 32 + 4 pad)
-constexpr int kBfSmem = 2 * kBfChunk * kBfPitch + 8 * kBfQPitch * 4 + 8 * kBfChunk * 4 + 8 * 4 * 4;
+// Block (item, (b, kv)) covers 64 consecutive slots of the 320-token BF16
+// segment; warp w attends over 16 of them on tensor cores, FlashAttention
+// style with the query heads as MMA rows: S = Q.K^T with A = the query rows
+// (row 2h and 2h+1 both hold head h; K and q are bf16, so the products are
+// exact), then O = P.V with A = P taken straight from S's accumulator layout
+// (row 2h carries the bf16 high part of p, row 2h+1 the rounded remainder, so
+// P keeps ~16 bits) and B = V via ldmatrix.trans.  The four warps' partial
+// states are merged in shared memory into one partial per block.
+constexpr int kBfWarps = 4;
+constexpr int kBfThreads = 32 * kBfWarps;
+constexpr int kBfItemTok = 16 * kBfWarps;          // tokens per block
+constexpr int kBfPitch = 528;                      // bytes per staged token row (512 + 16)
+constexpr int kBfWarpBytes = 16 * kBfPitch;        // also holds the warp's state [G][kD + 2] at the end
+constexpr int kBfSmem = kBfWarps * kBfWarpBytes;
+static_assert(8 * (kD + 2) * 4 <= kBfWarpBytes, "warp state must fit in the warp's row tile");
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], const void* p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(p)));
+}
 
 template <int G>
-__device__ void bf16_segment(const DecodeParams& p, int b, int kv, uint8_t* sm) {
-    uint8_t* buf = sm;                                                  // [2][kBfChunk][kBfPitch]
-    float* qsh = reinterpret_cast<float*>(sm + 2 * kBfChunk * kBfPitch);   // [G][kBfQPitch]
-    float* pw = qsh + 8 * kBfQPitch;                                   // [G][kBfChunk] weights
-    float* st = pw + 8 * kBfChunk;                                     // [G][4]: m, l, alpha
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int n = min(max(__ldg(p.bf16_len + b), 0), p.nslot);
-    const int nch = (n + kBfChunk - 1) / kBfChunk;
-    const size_t row_elems = (size_t)p.hk * 2 * kD;
-    const __nv_bfloat16* base = p.bf16_kv + ((size_t)b * p.nslot * p.hk + kv) * 2 * kD;
+__device__ void bf16_tile(const DecodeParams& p, int b, int kv, int t0, int nvalid, uint8_t* rows) {
+    const int lane = threadIdx.x & 31, gID = lane >> 2, tq = lane & 3;
+    float* st = reinterpret_cast<float*>(rows);  // [G][kD + 2] at the end
+    if (nvalid <= 0) {
+        for (int i = lane; i < G * (kD + 2); i += 32) {
+            const int c = i % (kD + 2);
+            st[i] = (c == kD) ? -INFINITY : 0.f;
+        }
+        return;
+    }
+    // stage the valid rows (K | V, 512 B each); zero the rest of the tile
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(p.bf16_kv) +
+                         (((size_t)b * p.nslot + t0) * p.hk + kv) * (2 * kD * 2);
+    const size_t row_stride = (size_t)p.hk * 2 * kD * 2;
+#pragma unroll 4
+    for (int r = 0; r < 16; ++r) {
+        if (r < nvalid) cp_async16(rows + r * kBfPitch + 16 * lane, src + r * row_stride + 16 * lane);
+        else *reinterpret_cast<uint4*>(rows + r * kBfPitch + 16 * lane) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
 
-    auto stage = [&](int c) {  // copy chunk c (its valid rows only)
-        uint8_t* dst = buf + (c & 1) * kBfChunk * kBfPitch;
-        const int t0 = c * kBfChunk, cnt = min(kBfChunk, n - t0);
-        for (int i = tid; i < cnt * 32; i += kBfThreads) {
-            const int r = i >> 5, k = i & 31;
-            cp_async16(dst + r * kBfPitch + 16 * k,
-                       reinterpret_cast<const uint8_t*>(base + (size_t)(t0 + r) * row_elems) + 16 * k);
-        }
-        cp_async_commit();
-    };
-    if (nch > 0) stage(0);
-    for (int i = tid; i < G * kD; i += kBfThreads) {
-        const int h = i / kD, d = i % kD;
-        qsh[h * kBfQPitch + (d >> 5) * 36 + (d & 31)] =
-            __bfloat162float(p.q[((size_t)b * p.hq + kv * G + h) * kD + d]) * p.qscale;
-    }
-    if (tid < G) {
-        st[tid * 4 + 0] = -INFINITY;
-        st[tid * 4 + 1] = 0.f;
-    }
-    float o[G];
+    // A = query rows: row r < 2G holds head r/2, the rest are zero
+    constexpr bool kHigh = (G == 8);                  // rows gID + 8 in use
+    const bool row_lo_on = gID < 2 * G;
+    const __nv_bfloat16* qa = p.q + ((size_t)b * p.hq + kv * G + (gID >> 1)) * kD;
+    const __nv_bfloat16* qb = p.q + ((size_t)b * p.hq + kv * G + ((gID + 8) >> 1)) * kD;
+    uint32_t qf[8][4];
 #pragma unroll
-    for (int h = 0; h < G; ++h) o[h] = 0.f;
+    for (int ks = 0; ks < 8; ++ks) {
+        const int d0 = 16 * ks + 2 * tq;
+        qf[ks][0] = row_lo_on ? *reinterpret_cast<const uint32_t*>(qa + d0) : 0u;
+        qf[ks][2] = row_lo_on ? *reinterpret_cast<const uint32_t*>(qa + d0 + 8) : 0u;
+        qf[ks][1] = kHigh ? *reinterpret_cast<const uint32_t*>(qb + d0) : 0u;
+        qf[ks][3] = kHigh ? *reinterpret_cast<const uint32_t*>(qb + d0 + 8) : 0u;
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncwarp();
 
-    for (int c = 0; c < nch; ++c) {
-        if (c + 1 < nch) {
-            stage(c + 1);
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
+    // S = Q.K^T for tokens 8nt .. 8nt+7 (B via ldmatrix: matrix i/8 = dims
+    // 16ks + 8(i/8) of token row i%8, covering k-steps ks and ks+1)
+    float sacc[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
+        const uint8_t* rb = rows + (8 * nt + (lane & 7)) * kBfPitch + 16 * (lane >> 3);
+#pragma unroll
+        for (int ks = 0; ks < 8; ks += 2) {
+            uint32_t kb[4];
+            ldsm_x4(kb, rb + 32 * ks);
+            mma_bf16_16816(sacc[nt], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], kb[0], kb[1]);
+            mma_bf16_16816(sacc[nt], qf[ks + 1][0], qf[ks + 1][1], qf[ks + 1][2], qf[ks + 1][3], kb[2], kb[3]);
         }
-        __syncthreads();
-        const uint8_t* cb = buf + (c & 1) * kBfChunk * kBfPitch;
-        const int cnt = min(kBfChunk, n - c * kBfChunk);
-        {  // logits: token t = tid / 4, quarter = tid % 4 (32 dims)
-            const int t = tid >> 2, qr = tid & 3;
-            float acc[G];
-#pragma unroll
-            for (int h = 0; h < G; ++h) acc[h] = 0.f;
-            const uint4* kr = reinterpret_cast<const uint4*>(cb + t * kBfPitch + qr * 64);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint4 w = kr[j];
-                const float k8[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
-                                     bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
-#pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    const float4 qa = *reinterpret_cast<const float4*>(qsh + h * kBfQPitch + qr * 36 + 8 * j);
-                    const float4 qb = *reinterpret_cast<const float4*>(qsh + h * kBfQPitch + qr * 36 + 8 * j + 4);
-                    acc[h] = fmaf(qa.x, k8[0], acc[h]);
-                    acc[h] = fmaf(qa.y, k8[1], acc[h]);
-                    acc[h] = fmaf(qa.z, k8[2], acc[h]);
-                    acc[h] = fmaf(qa.w, k8[3], acc[h]);
-                    acc[h] = fmaf(qb.x, k8[4], acc[h]);
-                    acc[h] = fmaf(qb.y, k8[5], acc[h]);
-                    acc[h] = fmaf(qb.z, k8[6], acc[h]);
-                    acc[h] = fmaf(qb.w, k8[7], acc[h]);
-                }
-            }
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                acc[h] += __shfl_xor_sync(kFull, acc[h], 1);
-                acc[h] += __shfl_xor_sync(kFull, acc[h], 2);
-                if (qr == 0) pw[h * kBfChunk + t] = (t < cnt) ? acc[h] : -INFINITY;
-            }
-        }
-        __syncthreads();
-        // softmax statistics: warp w handles heads w, w + 4
-        for (int h = warp; h < G; h += 4) {
-            const float x = pw[h * kBfChunk + lane];
-            float mx = x;
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
-            const float m_old = st[h * 4 + 0];
-            const float m_new = fmaxf(m_old, mx);
-            const float alpha = (m_old == -INFINITY) ? 0.f : ex2(m_old - m_new);
-            const float w = (x == -INFINITY) ? 0.f : ex2(x - m_new);
-            float sum = w;
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
-            pw[h * kBfChunk + lane] = w;
-            __syncwarp();
-            if (lane == 0) {
-                st[h * 4 + 0] = m_new;
-                st[h * 4 + 1] = st[h * 4 + 1] * alpha + sum;
-                st[h * 4 + 2] = alpha;
-            }
-        }
-        __syncthreads();
-        {  // values: thread = dimension
-            const int d = tid;
-            float acc[G];
-#pragma unroll
-            for (int h = 0; h < G; ++h) acc[h] = 0.f;
-            const uint8_t* vcol = cb + 256 + 2 * d;
-            // weights of masked / absent tokens are 0 and their rows are not read
-            const int cnt4 = cnt & ~3;
-            for (int t = 0; t < cnt4; t += 4) {
-                float v[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    v[u] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(vcol + (t + u) * kBfPitch));
-#pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    const float4 w = *reinterpret_cast<const float4*>(pw + h * kBfChunk + t);
-                    acc[h] = fmaf(w.x, v[0], acc[h]);
-                    acc[h] = fmaf(w.y, v[1], acc[h]);
-                    acc[h] = fmaf(w.z, v[2], acc[h]);
-                    acc[h] = fmaf(w.w, v[3], acc[h]);
-                }
-            }
-            for (int t = cnt4; t < cnt; ++t) {
-                const float v = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(vcol + t * kBfPitch));
-#pragma unroll
-                for (int h = 0; h < G; ++h) acc[h] = fmaf(pw[h * kBfChunk + t], v, acc[h]);
-            }
-#pragma unroll
-            for (int h = 0; h < G; ++h) o[h] = fmaf(o[h], st[h * 4 + 2], acc[h]);
-        }
-        __syncthreads();
     }
-    float* part = p.bf_part + (size_t)(b * p.hk + kv) * p.part_stride;
+    // scale to base 2, mask, row max / exp / sum (rows gID: e 0,1; gID+8: e 2,3)
+    float ma = -INFINITY, mb = -INFINITY;
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-        part[(size_t)h * kD + tid] = o[h];
-        if (tid == 0) {
-            part[(size_t)G * kD + h] = st[h * 4 + 0];
-            part[(size_t)G * kD + G + h] = st[h * 4 + 1];
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int tok = 8 * nt + 2 * tq + (e & 1);
+            sacc[nt][e] = (tok < nvalid) ? sacc[nt][e] * p.qscale : -INFINITY;
+            if (e < 2) ma = fmaxf(ma, sacc[nt][e]);
+            else mb = fmaxf(mb, sacc[nt][e]);
+        }
+    ma = fmaxf(ma, __shfl_xor_sync(kFull, ma, 1));
+    ma = fmaxf(ma, __shfl_xor_sync(kFull, ma, 2));
+    mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, 1));
+    mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, 2));
+    float la = 0.f, lb = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            sacc[nt][e] = ex2(sacc[nt][e] - (e < 2 ? ma : mb));
+            if (e < 2) la += sacc[nt][e];
+            else lb += sacc[nt][e];
+        }
+    la += __shfl_xor_sync(kFull, la, 1);
+    la += __shfl_xor_sync(kFull, la, 2);
+    lb += __shfl_xor_sync(kFull, lb, 1);
+    lb += __shfl_xor_sync(kFull, lb, 2);
+
+    // P as the A operand of O = P.V (k = the 16 tokens): even rows take the
+    // bf16 high part, odd rows the rounded remainder
+    const float2 take_lo = (gID & 1) ? make_float2(1.f, 1.f) : make_float2(0.f, 0.f);
+    const float2 one = make_float2(1.f, 1.f);
+    uint32_t pa[4];
+    pa[0] = row_lo_on ? split_w_pair(make_float2(sacc[0][0], sacc[0][1]), one, take_lo) : 0u;
+    pa[2] = row_lo_on ? split_w_pair(make_float2(sacc[1][0], sacc[1][1]), one, take_lo) : 0u;
+    pa[1] = kHigh ? split_w_pair(make_float2(sacc[0][2], sacc[0][3]), one, take_lo) : 0u;
+    pa[3] = kHigh ? split_w_pair(make_float2(sacc[1][2], sacc[1][3]), one, take_lo) : 0u;
+
+    // O = P.V over dims 8j .. 8j+7 (B via ldmatrix.trans: matrix i/8 = tokens
+    // 8((i/8)&1) + i%8, dims 16jp + 8(i/16))
+    float o[16][4];
+    const uint8_t* vb = rows + 256 + ((lane & 7) + 8 * ((lane >> 3) & 1)) * kBfPitch + 16 * (lane >> 4);
+#pragma unroll
+    for (int jp = 0; jp < 8; ++jp) {
+        uint32_t vf[4];
+        ldsm_x4_trans(vf, vb + 32 * jp);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[2 * jp][e] = o[2 * jp + 1][e] = 0.f;
+        mma_bf16_16816(o[2 * jp], pa[0], pa[1], pa[2], pa[3], vf[0], vf[1]);
+        mma_bf16_16816(o[2 * jp + 1], pa[0], pa[1], pa[2], pa[3], vf[2], vf[3]);
+    }
+    __syncwarp();  // all row reads done: the tile now holds the warp's state
+    // O_h = row 2h + row 2h + 1 (lanes gID and gID ^ 1)
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[j][e] += __shfl_xor_sync(kFull, o[j][e], 4);
+    if ((gID & 1) == 0) {
+        const int h = gID >> 1;
+        if (h < G) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                *reinterpret_cast<float2*>(st + h * (kD + 2) + 8 * j + 2 * tq) = make_float2(o[j][0], o[j][1]);
+            if (tq == 0) {
+                st[h * (kD + 2) + kD] = ma;
+                st[h * (kD + 2) + kD + 1] = la;
+            }
+        }
+        if (kHigh) {
+            const int h2 = h + 4;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                *reinterpret_cast<float2*>(st + h2 * (kD + 2) + 8 * j + 2 * tq) = make_float2(o[j][2], o[j][3]);
+            if (tq == 0) {
+                st[h2 * (kD + 2) + kD] = mb;
+                st[h2 * (kD + 2) + kD + 1] = lb;
+            }
         }
     }
 }
 
 __global__ void __launch_bounds__(kBfThreads) bf16_kernel(DecodeParams p) {
-    extern __shared__ __align__(16) uint8_t bsm[];
-    const int b = blockIdx.x / p.hk, kv = blockIdx.x % p.hk;
+    extern __shared__ __align__(128) uint8_t bsm[];
+    const int item = blockIdx.x, bk = blockIdx.y;
+    const int b = bk / p.hk, kv = bk % p.hk;
+    const int warp = threadIdx.x >> 5;
+    const int n = min(max(__ldg(p.bf16_len + b), 0), p.nslot);
+    const int t0 = item * kBfItemTok + 16 * warp;
+    uint8_t* rows = bsm + warp * kBfWarpBytes;
     switch (p.G) {
-        case 1: bf16_segment<1>(p, b, kv, bsm); break;
-        case 2: bf16_segment<2>(p, b, kv, bsm); break;
-        case 4: bf16_segment<4>(p, b, kv, bsm); break;
-        default: bf16_segment<8>(p, b, kv, bsm); break;
+        case 1: bf16_tile<1>(p, b, kv, t0, n - t0, rows); break;
+        case 2: bf16_tile<2>(p, b, kv, t0, n - t0, rows); break;
+        case 4: bf16_tile<4>(p, b, kv, t0, n - t0, rows); break;
+        default: bf16_tile<8>(p, b, kv, t0, n - t0, rows); break;
+    }
+    __syncthreads();
+    // merge the four warps: thread -> dimension
+    float* part = p.bf_part + ((size_t)bk * p.bf_items + item) * p.part_stride;
+    const int d = threadIdx.x;
+    for (int h = 0; h < p.G; ++h) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kBfWarps; ++w)
+            M = fmaxf(M, reinterpret_cast<const float*>(bsm + w * kBfWarpBytes)[h * (kD + 2) + kD]);
+        float acc = 0.f, L = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kBfWarps; ++w) {
+                const float* src = reinterpret_cast<const float*>(bsm + w * kBfWarpBytes) + h * (kD + 2);
+                const float sc = ex2(src[kD] - M);
+                acc = fmaf(sc, src[d], acc);
+                L = fmaf(sc, src[kD + 1], L);
+            }
+        }
+        part[(size_t)h * kD + d] = acc;
+        if (d == 0) {
+            part[(size_t)p.G * kD + h] = M;
+            part[(size_t)p.G * kD + p.G + h] = L;
+        }
     }
 }
 
@@ -941,8 +975,26 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(DecodeParams p) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) acc[c] = fmaf(wj, Us[(lane + 32 * c) * kD + jj], acc[c]);
     }
-    const float* bp = p.bf_part + (size_t)(b * p.hk + kv) * p.part_stride;
-    const float mb = bp[(size_t)p.G * kD + hh], lb = bp[(size_t)p.G * kD + p.G + hh];
+    // BF16 segment: log-sum-exp merge of its item partials (unrotated domain)
+    const float* bp = p.bf_part + (size_t)(b * p.hk + kv) * p.bf_items * p.part_stride;
+    float mb = -INFINITY;
+    for (int it = 0; it < p.bf_items; ++it) {
+        const float* pt = bp + (size_t)it * p.part_stride + (size_t)p.G * kD;
+        if (pt[p.G + hh] > 0.f) mb = fmaxf(mb, pt[hh]);
+    }
+    float lb = 0.f, ob[4] = {0.f, 0.f, 0.f, 0.f};
+    if (mb != -INFINITY) {
+        for (int it = 0; it < p.bf_items; ++it) {
+            const float* pt = bp + (size_t)it * p.part_stride;
+            const float li = pt[(size_t)p.G * kD + p.G + hh];
+            if (li > 0.f) {
+                const float sc = ex2(pt[(size_t)p.G * kD + hh] - mb);
+                lb = fmaf(sc, li, lb);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) ob[c] = fmaf(sc, pt[(size_t)hh * kD + lane + 32 * c], ob[c]);
+            }
+        }
+    }
     const float Mx = fmaxf(L > 0.f ? M : -INFINITY, lb > 0.f ? mb : -INFINITY);
     const float wi = (L > 0.f) ? ex2(M - Mx) * L : 0.f;
     const float wb = (lb > 0.f) ? ex2(mb - Mx) : 0.f;
@@ -952,7 +1004,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(DecodeParams p) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
         const int a2 = lane + 32 * c;
-        o[a2] = (wi * acc[c] + wb * bp[(size_t)hh * kD + a2]) * inv;
+        o[a2] = (wi * acc[c] + wb * ob[c]) * inv;
     }
 }
 
@@ -1012,7 +1064,7 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st, cudaEvent_t ev
         if (e != cudaSuccess) return e;
         at.setb = true;
     }
-    bf16_kernel<<<p.B * p.hk, kBfThreads, kBfSmem, st>>>(p);
+    bf16_kernel<<<dim3(p.bf_items, p.B * p.hk), kBfThreads, kBfSmem, st>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (!at.setm) {
         e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMergeSmem);

@@ -9,8 +9,9 @@
 // (FMA-based exact products, TwoSum accumulation: the "Dot2" scheme of
 // Ogita, Rump and Oishi, "Accurate sum and dot product", 2005), the fast
 // Walsh-Hadamard transform runs on the (hi, lo) float pairs, and the group
-// statistics and code decisions run in fp64, so the result follows a
-// float64 evaluation of the method.  Stored position p = bitrev7(j) =
+// statistics stay on the pairs, so every code decision is taken from a value
+// within 4e-7 code units of a float64 evaluation of the method (fp64
+// arithmetic is avoided: GB300 runs it at a small fraction of the fp32 rate).  Stored position p = bitrev7(j) =
 // 32*bitrev2(i) + bitrev5(l) for value i of lane l: each lane holds one
 // element of every group (group reductions are warp reductions), and the
 // four codes of one code byte (in-group index bitrev5(l) of groups 0..3).
@@ -118,32 +119,61 @@ __global__ void __launch_bounds__(128) evict_kernel(EvictParams p) {
         }
     }
 
-    // ---- per-group clip / scale / zero / codes in fp64 -----------------------
-    // value k of this lane: stored position 32*bitrev2(k) + bitrev5(lane)
-    const double cr = (double)__ldg(p.clip + kv * 2 + which);
-    double yd[4], amax[4], lo[4], hi[4];
+    // ---- per-group clip / scale / zero / codes ----------------------------------
+    // Values stay double-float: y = Y / sqrt(d) with 1/sqrt(d) as a float
+    // pair (0x3db504f3 + 0x30cfe77a).  Selections (max |y|, clamp, min, max)
+    // are exact on the pairs; the scale and zero are rounded to fp16 from the
+    // pair's fp32 value, and the code decision u = (y_c - z) / s is evaluated
+    // from the exact pair difference, so its error is below 4e-7 code units.
+    const float cr = __ldg(p.clip + kv * 2 + which);
+    const float kc_hi = __uint_as_float(0x3db504f3u), kc_lo = __uint_as_float(0x30cfe77au);
+    df yn[4];
+    float amax[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        yd[k] = ((double)y[k].hi + (double)y[k].lo) * kInvSqrtD;
-        amax[k] = fabs(yd[k]);
+        const float ph = __fmul_rn(y[k].hi, kc_hi);
+        float e = __fmaf_rn(y[k].hi, kc_hi, -ph);
+        e = __fmaf_rn(y[k].hi, kc_lo, e);
+        e = __fmaf_rn(y[k].lo, kc_hi, e);
+        yn[k] = fast_two_sum(ph, e);
+        amax[k] = fabsf(yn[k].hi);
     }
 #pragma unroll
     for (int m = 16; m > 0; m >>= 1)
 #pragma unroll
-        for (int k = 0; k < 4; ++k) amax[k] = fmax(amax[k], __shfl_xor_sync(kFull, amax[k], m));
+        for (int k = 0; k < 4; ++k) amax[k] = fmaxf(amax[k], __shfl_xor_sync(kFull, amax[k], m));
+    // clamp to +-t, t = c * max|y| (fp32: an error of 1 ulp in t moves the
+    // clipped values by 6e-8 relative)
+    df lo[4], hi[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        const double t = cr * amax[k];
-        yd[k] = fmin(fmax(yd[k], -t), t);
-        lo[k] = hi[k] = yd[k];
-    }
-#pragma unroll
-    for (int m = 16; m > 0; m >>= 1)
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            lo[k] = fmin(lo[k], __shfl_xor_sync(kFull, lo[k], m));
-            hi[k] = fmax(hi[k], __shfl_xor_sync(kFull, hi[k], m));
+        if (cr < 1.f) {  // warp-uniform; c >= 1 clips nothing
+            const float t = __fmul_rn(cr, amax[k]);
+            if (yn[k].hi > t || (yn[k].hi == t && yn[k].lo > 0.f)) yn[k] = {t, 0.f};
+            else if (yn[k].hi < -t || (yn[k].hi == -t && yn[k].lo < 0.f)) yn[k] = {-t, 0.f};
         }
+        lo[k] = hi[k] = yn[k];
+    }
+    // exact min / max of the pairs: reduce the high parts, then the low parts
+    // of the lanes that hold the extreme high part
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        float mx = hi[k].hi, mn = lo[k].hi;
+#pragma unroll
+        for (int m = 16; m > 0; m >>= 1) {
+            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, m));
+            mn = fminf(mn, __shfl_xor_sync(kFull, mn, m));
+        }
+        float mxl = (hi[k].hi == mx) ? hi[k].lo : -INFINITY;
+        float mnl = (lo[k].hi == mn) ? lo[k].lo : INFINITY;
+#pragma unroll
+        for (int m = 16; m > 0; m >>= 1) {
+            mxl = fmaxf(mxl, __shfl_xor_sync(kFull, mxl, m));
+            mnl = fminf(mnl, __shfl_xor_sync(kFull, mnl, m));
+        }
+        hi[k] = {mx, mxl};
+        lo[k] = {mn, mnl};
+    }
     unsigned short sb[4], zb[4];
     // value k of this lane is in-group index bitrev5(lane) of group bitrev2(k):
     // all four codes of code byte j = bitrev5(lane) are this lane's, group k in
@@ -151,15 +181,16 @@ __global__ void __launch_bounds__(128) evict_kernel(EvictParams p) {
     uint32_t byte = 0;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        sb[k] = f64_to_f16_bits((hi[k] - lo[k]) / 3.0);
-        zb[k] = f64_to_f16_bits(lo[k]);
-        const double sd = (double)__half2float(__ushort_as_half(sb[k]));
-        const double zd = (double)__half2float(__ushort_as_half(zb[k]));
+        const df d = df_add(hi[k], df_neg(lo[k]));
+        sb[k] = __half_as_ushort(__float2half_rn(__fdiv_rn(__fadd_rn(d.hi, d.lo), 3.0f)));
+        zb[k] = __half_as_ushort(__float2half_rn(__fadd_rn(lo[k].hi, lo[k].lo)));
+        const float sf = __half2float(__ushort_as_half(sb[k]));
+        const float zf = __half2float(__ushort_as_half(zb[k]));
         int code = 0;
-        if (sd != 0.0) {
-            double r = rint((yd[k] - zd) / sd);
-            r = fmin(fmax(r, 0.0), 3.0);
-            code = (int)r;
+        if (sf != 0.f) {
+            const df yz = df_add(yn[k], df{-zf, 0.f});
+            const float u = __fdiv_rn(__fadd_rn(yz.hi, yz.lo), sf);
+            code = (int)fminf(fmaxf(rintf(u), 0.f), 3.f);
         }
         byte |= (uint32_t)code << (2 * bitrev2(k));
     }
