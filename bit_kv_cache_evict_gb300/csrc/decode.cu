@@ -209,18 +209,21 @@ template <int NT>
 struct Int2Smem {
     static constexpr int G4 = NT * 4;  // head columns (padded to 4 per n-tile)
     // per-warp scratch: K s [64] float4 | K z-M s [64] float4 | V z-M s [64]
-    // float4 | V s [4][64] float (token order pv_slot within 16-token tiles)
-    // | P [G4][64] float (same token order).  Reused at an item's end for
+    // float4 | V s [4][72] float (token order pv_pos) | P [G4][72] float
+    // (same token order).  Reused at an item's end for
     // the warp's (o', m, l) state [G4][kD + 2].
-    static constexpr int kWKs = 0, kWKz = 1024, kWVz = 2048, kWVs = 3072, kWP = 4096;
-    static constexpr int kWarpBytes0 = kWP + G4 * 64 * 4;
+    static constexpr int kWKs = 0, kWKz = 1024, kWVz = 2048, kWVs = 3072, kWP = 3072 + 4 * 72 * 4;
+    static constexpr int kWarpBytes0 = kWP + G4 * 72 * 4;
     static constexpr int kMergeBytes = G4 * (kD + 2) * 4;
     static constexpr int kWarpBytes = kWarpBytes0 > kMergeBytes ? kWarpBytes0 : kMergeBytes;
     static constexpr int kStage = 0;
     static constexpr int kInfo = kStage + kStages * kBlock;
     static constexpr int kBars = kInfo + kStages * (int)sizeof(StageInfo);
     static constexpr int kWarp = kBars + (2 * kStages + 2) * 8;
-    static constexpr int kBytes = kWarp + kConsumerWarps * kWarpBytes;
+    // q' fragments of the current item, shared by the four consumer warps
+    // (all four are inside the same item between two item-end merges)
+    static constexpr int kQf = kWarp + kConsumerWarps * kWarpBytes;       // [NT][8][32] uint2
+    static constexpr int kBytes = kQf + NT * 8 * 32 * 8;
 };
 
 __device__ __forceinline__ int find_seq(const int32_t* item_start, int B, int item) {
@@ -255,6 +258,215 @@ __device__ __forceinline__ void v_operands(uint32_t r0, uint32_t r1, uint32_t r0
     a1 = unpack_pair<P, T>(r1, cm);
     a2 = unpack_pair<P, T>(r08, cm);
     a3 = unpack_pair<P, T>(r18, cm);
+}
+
+// Position of token t (0..63) in the warp's probability and V-scale rows.
+// The P.V products take the page's tokens in 16 groups of four: k-step m of
+// lane quad tq covers group q = 4 tq + m (tokens 4q .. 4q+3, whose V codes
+// are bytes 4q .. 4q+3 of every code plane, so one 16-byte load per plane
+// serves all four k-steps).  Group q sits in 16-byte chunk 4 tq + (m ^ tq)
+// of a row, which keeps the lanes of one shared-memory wavefront on
+// distinct banks; inside a chunk the order is pv_slot (tokens 4q, 4q+2 |
+// 4q+1, 4q+3 as the two B-operand pairs).
+__device__ __forceinline__ int pv_pos(int t) {
+    const int q = t >> 2, tq = q >> 2, m = q & 3;
+    return 4 * (4 * tq + (m ^ tq)) + pv_slot(t & 3);
+}
+constexpr int kPvRow = 72;  // floats per probability / V-scale row (64 + 8: conflict-free stores)
+
+// One page of INT2 history for one consumer warp: the page's scales, the
+// logits of its four 16-token tiles, one online-softmax update, and the P.V
+// products.  FULL (all 64 tokens valid, the common case) removes the
+// per-tile conditions of the logit phase so that the four tiles' work can
+// interleave.
+template <int NT, bool FULL>
+__device__ __forceinline__ void attend_page(const uint8_t* blk, int valid, uint8_t* wbuf, const uint2* qfS,
+                                            const float4 (&qsv)[NT], float (&m_run)[NT], float (&l_run)[NT],
+                                            float (&zacc)[NT][4], float (&acc_o)[NT][8][4], const CodeMul& cm,
+                                            const SplitSel& take_lo) {
+    using SM = Int2Smem<NT>;
+    const int lane = threadIdx.x & 31, gID = lane >> 2, tq = lane & 3;
+    if (FULL) valid = kPage;
+    float4* ksS = reinterpret_cast<float4*>(wbuf + SM::kWKs);   // [64] K s
+    float4* kzS = reinterpret_cast<float4*>(wbuf + SM::kWKz);   // [64] K z - M s
+    float4* vzS = reinterpret_cast<float4*>(wbuf + SM::kWVz);   // [64] V z - M s
+    float* vsS = reinterpret_cast<float*>(wbuf + SM::kWVs);     // [4][kPvRow] V s at pv_pos
+    float* pS = reinterpret_cast<float*>(wbuf + SM::kWP);       // [G4][kPvRow] P at pv_pos
+    const int ntile = FULL ? 4 : (valid + 15) >> 4;             // warp-uniform, 1..4
+
+    // -- scales of the page: fp16 (s, z) -> fp32 (s, z - M_g s); rows past
+    //    the valid tokens are zero
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int which = it >> 1, t = lane + 32 * (it & 1);
+        float sv[4], zz[4];
+        if (FULL || t < valid) {
+            const uint4 raw = *reinterpret_cast<const uint4*>(blk + (which ? kVScale : kKScale) + t * 16);
+            const uint32_t r[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {  // z - M_g s with the group's code offset M_g
+                sv[g] = half_lo(r[g]);
+                zz[g] = fmaf(which ? -v_magic(g) : -k_magic(g), sv[g], half_hi(r[g]));
+            }
+        } else {
+#pragma unroll
+            for (int g = 0; g < 4; ++g) sv[g] = zz[g] = 0.f;
+        }
+        if (which == 0) {
+            ksS[t] = make_float4(sv[0], sv[1], sv[2], sv[3]);
+            kzS[t] = make_float4(zz[0], zz[1], zz[2], zz[3]);
+        } else {
+            vzS[t] = make_float4(zz[0], zz[1], zz[2], zz[3]);
+            const int ps = pv_pos(t);
+#pragma unroll
+            for (int g = 0; g < 4; ++g) vsS[g * kPvRow + ps] = sv[g];
+        }
+    }
+    __syncwarp();
+
+    // -- logits of the page's tiles: A rows gID / gID+8 = tokens 16m+gID /
+    //    16m+gID+8; k-step (g, h) takes slot g of words 2tq+h of each token
+    float la[4][NT], lb[4][NT];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) la[m][nt] = lb[m][nt] = -INFINITY;
+        if (m < ntile) {
+            const int ta = 16 * m + gID;
+            const uint2 x = *reinterpret_cast<const uint2*>(blk + kKCodes + ta * 32 + 8 * tq);
+            const uint2 y = *reinterpret_cast<const uint2*>(blk + kKCodes + (ta + 8) * 32 + 8 * tq);
+            const uint32_t wa[2] = {x.x, x.y}, wb[2] = {y.x, y.y};
+            const uint32_t wa8[2] = {wa[0] >> 8, wa[1] >> 8}, wb8[2] = {wb[0] >> 8, wb[1] >> 8};
+            float acc[4][NT][4];
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc[g][nt][e] = 0.f;
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+                // half-major order: the four groups' accumulation chains interleave
+                const int h = it >> 2, g = it & 3, ks = 2 * g + h;
+                uint32_t a0, a1, a2, a3;
+                switch (g) {  // compile-time after unrolling
+                    case 0: k_operands<0>(wa[h], wb[h], wa8[h], wb8[h], cm, a0, a1, a2, a3); break;
+                    case 1: k_operands<1>(wa[h], wb[h], wa8[h], wb8[h], cm, a0, a1, a2, a3); break;
+                    case 2: k_operands<2>(wa[h], wb[h], wa8[h], wb8[h], cm, a0, a1, a2, a3); break;
+                    default: k_operands<3>(wa[h], wb[h], wa8[h], wb8[h], cm, a0, a1, a2, a3); break;
+                }
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const uint2 qb = qfS[(nt * 8 + ks) * 32 + lane];
+                    mma_bf16_16816(acc[g][nt], a0, a1, a2, a3, qb.x, qb.y);
+                }
+            }
+            const float4 sA = ksS[ta], sB = ksS[ta + 8], zA = kzS[ta], zB = kzS[ta + 8];
+            const float sa[4] = {sA.x, sA.y, sA.z, sA.w}, za[4] = {zA.x, zA.y, zA.z, zA.w};
+            const float sb[4] = {sB.x, sB.y, sB.z, sB.w}, zb[4] = {zB.x, zB.y, zB.z, zB.w};
+            const bool va = FULL || ta < valid, vb = FULL || ta + 8 < valid;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const float qg[4] = {qsv[nt].x, qsv[nt].y, qsv[nt].z, qsv[nt].w};
+                float xa = 0.f, xb = 0.f;
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    xa = fmaf(sa[g], acc[g][nt][0] + acc[g][nt][1], xa);
+                    xa = fmaf(za[g], qg[g], xa);
+                    xb = fmaf(sb[g], acc[g][nt][2] + acc[g][nt][3], xb);
+                    xb = fmaf(zb[g], qg[g], xb);
+                }
+                la[m][nt] = va ? xa : -INFINITY;
+                lb[m][nt] = vb ? xb : -INFINITY;
+            }
+        }
+    }
+
+    // -- online softmax (base 2), once per page; every token's p is written
+    //    (0 for the invalid ones)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        float mx = fmaxf(la[0][nt], lb[0][nt]);
+#pragma unroll
+        for (int m = 1; m < 4; ++m) mx = fmaxf(mx, fmaxf(la[m][nt], lb[m][nt]));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+        const float m_new = fmaxf(m_run[nt], mx);
+        if (__any_sync(kFull, m_new > m_run[nt])) {  // warp-uniform rescale
+            const float alpha = (m_new > m_run[nt]) ? ex2(m_run[nt] - m_new) : 1.f;
+            l_run[nt] *= alpha;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) zacc[nt][g] *= alpha;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc_o[nt][mt][e] *= alpha;
+            m_run[nt] = m_new;
+        }
+        const float m_sub = (m_new == -INFINITY) ? 0.f : m_new;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int ta = 16 * m + gID;
+            const float pa = ex2(la[m][nt] - m_sub), pb = ex2(lb[m][nt] - m_sub);
+            if (FULL || m < ntile) {
+                l_run[nt] += pa + pb;
+                const float4 vzA = vzS[ta], vzB = vzS[ta + 8];
+                zacc[nt][0] = fmaf(pa, vzA.x, fmaf(pb, vzB.x, zacc[nt][0]));
+                zacc[nt][1] = fmaf(pa, vzA.y, fmaf(pb, vzB.y, zacc[nt][1]));
+                zacc[nt][2] = fmaf(pa, vzA.z, fmaf(pb, vzB.z, zacc[nt][2]));
+                zacc[nt][3] = fmaf(pa, vzA.w, fmaf(pb, vzB.w, zacc[nt][3]));
+            }
+            pS[(nt * 4 + tq) * kPvRow + pv_pos(ta)] = pa;
+            pS[(nt * 4 + tq) * kPvRow + pv_pos(ta + 8)] = pb;
+        }
+    }
+    __syncwarp();
+
+    // -- values: A rows = dims (m-tile (g, half): in-group index 16 half +
+    //    row, code plane 16 half + row, slot g), k = token group 4 tq + m
+    //    (tokens 4q, 4q+2 | 4q+1, 4q+3), columns = heads (hi, lo)
+    uint4 pv4[4];  // bytes 16 tq .. 16 tq + 15 of planes gID, 8 + gID, 16 + gID, 24 + gID
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        pv4[k] = *reinterpret_cast<const uint4*>(blk + kVCodes + (gID + 8 * k) * kPage + 16 * tq);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const int chunk = 4 * (4 * tq + (m ^ tq));
+        float4 pp[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+            pp[nt] = *reinterpret_cast<const float4*>(pS + (nt * 4 + (gID >> 1)) * kPvRow + chunk);
+        uint32_t pw[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) pw[k] = m == 0 ? pv4[k].x : m == 1 ? pv4[k].y : m == 2 ? pv4[k].z : pv4[k].w;
+        const uint32_t pw8[4] = {pw[0] >> 8, pw[1] >> 8, pw[2] >> 8, pw[3] >> 8};
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const float4 sg = *reinterpret_cast<const float4*>(vsS + g * kPvRow + chunk);
+            uint32_t bb0[NT], bb1[NT];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                bb0[nt] = split_w_pair(make_float2(pp[nt].x, pp[nt].y), make_float2(sg.x, sg.y), take_lo);
+                bb1[nt] = split_w_pair(make_float2(pp[nt].z, pp[nt].w), make_float2(sg.z, sg.w), take_lo);
+            }
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const uint32_t r0 = pw[2 * half], r1 = pw[2 * half + 1];
+                const uint32_t r08 = pw8[2 * half], r18 = pw8[2 * half + 1];
+                uint32_t a0, a1, a2, a3;
+                switch (g) {
+                    case 0: v_operands<0>(r0, r1, r08, r18, cm, a0, a1, a2, a3); break;
+                    case 1: v_operands<1>(r0, r1, r08, r18, cm, a0, a1, a2, a3); break;
+                    case 2: v_operands<2>(r0, r1, r08, r18, cm, a0, a1, a2, a3); break;
+                    default: v_operands<3>(r0, r1, r08, r18, cm, a0, a1, a2, a3); break;
+                }
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                    mma_bf16_16816(acc_o[nt][2 * g + half], a0, a1, a2, a3, bb0[nt], bb1[nt]);
+            }
+        }
+    }
 }
 
 template <int NT>
@@ -357,12 +569,7 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
     // ------------------------------- consumers ---------------------------------
     const int gID = lane >> 2, tq = lane & 3;
     uint8_t* wbuf = smem + SM::kWarp + warp * SM::kWarpBytes;
-    float4* ksS = reinterpret_cast<float4*>(wbuf + SM::kWKs);   // [64] K s
-    float4* kzS = reinterpret_cast<float4*>(wbuf + SM::kWKz);   // [64] K z - M s
-    float4* vzS = reinterpret_cast<float4*>(wbuf + SM::kWVz);   // [64] V z - M s
-    float* vsS = reinterpret_cast<float*>(wbuf + SM::kWVs);     // [4][64] V s
-    float* pS = reinterpret_cast<float*>(wbuf + SM::kWP);       // [G4][64] P
-    const float2 take_lo = (gID & 1) ? make_float2(1.f, 1.f) : make_float2(0.f, 0.f);  // PV column: hi / lo
+    const SplitSel take_lo = split_sel(gID & 1);  // PV column: hi / lo
     const CodeMul cm = code_mul_regs(p.code_mul);
 
     uint32_t merge_phase = 0;
@@ -376,7 +583,7 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
         return __all_sync(kFull, w);
     };
 
-    uint32_t qf[NT][8][2];
+    uint2* qfS = reinterpret_cast<uint2*>(smem + SM::kQf);
     float4 qsv[NT];
     float m_run[NT], l_run[NT], zacc[NT][4], acc_o[NT][8][4];
 
@@ -398,11 +605,8 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
             for (int nt = 0; nt < NT; ++nt) {
                 const uint32_t* fr = p.qfrag + ((size_t)bk * NT + nt) * 8 * 32 * 2;
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint2 v = *reinterpret_cast<const uint2*>(fr + ((size_t)ks * 32 + lane) * 2);
-                    qf[nt][ks][0] = v.x;
-                    qf[nt][ks][1] = v.y;
-                }
+                for (int ks = 0; ks < 8; ++ks)  // every warp writes the same values
+                    qfS[(nt * 8 + ks) * 32 + lane] = *reinterpret_cast<const uint2*>(fr + ((size_t)ks * 32 + lane) * 2);
                 qsv[nt] = *reinterpret_cast<const float4*>(p.qsum + ((size_t)bk * NT * 4 + 4 * nt + tq) * 4);
                 m_run[nt] = -INFINITY;
                 l_run[nt] = 0.f;
@@ -416,181 +620,10 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
         }
 
         if (!(flags & kFlagPad)) {
-            const int ntile = (valid + 15) >> 4;  // warp-uniform, 1..4
-
-            // -- scales of the page: fp16 (s, z) -> fp32 (s, z - M_g s); rows
-            //    past the valid tokens are zero
-#pragma unroll
-            for (int it = 0; it < 4; ++it) {
-                const int which = it >> 1, t = lane + 32 * (it & 1);
-                if (t < 16 * ntile) {
-                    float sv[4], zz[4];
-                    if (t < valid) {
-                        const uint4 raw =
-                            *reinterpret_cast<const uint4*>(blk + (which ? kVScale : kKScale) + t * 16);
-                        const uint32_t r[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-                        for (int g = 0; g < 4; ++g) {  // z - M_g s with the group's code offset M_g
-                            sv[g] = half_lo(r[g]);
-                            zz[g] = fmaf(which ? -v_magic(g) : -k_magic(g), sv[g], half_hi(r[g]));
-                        }
-                    } else {
-#pragma unroll
-                        for (int g = 0; g < 4; ++g) sv[g] = zz[g] = 0.f;
-                    }
-                    if (which == 0) {
-                        ksS[t] = make_float4(sv[0], sv[1], sv[2], sv[3]);
-                        kzS[t] = make_float4(zz[0], zz[1], zz[2], zz[3]);
-                    } else {
-                        vzS[t] = make_float4(zz[0], zz[1], zz[2], zz[3]);
-                        const int ts = (t & ~15) | pv_slot(t & 15);
-#pragma unroll
-                        for (int g = 0; g < 4; ++g) vsS[g * 64 + ts] = sv[g];
-                    }
-                }
-            }
-            __syncwarp();
-
-            // -- logits of the page's tiles: A rows gID / gID+8 = tokens
-            //    16m+gID / 16m+gID+8; k-step (g, h) takes slot g of words
-            //    2tq+h of each token
-            float la[4][NT], lb[4][NT];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) la[m][nt] = lb[m][nt] = -INFINITY;
-                if (m < ntile) {
-                    const int ta = 16 * m + gID;
-                    const uint2 x = *reinterpret_cast<const uint2*>(blk + kKCodes + ta * 32 + 8 * tq);
-                    const uint2 y = *reinterpret_cast<const uint2*>(blk + kKCodes + (ta + 8) * 32 + 8 * tq);
-                    const uint32_t wa[2] = {x.x, x.y}, wb[2] = {y.x, y.y};
-                    const uint32_t wa8[2] = {wa[0] >> 8, wa[1] >> 8}, wb8[2] = {wb[0] >> 8, wb[1] >> 8};
-                    float acc[4][NT][4];
-#pragma unroll
-                    for (int g = 0; g < 4; ++g)
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) acc[g][nt][e] = 0.f;
-#pragma unroll
-                    for (int it = 0; it < 8; ++it) {
-                        // half-major order: the four groups' accumulation chains interleave
-                        const int h = it >> 2, g = it & 3, ks = 2 * g + h;
-                        uint32_t a0, a1, a2, a3;
-                        switch (g) {  // compile-time after unrolling
-                            case 0: k_operands<0>(wa[h], wb[h], wa8[h], wb8[h], cm, a0, a1, a2, a3); break;
-                            case 1: k_operands<1>(wa[h], wb[h], wa8[h], wb8[h], cm, a0, a1, a2, a3); break;
-                            case 2: k_operands<2>(wa[h], wb[h], wa8[h], wb8[h], cm, a0, a1, a2, a3); break;
-                            default: k_operands<3>(wa[h], wb[h], wa8[h], wb8[h], cm, a0, a1, a2, a3); break;
-                        }
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt)
-                            mma_bf16_16816(acc[g][nt], a0, a1, a2, a3, qf[nt][ks][0], qf[nt][ks][1]);
-                    }
-                    const float4 sA = ksS[ta], sB = ksS[ta + 8], zA = kzS[ta], zB = kzS[ta + 8];
-                    const float sa[4] = {sA.x, sA.y, sA.z, sA.w}, za[4] = {zA.x, zA.y, zA.z, zA.w};
-                    const float sb[4] = {sB.x, sB.y, sB.z, sB.w}, zb[4] = {zB.x, zB.y, zB.z, zB.w};
-                    const bool va = ta < valid, vb = ta + 8 < valid;
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        const float qg[4] = {qsv[nt].x, qsv[nt].y, qsv[nt].z, qsv[nt].w};
-                        float xa = 0.f, xb = 0.f;
-#pragma unroll
-                        for (int g = 0; g < 4; ++g) {
-                            xa = fmaf(sa[g], acc[g][nt][0] + acc[g][nt][1], xa);
-                            xa = fmaf(za[g], qg[g], xa);
-                            xb = fmaf(sb[g], acc[g][nt][2] + acc[g][nt][3], xb);
-                            xb = fmaf(zb[g], qg[g], xb);
-                        }
-                        la[m][nt] = va ? xa : -INFINITY;
-                        lb[m][nt] = vb ? xb : -INFINITY;
-                    }
-                }
-            }
-
-            // -- online softmax (base 2), once per page
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                float mx = fmaxf(la[0][nt], lb[0][nt]);
-#pragma unroll
-                for (int m = 1; m < 4; ++m) mx = fmaxf(mx, fmaxf(la[m][nt], lb[m][nt]));
-                mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
-                mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
-                mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
-                const float m_new = fmaxf(m_run[nt], mx);
-                if (__any_sync(kFull, m_new > m_run[nt])) {  // warp-uniform rescale
-                    const float alpha = (m_new > m_run[nt]) ? ex2(m_run[nt] - m_new) : 1.f;
-                    l_run[nt] *= alpha;
-#pragma unroll
-                    for (int g = 0; g < 4; ++g) zacc[nt][g] *= alpha;
-#pragma unroll
-                    for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) acc_o[nt][mt][e] *= alpha;
-                    m_run[nt] = m_new;
-                }
-                const float m_sub = (m_new == -INFINITY) ? 0.f : m_new;
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    if (m < ntile) {
-                        const int ta = 16 * m + gID;
-                        const float pa = ex2(la[m][nt] - m_sub), pb = ex2(lb[m][nt] - m_sub);
-                        l_run[nt] += pa + pb;
-                        const float4 vzA = vzS[ta], vzB = vzS[ta + 8];
-                        zacc[nt][0] = fmaf(pa, vzA.x, fmaf(pb, vzB.x, zacc[nt][0]));
-                        zacc[nt][1] = fmaf(pa, vzA.y, fmaf(pb, vzB.y, zacc[nt][1]));
-                        zacc[nt][2] = fmaf(pa, vzA.z, fmaf(pb, vzB.z, zacc[nt][2]));
-                        zacc[nt][3] = fmaf(pa, vzA.w, fmaf(pb, vzB.w, zacc[nt][3]));
-                        pS[(nt * 4 + tq) * 64 + 16 * m + pv_slot(gID)] = pa;
-                        pS[(nt * 4 + tq) * 64 + 16 * m + pv_slot(gID + 8)] = pb;
-                    }
-                }
-            }
-            __syncwarp();
-
-            // -- values: A rows = dims (m-tile (g, half): in-group index 16 half +
-            //    row, code plane 16 half + row, slot g), k = the 16 tokens of
-            //    tile m (4tq, 4tq+2 | 4tq+1, 4tq+3), columns = heads (hi, lo)
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                if (m < ntile) {
-                    float4 pp[NT];
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-                        pp[nt] = *reinterpret_cast<const float4*>(pS + (nt * 4 + (gID >> 1)) * 64 + 16 * m + 4 * tq);
-                    const uint8_t* vrow = blk + kVCodes + 16 * m + 4 * tq;
-                    const uint32_t pw[4] = {*reinterpret_cast<const uint32_t*>(vrow + gID * kPage),
-                                            *reinterpret_cast<const uint32_t*>(vrow + (8 + gID) * kPage),
-                                            *reinterpret_cast<const uint32_t*>(vrow + (16 + gID) * kPage),
-                                            *reinterpret_cast<const uint32_t*>(vrow + (24 + gID) * kPage)};
-                    const uint32_t pw8[4] = {pw[0] >> 8, pw[1] >> 8, pw[2] >> 8, pw[3] >> 8};
-#pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        const float4 sg = *reinterpret_cast<const float4*>(vsS + g * 64 + 16 * m + 4 * tq);
-                        uint32_t bb0[NT], bb1[NT];
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) {
-                            bb0[nt] = split_w_pair(make_float2(pp[nt].x, pp[nt].y), make_float2(sg.x, sg.y), take_lo);
-                            bb1[nt] = split_w_pair(make_float2(pp[nt].z, pp[nt].w), make_float2(sg.z, sg.w), take_lo);
-                        }
-#pragma unroll
-                        for (int half = 0; half < 2; ++half) {
-                            const uint32_t r0 = pw[2 * half], r1 = pw[2 * half + 1];
-                            const uint32_t r08 = pw8[2 * half], r18 = pw8[2 * half + 1];
-                            uint32_t a0, a1, a2, a3;
-                            switch (g) {
-                                case 0: v_operands<0>(r0, r1, r08, r18, cm, a0, a1, a2, a3); break;
-                                case 1: v_operands<1>(r0, r1, r08, r18, cm, a0, a1, a2, a3); break;
-                                case 2: v_operands<2>(r0, r1, r08, r18, cm, a0, a1, a2, a3); break;
-                                default: v_operands<3>(r0, r1, r08, r18, cm, a0, a1, a2, a3); break;
-                            }
-#pragma unroll
-                            for (int nt = 0; nt < NT; ++nt)
-                                mma_bf16_16816(acc_o[nt][2 * g + half], a0, a1, a2, a3, bb0[nt], bb1[nt]);
-                        }
-                    }
-                }
-            }
+            if (valid == kPage)
+                attend_page<NT, true>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o, cm, take_lo);
+            else
+                attend_page<NT, false>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o, cm, take_lo);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
@@ -782,13 +815,12 @@ __device__ void bf16_tile(const DecodeParams& p, int b, int kv, int t0, int nval
 
     // P as the A operand of O = P.V (k = the 16 tokens): even rows take the
     // bf16 high part, odd rows the rounded remainder
-    const float2 take_lo = (gID & 1) ? make_float2(1.f, 1.f) : make_float2(0.f, 0.f);
-    const float2 one = make_float2(1.f, 1.f);
+    const SplitSel take_lo = split_sel(gID & 1);
     uint32_t pa[4];
-    pa[0] = row_lo_on ? split_w_pair(make_float2(sacc[0][0], sacc[0][1]), one, take_lo) : 0u;
-    pa[2] = row_lo_on ? split_w_pair(make_float2(sacc[1][0], sacc[1][1]), one, take_lo) : 0u;
-    pa[1] = kHigh ? split_w_pair(make_float2(sacc[0][2], sacc[0][3]), one, take_lo) : 0u;
-    pa[3] = kHigh ? split_w_pair(make_float2(sacc[1][2], sacc[1][3]), one, take_lo) : 0u;
+    pa[0] = row_lo_on ? split_pair(make_float2(sacc[0][0], sacc[0][1]), take_lo) : 0u;
+    pa[2] = row_lo_on ? split_pair(make_float2(sacc[1][0], sacc[1][1]), take_lo) : 0u;
+    pa[1] = kHigh ? split_pair(make_float2(sacc[0][2], sacc[0][3]), take_lo) : 0u;
+    pa[3] = kHigh ? split_pair(make_float2(sacc[1][2], sacc[1][3]), take_lo) : 0u;
 
     // O = P.V over dims 8j .. 8j+7 (B via ldmatrix.trans: matrix i/8 = tokens
     // 8((i/8)&1) + i%8, dims 16jp + 8(i/16))

@@ -146,19 +146,40 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
     return r;
 }
 
-// B-operand register of two products w = p * s, split into bf16 hi + lo:
-// hi = w with its low 16 bits cleared (exact in bf16), w - hi exact in fp32.
-// Returns the hi parts (take_lo = 0) or the rounded w - hi (take_lo = 1),
-// chosen arithmetically so that hi and lo lanes run the same instructions.
+// (x & mask) ^ bits in one LOP3
+__device__ __forceinline__ uint32_t lop3_and_xor(uint32_t x, uint32_t mask, uint32_t bits) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(r) : "r"(x), "r"(mask), "r"(bits));
+    return r;
+}
+
+// Selector of the bf16 hi / lo split below: a lane taking the hi parts uses
+// (a, sign) = (0, 0), a lane taking the lo parts (1, 0x80000000).
+struct SplitSel {
+    float2 a;
+    uint32_t sign;
+};
+__device__ __forceinline__ SplitSel split_sel(bool take_lo) {
+    return take_lo ? SplitSel{make_float2(1.f, 1.f), 0x80000000u} : SplitSel{make_float2(0.f, 0.f), 0u};
+}
+
+// A bf16x2 MMA operand register from two fp32 values w, split into bf16
+// hi + lo: hi = w with its low 16 bits cleared (exact in bf16), lo = w - hi
+// (exact in fp32, then rounded).  Returns the hi pair or the rounded lo
+// pair, chosen arithmetically so that hi and lo lanes run the same
+// instructions: x = a * w + (hi with its sign flipped by `sign`).
 // (hi is taken by masking, not by the rounding-based Veltkamp split: the
 // packed c - (c - w) form is exposed to algebraic simplification.)
-__device__ __forceinline__ uint32_t split_w_pair(float2 p, float2 s, float2 take_lo) {
-    const float2 w = mul2(p, s);
-    const float2 hi = make_float2(__uint_as_float(__float_as_uint(w.x) & 0xffff0000u),
-                                  __uint_as_float(__float_as_uint(w.y) & 0xffff0000u));
-    const float2 e = fma2(make_float2(-2.0f, -2.0f), hi, w);  // w - 2 hi, exact
-    const float2 x = fma2(take_lo, e, hi);                     // hi or w - hi
+__device__ __forceinline__ uint32_t split_pair(float2 w, const SplitSel& sel) {
+    const float2 hs = make_float2(__uint_as_float(lop3_and_xor(__float_as_uint(w.x), 0xffff0000u, sel.sign)),
+                                  __uint_as_float(lop3_and_xor(__float_as_uint(w.y), 0xffff0000u, sel.sign)));
+    const float2 x = fma2(sel.a, w, hs);  // hi, or w - hi
     return pack_bf16x2_rn(x.x, x.y);
+}
+
+// the same for the products w = p * s
+__device__ __forceinline__ uint32_t split_w_pair(float2 p, float2 s, const SplitSel& sel) {
+    return split_pair(mul2(p, s), sel);
 }
 
 // Token order inside the shared probability / V-scale rows of a 16-token
