@@ -45,7 +45,19 @@ constexpr int kPrepSeqs = 2;
 constexpr int kPrepThreads = 256;
 constexpr int kPrepSmem = kD * kD * 4 + (kPrepThreads / 32) * kD * 4;
 
+__device__ __forceinline__ void prep_body(const DecodeParams& p);
+
+// Launched as a programmatic dependent of the eviction (it reads neither the
+// pool nor the BF16 segment), so the two overlap; it waits for the
+// eviction's completion before it exits, so that everything launched after
+// it sees the evicted tokens.
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(DecodeParams p) {
+    pdl_trigger();
+    prep_body(p);
+    if (threadIdx.x == 0) pdl_wait();
+}
+
+__device__ __forceinline__ void prep_body(const DecodeParams& p) {
     extern __shared__ __align__(16) float psm[];
     float* Us = psm;                       // [a][k] = U_K[a][k]
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -489,6 +501,8 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
         fence_mbar_init();
     }
     __syncthreads();
+    pdl_wait();     // q' fragments, plan and counter come from prep_kernel
+    pdl_trigger();  // the BF16 segment kernel may take SMs as this grid retires
 
     if (warp == kConsumerWarps) {
         // ------------------------------ producer ------------------------------
@@ -865,8 +879,12 @@ __device__ void bf16_tile(const DecodeParams& p, int b, int kv, int t0, int nval
     }
 }
 
+// Launched as a programmatic dependent of int2_kernel, whose results it does
+// not read; it waits for int2_kernel's completion before it exits, so that
+// the merge after it sees both.
 __global__ void __launch_bounds__(kBfThreads) bf16_kernel(DecodeParams p) {
     extern __shared__ __align__(128) uint8_t bsm[];
+    pdl_trigger();
     const int item = blockIdx.x, bk = blockIdx.y;
     const int b = bk / p.hk, kv = bk % p.hk;
     const int warp = threadIdx.x >> 5;
@@ -904,6 +922,7 @@ __global__ void __launch_bounds__(kBfThreads) bf16_kernel(DecodeParams p) {
             part[(size_t)p.G * kD + p.G + h] = L;
         }
     }
+    if (threadIdx.x == 0) pdl_wait();
 }
 
 // ---------------------------------------------------------------------------
@@ -932,6 +951,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(DecodeParams p) {
                          : "memory");
         asm volatile("cp.async.commit_group;" ::: "memory");
     }
+    pdl_wait();  // partials of int2_kernel and bf16_kernel
     const int r = blockIdx.x * kMergeRows + warp;
     const bool active = r < p.B * p.G;
     const int b = active ? r / p.G : 0, hh = active ? r % p.G : 0;
@@ -1065,8 +1085,26 @@ static cudaError_t launch_int2(const DecodeParams& p, cudaStream_t st, int sms, 
     const int max_items = p.B * p.hk * ((p.max_pages + p.pps - 1) / p.pps);
     int blocks = min(per_sm * sms, max_items);
     if (blocks < 1) blocks = 1;
-    int2_kernel<NT><<<blocks, kInt2Threads, smem, st>>>(p);
-    return cudaGetLastError();
+    cudaError_t e = launch_pdl(int2_kernel<NT>, dim3(blocks), dim3(kInt2Threads), smem, st, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// Launch with a programmatic dependency on the previous kernel in the stream
+// (the kernel itself decides where it waits, see pdl_wait).
+template <typename... Args>
+static cudaError_t launch_pdl(void (*kernel)(Args...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              const DecodeParams& p) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st, cudaEvent_t ev_int2_start,
@@ -1085,8 +1123,7 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st, cudaEvent_t ev
         at.setp = true;
     }
     dim3 pg((p.B + kPrepSeqs - 1) / kPrepSeqs + 1, p.hk);
-    prep_kernel<<<pg, kPrepThreads, kPrepSmem, st>>>(p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_pdl(prep_kernel, pg, dim3(kPrepThreads), kPrepSmem, st, p)) != cudaSuccess) return e;
     if (ev_int2_start && (e = cudaEventRecord(ev_int2_start, st)) != cudaSuccess) return e;
     e = (p.NT == 1) ? launch_int2<1>(p, st, at.sms, at.set1) : launch_int2<2>(p, st, at.sms, at.set2);
     if (e != cudaSuccess) return e;
@@ -1096,16 +1133,15 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st, cudaEvent_t ev
         if (e != cudaSuccess) return e;
         at.setb = true;
     }
-    bf16_kernel<<<dim3(p.bf_items, p.B * p.hk), kBfThreads, kBfSmem, st>>>(p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    e = launch_pdl(bf16_kernel, dim3(p.bf_items, p.B * p.hk), dim3(kBfThreads), kBfSmem, st, p);
+    if (e != cudaSuccess) return e;
     if (!at.setm) {
         e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMergeSmem);
         if (e != cudaSuccess) return e;
         at.setm = true;
     }
     dim3 mg((p.B * p.G + kMergeRows - 1) / kMergeRows, p.hk);
-    merge_kernel<<<mg, kMergeThreads, kMergeSmem, st>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(merge_kernel, mg, dim3(kMergeThreads), kMergeSmem, st, p);
 }
 
 }  // namespace oscar

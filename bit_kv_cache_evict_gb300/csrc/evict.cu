@@ -49,6 +49,7 @@ __device__ __forceinline__ df df_neg(df a) { return {-a.hi, -a.lo}; }
 // exactly and finishes the vector.
 __global__ void __launch_bounds__(128) evict_kernel(EvictParams p) {
     __shared__ df part[4][kD];
+    pdl_trigger();  // the decode's query preparation does not read what this kernel writes
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int vec = blockIdx.x;
     const int i = vec / (p.hk * 2);

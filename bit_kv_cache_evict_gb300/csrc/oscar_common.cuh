@@ -47,6 +47,12 @@ __device__ __forceinline__ unsigned short f64_to_f16_bits(double x) {
     return h;
 }
 
+// Programmatic dependent launch: let the next kernel in the stream start
+// launching now / wait until the kernels this one overlaps with are complete
+// and their writes visible (a no-op without a programmatic dependency).
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

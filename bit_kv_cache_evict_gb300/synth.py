@@ -87,6 +87,10 @@ WORKLOADS: dict[str, Workload] = {
                        ctx_hi=131072, prefix_seqs=32, prefix_tokens=2048),
     # Qwen3-8B layout, batch 64, context exactly 32768, one layer.
     "gate": Workload(6, "gate", batch=64, hq=32, hk=8),
+    # One sequence of 100K tokens (the long-context, batch-1 decode of a full
+    # prefix-cache hit: all of the history is already in the pool), Qwen3-8B
+    # heads, 36 layers; the split-K plan has to fill the GPU from one sequence.
+    "longctx_b1": Workload(7, "longctx_b1", batch=1, hq=32, hk=8, layers=36, ctx_lo=100000, ctx_hi=100000),
 }
 
 

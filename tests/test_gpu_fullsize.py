@@ -45,6 +45,8 @@ def pick_units(w: S.Workload, ctx: np.ndarray):
     if w.prefix_seqs:
         seqs.append(1)
     seqs = list(dict.fromkeys(seqs))
+    if len(seqs) == 1:  # one sequence: two of its KV heads
+        return [(seqs[0], 1), (seqs[0], w.hk - 2)]
     return [(b, (3 * i + 1) % w.hk) for i, b in enumerate(seqs)]
 
 
@@ -72,7 +74,7 @@ def inject(st, w, b, kv, orc):
     return sc
 
 
-@pytest.mark.parametrize("name", ["qwen3_4b", "gate", "qwen3_8b_36l", "qwen3_32b", "stress"])
+@pytest.mark.parametrize("name", ["qwen3_4b", "gate", "qwen3_8b_36l", "qwen3_32b", "stress", "longctx_b1"])
 def test_full_size_sampled(orc, name):
     w = S.WORKLOADS[name]
     st = bench.GpuState(w, 1, 1, 0)
