@@ -185,8 +185,15 @@ __device__ __forceinline__ void prep_body(const DecodeParams& p) {
         const uint32_t h01 = pack_bf16x2_rn(v0, v1), h23 = pack_bf16x2_rn(v2, v3);
         const uint32_t l01 = pack_bf16x2_rn(v0 - bf16_lo(h01), v1 - bf16_hi(h01));
         const uint32_t l23 = pack_bf16x2_rn(v2 - bf16_lo(h23), v3 - bf16_hi(h23));
-        *reinterpret_cast<uint2*>(frag + ((size_t)ks * 32 + (2 * hh) * 4 + tq) * 2) = make_uint2(h01, h23);
-        *reinterpret_cast<uint2*>(frag + ((size_t)ks * 32 + (2 * hh + 1) * 4 + tq) * 2) = make_uint2(l01, l23);
+        if (p.NT == 2) {
+            // eight heads: column = head, hi and lo parts in two fragment sets
+            uint32_t* fr = p.qfrag + (size_t)bk * 2 * 8 * 32 * 2;  // [part][ks][32] uint2
+            *reinterpret_cast<uint2*>(fr + ((size_t)(0 * 8 + ks) * 32 + 4 * hl + tq) * 2) = make_uint2(h01, h23);
+            *reinterpret_cast<uint2*>(fr + ((size_t)(1 * 8 + ks) * 32 + 4 * hl + tq) * 2) = make_uint2(l01, l23);
+        } else {
+            *reinterpret_cast<uint2*>(frag + ((size_t)ks * 32 + (2 * hh) * 4 + tq) * 2) = make_uint2(h01, h23);
+            *reinterpret_cast<uint2*>(frag + ((size_t)ks * 32 + (2 * hh + 1) * 4 + tq) * 2) = make_uint2(l01, l23);
+        }
     }
 }
 
@@ -481,6 +488,192 @@ __device__ __forceinline__ void attend_page(const uint8_t* blk, int valid, uint8
     }
 }
 
+// Split two fp32 values into bf16x2 registers of their high parts (the
+// values with the low 16 bits cleared) and of the rounded remainders.
+__device__ __forceinline__ void split_both(float2 w, uint32_t& hi, uint32_t& lo) {
+    const uint32_t wx = __float_as_uint(w.x), wy = __float_as_uint(w.y);
+    hi = __byte_perm(wx, wy, 0x7632);
+    const float2 r = sub2(w, make_float2(__uint_as_float(wx & 0xffff0000u), __uint_as_float(wy & 0xffff0000u)));
+    lo = pack_bf16x2_rn(r.x, r.y);
+}
+
+// attend_page for eight query heads per KV head: the MMA columns are the
+// heads, and the hi / lo parts of q' and of P*s enter as two MMAs on the
+// same A fragment (accumulating into the same registers).  Lane (gID, tq)
+// holds heads 2tq and 2tq + 1.
+template <bool FULL>
+__device__ __forceinline__ void attend_page_g8(const uint8_t* blk, int valid, uint8_t* wbuf, const uint2* qfS,
+                                               const float4 (&qsv)[2], float (&m_run)[2], float (&l_run)[2],
+                                               float (&zacc)[2][4], float (&acc_o)[8][4], const CodeMul& cm) {
+    using SM = Int2Smem<2>;
+    const int lane = threadIdx.x & 31, gID = lane >> 2, tq = lane & 3;
+    if (FULL) valid = kPage;
+    float4* ksS = reinterpret_cast<float4*>(wbuf + SM::kWKs);
+    float4* kzS = reinterpret_cast<float4*>(wbuf + SM::kWKz);
+    float4* vzS = reinterpret_cast<float4*>(wbuf + SM::kWVz);
+    float* vsS = reinterpret_cast<float*>(wbuf + SM::kWVs);
+    float* pS = reinterpret_cast<float*>(wbuf + SM::kWP);       // [8 heads][kPvRow]
+    const int ntile = FULL ? 4 : (valid + 15) >> 4;
+
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int which = it >> 1, t = lane + 32 * (it & 1);
+        float sv[4], zz[4];
+        if (FULL || t < valid) {
+            const uint4 raw = *reinterpret_cast<const uint4*>(blk + (which ? kVScale : kKScale) + t * 16);
+            const uint32_t r[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                sv[g] = half_lo(r[g]);
+                zz[g] = fmaf(which ? -v_magic(g) : -k_magic(g), sv[g], half_hi(r[g]));
+            }
+        } else {
+#pragma unroll
+            for (int g = 0; g < 4; ++g) sv[g] = zz[g] = 0.f;
+        }
+        if (which == 0) {
+            ksS[t] = make_float4(sv[0], sv[1], sv[2], sv[3]);
+            kzS[t] = make_float4(zz[0], zz[1], zz[2], zz[3]);
+        } else {
+            vzS[t] = make_float4(zz[0], zz[1], zz[2], zz[3]);
+            const int ps = pv_pos(t);
+#pragma unroll
+            for (int g = 0; g < 4; ++g) vsS[g * kPvRow + ps] = sv[g];
+        }
+    }
+    __syncwarp();
+
+    // -- logits: lg[m] = (token a, head 2tq), (a, 2tq+1), (b, 2tq), (b, 2tq+1)
+    //    with a = 16m + gID, b = a + 8
+    float lg[4][4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) lg[m][e] = -INFINITY;
+        if (m < ntile) {
+            const int ta = 16 * m + gID;
+            const uint2 x = *reinterpret_cast<const uint2*>(blk + kKCodes + ta * 32 + 8 * tq);
+            const uint2 y = *reinterpret_cast<const uint2*>(blk + kKCodes + (ta + 8) * 32 + 8 * tq);
+            const uint32_t wa[2] = {x.x, x.y}, wb[2] = {y.x, y.y};
+            const uint32_t wa8[2] = {wa[0] >> 8, wa[1] >> 8}, wb8[2] = {wb[0] >> 8, wb[1] >> 8};
+            float acc[4][4];
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[g][e] = 0.f;
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+                const int h = it >> 2, g = it & 3, ks = 2 * g + h;
+                uint32_t a0, a1, a2, a3;
+                switch (g) {
+                    case 0: k_operands<0>(wa[h], wb[h], wa8[h], wb8[h], cm, a0, a1, a2, a3); break;
+                    case 1: k_operands<1>(wa[h], wb[h], wa8[h], wb8[h], cm, a0, a1, a2, a3); break;
+                    case 2: k_operands<2>(wa[h], wb[h], wa8[h], wb8[h], cm, a0, a1, a2, a3); break;
+                    default: k_operands<3>(wa[h], wb[h], wa8[h], wb8[h], cm, a0, a1, a2, a3); break;
+                }
+                const uint2 qh = qfS[(0 * 8 + ks) * 32 + lane], ql = qfS[(1 * 8 + ks) * 32 + lane];
+                mma_bf16_16816(acc[g], a0, a1, a2, a3, qh.x, qh.y);
+                mma_bf16_16816(acc[g], a0, a1, a2, a3, ql.x, ql.y);
+            }
+            const float4 sA = ksS[ta], sB = ksS[ta + 8], zA = kzS[ta], zB = kzS[ta + 8];
+            const float sa[4] = {sA.x, sA.y, sA.z, sA.w}, za[4] = {zA.x, zA.y, zA.z, zA.w};
+            const float sb[4] = {sB.x, sB.y, sB.z, sB.w}, zb[4] = {zB.x, zB.y, zB.z, zB.w};
+            const float q0[4] = {qsv[0].x, qsv[0].y, qsv[0].z, qsv[0].w};
+            const float q1[4] = {qsv[1].x, qsv[1].y, qsv[1].z, qsv[1].w};
+            float xa0 = 0.f, xa1 = 0.f, xb0 = 0.f, xb1 = 0.f;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                xa0 = fmaf(sa[g], acc[g][0], fmaf(za[g], q0[g], xa0));
+                xa1 = fmaf(sa[g], acc[g][1], fmaf(za[g], q1[g], xa1));
+                xb0 = fmaf(sb[g], acc[g][2], fmaf(zb[g], q0[g], xb0));
+                xb1 = fmaf(sb[g], acc[g][3], fmaf(zb[g], q1[g], xb1));
+            }
+            const bool va = FULL || ta < valid, vb = FULL || ta + 8 < valid;
+            lg[m][0] = va ? xa0 : -INFINITY;
+            lg[m][1] = va ? xa1 : -INFINITY;
+            lg[m][2] = vb ? xb0 : -INFINITY;
+            lg[m][3] = vb ? xb1 : -INFINITY;
+        }
+    }
+
+    // -- online softmax per head (j: head 2tq + j)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        float mx = fmaxf(lg[0][j], lg[0][2 + j]);
+#pragma unroll
+        for (int m = 1; m < 4; ++m) mx = fmaxf(mx, fmaxf(lg[m][j], lg[m][2 + j]));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+        const float m_new = fmaxf(m_run[j], mx);
+        if (__any_sync(kFull, m_new > m_run[j])) {
+            const float alpha = (m_new > m_run[j]) ? ex2(m_run[j] - m_new) : 1.f;
+            l_run[j] *= alpha;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) zacc[j][g] *= alpha;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                acc_o[mt][j] *= alpha;
+                acc_o[mt][2 + j] *= alpha;
+            }
+            m_run[j] = m_new;
+        }
+        const float m_sub = (m_new == -INFINITY) ? 0.f : m_new;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int ta = 16 * m + gID;
+            const float pa = ex2(lg[m][j] - m_sub), pb = ex2(lg[m][2 + j] - m_sub);
+            if (FULL || m < ntile) {
+                l_run[j] += pa + pb;
+                const float4 vzA = vzS[ta], vzB = vzS[ta + 8];
+                zacc[j][0] = fmaf(pa, vzA.x, fmaf(pb, vzB.x, zacc[j][0]));
+                zacc[j][1] = fmaf(pa, vzA.y, fmaf(pb, vzB.y, zacc[j][1]));
+                zacc[j][2] = fmaf(pa, vzA.z, fmaf(pb, vzB.z, zacc[j][2]));
+                zacc[j][3] = fmaf(pa, vzA.w, fmaf(pb, vzB.w, zacc[j][3]));
+            }
+            pS[(2 * tq + j) * kPvRow + pv_pos(ta)] = pa;
+            pS[(2 * tq + j) * kPvRow + pv_pos(ta + 8)] = pb;
+        }
+    }
+    __syncwarp();
+
+    // -- values: as attend_page, with B column gID = head gID (hi, then lo)
+    uint4 pv4[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        pv4[k] = *reinterpret_cast<const uint4*>(blk + kVCodes + (gID + 8 * k) * kPage + 16 * tq);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const int chunk = 4 * (4 * tq + (m ^ tq));
+        const float4 pp = *reinterpret_cast<const float4*>(pS + gID * kPvRow + chunk);
+        uint32_t pw[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) pw[k] = m == 0 ? pv4[k].x : m == 1 ? pv4[k].y : m == 2 ? pv4[k].z : pv4[k].w;
+        const uint32_t pw8[4] = {pw[0] >> 8, pw[1] >> 8, pw[2] >> 8, pw[3] >> 8};
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const float4 sg = *reinterpret_cast<const float4*>(vsS + g * kPvRow + chunk);
+            uint32_t bh0, bl0, bh1, bl1;
+            split_both(mul2(make_float2(pp.x, pp.y), make_float2(sg.x, sg.y)), bh0, bl0);
+            split_both(mul2(make_float2(pp.z, pp.w), make_float2(sg.z, sg.w)), bh1, bl1);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const uint32_t r0 = pw[2 * half], r1 = pw[2 * half + 1];
+                const uint32_t r08 = pw8[2 * half], r18 = pw8[2 * half + 1];
+                uint32_t a0, a1, a2, a3;
+                switch (g) {
+                    case 0: v_operands<0>(r0, r1, r08, r18, cm, a0, a1, a2, a3); break;
+                    case 1: v_operands<1>(r0, r1, r08, r18, cm, a0, a1, a2, a3); break;
+                    case 2: v_operands<2>(r0, r1, r08, r18, cm, a0, a1, a2, a3); break;
+                    default: v_operands<3>(r0, r1, r08, r18, cm, a0, a1, a2, a3); break;
+                }
+                mma_bf16_16816(acc_o[2 * g + half], a0, a1, a2, a3, bh0, bh1);
+                mma_bf16_16816(acc_o[2 * g + half], a0, a1, a2, a3, bl0, bl1);
+            }
+        }
+    }
+}
+
 template <int NT>
 __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(DecodeParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -621,7 +814,9 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)  // every warp writes the same values
                     qfS[(nt * 8 + ks) * 32 + lane] = *reinterpret_cast<const uint2*>(fr + ((size_t)ks * 32 + lane) * 2);
-                qsv[nt] = *reinterpret_cast<const float4*>(p.qsum + ((size_t)bk * NT * 4 + 4 * nt + tq) * 4);
+                // head of the lane's column: 4nt + tq (up to four heads), 2tq + nt (eight)
+                const int hq = (NT == 2) ? 2 * tq + nt : 4 * nt + tq;
+                qsv[nt] = *reinterpret_cast<const float4*>(p.qsum + ((size_t)bk * NT * 4 + hq) * 4);
                 m_run[nt] = -INFINITY;
                 l_run[nt] = 0.f;
 #pragma unroll
@@ -634,10 +829,17 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
         }
 
         if (!(flags & kFlagPad)) {
-            if (valid == kPage)
-                attend_page<NT, true>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o, cm, take_lo);
-            else
-                attend_page<NT, false>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o, cm, take_lo);
+            if constexpr (NT == 2) {
+                if (valid == kPage)
+                    attend_page_g8<true>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o[0], cm);
+                else
+                    attend_page_g8<false>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o[0], cm);
+            } else {
+                if (valid == kPage)
+                    attend_page<NT, true>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o, cm, take_lo);
+                else
+                    attend_page<NT, false>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o, cm, take_lo);
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
@@ -658,6 +860,21 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
                     z[g] += __shfl_xor_sync(kFull, z[g], 4);
                     z[g] += __shfl_xor_sync(kFull, z[g], 8);
                     z[g] += __shfl_xor_sync(kFull, z[g], 16);
+                }
+                if constexpr (NT == 2) {  // column = head 2tq + nt (hi and lo summed by the MMA)
+                    float* o = mw + (size_t)(2 * tq + nt) * (kD + 2);
+#pragma unroll
+                    for (int g = 0; g < 4; ++g)
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            o[32 * g + 16 * half + gID] = acc_o[0][2 * g + half][nt] + z[g];
+                            o[32 * g + 16 * half + 8 + gID] = acc_o[0][2 * g + half][2 + nt] + z[g];
+                        }
+                    if (gID == 0) {
+                        o[kD] = m_run[nt];
+                        o[kD + 1] = l;
+                    }
+                    continue;
                 }
                 float* o = mw + (size_t)(4 * nt + tq) * (kD + 2);
 #pragma unroll
