@@ -264,6 +264,13 @@ oscar_status oscar_decode_attn(const oscar_shape* shape, int32_t batch, const vo
     p.NT = w.NT;
     p.nslot = shape->sink + shape->recent;
     p.bf_items = bf16_items(shape);
+    {   // merge warps per row: more when rows are few and split-K partials many
+        const int splits = (max_pages + w.pps - 1) / w.pps;
+        const int rows = batch * p.G;
+        int wpr = 1;
+        while (wpr < 8 && splits > 16 * wpr && rows * wpr < 4096) wpr *= 2;
+        p.merge_wpr = wpr;
+    }
     p.max_pages = max_pages;
     p.num_pages = num_pages;
     p.pps = w.pps;

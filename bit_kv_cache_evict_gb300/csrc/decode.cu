@@ -97,10 +97,14 @@ __device__ __forceinline__ void prep_body(const DecodeParams& p) {
     const int kv = blockIdx.y;
     const int b0 = blockIdx.x * kPrepSeqs;
     const int nseq = min(kPrepSeqs, p.B - b0);
-    {
-        const float4* src = reinterpret_cast<const float4*>(p.U + ((size_t)kv * 2 + 0) * kD * kD);
-        float4* dst = reinterpret_cast<float4*>(Us);
-        for (int i = threadIdx.x; i < kD * kD / 4; i += kPrepThreads) dst[i] = __ldg(src + i);
+    {   // U_K -> shared memory, all copies in flight at once
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(p.U + ((size_t)kv * 2 + 0) * kD * kD);
+        uint8_t* dst = reinterpret_cast<uint8_t*>(Us);
+        for (int i = threadIdx.x; i < kD * kD / 4; i += kPrepThreads)
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst + 16 * i)), "l"(src + 16 * i)
+                         : "memory");
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
     }
     __syncthreads();
 
@@ -1145,19 +1149,23 @@ __global__ void __launch_bounds__(kBfThreads) bf16_kernel(DecodeParams p) {
 // ---------------------------------------------------------------------------
 // merge: INT2 splits -> un-rotate -> merge with the BF16 partial
 // ---------------------------------------------------------------------------
-// One warp per output row (b, head), eight rows per block, block y = KV
-// head.  U_V is copied row-major into shared memory with cp.async while the
-// warps merge their split-K partials; the un-rotation o = w . U_V^T then
-// reads U_V in a lane-rotated order (lane l takes index (j + l) mod 128 at
-// step j) so that every shared-memory access is conflict-free.
-constexpr int kMergeRows = 8;
-constexpr int kMergeThreads = 32 * kMergeRows;
-constexpr int kMergeSmem = (kD * kD + kMergeRows * kD) * 4;
+// Block = 8 warps, block y = KV head.  Each output row (b, head) is served by
+// p.merge_wpr warps (1, 2, 4 or 8: more when rows are few and splits many,
+// e.g. one long sequence): the row's split-K partials are dealt round-robin
+// to its warps, each warp merges its share (log-sum-exp in base 2), and the
+// row's first warp combines the shares.  U_V is copied row-major into shared
+// memory with cp.async meanwhile; the un-rotation o = w . U_V^T then reads
+// U_V in a lane-rotated order (lane l takes index (j + l) mod 128 at step j)
+// so that every shared-memory access is conflict-free.
+constexpr int kMergeWarps = 8;
+constexpr int kMergeThreads = 32 * kMergeWarps;
+constexpr int kMergeRow = kD + 4;  // floats per warp row (y[128], M, L; a multiple of 4 for float4 access)
+constexpr int kMergeSmem = (kD * kD + kMergeWarps * kMergeRow) * 4;
 
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(DecodeParams p) {
     extern __shared__ __align__(16) float msm[];
     float* Us = msm;                  // [a][j] = U_V[a][j]
-    float* Wr = msm + kD * kD;        // [warp][j]: normalised o'.P.H (Hadamard domain)
+    float* Ws = msm + kD * kD;        // [warp][kMergeRow]: a warp's share (y, M, L), then the row's w
     const int kv = blockIdx.y;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     {
@@ -1169,26 +1177,25 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(DecodeParams p) {
         asm volatile("cp.async.commit_group;" ::: "memory");
     }
     pdl_wait();  // partials of int2_kernel and bf16_kernel
-    const int r = blockIdx.x * kMergeRows + warp;
+    const int wpr = p.merge_wpr, rpb = kMergeWarps / wpr;
+    const int r = blockIdx.x * rpb + warp / wpr, sub = warp % wpr;
     const bool active = r < p.B * p.G;
     const int b = active ? r / p.G : 0, hh = active ? r % p.G : 0;
-    float M = -INFINITY, L = 0.f;
+    const int r5 = bitrev5(lane);
+    // lane handles Hadamard indices j = 4 lane + k, stored at bitrev7(j)
+    float M = -INFINITY, L = 0.f, y[4] = {0.f, 0.f, 0.f, 0.f};
     if (active) {
         const int s0 = __ldg(p.item_start + b);
         const int splits = (__ldg(p.item_start + b + 1) - s0) / p.hk;
         const int first = s0 + kv * splits;
-        const int r5 = bitrev5(lane);
-        // lane handles Hadamard indices j = 4 lane + k, stored at bitrev7(j);
-        // split statistics are read lane-parallel, then the partial vectors
-        // are accumulated with independent loads
-        for (int s = lane; s < splits; s += 32)
+        // this warp's splits: sub, sub + wpr, ...; statistics lane-parallel
+        for (int s = sub + wpr * lane; s < splits; s += 32 * wpr)
             M = fmaxf(M, p.part[(size_t)(first + s) * p.part_stride + (size_t)p.G * kD + hh]);
 #pragma unroll
         for (int mm = 16; mm > 0; mm >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, mm));
-        float y[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int s0b = 0; s0b < splits; s0b += 32) {
+        for (int s0b = sub; s0b < splits; s0b += 32 * wpr) {
             float sc = 0.f;
-            const int sl = s0b + lane;
+            const int sl = s0b + wpr * lane;
             if (sl < splits) {
                 const float* pt = p.part + (size_t)(first + sl) * p.part_stride + (size_t)p.G * kD;
                 const float ls = pt[p.G + hh];
@@ -1197,17 +1204,52 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(DecodeParams p) {
                     L += sc * ls;
                 }
             }
-            const int cnt = min(32, splits - s0b);
-#pragma unroll 4
+            const int cnt = min(32, (splits - s0b + wpr - 1) / wpr);
+#pragma unroll 8
             for (int i = 0; i < cnt; ++i) {
                 const float w = __shfl_sync(kFull, sc, i);
-                const float* o = p.part + (size_t)(first + s0b + i) * p.part_stride + (size_t)hh * kD;
+                const float* o = p.part + (size_t)(first + s0b + wpr * i) * p.part_stride + (size_t)hh * kD;
 #pragma unroll
                 for (int k = 0; k < 4; ++k) y[k] = fmaf(w, o[32 * bitrev2(k) + r5], y[k]);
             }
         }
 #pragma unroll
         for (int mm = 16; mm > 0; mm >>= 1) L += __shfl_xor_sync(kFull, L, mm);
+    }
+    if (wpr > 1) {  // combine the row's shares in its first warp
+        float* ws = Ws + (size_t)warp * kMergeRow;
+        *reinterpret_cast<float4*>(ws + 4 * lane) = make_float4(y[0], y[1], y[2], y[3]);
+        if (lane == 0) {
+            ws[kD] = M;
+            ws[kD + 1] = L;
+        }
+        __syncthreads();
+        if (sub == 0 && active) {
+            float Mt = -INFINITY;
+            for (int i = 0; i < wpr; ++i) Mt = fmaxf(Mt, Ws[(size_t)(warp + i) * kMergeRow + kD]);
+            float Lt = 0.f, yt[4] = {0.f, 0.f, 0.f, 0.f};
+            if (Mt != -INFINITY) {
+                for (int i = 0; i < wpr; ++i) {
+                    const float* wi = Ws + (size_t)(warp + i) * kMergeRow;
+                    if (wi[kD] == -INFINITY) continue;
+                    const float sc = ex2(wi[kD] - Mt);
+                    Lt = fmaf(sc, wi[kD + 1], Lt);
+                    const float4 v = *reinterpret_cast<const float4*>(wi + 4 * lane);
+                    yt[0] = fmaf(sc, v.x, yt[0]);
+                    yt[1] = fmaf(sc, v.y, yt[1]);
+                    yt[2] = fmaf(sc, v.z, yt[2]);
+                    yt[3] = fmaf(sc, v.w, yt[3]);
+                }
+            }
+            M = Mt;
+            L = Lt;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) y[k] = yt[k];
+        }
+        __syncthreads();  // shares read before the rows' w overwrite them
+    }
+    const bool lead = active && sub == 0;
+    if (lead) {
         const float inv = (L > 0.f) ? 1.f / L : 0.f;
 #pragma unroll
         for (int k = 0; k < 4; ++k) y[k] *= inv;
@@ -1227,15 +1269,15 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(DecodeParams p) {
                 y[k] = upper ? o - y[k] : y[k] + o;
             }
         }
-        *reinterpret_cast<float4*>(Wr + (size_t)warp * kD + 4 * lane) =
+        *reinterpret_cast<float4*>(Ws + (size_t)warp * kMergeRow + 4 * lane) =
             make_float4(y[0] * (float)kInvSqrtD, y[1] * (float)kInvSqrtD, y[2] * (float)kInvSqrtD,
                         y[3] * (float)kInvSqrtD);
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
     __syncthreads();
-    if (!active) return;
+    if (!lead) return;
     // o[a] = sum_j w[j] U_V[a][j] for a = lane + 32 c
-    const float* w = Wr + (size_t)warp * kD;
+    const float* w = Ws + (size_t)warp * kMergeRow;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 8
     for (int j = 0; j < kD; ++j) {
@@ -1357,7 +1399,8 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st, cudaEvent_t ev
         if (e != cudaSuccess) return e;
         at.setm = true;
     }
-    dim3 mg((p.B * p.G + kMergeRows - 1) / kMergeRows, p.hk);
+    const int rpb = kMergeWarps / p.merge_wpr;
+    dim3 mg((p.B * p.G + rpb - 1) / rpb, p.hk);
     return launch_pdl(merge_kernel, mg, dim3(kMergeThreads), kMergeSmem, st, p);
 }
 

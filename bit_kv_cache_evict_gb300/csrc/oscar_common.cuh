@@ -295,6 +295,7 @@ struct DecodeParams {
     float* bf_part;       // [B*Hk][bf_items][part_stride]
     int B, hq, hk, G, NT, nslot, max_pages, num_pages, pps, part_stride;
     int bf_items;  // 64-token blocks of the BF16 segment: ceil(nslot / 64)
+    int merge_wpr; // merge warps per output row (1, 2, 4, 8)
     float qscale;  // sm_scale * log2(e)
     // multipliers that move a code pair from bits (P, P+16) to (4, 20):
     // index P/2; 2^(4-P) for P < 4 (low product), 2^(36-P) for P > 4 (high
