@@ -37,7 +37,12 @@ from bit_kv_cache_evict_gb300 import synth as S  # noqa: E402
 
 METRIC = "decode context-tokens/s attended"
 UNIT = "tokens/s"
-HIST_BYTES_PER_TOKEN_HEAD = 96      # 2 x 32 B codes + 2 x 4 x (fp16 s, fp16 z)
+HIST_BYTES_PER_TOKEN_HEAD = 96      # 2 x 32 B codes + 2 x 4 x (fp16 s, fp16 z) at 32 positions per group
+
+
+def hist_bytes_per_token_head(g: int) -> int:
+    """INT2 history bytes per (token, KV head): K and V codes + (s, z) pairs."""
+    return 2 * 32 + 2 * (128 // g) * 4
 BF16_BYTES_PER_TOKEN_HEAD = 2 * 128 * 2
 DEFAULT_WORKLOAD = "qwen3_8b_36l"
 
@@ -84,6 +89,8 @@ def parse_args():
                     help="oracle steps timed for cpu_baseline (about 10 s of host work)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--quant-group", type=int, default=32, choices=[32, 64, 128],
+                    help="stored positions per fp16 scale/zero pair (32 is the configured format)")
     return ap.parse_args()
 
 
@@ -219,7 +226,7 @@ def load_peaks() -> dict:
 class GpuState:
     """Pools, BF16 segments, queries and per-step metadata for every layer."""
 
-    def __init__(self, w: S.Workload, layers: int, steps_total: int, rank: int):
+    def __init__(self, w: S.Workload, layers: int, steps_total: int, rank: int, quant_group: int = 32):
         import torch
         from bit_kv_cache_evict_gb300 import oscar as O
         self.O, self.torch = O, torch
@@ -227,7 +234,8 @@ class GpuState:
         dev = torch.device("cuda")
         self.dev = dev
         B, Hq, Hk, d = w.batch, w.hq, w.hk, S.D
-        self.shape = O.make_shape(Hq, Hk)
+        self.shape = O.make_shape(Hq, Hk, quant_group=quant_group)
+        self.hist_tok_bytes = hist_bytes_per_token_head(quant_group)
         ctx = S.context_lengths(w)
         self.ctx0 = ctx
         hist0 = np.maximum(ctx - S.NSLOT, 0).astype(np.int64)
@@ -320,17 +328,17 @@ class GpuState:
         with shared prefix pages counted per sequence and once."""
         hist = self.hist0 + s + 1
         elems = float((hist + S.NSLOT).sum()) * 2 * S.D
-        hist_bits = float(hist.sum()) * HIST_BYTES_PER_TOKEN_HEAD * 8
+        hist_bits = float(hist.sum()) * self.hist_tok_bytes * 8
         bf16_bits = float(self.B * S.NSLOT) * BF16_BYTES_PER_TOKEN_HEAD * 8
-        out = {"int2_history": HIST_BYTES_PER_TOKEN_HEAD * 8 / (2 * S.D),
+        out = {"int2_history": self.hist_tok_bytes * 8 / (2 * S.D),
                "all_tokens": (hist_bits + bf16_bits) / elems}
         if self.w.prefix_seqs:
-            dup = (self.w.prefix_seqs - 1) * self.w.shared_hist_tokens * HIST_BYTES_PER_TOKEN_HEAD * 8
+            dup = (self.w.prefix_seqs - 1) * self.w.shared_hist_tokens * self.hist_tok_bytes * 8
             out["all_tokens_shared_pages_once"] = (hist_bits - dup + bf16_bits) / elems
         return out
 
     def step_bytes(self, s: int) -> float:
-        hist = self.hist_tokens_after(s) * self.Hk * HIST_BYTES_PER_TOKEN_HEAD
+        hist = self.hist_tokens_after(s) * self.Hk * self.hist_tok_bytes
         bf16 = self.B * S.NSLOT * self.Hk * BF16_BYTES_PER_TOKEN_HEAD
         qo = self.B * self.Hq * S.D * (2 + 4)
         evict = self.B * self.Hk * 2 * (S.D * 2 * 2 + 48)    # read old + write new row, write codes + s/z
@@ -440,11 +448,11 @@ def run_reference(args, rank: int, world: int) -> None:
     print(json.dumps(line), flush=True)
 
 
-def config_of(w: S.Workload, layers: int) -> dict:
+def config_of(w: S.Workload, layers: int, quant_group: int = 32) -> dict:
     ctx = {"fixed": f"{w.ctx_lo}", "uniform": f"uniform[{w.ctx_lo},{w.ctx_hi}]",
            "loguniform": f"loguniform[{w.ctx_lo},{w.ctx_hi}]"}[w.ctx_kind]
     cfg = {"workload": w.name, "batch_per_gpu": w.batch, "layers": layers, "q_heads": w.hq, "kv_heads": w.hk,
-           "head_dim": S.D, "context": ctx, "sink": S.SINK, "recent": S.RECENT, "quant_group": S.GROUP,
+           "head_dim": S.D, "context": ctx, "sink": S.SINK, "recent": S.RECENT, "quant_group": quant_group,
            "page": S.PAGE, "page_table": "shuffled" if w.shuffled else "contiguous",
            "kv_values": w.dist, "l2": "inputs larger than L2 (a distinct pool per layer)",
            "parallelism": "replicas (independent sequences per GPU)"}
@@ -466,7 +474,7 @@ def run_oscar(args, rank: int, world: int, local: int) -> None:
     e2e_steps = 0 if args.no_e2e else K
     total_steps = W + K + e2e_steps
     t0 = time.time()
-    st = GpuState(w, L, total_steps, rank)
+    st = GpuState(w, L, total_steps, rank, args.quant_group)
     setup_s = time.time() - t0
     stream = torch.cuda.current_stream()
 
@@ -509,7 +517,7 @@ def run_oscar(args, rank: int, world: int, local: int) -> None:
     value, t_ms_max = aggregate(t_ms, att, world, dev)
     ms_per_step = t_ms_max / K
     step_bytes = sum(st.step_bytes(W + k) for k in range(K)) * L / K
-    hist_bytes = [st.hist_tokens_after(W + k) * st.Hk * HIST_BYTES_PER_TOKEN_HEAD for k in range(K)]
+    hist_bytes = [st.hist_tokens_after(W + k) * st.Hk * st.hist_tok_bytes for k in range(K)]
     int2_avg_ms = statistics.mean(int2_ms)
     int2_bytes = statistics.mean(hist_bytes)
     peaks = load_peaks()
@@ -558,14 +566,14 @@ def run_oscar(args, rank: int, world: int, local: int) -> None:
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
             "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "int2 codes x bf16 hi/lo on tensor cores, fp32 accumulate", "data": "synthetic",
-            "config": config_of(w, L),
+            "config": config_of(w, L, args.quant_group),
             "decode_tokens_per_s": world * w.batch * K / (t_ms_max / 1e3),
             "bits_per_element": st.bits_per_element(W + K - 1),
             "step_algorithmic_gbs": step_bytes / (ms_per_step * 1e-3) / 1e9,
             "roofline": {"kernel": "int2_kernel (split-K INT2 history attention)", "bound": "hbm",
                          "achieved": achieved, "peak": peaks["hbm_gbs"], "peak_source": peaks["source"],
                          "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                         "traffic": int2_traffic(w.name, int2_bytes),
+                         "traffic": int2_traffic(w.name if args.quant_group == 32 else "", int2_bytes),
                          "bytes_per_launch": int2_bytes, "launch_ms": int2_avg_ms,
                          "share_of_step": int2_avg_ms * L / ms_per_step,
                          "launches_timed": len(int2_ms)},

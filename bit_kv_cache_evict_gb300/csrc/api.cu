@@ -43,13 +43,19 @@ static oscar_status check_shape(const oscar_shape* s) {
         s->head_dim % s->quant_group != 0)
         return OSCAR_ERR_INVALID_ARG;
     const int G = s->num_q_heads / s->num_kv_heads;
-    if (s->head_dim != kD || s->quant_group != kGroup || s->page_size != kPage) return OSCAR_ERR_UNSUPPORTED;
+    if (s->head_dim != kD || s->page_size != kPage) return OSCAR_ERR_UNSUPPORTED;
+    if (s->quant_group != 32 && s->quant_group != 64 && s->quant_group != 128) return OSCAR_ERR_UNSUPPORTED;
     if (G != 1 && G != 2 && G != 4 && G != 8) return OSCAR_ERR_UNSUPPORTED;
     if (s->sink + s->recent > 320) return OSCAR_ERR_UNSUPPORTED;
     return OSCAR_OK;
 }
 
 static int bf16_items(const oscar_shape* s) { return (s->sink + s->recent + 63) / 64; }
+
+// log2(quant_group / 32) and the (page, KV head) block size: K and V codes
+// (2 x 2048 B) + K and V (s, z) pairs (2 x 64 tokens x d/g x 4 B)
+static int gshift_of(const oscar_shape* s) { return s->quant_group == 32 ? 0 : (s->quant_group == 64 ? 1 : 2); }
+static int block_bytes_of(const oscar_shape* s) { return 4096 + 512 * (kD / s->quant_group); }
 
 struct WsLayout {
     size_t counter, item_start, qfrag, qsum, part, bf_part, total;
@@ -98,7 +104,7 @@ extern "C" {
 
 size_t oscar_block_bytes(const oscar_shape* shape) {
     if (check_shape(shape) != OSCAR_OK) return 0;
-    return (size_t)kBlock;
+    return (size_t)block_bytes_of(shape);
 }
 
 const char* oscar_status_string(oscar_status st) {
@@ -178,7 +184,8 @@ oscar_status oscar_pool_layout(const oscar_shape* shape, int32_t batch, const in
     }
     if (batch > 0) std::memcpy(page_table, table.data(), table.size() * sizeof(int32_t));
     if (num_pages_out) *num_pages_out = (int32_t)next;
-    if (pool_bytes_out) *pool_bytes_out = (uint64_t)next * (uint64_t)shape->num_kv_heads * (uint64_t)kBlock;
+    if (pool_bytes_out)
+        *pool_bytes_out = (uint64_t)next * (uint64_t)shape->num_kv_heads * (uint64_t)block_bytes_of(shape);
     return OSCAR_OK;
 }
 
@@ -215,6 +222,8 @@ oscar_status oscar_evict_quantize(const oscar_shape* shape, int32_t n_tok, const
     p.batch = batch;
     p.max_pages = max_pages;
     p.num_pages = num_pages;
+    p.gshift = gshift_of(shape);
+    p.block_bytes = block_bytes_of(shape);
     const cudaError_t e = launch_evict(p, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? OSCAR_OK : cuda_fail(e);
 }
@@ -273,6 +282,8 @@ oscar_status oscar_decode_attn(const oscar_shape* shape, int32_t batch, const vo
     }
     p.max_pages = max_pages;
     p.num_pages = num_pages;
+    p.gshift = gshift_of(shape);
+    p.block_bytes = block_bytes_of(shape);
     p.pps = w.pps;
     p.part_stride = w.part_stride;
     p.qscale = sm_scale * kLog2e;

@@ -297,6 +297,70 @@ __device__ __forceinline__ int pv_pos(int t) {
 }
 constexpr int kPvRow = 72;  // floats per probability / V-scale row (64 + 8: conflict-free stores)
 
+// The page's scales into the warp's scratch: for each token row and each
+// 32-position block b (quantisation group b >> GS), fp32 s and z - M_b s with
+// the block's code offset M_b; rows past the valid tokens are zero.  K rows:
+// s and z - M s as float4 per token; V rows: z - M s per token, and s in the
+// P.V token order (pv_pos).
+template <bool FULL, int GS>
+__device__ __forceinline__ void page_scales_g(const uint8_t* blk, int valid, float4* ksS, float4* kzS, float4* vzS,
+                                              float* vsS) {
+    constexpr int NG = 4 >> GS;  // (s, z) pairs per token vector
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int which = it >> 1, t = lane + 32 * (it & 1);
+        float sv[4], zz[4];
+        if (FULL || t < valid) {
+            const uint8_t* base = blk + (which ? v_scale_off(GS) : kKScale) + t * 4 * NG;
+            uint32_t w[NG];
+            if constexpr (NG == 4) {
+                const uint4 v = *reinterpret_cast<const uint4*>(base);
+                w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+            } else if constexpr (NG == 2) {
+                const uint2 v = *reinterpret_cast<const uint2*>(base);
+                w[0] = v.x; w[1] = v.y;
+            } else {
+                w[0] = *reinterpret_cast<const uint32_t*>(base);
+            }
+            float s_g[NG], z_g[NG];
+#pragma unroll
+            for (int k = 0; k < NG; ++k) {
+                s_g[k] = half_lo(w[k]);
+                z_g[k] = half_hi(w[k]);
+            }
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                sv[b] = s_g[b >> GS];
+                zz[b] = fmaf(which ? -v_magic(b) : -k_magic(b), sv[b], z_g[b >> GS]);
+            }
+        } else {
+#pragma unroll
+            for (int b = 0; b < 4; ++b) sv[b] = zz[b] = 0.f;
+        }
+        if (which == 0) {
+            ksS[t] = make_float4(sv[0], sv[1], sv[2], sv[3]);
+            kzS[t] = make_float4(zz[0], zz[1], zz[2], zz[3]);
+        } else {
+            vzS[t] = make_float4(zz[0], zz[1], zz[2], zz[3]);
+            const int ps = pv_pos(t);
+#pragma unroll
+            for (int b = 0; b < 4; ++b) vsS[b * kPvRow + ps] = sv[b];
+        }
+    }
+}
+
+template <bool FULL>
+__device__ __forceinline__ void page_scales(const uint8_t* blk, int valid, int gshift, float4* ksS, float4* kzS,
+                                            float4* vzS, float* vsS) {
+    switch (gshift) {  // warp-uniform, once per page
+        case 0: page_scales_g<FULL, 0>(blk, valid, ksS, kzS, vzS, vsS); break;
+        case 1: page_scales_g<FULL, 1>(blk, valid, ksS, kzS, vzS, vsS); break;
+        default: page_scales_g<FULL, 2>(blk, valid, ksS, kzS, vzS, vsS); break;
+    }
+}
+
+
 // One page of INT2 history for one consumer warp: the page's scales, the
 // logits of its four 16-token tiles, one online-softmax update, and the P.V
 // products.  FULL (all 64 tokens valid, the common case) removes the
@@ -306,7 +370,7 @@ template <int NT, bool FULL>
 __device__ __forceinline__ void attend_page(const uint8_t* blk, int valid, uint8_t* wbuf, const uint2* qfS,
                                             const float4 (&qsv)[NT], float (&m_run)[NT], float (&l_run)[NT],
                                             float (&zacc)[NT][4], float (&acc_o)[NT][8][4], const CodeMul& cm,
-                                            const SplitSel& take_lo) {
+                                            const SplitSel& take_lo, int gshift) {
     using SM = Int2Smem<NT>;
     const int lane = threadIdx.x & 31, gID = lane >> 2, tq = lane & 3;
     if (FULL) valid = kPage;
@@ -317,34 +381,7 @@ __device__ __forceinline__ void attend_page(const uint8_t* blk, int valid, uint8
     float* pS = reinterpret_cast<float*>(wbuf + SM::kWP);       // [G4][kPvRow] P at pv_pos
     const int ntile = FULL ? 4 : (valid + 15) >> 4;             // warp-uniform, 1..4
 
-    // -- scales of the page: fp16 (s, z) -> fp32 (s, z - M_g s); rows past
-    //    the valid tokens are zero
-#pragma unroll
-    for (int it = 0; it < 4; ++it) {
-        const int which = it >> 1, t = lane + 32 * (it & 1);
-        float sv[4], zz[4];
-        if (FULL || t < valid) {
-            const uint4 raw = *reinterpret_cast<const uint4*>(blk + (which ? kVScale : kKScale) + t * 16);
-            const uint32_t r[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {  // z - M_g s with the group's code offset M_g
-                sv[g] = half_lo(r[g]);
-                zz[g] = fmaf(which ? -v_magic(g) : -k_magic(g), sv[g], half_hi(r[g]));
-            }
-        } else {
-#pragma unroll
-            for (int g = 0; g < 4; ++g) sv[g] = zz[g] = 0.f;
-        }
-        if (which == 0) {
-            ksS[t] = make_float4(sv[0], sv[1], sv[2], sv[3]);
-            kzS[t] = make_float4(zz[0], zz[1], zz[2], zz[3]);
-        } else {
-            vzS[t] = make_float4(zz[0], zz[1], zz[2], zz[3]);
-            const int ps = pv_pos(t);
-#pragma unroll
-            for (int g = 0; g < 4; ++g) vsS[g * kPvRow + ps] = sv[g];
-        }
-    }
+    page_scales<FULL>(blk, valid, gshift, ksS, kzS, vzS, vsS);
     __syncwarp();
 
     // -- logits of the page's tiles: A rows gID / gID+8 = tokens 16m+gID /
@@ -508,7 +545,8 @@ __device__ __forceinline__ void split_both(float2 w, uint32_t& hi, uint32_t& lo)
 template <bool FULL>
 __device__ __forceinline__ void attend_page_g8(const uint8_t* blk, int valid, uint8_t* wbuf, const uint2* qfS,
                                                const float4 (&qsv)[2], float (&m_run)[2], float (&l_run)[2],
-                                               float (&zacc)[2][4], float (&acc_o)[8][4], const CodeMul& cm) {
+                                               float (&zacc)[2][4], float (&acc_o)[8][4], const CodeMul& cm,
+                                               int gshift) {
     using SM = Int2Smem<2>;
     const int lane = threadIdx.x & 31, gID = lane >> 2, tq = lane & 3;
     if (FULL) valid = kPage;
@@ -519,32 +557,7 @@ __device__ __forceinline__ void attend_page_g8(const uint8_t* blk, int valid, ui
     float* pS = reinterpret_cast<float*>(wbuf + SM::kWP);       // [8 heads][kPvRow]
     const int ntile = FULL ? 4 : (valid + 15) >> 4;
 
-#pragma unroll
-    for (int it = 0; it < 4; ++it) {
-        const int which = it >> 1, t = lane + 32 * (it & 1);
-        float sv[4], zz[4];
-        if (FULL || t < valid) {
-            const uint4 raw = *reinterpret_cast<const uint4*>(blk + (which ? kVScale : kKScale) + t * 16);
-            const uint32_t r[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                sv[g] = half_lo(r[g]);
-                zz[g] = fmaf(which ? -v_magic(g) : -k_magic(g), sv[g], half_hi(r[g]));
-            }
-        } else {
-#pragma unroll
-            for (int g = 0; g < 4; ++g) sv[g] = zz[g] = 0.f;
-        }
-        if (which == 0) {
-            ksS[t] = make_float4(sv[0], sv[1], sv[2], sv[3]);
-            kzS[t] = make_float4(zz[0], zz[1], zz[2], zz[3]);
-        } else {
-            vzS[t] = make_float4(zz[0], zz[1], zz[2], zz[3]);
-            const int ps = pv_pos(t);
-#pragma unroll
-            for (int g = 0; g < 4; ++g) vsS[g * kPvRow + ps] = sv[g];
-        }
-    }
+    page_scales<FULL>(blk, valid, gshift, ksS, kzS, vzS, vsS);
     __syncwarp();
 
     // -- logits: lg[m] = (token a, head 2tq), (a, 2tq+1), (b, 2tq), (b, 2tq+1)
@@ -726,8 +739,9 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
                 if (item < 0 || (flags & kFlagPad)) {
                     mbar_arrive(&full[s]);
                 } else {
-                    mbar_arrive_expect_tx(&full[s], kBlock);
-                    bulk_g2s(stages + s * kBlock, p.pool + ((size_t)pid * p.hk + kv) * kBlock, kBlock, &full[s]);
+                    mbar_arrive_expect_tx(&full[s], p.block_bytes);
+                    bulk_g2s(stages + s * kBlock, p.pool + ((size_t)pid * p.hk + kv) * p.block_bytes,
+                             p.block_bytes, &full[s]);
                 }
             }
             __syncwarp();
@@ -835,14 +849,14 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
         if (!(flags & kFlagPad)) {
             if constexpr (NT == 2) {
                 if (valid == kPage)
-                    attend_page_g8<true>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o[0], cm);
+                    attend_page_g8<true>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o[0], cm, p.gshift);
                 else
-                    attend_page_g8<false>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o[0], cm);
+                    attend_page_g8<false>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o[0], cm, p.gshift);
             } else {
                 if (valid == kPage)
-                    attend_page<NT, true>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o, cm, take_lo);
+                    attend_page<NT, true>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o, cm, take_lo, p.gshift);
                 else
-                    attend_page<NT, false>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o, cm, take_lo);
+                    attend_page<NT, false>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o, cm, take_lo, p.gshift);
             }
         }
         __syncwarp();

@@ -44,6 +44,17 @@ __device__ __forceinline__ df df_add(df a, df b) {
 
 __device__ __forceinline__ df df_neg(df a) { return {-a.hi, -a.lo}; }
 
+// exact order of normalised pairs: compare high parts, then low parts
+__device__ __forceinline__ bool df_less(df a, df b) { return a.hi < b.hi || (a.hi == b.hi && a.lo < b.lo); }
+
+// merge two blocks' (max, min) into both: the extremes of their union
+__device__ __forceinline__ void df_group_extremes(df& hi_a, df& hi_b, df& lo_a, df& lo_b) {
+    const df h = df_less(hi_a, hi_b) ? hi_b : hi_a;
+    const df l = df_less(lo_b, lo_a) ? lo_b : lo_a;
+    hi_a = hi_b = h;
+    lo_a = lo_b = l;
+}
+
 // Block = one (token, KV head, K|V) vector; warp w accumulates the terms
 // a in [32w, 32w + 32) of y = x . U, warp 0 adds the four partial sums
 // exactly and finishes the vector.
@@ -143,6 +154,13 @@ __global__ void __launch_bounds__(128) evict_kernel(EvictParams p) {
     for (int m = 16; m > 0; m >>= 1)
 #pragma unroll
         for (int k = 0; k < 4; ++k) amax[k] = fmaxf(amax[k], __shfl_xor_sync(kFull, amax[k], m));
+    // value k's 32-position block is bitrev2(k); a group of 64 (128) stored
+    // positions is blocks {0,1}, {2,3} (all four): k = {0,2}, {1,3} (all)
+    if (p.gshift >= 1) {
+        amax[0] = amax[2] = fmaxf(amax[0], amax[2]);
+        amax[1] = amax[3] = fmaxf(amax[1], amax[3]);
+    }
+    if (p.gshift >= 2) amax[0] = amax[1] = amax[2] = amax[3] = fmaxf(amax[0], amax[1]);
     // clamp to +-t, t = c * max|y| (fp32: an error of 1 ulp in t moves the
     // clipped values by 6e-8 relative)
     df lo[4], hi[4];
@@ -174,6 +192,15 @@ __global__ void __launch_bounds__(128) evict_kernel(EvictParams p) {
         }
         hi[k] = {mx, mxl};
         lo[k] = {mn, mnl};
+    }
+    if (p.gshift >= 1) {
+        df_group_extremes(hi[0], hi[2], lo[0], lo[2]);
+        df_group_extremes(hi[1], hi[3], lo[1], lo[3]);
+    }
+    if (p.gshift >= 2) {
+        df_group_extremes(hi[0], hi[1], lo[0], lo[1]);
+        hi[2] = hi[3] = hi[0];
+        lo[2] = lo[3] = lo[0];
     }
     unsigned short sb[4], zb[4];
     // value k of this lane is in-group index bitrev5(lane) of group bitrev2(k):
@@ -209,17 +236,20 @@ __global__ void __launch_bounds__(128) evict_kernel(EvictParams p) {
         return;
     }
     const int slot = pos % kPage;
-    uint8_t* blk = p.pool + ((size_t)page * p.hk + kv) * kBlock;
+    uint8_t* blk = p.pool + ((size_t)page * p.hk + kv) * p.block_bytes;
     const int j = bitrev5(lane);
     if (which == 0) blk[kKCodes + slot * (kD / 4) + j] = (uint8_t)byte;
     else blk[kVCodes + j * kPage + slot] = (uint8_t)byte;
     if (lane == 0) {
-        // group of value k is bitrev2(k); scale/zero words in group order
+        // group of value k is bitrev2(k) >> gshift; scale/zero words in group order
         uint32_t w[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) w[bitrev2(k)] = (uint32_t)sb[k] | ((uint32_t)zb[k] << 16);
-        *reinterpret_cast<uint4*>(blk + (which == 0 ? kKScale : kVScale) + slot * 16) =
-            make_uint4(w[0], w[1], w[2], w[3]);
+        for (int k = 0; k < 4; ++k) w[bitrev2(k) >> p.gshift] = (uint32_t)sb[k] | ((uint32_t)zb[k] << 16);
+        const int ng = sz_pairs(p.gshift);
+        uint8_t* sz = blk + (which == 0 ? kKScale : v_scale_off(p.gshift)) + slot * 4 * ng;
+        if (ng == 4) *reinterpret_cast<uint4*>(sz) = make_uint4(w[0], w[1], w[2], w[3]);
+        else if (ng == 2) *reinterpret_cast<uint2*>(sz) = make_uint2(w[0], w[1]);
+        else *reinterpret_cast<uint32_t*>(sz) = w[0];
     }
 }
 

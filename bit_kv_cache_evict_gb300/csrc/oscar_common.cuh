@@ -274,7 +274,14 @@ struct EvictParams {
     const int32_t* page_table;
     int32_t* status;
     int n_tok, hk, src_rows, batch, max_pages, num_pages;
+    int gshift;       // log2(quant_group / 32): 0, 1, 2
+    int block_bytes;  // bytes per (page, KV head) block: 4096 + 512 * (4 >> gshift)
 };
+
+// Scale/zero pairs per token vector (4, 2 or 1) and the V scale/zero offset
+// inside a block (the K pairs start at kKScale).
+__host__ __device__ __forceinline__ int sz_pairs(int gshift) { return 4 >> gshift; }
+__host__ __device__ __forceinline__ int v_scale_off(int gshift) { return kKScale + kPage * 4 * (4 >> gshift); }
 
 struct DecodeParams {
     const __nv_bfloat16* q;
@@ -296,6 +303,8 @@ struct DecodeParams {
     int B, hq, hk, G, NT, nslot, max_pages, num_pages, pps, part_stride;
     int bf_items;  // 64-token blocks of the BF16 segment: ceil(nslot / 64)
     int merge_wpr; // merge warps per output row (1, 2, 4, 8)
+    int gshift;    // log2(quant_group / 32)
+    int block_bytes;
     float qscale;  // sm_scale * log2(e)
     // multipliers that move a code pair from bits (P, P+16) to (4, 20):
     // index P/2; 2^(4-P) for P < 4 (low product), 2^(36-P) for P > 4 (high

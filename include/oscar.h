@@ -35,9 +35,9 @@
  *     device are skipped (a skipped history page contributes nothing) and
  *     reported by OR-ing bits into *dev_status when dev_status (a device
  *     int32) is not NULL: OSCAR_STATUS_BAD_PAGE, OSCAR_STATUS_BAD_POS.
- *   - Only head_dim 128, quant_group 32, page_size 64 and query-per-KV-head
- *     groups G = Hq/Hk in {1, 2, 4, 8} are supported; other shapes return
- *     OSCAR_ERR_UNSUPPORTED.
+ *   - Only head_dim 128, quant_group 32, 64 or 128, page_size 64 and
+ *     query-per-KV-head groups G = Hq/Hk in {1, 2, 4, 8} are supported;
+ *     other shapes return OSCAR_ERR_UNSUPPORTED.
  *
  * Data layouts (row-major, little-endian)
  *   K/V token rows   bf16 [rows][Hk][2][d]           (index 0 = K, 1 = V)
@@ -52,14 +52,16 @@
  *   page_table       int32 [B][max_pages]: history position pos of sequence
  *                    b lives in page page_table[b*max_pages + pos/64],
  *                    slot pos % 64
- *   pool             num_pages * Hk blocks of OSCAR_BLOCK_BYTES (6144 B);
- *                    block (page, kv) starts at (page*Hk + kv) * 6144 and
- *                    holds 64 token slots t:
+ *   pool             num_pages * Hk blocks of oscar_block_bytes(shape) bytes
+ *                    (OSCAR_BLOCK_BYTES = 6144 at g = 32; 5120 at g = 64,
+ *                    4608 at g = 128); block (page, kv) starts at
+ *                    (page*Hk + kv) * block_bytes and holds 64 token slots t;
+ *                    with ng = 128 / g scale/zero pairs per vector:
  *       [0, 2048)     K codes, token-major: byte t*32 + j
  *       [2048, 4096)  V codes, byte-plane-major: byte 2048 + j*64 + t
- *       [4096, 5120)  K scale/zero: at 4096 + t*16 + k*4, fp16 s then fp16 z
- *       [5120, 6144)  V scale/zero: at 5120 + t*16 + k*4
- *                    Group k is stored positions 32k..32k+31; code byte j
+ *       [4096, ...)   K scale/zero: at 4096 + t*4*ng + k*4, fp16 s then fp16 z
+ *       [4096 + 256*ng, ...)  V scale/zero: at 4096 + 256*ng + t*4*ng + k*4
+ *                    Group k is stored positions g*k .. g*k + g - 1; code byte j
  *                    (j = 0..31) holds in-group index j of each group: stored
  *                    position 32i + j in bits 2i..2i+1 (i = 0..3); stored
  *                    position p holds Hadamard output bitrev7(p) (the
@@ -94,7 +96,7 @@ typedef enum {
 
 typedef struct {
     int32_t head_dim;     /* d = 128 */
-    int32_t quant_group;  /* g = 32 elements per fp16 scale/zero */
+    int32_t quant_group;  /* g = 32, 64 or 128 elements per fp16 scale/zero */
     int32_t sink;         /* BF16 sink tokens (64) */
     int32_t recent;       /* BF16 recent-window tokens (256) */
     int32_t page_size;    /* tokens per history page (64) */

@@ -39,11 +39,15 @@ def u8_t(a) -> torch.Tensor:
 
 
 def shape_of(sc) -> O.oscar_shape:
-    return O.make_shape(sc.shape.num_q_heads, sc.shape.num_kv_heads)
+    return O.make_shape(sc.shape.num_q_heads, sc.shape.num_kv_heads, quant_group=sc.shape.quant_group)
+
+
+def block_bytes_g(g: int) -> int:
+    return 4096 + 512 * (128 // g)
 
 
 def num_pages_of(sc) -> int:
-    return sc.pool.size // (sc.shape.num_kv_heads * O.BLOCK_BYTES)
+    return sc.pool.size // (sc.shape.num_kv_heads * block_bytes_g(sc.shape.quant_group))
 
 
 def gpu_step(sc, stream=None, status=None):
@@ -84,17 +88,19 @@ def gpu_step(sc, stream=None, status=None):
             bf16_len)
 
 
-def read_vec(pool, table, b, pos, kv, which, Hk):
-    """Raw codes[128], s16[4], z16[4] of one stored token-vector (numpy)."""
+def read_vec(pool, table, b, pos, kv, which, Hk, g=32):
+    """Raw codes[128], s16[128/g], z16[128/g] of one stored token-vector (numpy)."""
+    bb, ng = block_bytes_g(g), 128 // g
     page = table[b, pos // 64]
     t = pos % 64
-    blk = pool[(page * Hk + kv) * 6144:(page * Hk + kv + 1) * 6144]
+    blk = pool[(page * Hk + kv) * bb:(page * Hk + kv + 1) * bb]
     if which == 0:
         byts = blk[t * 32:(t + 1) * 32]
     else:
         byts = blk[2048 + np.arange(32) * 64 + t]
     codes = ((byts[None, :] >> np.array([0, 2, 4, 6], np.uint8)[:, None]) & 3).reshape(-1)  # byte j: j + 32 i
-    sz = blk[4096 + which * 1024 + t * 16: 4096 + which * 1024 + (t + 1) * 16].view(np.uint16)
+    off = 4096 + which * 256 * ng + t * 4 * ng
+    sz = blk[off:off + 4 * ng].view(np.uint16)
     return codes, sz[0::2].copy(), sz[1::2].copy()
 
 
@@ -110,7 +116,7 @@ def near_f16_midpoint(v: float) -> bool:
     return any(abs(v - m) <= MIDPOINT_REL * abs(v) for m in mids)
 
 
-def compare_evicted(pool_g, pool_o, table, items, aux, Hk):
+def compare_evicted(pool_g, pool_o, table, items, aux, Hk, g=32):
     """items: list of (b, pos, aux_index); aux = (u, s_pre, z_pre) from the
     oracle [n][Hk][2][...].  Returns the list of exempt codes; asserts the
     rest are bit-exact."""
@@ -120,11 +126,11 @@ def compare_evicted(pool_g, pool_o, table, items, aux, Hk):
     for (b, pos, ai) in items:
         for kv in range(Hk):
             for which in range(2):
-                cg, sg, zg = read_vec(pool_g, table, b, pos, kv, which, Hk)
-                co, so, zo = read_vec(pool_o, table, b, pos, kv, which, Hk)
+                cg, sg, zg = read_vec(pool_g, table, b, pos, kv, which, Hk, g)
+                co, so, zo = read_vec(pool_o, table, b, pos, kv, which, Hk, g)
                 total += cg.size
-                group_exempt = np.zeros(4, bool)
-                for k in range(4):
+                group_exempt = np.zeros(128 // g, bool)
+                for k in range(128 // g):
                     if sg[k] != so[k] or zg[k] != zo[k]:
                         assert near_f16_midpoint(sp[ai, kv, which, k]) or near_f16_midpoint(zp[ai, kv, which, k]), \
                             (b, pos, kv, which, k, hex(sg[k]), hex(so[k]), hex(zg[k]), hex(zo[k]))
@@ -133,7 +139,7 @@ def compare_evicted(pool_g, pool_o, table, items, aux, Hk):
                 for j in bad:
                     uu = u[ai, kv, which, j]
                     near = abs((uu - np.floor(uu)) - 0.5) < BOUNDARY
-                    assert near or group_exempt[j // 32], (b, pos, kv, which, j, int(cg[j]), int(co[j]), uu)
+                    assert near or group_exempt[j // g], (b, pos, kv, which, j, int(cg[j]), int(co[j]), uu)
                     exempt.append((b, pos, kv, which, int(j), float(uu)))
     assert len(exempt) <= max(1, MAX_EXEMPT_FRAC * total), (len(exempt), total)
     return exempt

@@ -214,16 +214,18 @@ def check_minmax_textbook(o: oracle.Oracle):
     """Clip ratio 1 reduces to textbook asymmetric min-max INT2 with an
     fp16 scale/zero (numpy float16 rounding, numpy half-to-even rint)."""
     rng = np.random.default_rng(9)
-    for trial in range(100):
-        y = rng.standard_normal(128) * 3
-        c, s16, z16, *_ = o.quantize_vec(y, 32, 1.0)
-        for k in range(4):
-            yg = y[32 * k:32 * k + 32]
-            s = np.float16((yg.max() - yg.min()) / 3)
-            z = np.float16(yg.min())
-            ref = np.clip(np.rint((yg - np.float64(z)) / np.float64(s)), 0, 3)
-            assert s16[k] == s.view(np.uint16) and z16[k] == z.view(np.uint16)
-            assert np.array_equal(c[32 * k:32 * k + 32], ref)
+    for g in (32, 64, 128):
+        for trial in range(100):
+            y = rng.standard_normal(128) * 3
+            c, s16, z16, *_ = o.quantize_vec(y, g, 1.0)
+            assert len(s16) == 128 // g
+            for k in range(128 // g):
+                yg = y[g * k:g * k + g]
+                s = np.float16((yg.max() - yg.min()) / 3)
+                z = np.float16(yg.min())
+                ref = np.clip(np.rint((yg - np.float64(z)) / np.float64(s)), 0, 3)
+                assert s16[k] == s.view(np.uint16) and z16[k] == z.view(np.uint16)
+                assert np.array_equal(c[g * k:g * k + g], ref)
 
 
 def check_clip(o: oracle.Oracle):
@@ -234,15 +236,16 @@ def check_clip(o: oracle.Oracle):
         y = rng.standard_normal(128)
         y[5] = 40.0
         y[70] = -35.0
-        c, s16, z16, u, sp, zp = o.quantize_vec(y, 32, 0.5)
-        for k in range(4):
-            yg = y[32 * k:32 * k + 32]
-            t = 0.5 * np.max(np.abs(yg))
-            yc = np.clip(yg, -t, t)
-            assert abs(sp[k] - (yc.max() - yc.min()) / 3) <= 1e-15 * abs(sp[k]) + 1e-300
-            assert zp[k] == yc.min()
-        assert c[5] == 3 and c[70] == 0
-        assert sp[0] < (40.0 + 1.0) / 3
+        for g in (32, 128):
+            c, s16, z16, u, sp, zp = o.quantize_vec(y, g, 0.5)
+            for k in range(128 // g):
+                yg = y[g * k:g * k + g]
+                t = 0.5 * np.max(np.abs(yg))
+                yc = np.clip(yg, -t, t)
+                assert abs(sp[k] - (yc.max() - yc.min()) / 3) <= 1e-15 * abs(sp[k]) + 1e-300
+                assert zp[k] == yc.min()
+            assert c[5] == 3 and c[70] == 0
+            assert sp[0] < (40.0 + 1.0) / 3
 
 
 def check_degenerate(o: oracle.Oracle):

@@ -24,9 +24,18 @@ def test_exports_every_declared_symbol(lib):
         assert hasattr(lib, n), n
 
 
+def orc_block_bytes(g):
+    import oracle as orcmod
+    return orcmod.get().block_bytes(128, g, 64)
+
+
 def test_block_bytes_and_status_strings(lib):
     assert O.block_bytes(O.make_shape(32, 8)) == 6144
-    assert O.block_bytes(O.make_shape(32, 8, quant_group=64)) == 0       # unsupported
+    assert O.block_bytes(O.make_shape(32, 8, quant_group=64)) == 5120
+    assert O.block_bytes(O.make_shape(32, 8, quant_group=128)) == 4608
+    assert O.block_bytes(O.make_shape(32, 8, quant_group=16)) == 0       # unsupported
+    for g in (32, 64, 128):   # the oracle's block size for the same shape
+        assert O.block_bytes(O.make_shape(32, 8, quant_group=g)) == orc_block_bytes(g)
     for st in range(6):
         assert lib.oscar_status_string(st)
 
@@ -40,12 +49,13 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("g", [32, 128])
 @pytest.mark.parametrize("cap,grp,shared,seed", CASES)
-def test_pool_layout_matches_oracle(lib, orc, cap, grp, shared, seed):
-    sh = O.make_shape(32, 8)
+def test_pool_layout_matches_oracle(lib, orc, cap, grp, shared, seed, g):
+    sh = O.make_shape(32, 8, quant_group=g)
     mp = int(max(1, (cap.max() + 63) // 64)) + 1
     t, n, nb = O.oscar_pool_layout(sh, cap, grp, shared, seed, mp)
-    rc, t2, n2, nb2 = orc.pool_layout(oracle.Shape(128, 32, 64, 256, 64, 32, 8), cap, grp, shared, seed, mp)
+    rc, t2, n2, nb2 = orc.pool_layout(oracle.Shape(128, g, 64, 256, 64, 32, 8), cap, grp, shared, seed, mp)
     assert rc == 0
     assert np.array_equal(t, t2) and n == n2 and nb == nb2
 

@@ -38,7 +38,8 @@ def run_and_compare(orc, sc, label=""):
     exempt = []
     if seqs.size:
         items = [(int(b), int(sc.hist_len[b]), i) for i, b in enumerate(seqs)]
-        exempt = H.compare_evicted(pool_g, pool_o, sc.page_table, items, aux, sc.shape.num_kv_heads)
+        exempt = H.compare_evicted(pool_g, pool_o, sc.page_table, items, aux, sc.shape.num_kv_heads,
+                                   sc.shape.quant_group)
     # the rest of the pool is untouched
     same = pool_g == pool_o
     if not same.all():
@@ -82,11 +83,12 @@ def test_prefix_sharing(orc):
     run_and_compare(orc, sc, "prefix")
 
 
-def test_bulk_evict_matches_oracle(orc):
+@pytest.mark.parametrize("g", [32, 64, 128])
+def test_bulk_evict_matches_oracle(orc, g):
     """Bulk eviction (no src_row, no append) of a whole history at once,
-    across page boundaries of a shuffled table."""
+    across page boundaries of a shuffled table, for each group size."""
     w = S.Workload(56, "bulk", batch=2, hq=8, hk=2, n_outlier=4)
-    sh = oracle.Shape(128, 32, 64, 256, 64, 8, 2)
+    sh = oracle.Shape(128, g, 64, 256, 64, 8, 2)
     rng = S.rng_for(w, 3)
     n = 700
     toks = S.kv_tokens(w, n, rng, S.channel_profile(w))
@@ -99,13 +101,24 @@ def test_bulk_evict_matches_oracle(orc):
     aux = orc.evict(sh, toks, seq, pos, U.astype(np.float64), clip, pool_o, table, 8, want_aux=True)
     pool = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    O.oscar_evict_quantize(O.make_shape(8, 2), H.bf16_t(toks), H.i32_t(seq), H.i32_t(pos), H.f32_t(U),
+    O.oscar_evict_quantize(O.make_shape(8, 2, quant_group=g), H.bf16_t(toks), H.i32_t(seq), H.i32_t(pos), H.f32_t(U),
                            H.f32_t(clip), pool, H.i32_t(table), 2, 8, npages, dev_status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     items = [(int(seq[i]), int(pos[i]), i) for i in range(n)]
-    exempt = H.compare_evicted(pool.cpu().numpy(), pool_o, table, items, aux, 2)
+    exempt = H.compare_evicted(pool.cpu().numpy(), pool_o, table, items, aux, 2, g)
     print("bulk exempt", exempt)
+
+
+@pytest.mark.parametrize("g", [64, 128])
+def test_quant_groups_64_128(orc, g):
+    """One decode step with scale/zero groups of 64 and 128 stored positions
+    (one (s, z) pair per two / four 32-position MMA blocks), G = 4 and 8."""
+    for hq, hk in ((8, 2), (8, 1)):
+        w = S.Workload(95 + g, f"g{g}", batch=6, hq=hq, hk=hk, n_outlier=2)
+        sc = make_scene(w, ctx=np.array([3000, 1025, 700, 321, 5000, 64], np.int32), perm_seed=3, orc=orc,
+                        quant_group=g)
+        run_and_compare(orc, sc, f"g={g} G={hq // hk}")
 
 
 def test_degenerate_and_extreme_groups(orc):
