@@ -12,10 +12,13 @@ namespace oscar {
 
 // History pages per split-K work item: about 8192 items for the largest
 // request the table allows, between 4 and 64 pages.
+// Pages per split-K item: about 4096 items for the whole batch at most,
+// 16-64 pages each (an item ends with a merge of the four consumer warps'
+// states, so short items pay it per page or two; 16 pages is 4 per warp).
 static int pages_per_split(int batch, int hk, int max_pages) {
     const int64_t cap = (int64_t)batch * hk * max_pages;
-    int64_t pps = (cap + 8191) / 8192;
-    if (pps < 4) pps = 4;
+    int64_t pps = (cap + 4095) / 4096;
+    if (pps < 16) pps = 16;
     if (pps > 64) pps = 64;
     return (int)pps;
 }
@@ -288,7 +291,8 @@ oscar_status oscar_decode_attn(const oscar_shape* shape, int32_t batch, const vo
     p.part_stride = w.part_stride;
     p.qscale = sm_scale * kLog2e;
     for (int i = 0; i < 8; ++i) p.code_mul[i] = 0;
-    p.code_mul[1] = 4u;          // code pair bits 0-1 -> 2-3
+    p.code_mul[1] = 4u;          // code pair up by 2 bits
+    p.code_mul[2] = 16u;         // code pair up by 4 bits
     p.code_mul[3] = 1u << 30;    // bits 6-7 -> 4-5 (high word of the product)
     cudaEvent_t ev0 = g_int2_ev_start, ev1 = g_int2_ev_stop;
     g_int2_ev_start = g_int2_ev_stop = nullptr;

@@ -20,15 +20,16 @@
 //                     BF16 partial.
 //
 // Exact factoring used by int2_kernel.  With codes c, per-(token, group)
-// fp16 scale s and zero z, and A-operand values 8 + c (the code placed in
-// bf16 mantissa bits, see codes_to_bf16x2):
-//   logit_t = sum_g s_tg * D_tg + (z_tg - 8 s_tg) * Q_g,
-//       D_tg = sum_{j in g} (8 + c_tj) q'_j  (MMA, tokens x heads),
-//       Q_g  = sum_{j in g} q'_j;
-//   o'_j   = sum_t W_t,g(j) (8 + c_tj) + sum_t p_t (z_tg - 8 s_tg),
-//       W_tg = p_t s_tg                     (MMA, dims x heads).
-// q' and W are split into bf16 hi + lo (two MMA columns per head), so the
-// products keep ~2^-17 relative precision; codes are exact in bf16.
+// fp16 scale s and zero z, and A-operand values M_b + c for the 32-position
+// block b (the code placed in bf16 mantissa bits under the exponent of M_b,
+// see unpack_pair; M = 128/32/8/8 for K, 8 for V):
+//   logit_t = sum_b s_tb * D_tb + (z_tb - M_b s_tb) * Q_b,
+//       D_tb = sum_{j in b} (M_b + c_tj) q'_j  (MMA, tokens x heads),
+//       Q_b  = sum_{j in b} q'_j;
+//   o'_j   = sum_t W_t,b(j) (8 + c_tj) + sum_t p_t (z_tb - 8 s_tb),
+//       W_tb = p_t s_tb                       (MMA, dims x heads).
+// q' and W are split into bf16 hi + lo, so the products keep ~2^-17 relative
+// precision; codes are exact in bf16.
 #include "oscar_common.cuh"
 
 namespace oscar {
@@ -276,7 +277,7 @@ __device__ __forceinline__ void k_operands(uint32_t wa, uint32_t wb, uint32_t wa
 template <int G>
 __device__ __forceinline__ void v_operands(uint32_t r0, uint32_t r1, uint32_t r08, uint32_t r18, const CodeMul& cm,
                                            uint32_t& a0, uint32_t& a1, uint32_t& a2, uint32_t& a3) {
-    constexpr int P = 2 * G, T = (G == 0) ? 2 : ((G == 3) ? 4 : 2 * G);
+    constexpr int P = 2 * G, T = 4;  // every V group at M = 8
     a0 = unpack_pair<P, T>(r0, cm);
     a1 = unpack_pair<P, T>(r1, cm);
     a2 = unpack_pair<P, T>(r08, cm);

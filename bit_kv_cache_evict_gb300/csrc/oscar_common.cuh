@@ -87,20 +87,23 @@ __device__ __forceinline__ uint32_t rotr(uint32_t x, uint32_t n) { return __funn
 // down by 8).  Placed in bf16 mantissa bits T..T+1 under the exponent of
 // M = 2^(7-T), a code c reads as the exact value M + c, so a group whose
 // codes already sit at T = P in {0, 2, 4} needs a single logic op; the
-// offset M is removed afterwards with the zero point (z - M s).  Pairs at
-// P = 6 are moved to T = 4 by the high word of a multiply by 2^30, and
-// pairs at P = 0 to T = 2 by a multiply by 4.  K may use M = 128 (its
-// accumulator restarts every 16 tokens) while V keeps M <= 32 (its
-// accumulators run over a whole split).  The multipliers are held in
-// registers made opaque by a warp shuffle, so the compiler keeps them as
-// integer multiply-adds (FMA pipe) instead of shifts or constant loads.
+// offset M is removed afterwards with the zero point (z - M s).  Pairs are
+// moved up by T - P bits with a multiply by 4 or 16, and pairs at P = 6 down
+// to T = 4 by the high word of a multiply by 2^30.  K may use M = 128 (its
+// accumulator restarts every 16 tokens); V uses M = 8 for every group: its
+// accumulators run over a whole split-K item, and the fp32 accumulation
+// error of the tensor core scales with the magnitude M * sum(p s) it carries.
+// The multipliers are held in registers made opaque by a warp shuffle, so
+// the compiler keeps them as integer multiply-adds (FMA pipe) instead of
+// shifts or constant loads.
 struct CodeMul {
-    uint32_t m4, mh30;
+    uint32_t m4, m16, mh30;
 };
 
 __device__ __forceinline__ CodeMul code_mul_regs(const uint32_t* mul_param) {
     CodeMul c;
     c.m4 = __shfl_sync(kFull, mul_param[1], 0);
+    c.m16 = __shfl_sync(kFull, mul_param[2], 0);
     c.mh30 = __shfl_sync(kFull, mul_param[3], 0);
     return c;
 }
@@ -118,8 +121,10 @@ __device__ __forceinline__ uint32_t unpack_pair(uint32_t x, const CodeMul& m) {
     uint32_t r;
     if constexpr (P == T) {
         r = lop3_and_or(x, kMask, Magic<T>::bits);
-    } else if constexpr (P == 0 && T == 2) {
+    } else if constexpr (T - P == 2) {
         asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(r) : "r"(x & kMask), "r"(m.m4), "r"(Magic<T>::bits));
+    } else if constexpr (T - P == 4) {
+        asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(r) : "r"(x & kMask), "r"(m.m16), "r"(Magic<T>::bits));
     } else {
         static_assert(P == 6 && T == 4, "unsupported code move");
         asm("mad.hi.u32 %0, %1, %2, %3;" : "=r"(r) : "r"(x & kMask), "r"(m.mh30), "r"(Magic<T>::bits));
@@ -129,7 +134,7 @@ __device__ __forceinline__ uint32_t unpack_pair(uint32_t x, const CodeMul& m) {
 
 // offsets M per group: K (accumulator restarted per tile) and V
 __device__ __forceinline__ constexpr float k_magic(int g) { return g == 0 ? 128.f : (g == 1 ? 32.f : 8.f); }
-__device__ __forceinline__ constexpr float v_magic(int g) { return g <= 1 ? 32.f : 8.f; }
+__device__ __forceinline__ constexpr float v_magic(int) { return 8.f; }
 
 // ---- packed fp32x2 arithmetic (two lanes of fp32 per instruction) --------
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
@@ -306,10 +311,10 @@ struct DecodeParams {
     int gshift;    // log2(quant_group / 32)
     int block_bytes;
     float qscale;  // sm_scale * log2(e)
-    // multipliers that move a code pair from bits (P, P+16) to (4, 20):
-    // index P/2; 2^(4-P) for P < 4 (low product), 2^(36-P) for P > 4 (high
-    // product).  Passed at run time so the compiler keeps them as integer
-    // multiply-adds (FMA pipe) instead of turning them into shifts.
+    // multipliers that move a code pair from bits (P, P+16) to (T, T+16):
+    // [1] = 4 and [2] = 16 (low product, T - P = 2 or 4), [3] = 2^30 (high
+    // product, P = 6 to T = 4).  Passed at run time so the compiler keeps
+    // them as integer multiply-adds (FMA pipe) instead of shifts.
     uint32_t code_mul[8];
 };
 
