@@ -22,7 +22,7 @@
 // Exact factoring used by int2_kernel.  With codes c, per-(token, group)
 // fp16 scale s and zero z, and A-operand values M_b + c for the 32-position
 // block b (the code placed in bf16 mantissa bits under the exponent of M_b,
-// see unpack_pair; M = 128/32/8/8 for K, 8 for V):
+// see unpack_pair; M = 8 for every block of K and V):
 //   logit_t = sum_b s_tb * D_tb + (z_tb - M_b s_tb) * Q_b,
 //       D_tb = sum_{j in b} (M_b + c_tj) q'_j  (MMA, tokens x heads),
 //       Q_b  = sum_{j in b} q'_j;
@@ -265,7 +265,7 @@ __device__ __forceinline__ int find_seq(const int32_t* item_start, int B, int it
 template <int G>
 __device__ __forceinline__ void k_operands(uint32_t wa, uint32_t wb, uint32_t wa8, uint32_t wb8, const CodeMul& cm,
                                            uint32_t& a0, uint32_t& a1, uint32_t& a2, uint32_t& a3) {
-    constexpr int P = 2 * G, T = (G == 3) ? 4 : 2 * G;
+    constexpr int P = 2 * G, T = 4;  // every K group at M = 8
     a0 = unpack_pair<P, T>(wa, cm);
     a1 = unpack_pair<P, T>(wb, cm);
     a2 = unpack_pair<P, T>(wa8, cm);

@@ -89,10 +89,11 @@ __device__ __forceinline__ uint32_t rotr(uint32_t x, uint32_t n) { return __funn
 // codes already sit at T = P in {0, 2, 4} needs a single logic op; the
 // offset M is removed afterwards with the zero point (z - M s).  Pairs are
 // moved up by T - P bits with a multiply by 4 or 16, and pairs at P = 6 down
-// to T = 4 by the high word of a multiply by 2^30.  K may use M = 128 (its
-// accumulator restarts every 16 tokens); V uses M = 8 for every group: its
-// accumulators run over a whole split-K item, and the fp32 accumulation
-// error of the tensor core scales with the magnitude M * sum(p s) it carries.
+// to T = 4 by the high word of a multiply by 2^30.  K and V use M = 8 for
+// every group: the tensor core's fp32 accumulation error scales with the
+// magnitude M * (sum of the other operand) the accumulator carries, and a
+// larger offset (128 for K, 32 for V) cost a factor two of the attention
+// error budget on heavy-tailed data.
 // The multipliers are held in registers made opaque by a warp shuffle, so
 // the compiler keeps them as integer multiply-adds (FMA pipe) instead of
 // shifts or constant loads.
@@ -132,8 +133,8 @@ __device__ __forceinline__ uint32_t unpack_pair(uint32_t x, const CodeMul& m) {
     return r;
 }
 
-// offsets M per group: K (accumulator restarted per tile) and V
-__device__ __forceinline__ constexpr float k_magic(int g) { return g == 0 ? 128.f : (g == 1 ? 32.f : 8.f); }
+// code offset M of each 32-position block: 8 for K and V
+__device__ __forceinline__ constexpr float k_magic(int) { return 8.f; }
 __device__ __forceinline__ constexpr float v_magic(int) { return 8.f; }
 
 // ---- packed fp32x2 arithmetic (two lanes of fp32 per instruction) --------
