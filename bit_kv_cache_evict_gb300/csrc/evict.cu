@@ -56,10 +56,14 @@ __device__ __forceinline__ void df_group_extremes(df& hi_a, df& hi_b, df& lo_a, 
 }
 
 // Block = one (token, KV head, K|V) vector; warp w accumulates the terms
-// a in [32w, 32w + 32) of y = x . U, warp 0 adds the four partial sums
-// exactly and finishes the vector.
-__global__ void __launch_bounds__(128) evict_kernel(EvictParams p) {
-    __shared__ df part[4][kD];
+// a in [w*128/W, (w+1)*128/W) of y = x . U, warp 0 adds the W partial sums
+// exactly and finishes the vector.  W = 8 when there are few vectors (a
+// decode step at small batch: shorter dependent chains per warp), 4 when
+// there are many.
+template <int kEvictWarps>
+__global__ void __launch_bounds__(32 * kEvictWarps) evict_kernel(EvictParams p) {
+    constexpr int kEvictTerms = kD / kEvictWarps;
+    __shared__ df part[kEvictWarps][kD];
     pdl_trigger();  // the decode's query preparation does not read what this kernel writes
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int vec = blockIdx.x;
@@ -80,8 +84,8 @@ __global__ void __launch_bounds__(128) evict_kernel(EvictParams p) {
     const float* Um = p.U + ((size_t)kv * 2 + which) * kD * kD;
     float s[4] = {0.f, 0.f, 0.f, 0.f}, c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
-    for (int aa = 0; aa < 32; ++aa) {
-        const int a = 32 * warp + aa;
+    for (int aa = 0; aa < kEvictTerms; ++aa) {
+        const int a = kEvictTerms * warp + aa;
         const float xa = __shfl_sync(kFull, x[aa & 3], a >> 2);
         const float4 u = __ldg(reinterpret_cast<const float4*>(Um + (size_t)a * kD + 4 * lane));
         const float uu[4] = {u.x, u.y, u.z, u.w};
@@ -108,7 +112,7 @@ __global__ void __launch_bounds__(128) evict_kernel(EvictParams p) {
     for (int k = 0; k < 4; ++k) {
         y[k] = part[0][4 * lane + k];
 #pragma unroll
-        for (int w = 1; w < 4; ++w) y[k] = df_add(y[k], part[w][4 * lane + k]);
+        for (int w = 1; w < kEvictWarps; ++w) y[k] = df_add(y[k], part[w][4 * lane + k]);
     }
 
     // ---- Walsh-Hadamard transform (unnormalised), Sylvester order ------------
@@ -256,7 +260,8 @@ __global__ void __launch_bounds__(128) evict_kernel(EvictParams p) {
 cudaError_t launch_evict(const EvictParams& p, cudaStream_t st) {
     const int vecs = p.n_tok * p.hk * 2;
     if (vecs == 0) return cudaSuccess;
-    evict_kernel<<<vecs, 128, 0, st>>>(p);
+    if (vecs < 512) evict_kernel<8><<<vecs, 256, 0, st>>>(p);
+    else evict_kernel<4><<<vecs, 128, 0, st>>>(p);
     return cudaGetLastError();
 }
 
