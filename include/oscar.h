@@ -23,9 +23,9 @@
  *
  * Conventions for every call
  *   - Device pointers are caller-owned (allocate them with any allocator);
- *     the library never allocates, frees or keeps device memory, and keeps
- *     no state between calls except a per-device cache of kernel
- *     attributes.
+ *     the library never allocates or frees device memory, and keeps no state
+ *     between calls except a per-device cache of kernel attributes (and the
+ *     fixed scratch array of oscar_decode_attn_noalloc, below).
  *   - Device calls are asynchronous on the given stream (a cudaStream_t
  *     passed as void*; NULL = the legacy default stream).  They validate
  *     their host-visible arguments first and return an error before any
