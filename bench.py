@@ -524,8 +524,14 @@ def run_oscar(args, rank: int, world: int, local: int) -> None:
     achieved = int2_bytes / (int2_avg_ms * 1e-3) / 1e9
 
     # end to end through the C ABI from pinned host buffers: per layer, copy
-    # the step's query and new token in, run the step, copy the output out
+    # the step's query and new token in, run the step, copy the output out.
+    # When a layer's kernels run long enough to hide the extra host work
+    # (0.2 ms), the copies run on two copy streams ordered with events, so
+    # that the next layer's upload and the previous layer's download overlap
+    # the current layer's kernels (as a serving loop would); otherwise they
+    # run in the compute stream.
     e2e = None
+    overlap_copies = ms_per_step / L > 0.2
     if e2e_steps:
         hq = [torch.empty_like(l["q"], device="cpu").pin_memory() for l in st.layers]
         hn = [torch.empty_like(l["new_kv"], device="cpu").pin_memory() for l in st.layers]
@@ -535,16 +541,38 @@ def run_oscar(args, rank: int, world: int, local: int) -> None:
             hn[layer].copy_(st.layers[layer]["new_kv"])
         torch.cuda.synchronize()
         barrier(world)
+        h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
+        ev_in = [torch.cuda.Event() for _ in range(L)]     # layer's inputs uploaded
+        ev_done = [torch.cuda.Event() for _ in range(L)]   # layer's step finished: inputs free, output ready
+        ev_out = [torch.cuda.Event() for _ in range(L)]    # layer's output downloaded
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
+        for ev in ev_done + ev_out:
+            ev.record(stream)
         for k in range(e2e_steps):
             s = W + K + k
             for layer in range(L):
                 lay = st.layers[layer]
-                lay["q"].copy_(hq[layer], non_blocking=True)
-                lay["new_kv"].copy_(hn[layer], non_blocking=True)
+                if not overlap_copies:
+                    lay["q"].copy_(hq[layer], non_blocking=True)
+                    lay["new_kv"].copy_(hn[layer], non_blocking=True)
+                    st.layer_step(layer, s)
+                    ho[layer].copy_(lay["out"], non_blocking=True)
+                    continue
+                with torch.cuda.stream(h2d_s):
+                    h2d_s.wait_event(ev_done[layer])
+                    lay["q"].copy_(hq[layer], non_blocking=True)
+                    lay["new_kv"].copy_(hn[layer], non_blocking=True)
+                    ev_in[layer].record(h2d_s)
+                stream.wait_event(ev_in[layer])
+                stream.wait_event(ev_out[layer])
                 st.layer_step(layer, s)
-                ho[layer].copy_(lay["out"], non_blocking=True)
+                ev_done[layer].record(stream)
+                with torch.cuda.stream(d2h_s):
+                    d2h_s.wait_event(ev_done[layer])
+                    ho[layer].copy_(lay["out"], non_blocking=True)
+                    ev_out[layer].record(d2h_s)
+        stream.wait_stream(d2h_s)
         e1.record(stream)
         torch.cuda.synchronize()
         e_att = sum(st.attended_tokens(W + K + k) for k in range(e2e_steps)) * L
@@ -552,7 +580,8 @@ def run_oscar(args, rank: int, world: int, local: int) -> None:
         h2d = L * (st.layers[0]["q"].numel() * 2 + st.layers[0]["new_kv"].numel() * 2)
         d2h = L * st.layers[0]["out"].numel() * 4
         e2e = {"value": e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": e_ms / e2e_steps}
+               "ms_per_step": e_ms / e2e_steps,
+               "copies": "overlapped on copy streams" if overlap_copies else "in the compute stream"}
 
     cpu = None
     if rank == 0 and not args.no_cpu:
