@@ -290,10 +290,6 @@ oscar_status oscar_decode_attn(const oscar_shape* shape, int32_t batch, const vo
     p.pps = w.pps;
     p.part_stride = w.part_stride;
     p.qscale = sm_scale * kLog2e;
-    for (int i = 0; i < 8; ++i) p.code_mul[i] = 0;
-    p.code_mul[1] = 4u;          // code pair up by 2 bits
-    p.code_mul[2] = 16u;         // code pair up by 4 bits
-    p.code_mul[3] = 1u << 30;    // bits 6-7 -> 4-5 (high word of the product)
     cudaEvent_t ev0 = g_int2_ev_start, ev1 = g_int2_ev_stop;
     g_int2_ev_start = g_int2_ev_stop = nullptr;
     if (!ev0 || !ev1) ev0 = ev1 = nullptr;

@@ -20,16 +20,16 @@
 //                     BF16 partial.
 //
 // Exact factoring used by int2_kernel.  With codes c, per-(token, group)
-// fp16 scale s and zero z, and A-operand values M_b + c for the 32-position
-// block b (the code placed in bf16 mantissa bits under the exponent of M_b,
-// see unpack_pair; M = 8 for every block of K and V):
-//   logit_t = sum_b s_tb * D_tb + (z_tb - M_b s_tb) * Q_b,
-//       D_tb = sum_{j in b} (M_b + c_tj) q'_j  (MMA, tokens x heads),
-//       Q_b  = sum_{j in b} q'_j;
-//   o'_j   = sum_t W_t,b(j) (8 + c_tj) + sum_t p_t (z_tb - 8 s_tb),
-//       W_tb = p_t s_tb                       (MMA, dims x heads).
+// fp16 scale s and zero z, and A-operand values c * 2^(P_b - 133) for the
+// 32-position block b (the code left in an otherwise clear bf16 pattern at
+// bit P_b, see code_pair_lo):
+//   logit_t = sum_b s~_tb * D_tb + z_tb * Q_b,
+//       D_tb = sum_{j in b} c_tj 2^(P_b - 133) q'_j 2^kQUp  (MMA, tokens x heads),
+//       s~_tb = s_tb 2^(133 - kQUp - P_b),  Q_b = sum_{j in b} q'_j;
+//   o'_j   = 2^(133 - kVUp) sum_t W_t,b(j) c_tj 2^(P_b - 133) + sum_t p_t z_tb,
+//       W_tb = p_t s_tb 2^(kVUp - P_b)                  (MMA, dims x heads).
 // q' and W are split into bf16 hi + lo, so the products keep ~2^-17 relative
-// precision; codes are exact in bf16.
+// precision; codes are exact in bf16 and carry no offset.
 #include "oscar_common.cuh"
 
 namespace oscar {
@@ -185,8 +185,9 @@ __device__ __forceinline__ void prep_body(const DecodeParams& p) {
         // four codes of bytes 4(2tq+h)..4(2tq+h)+3 of group g's slot; column
         // 2hh = hi, 2hh+1 = lo
         const int base = 32 * (ks >> 1) + 8 * tq + 4 * (ks & 1);
-        const float v0 = qs[base], v1 = qs[base + 2];
-        const float v2 = qs[base + 1], v3 = qs[base + 3];
+        constexpr float up = pow2f(kQUp);  // exact; see the scalings in oscar_common.cuh
+        const float v0 = qs[base] * up, v1 = qs[base + 2] * up;
+        const float v2 = qs[base + 1] * up, v3 = qs[base + 3] * up;
         const uint32_t h01 = pack_bf16x2_rn(v0, v1), h23 = pack_bf16x2_rn(v2, v3);
         const uint32_t l01 = pack_bf16x2_rn(v0 - bf16_lo(h01), v1 - bf16_hi(h01));
         const uint32_t l23 = pack_bf16x2_rn(v2 - bf16_lo(h23), v3 - bf16_hi(h23));
@@ -260,28 +261,26 @@ __device__ __forceinline__ int find_seq(const int32_t* item_start, int B, int it
     return lo;
 }
 
-// A-operand registers of one K k-step (group g, word half h) from the
+// A-operand registers of one K k-step (slot g, word half h) from the
 // token-row words of rows gID and gID + 8 (w*) and their >> 8 copies (w*8).
 template <int G>
-__device__ __forceinline__ void k_operands(uint32_t wa, uint32_t wb, uint32_t wa8, uint32_t wb8, const CodeMul& cm,
-                                           uint32_t& a0, uint32_t& a1, uint32_t& a2, uint32_t& a3) {
-    constexpr int P = 2 * G, T = 4;  // every K group at M = 8
-    a0 = unpack_pair<P, T>(wa, cm);
-    a1 = unpack_pair<P, T>(wb, cm);
-    a2 = unpack_pair<P, T>(wa8, cm);
-    a3 = unpack_pair<P, T>(wb8, cm);
+__device__ __forceinline__ void k_operands(uint32_t wa, uint32_t wb, uint32_t wa8, uint32_t wb8, uint32_t& a0,
+                                           uint32_t& a1, uint32_t& a2, uint32_t& a3) {
+    a0 = code_pair_lo<G>(wa);
+    a1 = code_pair_lo<G>(wb);
+    a2 = code_pair_hi<G>(wa, wa8);
+    a3 = code_pair_hi<G>(wb, wb8);
 }
 
-// A-operand registers of one V m-tile half (group g): plane words r0, r1 and
+// A-operand registers of one V m-tile half (slot g): plane words r0, r1 and
 // their >> 8 copies.
 template <int G>
-__device__ __forceinline__ void v_operands(uint32_t r0, uint32_t r1, uint32_t r08, uint32_t r18, const CodeMul& cm,
-                                           uint32_t& a0, uint32_t& a1, uint32_t& a2, uint32_t& a3) {
-    constexpr int P = 2 * G, T = 4;  // every V group at M = 8
-    a0 = unpack_pair<P, T>(r0, cm);
-    a1 = unpack_pair<P, T>(r1, cm);
-    a2 = unpack_pair<P, T>(r08, cm);
-    a3 = unpack_pair<P, T>(r18, cm);
+__device__ __forceinline__ void v_operands(uint32_t r0, uint32_t r1, uint32_t r08, uint32_t r18, uint32_t& a0,
+                                           uint32_t& a1, uint32_t& a2, uint32_t& a3) {
+    a0 = code_pair_lo<G>(r0);
+    a1 = code_pair_lo<G>(r1);
+    a2 = code_pair_hi<G>(r0, r08);
+    a3 = code_pair_hi<G>(r1, r18);
 }
 
 // Position of token t (0..63) in the warp's probability and V-scale rows.
@@ -299,10 +298,10 @@ __device__ __forceinline__ int pv_pos(int t) {
 constexpr int kPvRow = 72;  // floats per probability / V-scale row (64 + 8: conflict-free stores)
 
 // The page's scales into the warp's scratch: for each token row and each
-// 32-position block b (quantisation group b >> GS), fp32 s and z - M_b s with
-// the block's code offset M_b; rows past the valid tokens are zero.  K rows:
-// s and z - M s as float4 per token; V rows: z - M s per token, and s in the
-// P.V token order (pv_pos).
+// 32-position block b (quantisation group b >> GS), fp32 s scaled by the
+// block's fixed power of two (k_scale_up / v_scale_up) and z; rows past the
+// valid tokens are zero.  K rows: s~ and z as float4 per token; V rows: z per
+// token, and s~ in the P.V token order (pv_pos).
 template <bool FULL, int GS>
 __device__ __forceinline__ void page_scales_g(const uint8_t* blk, int valid, float4* ksS, float4* kzS, float4* vzS,
                                               float* vsS) {
@@ -332,8 +331,8 @@ __device__ __forceinline__ void page_scales_g(const uint8_t* blk, int valid, flo
             }
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
-                sv[b] = s_g[b >> GS];
-                zz[b] = fmaf(which ? -v_magic(b) : -k_magic(b), sv[b], z_g[b >> GS]);
+                sv[b] = s_g[b >> GS] * (which ? v_scale_up(b) : k_scale_up(b));
+                zz[b] = z_g[b >> GS];
             }
         } else {
 #pragma unroll
@@ -370,7 +369,7 @@ __device__ __forceinline__ void page_scales(const uint8_t* blk, int valid, int g
 template <int NT, bool FULL>
 __device__ __forceinline__ void attend_page(const uint8_t* blk, int valid, uint8_t* wbuf, const uint2* qfS,
                                             const float4 (&qsv)[NT], float (&m_run)[NT], float (&l_run)[NT],
-                                            float (&zacc)[NT][4], float (&acc_o)[NT][8][4], const CodeMul& cm,
+                                            float (&zacc)[NT][4], float (&acc_o)[NT][8][4],
                                             const SplitSel& take_lo, int gshift) {
     using SM = Int2Smem<NT>;
     const int lane = threadIdx.x & 31, gID = lane >> 2, tq = lane & 3;
@@ -411,10 +410,10 @@ __device__ __forceinline__ void attend_page(const uint8_t* blk, int valid, uint8
                 const int h = it >> 2, g = it & 3, ks = 2 * g + h;
                 uint32_t a0, a1, a2, a3;
                 switch (g) {  // compile-time after unrolling
-                    case 0: k_operands<0>(wa[h], wb[h], wa8[h], wb8[h], cm, a0, a1, a2, a3); break;
-                    case 1: k_operands<1>(wa[h], wb[h], wa8[h], wb8[h], cm, a0, a1, a2, a3); break;
-                    case 2: k_operands<2>(wa[h], wb[h], wa8[h], wb8[h], cm, a0, a1, a2, a3); break;
-                    default: k_operands<3>(wa[h], wb[h], wa8[h], wb8[h], cm, a0, a1, a2, a3); break;
+                    case 0: k_operands<0>(wa[h], wb[h], wa8[h], wb8[h], a0, a1, a2, a3); break;
+                    case 1: k_operands<1>(wa[h], wb[h], wa8[h], wb8[h], a0, a1, a2, a3); break;
+                    case 2: k_operands<2>(wa[h], wb[h], wa8[h], wb8[h], a0, a1, a2, a3); break;
+                    default: k_operands<3>(wa[h], wb[h], wa8[h], wb8[h], a0, a1, a2, a3); break;
                 }
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
@@ -517,10 +516,10 @@ __device__ __forceinline__ void attend_page(const uint8_t* blk, int valid, uint8
                 const uint32_t r08 = pw8[2 * half], r18 = pw8[2 * half + 1];
                 uint32_t a0, a1, a2, a3;
                 switch (g) {
-                    case 0: v_operands<0>(r0, r1, r08, r18, cm, a0, a1, a2, a3); break;
-                    case 1: v_operands<1>(r0, r1, r08, r18, cm, a0, a1, a2, a3); break;
-                    case 2: v_operands<2>(r0, r1, r08, r18, cm, a0, a1, a2, a3); break;
-                    default: v_operands<3>(r0, r1, r08, r18, cm, a0, a1, a2, a3); break;
+                    case 0: v_operands<0>(r0, r1, r08, r18, a0, a1, a2, a3); break;
+                    case 1: v_operands<1>(r0, r1, r08, r18, a0, a1, a2, a3); break;
+                    case 2: v_operands<2>(r0, r1, r08, r18, a0, a1, a2, a3); break;
+                    default: v_operands<3>(r0, r1, r08, r18, a0, a1, a2, a3); break;
                 }
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
@@ -546,7 +545,7 @@ __device__ __forceinline__ void split_both(float2 w, uint32_t& hi, uint32_t& lo)
 template <bool FULL>
 __device__ __forceinline__ void attend_page_g8(const uint8_t* blk, int valid, uint8_t* wbuf, const uint2* qfS,
                                                const float4 (&qsv)[2], float (&m_run)[2], float (&l_run)[2],
-                                               float (&zacc)[2][4], float (&acc_o)[8][4], const CodeMul& cm,
+                                               float (&zacc)[2][4], float (&acc_o)[8][4],
                                                int gshift) {
     using SM = Int2Smem<2>;
     const int lane = threadIdx.x & 31, gID = lane >> 2, tq = lane & 3;
@@ -584,10 +583,10 @@ __device__ __forceinline__ void attend_page_g8(const uint8_t* blk, int valid, ui
                 const int h = it >> 2, g = it & 3, ks = 2 * g + h;
                 uint32_t a0, a1, a2, a3;
                 switch (g) {
-                    case 0: k_operands<0>(wa[h], wb[h], wa8[h], wb8[h], cm, a0, a1, a2, a3); break;
-                    case 1: k_operands<1>(wa[h], wb[h], wa8[h], wb8[h], cm, a0, a1, a2, a3); break;
-                    case 2: k_operands<2>(wa[h], wb[h], wa8[h], wb8[h], cm, a0, a1, a2, a3); break;
-                    default: k_operands<3>(wa[h], wb[h], wa8[h], wb8[h], cm, a0, a1, a2, a3); break;
+                    case 0: k_operands<0>(wa[h], wb[h], wa8[h], wb8[h], a0, a1, a2, a3); break;
+                    case 1: k_operands<1>(wa[h], wb[h], wa8[h], wb8[h], a0, a1, a2, a3); break;
+                    case 2: k_operands<2>(wa[h], wb[h], wa8[h], wb8[h], a0, a1, a2, a3); break;
+                    default: k_operands<3>(wa[h], wb[h], wa8[h], wb8[h], a0, a1, a2, a3); break;
                 }
                 const uint2 qh = qfS[(0 * 8 + ks) * 32 + lane], ql = qfS[(1 * 8 + ks) * 32 + lane];
                 mma_bf16_16816(acc[g], a0, a1, a2, a3, qh.x, qh.y);
@@ -680,10 +679,10 @@ __device__ __forceinline__ void attend_page_g8(const uint8_t* blk, int valid, ui
                 const uint32_t r08 = pw8[2 * half], r18 = pw8[2 * half + 1];
                 uint32_t a0, a1, a2, a3;
                 switch (g) {
-                    case 0: v_operands<0>(r0, r1, r08, r18, cm, a0, a1, a2, a3); break;
-                    case 1: v_operands<1>(r0, r1, r08, r18, cm, a0, a1, a2, a3); break;
-                    case 2: v_operands<2>(r0, r1, r08, r18, cm, a0, a1, a2, a3); break;
-                    default: v_operands<3>(r0, r1, r08, r18, cm, a0, a1, a2, a3); break;
+                    case 0: v_operands<0>(r0, r1, r08, r18, a0, a1, a2, a3); break;
+                    case 1: v_operands<1>(r0, r1, r08, r18, a0, a1, a2, a3); break;
+                    case 2: v_operands<2>(r0, r1, r08, r18, a0, a1, a2, a3); break;
+                    default: v_operands<3>(r0, r1, r08, r18, a0, a1, a2, a3); break;
                 }
                 mma_bf16_16816(acc_o[2 * g + half], a0, a1, a2, a3, bh0, bh1);
                 mma_bf16_16816(acc_o[2 * g + half], a0, a1, a2, a3, bl0, bl1);
@@ -796,7 +795,6 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
     const int gID = lane >> 2, tq = lane & 3;
     uint8_t* wbuf = smem + SM::kWarp + warp * SM::kWarpBytes;
     const SplitSel take_lo = split_sel(gID & 1);  // PV column: hi / lo
-    const CodeMul cm = code_mul_regs(p.code_mul);
 
     uint32_t merge_phase = 0;
     // bounded rendezvous of the four consumer warps (an mbarrier, so that a
@@ -850,14 +848,14 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
         if (!(flags & kFlagPad)) {
             if constexpr (NT == 2) {
                 if (valid == kPage)
-                    attend_page_g8<true>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o[0], cm, p.gshift);
+                    attend_page_g8<true>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o[0], p.gshift);
                 else
-                    attend_page_g8<false>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o[0], cm, p.gshift);
+                    attend_page_g8<false>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o[0], p.gshift);
             } else {
                 if (valid == kPage)
-                    attend_page<NT, true>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o, cm, take_lo, p.gshift);
+                    attend_page<NT, true>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o, take_lo, p.gshift);
                 else
-                    attend_page<NT, false>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o, cm, take_lo, p.gshift);
+                    attend_page<NT, false>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o, take_lo, p.gshift);
             }
         }
         __syncwarp();
@@ -886,8 +884,8 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
                     for (int g = 0; g < 4; ++g)
 #pragma unroll
                         for (int half = 0; half < 2; ++half) {
-                            o[32 * g + 16 * half + gID] = acc_o[0][2 * g + half][nt] + z[g];
-                            o[32 * g + 16 * half + 8 + gID] = acc_o[0][2 * g + half][2 + nt] + z[g];
+                            o[32 * g + 16 * half + gID] = fmaf(acc_o[0][2 * g + half][nt], kVOutScale, z[g]);
+                            o[32 * g + 16 * half + 8 + gID] = fmaf(acc_o[0][2 * g + half][2 + nt], kVOutScale, z[g]);
                         }
                     if (gID == 0) {
                         o[kD] = m_run[nt];
@@ -900,9 +898,10 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
                 for (int g = 0; g < 4; ++g)
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
-                        o[32 * g + 16 * half + gID] = acc_o[nt][2 * g + half][0] + acc_o[nt][2 * g + half][1] + z[g];
+                        o[32 * g + 16 * half + gID] =
+                            fmaf(acc_o[nt][2 * g + half][0] + acc_o[nt][2 * g + half][1], kVOutScale, z[g]);
                         o[32 * g + 16 * half + 8 + gID] =
-                            acc_o[nt][2 * g + half][2] + acc_o[nt][2 * g + half][3] + z[g];
+                            fmaf(acc_o[nt][2 * g + half][2] + acc_o[nt][2 * g + half][3], kVOutScale, z[g]);
                     }
                 if (gID == 0) {
                     o[kD] = m_run[nt];

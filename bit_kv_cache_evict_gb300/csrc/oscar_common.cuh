@@ -59,20 +59,6 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// (x & mask) | bits in one LOP3
-__device__ __forceinline__ uint32_t lop3_and_or(uint32_t x, uint32_t mask, uint32_t bits) {
-    uint32_t r;
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(x), "r"(mask), "r"(bits));
-    return r;
-}
-
-// Two 2-bit codes at bits 4-5 and 20-21 of x -> bf16x2 (8 + c_lo, 8 + c_hi):
-// bf16 0x4100 is 8.0 with 7 mantissa bits, so code c placed in mantissa
-// bits 4-5 reads as 8 + c exactly.
-__device__ __forceinline__ uint32_t codes_to_bf16x2(uint32_t x) {
-    return lop3_and_or(x, 0x00300030u, 0x41004100u);
-}
-
 // bf16x2 with lo -> bits 0-15, hi -> bits 16-31, round to nearest even
 __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
     uint32_t r;
@@ -82,60 +68,59 @@ __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
 
 __device__ __forceinline__ uint32_t rotr(uint32_t x, uint32_t n) { return __funnelshift_r(x, x, n); }
 
-// Code pairs -> bf16x2 MMA operands.  A code pair sits at bits (P, P+16) of
-// a 32-bit word (P = 2 * group in bytes 0/2; bytes 1/3 are first shifted
-// down by 8).  Placed in bf16 mantissa bits T..T+1 under the exponent of
-// M = 2^(7-T), a code c reads as the exact value M + c, so a group whose
-// codes already sit at T = P in {0, 2, 4} needs a single logic op; the
-// offset M is removed afterwards with the zero point (z - M s).  Pairs are
-// moved up by T - P bits with a multiply by 4 or 16, and pairs at P = 6 down
-// to T = 4 by the high word of a multiply by 2^30.  K and V use M = 8 for
-// every group: the tensor core's fp32 accumulation error scales with the
-// magnitude M * (sum of the other operand) the accumulator carries, and a
-// larger offset (128 for K, 32 for V) cost a factor two of the attention
-// error budget on heavy-tailed data.
-// The multipliers are held in registers made opaque by a warp shuffle, so
-// the compiler keeps them as integer multiply-adds (FMA pipe) instead of
-// shifts or constant loads.
-struct CodeMul {
-    uint32_t m4, m16, mh30;
-};
+// Code pairs -> bf16x2 MMA operands, with no offset and no arithmetic.
+// A 16-bit pattern below 0x0100 (exponent field 0 or 1) is a bf16 whose value
+// is exactly pattern * 2^-133: the subnormals and the first normal binade
+// join without a gap.  So a 2-bit code c left at bits P, P+1 of an otherwise
+// clear half reads as c * 2^(P-133), and one AND turns a code word into an
+// operand register.  The tensor core keeps the products of such subnormal
+// operands to a fixed number of bits below their nominal (biased) exponent,
+// so each leading zero of the 8-bit pattern costs one bit of the product:
+// codes at bits 6-7 lose nothing, at 4-5 two bits, at 2-3 four bits, at 0-1
+// six.  The codes of byte slot 0 (bits 0-1) are therefore moved up to bits
+// 6-7 first; slots 1-3 are used in place.  The power 2^(P-133) of each slot
+// is folded into the scales (and the query is scaled up so that every
+// product stays a normal fp32 number).
+//
+// Slot k of a byte holds the code of stored position 32k + j of the byte's
+// vector (j = byte index); slot_bit(k) is the bit of that code inside the
+// operand half.
+__host__ __device__ __forceinline__ constexpr int slot_bit(int k) { return k == 1 ? 2 : k == 2 ? 4 : 6; }
 
-__device__ __forceinline__ CodeMul code_mul_regs(const uint32_t* mul_param) {
-    CodeMul c;
-    c.m4 = __shfl_sync(kFull, mul_param[1], 0);
-    c.m16 = __shfl_sync(kFull, mul_param[2], 0);
-    c.mh30 = __shfl_sync(kFull, mul_param[3], 0);
-    return c;
+// Operand from the slot-k codes of bytes 0 and 2 of x (k-index 0 and 1 of
+// the register).
+template <int SLOT>
+__device__ __forceinline__ uint32_t code_pair_lo(uint32_t x) {
+    if constexpr (SLOT == 0) return (x << 6) & 0x00C000C0u;
+    else return x & (0x00030003u << (2 * SLOT));
+}
+// Operand from the slot-k codes of bytes 1 and 3 of x; x8 = x >> 8.
+template <int SLOT>
+__device__ __forceinline__ uint32_t code_pair_hi(uint32_t x, uint32_t x8) {
+    if constexpr (SLOT == 0) return (x >> 2) & 0x00C000C0u;
+    else return x8 & (0x00030003u << (2 * SLOT));
 }
 
-// bf16 exponent bits of M = 2^(7-T) in both halves
-template <int T>
-struct Magic {
-    static constexpr uint32_t bits = T == 0 ? 0x43004300u : (T == 2 ? 0x42004200u : 0x41004100u);
-};
-
-// pair at bits (P, P+16) -> bf16x2 (M + c_lo, M + c_hi), M = 2^(7-T)
-template <int P, int T>
-__device__ __forceinline__ uint32_t unpack_pair(uint32_t x, const CodeMul& m) {
-    constexpr uint32_t kMask = 0x00030003u << P;
-    uint32_t r;
-    if constexpr (P == T) {
-        r = lop3_and_or(x, kMask, Magic<T>::bits);
-    } else if constexpr (T - P == 2) {
-        asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(r) : "r"(x & kMask), "r"(m.m4), "r"(Magic<T>::bits));
-    } else if constexpr (T - P == 4) {
-        asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(r) : "r"(x & kMask), "r"(m.m16), "r"(Magic<T>::bits));
-    } else {
-        static_assert(P == 6 && T == 4, "unsupported code move");
-        asm("mad.hi.u32 %0, %1, %2, %3;" : "=r"(r) : "r"(x & kMask), "r"(m.mh30), "r"(Magic<T>::bits));
-    }
+// Fixed power-of-two scalings of the INT2 decode (all exact):
+//   q' enters the K products as q' * 2^kQUp;
+//   the K products of slot k are then c q' 2^(slot_bit(k) - 133 + kQUp), so
+//   the K scale s is stored as s * 2^(133 - kQUp - slot_bit(k));
+//   the V products use B = p * s * 2^(kVUp - slot_bit(k)), which puts every
+//   P.V accumulator at 2^(kVUp - 133) * sum(p s c);
+//   the item's output multiplies the accumulators back by 2^(133 - kVUp).
+// Ranges: |q'| < 2^64 and s <= 65504 keep every operand finite in bf16; a
+// product falls below the normal fp32 range only for |q'| < 2^-57 or
+// p * s < 2^-96, far below anything that moves a logit or an output.
+constexpr int kQUp = 64, kVUp = 103;
+__host__ __device__ __forceinline__ constexpr float pow2f(int e) {
+    float r = 1.f;
+    for (int i = 0; i < e; ++i) r *= 2.f;
+    for (int i = 0; i > e; --i) r *= 0.5f;
     return r;
 }
-
-// code offset M of each 32-position block: 8 for K and V
-__device__ __forceinline__ constexpr float k_magic(int) { return 8.f; }
-__device__ __forceinline__ constexpr float v_magic(int) { return 8.f; }
+__device__ __forceinline__ constexpr float k_scale_up(int slot) { return pow2f(133 - kQUp - slot_bit(slot)); }
+__device__ __forceinline__ constexpr float v_scale_up(int slot) { return pow2f(kVUp - slot_bit(slot)); }
+constexpr float kVOutScale = 1073741824.f;  // 2^(133 - kVUp) = 2^30
 
 // ---- packed fp32x2 arithmetic (two lanes of fp32 per instruction) --------
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
@@ -312,11 +297,6 @@ struct DecodeParams {
     int gshift;    // log2(quant_group / 32)
     int block_bytes;
     float qscale;  // sm_scale * log2(e)
-    // multipliers that move a code pair from bits (P, P+16) to (T, T+16):
-    // [1] = 4 and [2] = 16 (low product, T - P = 2 or 4), [3] = 2^30 (high
-    // product, P = 6 to T = 4).  Passed at run time so the compiler keeps
-    // them as integer multiply-adds (FMA pipe) instead of shifts.
-    uint32_t code_mul[8];
 };
 
 cudaError_t launch_evict(const EvictParams& p, cudaStream_t st);
