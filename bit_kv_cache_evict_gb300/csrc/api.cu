@@ -60,9 +60,14 @@ static int bf16_items(const oscar_shape* s) { return (s->sink + s->recent + 63) 
 static int gshift_of(const oscar_shape* s) { return s->quant_group == 32 ? 0 : (s->quant_group == 64 ? 1 : 2); }
 static int block_bytes_of(const oscar_shape* s) { return 4096 + 512 * (kD / s->quant_group); }
 
+// Pages at the end of each (sequence, KV head) that go to short items
+// queued after all the long ones, so that the last waves of the persistent
+// INT2 grid are short (used when long items are longer than short ones).
+static int tail_pages_of(int pps) { return pps > kShortItemPages ? 2 * kShortItemPages : 0; }
+
 struct WsLayout {
-    size_t counter, item_start, qfrag, qsum, part, bf_part, total;
-    int NT, pps, part_stride, max_items;
+    size_t counter, item_start, item_start2, qfrag, qsum, part, bf_part, total;
+    int NT, pps, tail_pg, part_stride, max_items;
 };
 
 static WsLayout ws_layout(const oscar_shape* s, int batch, int max_pages) {
@@ -71,11 +76,14 @@ static WsLayout ws_layout(const oscar_shape* s, int batch, int max_pages) {
     w.NT = (G + 3) / 4;
     w.pps = pages_per_split(batch, hk, max_pages);
     w.part_stride = (int)round_up((size_t)G * (kD + 2), 4);
-    w.max_items = batch * hk * ((max_pages + w.pps - 1) / w.pps);
+    w.tail_pg = tail_pages_of(w.pps);
+    w.max_items = batch * hk * ((max_pages + w.pps - 1) / w.pps + w.tail_pg / kShortItemPages);
     size_t off = 0;
     w.counter = off;
     off += 256;
     w.item_start = off;
+    off = round_up(off + (size_t)(batch + 1) * 4, 256);
+    w.item_start2 = off;
     off = round_up(off + (size_t)(batch + 1) * 4, 256);
     w.qfrag = off;
     off = round_up(off + (size_t)batch * hk * w.NT * 8 * 32 * 2 * 4, 256);
@@ -265,6 +273,7 @@ oscar_status oscar_decode_attn(const oscar_shape* shape, int32_t batch, const vo
     p.status = dev_status;
     p.counter = reinterpret_cast<int32_t*>(ws + w.counter);
     p.item_start = reinterpret_cast<int32_t*>(ws + w.item_start);
+    p.item_start2 = reinterpret_cast<int32_t*>(ws + w.item_start2);
     p.qfrag = reinterpret_cast<uint32_t*>(ws + w.qfrag);
     p.qsum = reinterpret_cast<float*>(ws + w.qsum);
     p.part = reinterpret_cast<float*>(ws + w.part);
@@ -277,7 +286,7 @@ oscar_status oscar_decode_attn(const oscar_shape* shape, int32_t batch, const vo
     p.nslot = shape->sink + shape->recent;
     p.bf_items = bf16_items(shape);
     {   // merge warps per row: more when rows are few and split-K partials many
-        const int splits = (max_pages + w.pps - 1) / w.pps;
+        const int splits = (max_pages + w.pps - 1) / w.pps + w.tail_pg / kShortItemPages;
         const int rows = batch * p.G;
         int wpr = 1;
         while (wpr < 8 && splits > 16 * wpr && rows * wpr < 4096) wpr *= 2;
@@ -288,6 +297,7 @@ oscar_status oscar_decode_attn(const oscar_shape* shape, int32_t batch, const vo
     p.gshift = gshift_of(shape);
     p.block_bytes = block_bytes_of(shape);
     p.pps = w.pps;
+    p.tail_pg = w.tail_pg;
     p.part_stride = w.part_stride;
     p.qscale = sm_scale * kLog2e;
     cudaEvent_t ev0 = g_int2_ev_start, ev1 = g_int2_ev_stop;

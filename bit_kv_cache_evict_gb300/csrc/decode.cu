@@ -66,31 +66,40 @@ __device__ __forceinline__ void prep_body(const DecodeParams& p) {
 
     if (blockIdx.x == gridDim.x - 1) {  // plan
         if (blockIdx.y != 0 || warp != 0) return;
-        int running = 0;
+        // long items of every sequence first, then the short tail items
+        int run_long = 0, run_short = 0;
         if (lane == 0) {
             p.item_start[0] = 0;
+            p.item_start2[0] = 0;
             *p.counter = 0;
         }
         for (int base = 0; base < p.B; base += 32) {
             const int b = base + lane;
-            int items = 0;
+            int n_long = 0, n_short = 0;
             if (b < p.B) {
                 int h = p.hist_len[b];
                 if (h < 0 || h > p.max_pages * kPage) {
                     report(p.status, OSCAR_STATUS_BAD_POS);
                     h = min(max(h, 0), p.max_pages * kPage);
                 }
-                const int npg = (h + kPage - 1) / kPage;
-                items = ((npg + p.pps - 1) / p.pps) * p.hk;
+                const SeqSplits sp = seq_splits((h + kPage - 1) / kPage, p.pps, p.tail_pg);
+                n_long = sp.n_long * p.hk;
+                n_short = sp.n_short * p.hk;
             }
-            int incl = items;
 #pragma unroll
             for (int m = 1; m < 32; m <<= 1) {
-                const int v = __shfl_up_sync(kFull, incl, m);
-                if (lane >= m) incl += v;
+                const int v = __shfl_up_sync(kFull, n_long, m), w = __shfl_up_sync(kFull, n_short, m);
+                if (lane >= m) {
+                    n_long += v;
+                    n_short += w;
+                }
             }
-            if (b < p.B) p.item_start[b + 1] = running + incl;
-            running += __shfl_sync(kFull, incl, 31);
+            if (b < p.B) {
+                p.item_start[b + 1] = run_long + n_long;
+                p.item_start2[b + 1] = run_short + n_short;
+            }
+            run_long += __shfl_sync(kFull, n_long, 31);
+            run_short += __shfl_sync(kFull, n_short, 31);
         }
         return;
     }
@@ -716,7 +725,8 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
 
     if (warp == kConsumerWarps) {
         // ------------------------------ producer ------------------------------
-        const int total = __ldg(p.item_start + p.B);
+        const int total_long = __ldg(p.item_start + p.B);
+        const int total = total_long + __ldg(p.item_start2 + p.B);
         uint32_t n = 0;      // slots issued so far (stage n % kStages, warp n % 4)
         bool ok = true;
         // one slot: wait for the stage, then publish its info (and copy)
@@ -756,14 +766,19 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
                 for (int i = 0; i < kConsumerWarps && ok; ++i) ok = post(-1, 0, 0, 0, 0, 0);
                 break;
             }
-            const int b = find_seq(p.item_start, p.B, item);
-            const int s0 = __ldg(p.item_start + b);
-            const int splits = (__ldg(p.item_start + b + 1) - s0) / p.hk;
-            const int kv = (item - s0) / splits;
-            const int split = (item - s0) % splits;
+            const bool is_long = item < total_long;
+            const int32_t* starts = is_long ? p.item_start : p.item_start2;
+            const int rel = is_long ? item : item - total_long;
+            const int b = find_seq(starts, p.B, rel);
+            const int s0 = __ldg(starts + b);
+            const int splits = (__ldg(starts + b + 1) - s0) / p.hk;
+            const int kv = (rel - s0) / splits;
+            const int split = (rel - s0) % splits;
             const int hist = min(max(__ldg(p.hist_len + b), 0), p.max_pages * kPage);
-            const int pg0 = split * p.pps;
-            const int npg = min(p.pps, (hist + kPage - 1) / kPage - pg0);
+            const int seq_pages = (hist + kPage - 1) / kPage;
+            const SeqSplits sp = seq_splits(seq_pages, p.pps, p.tail_pg);
+            const int pg0 = is_long ? split * p.pps : sp.long_pages + split * kShortItemPages;
+            const int npg = is_long ? min(p.pps, sp.long_pages - pg0) : min(kShortItemPages, seq_pages - pg0);
             const int nslots = (npg + kConsumerWarps - 1) / kConsumerWarps * kConsumerWarps;
             for (int c = 0; c < nslots && ok; c += 32) {
                 // page ids of the next 32 slots, one per lane
@@ -1199,19 +1214,24 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(DecodeParams p) {
     // lane handles Hadamard indices j = 4 lane + k, stored at bitrev7(j)
     float M = -INFINITY, L = 0.f, y[4] = {0.f, 0.f, 0.f, 0.f};
     if (active) {
-        const int s0 = __ldg(p.item_start + b);
-        const int splits = (__ldg(p.item_start + b + 1) - s0) / p.hk;
-        const int first = s0 + kv * splits;
+        // the (sequence, KV head)'s partials: n_long long items, then n_short short ones
+        const int s0 = __ldg(p.item_start + b), t0 = __ldg(p.item_start2 + b);
+        const int n_long = (__ldg(p.item_start + b + 1) - s0) / p.hk;
+        const int n_short = (__ldg(p.item_start2 + b + 1) - t0) / p.hk;
+        const int splits = n_long + n_short;
+        const int first = s0 + kv * n_long;
+        const int first2 = __ldg(p.item_start + p.B) + t0 + kv * n_short - n_long;
+        auto part_of = [&](int s) { return (size_t)(s < n_long ? first + s : first2 + s); };
         // this warp's splits: sub, sub + wpr, ...; statistics lane-parallel
         for (int s = sub + wpr * lane; s < splits; s += 32 * wpr)
-            M = fmaxf(M, p.part[(size_t)(first + s) * p.part_stride + (size_t)p.G * kD + hh]);
+            M = fmaxf(M, p.part[part_of(s) * p.part_stride + (size_t)p.G * kD + hh]);
 #pragma unroll
         for (int mm = 16; mm > 0; mm >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, mm));
         for (int s0b = sub; s0b < splits; s0b += 32 * wpr) {
             float sc = 0.f;
             const int sl = s0b + wpr * lane;
             if (sl < splits) {
-                const float* pt = p.part + (size_t)(first + sl) * p.part_stride + (size_t)p.G * kD;
+                const float* pt = p.part + part_of(sl) * p.part_stride + (size_t)p.G * kD;
                 const float ls = pt[p.G + hh];
                 if (ls > 0.f) {
                     sc = ex2(pt[hh] - M);
@@ -1222,7 +1242,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(DecodeParams p) {
 #pragma unroll 8
             for (int i = 0; i < cnt; ++i) {
                 const float w = __shfl_sync(kFull, sc, i);
-                const float* o = p.part + (size_t)(first + s0b + wpr * i) * p.part_stride + (size_t)hh * kD;
+                const float* o = p.part + part_of(s0b + wpr * i) * p.part_stride + (size_t)hh * kD;
 #pragma unroll
                 for (int k = 0; k < 4; ++k) y[k] = fmaf(w, o[32 * bitrev2(k) + r5], y[k]);
             }
@@ -1355,7 +1375,7 @@ static cudaError_t launch_int2(const DecodeParams& p, cudaStream_t st, int sms, 
         attr_set = true;
     }
     const int per_sm = (NT == 1) ? 3 : 2;
-    const int max_items = p.B * p.hk * ((p.max_pages + p.pps - 1) / p.pps);
+    const int max_items = p.B * p.hk * ((p.max_pages + p.pps - 1) / p.pps + p.tail_pg / kShortItemPages);
     int blocks = min(per_sm * sms, max_items);
     if (blocks < 1) blocks = 1;
     cudaError_t e = launch_pdl(int2_kernel<NT>, dim3(blocks), dim3(kInt2Threads), smem, st, p);

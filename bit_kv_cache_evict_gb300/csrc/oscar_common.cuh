@@ -15,6 +15,7 @@ constexpr int kD = 128;           // head_dim
 constexpr int kGroup = 32;        // quantisation group
 constexpr int kNumGroups = kD / kGroup;
 constexpr int kPage = 64;         // tokens per page
+constexpr int kShortItemPages = 16; // pages per short split-K item (the queue's tail)
 constexpr int kBlock = OSCAR_BLOCK_BYTES;
 constexpr int kKCodes = 0;        // byte offsets inside a (page, kv) block
 constexpr int kVCodes = 2048;
@@ -286,18 +287,35 @@ struct DecodeParams {
     int32_t* status;
     // workspace sections
     int32_t* counter;     // [1]
-    int32_t* item_start;  // [B + 1]
+    int32_t* item_start;  // [B + 1] long items before sequence b (prefix sums)
+    int32_t* item_start2; // [B + 1] short tail items before sequence b
     uint32_t* qfrag;      // [B*Hk][NT][8][32][2]
     float* qsum;          // [B*Hk][NT*4][4]
     float* part;          // [max_items][part_stride]
     float* bf_part;       // [B*Hk][bf_items][part_stride]
     int B, hq, hk, G, NT, nslot, max_pages, num_pages, pps, part_stride;
+    int tail_pg;   // last pages of each (sequence, KV head) in short items (0 or 2 * kShortItemPages)
     int bf_items;  // 64-token blocks of the BF16 segment: ceil(nslot / 64)
     int merge_wpr; // merge warps per output row (1, 2, 4, 8)
     int gshift;    // log2(quant_group / 32)
     int block_bytes;
     float qscale;  // sm_scale * log2(e)
 };
+
+// Split-K geometry of one sequence with npg history pages: the last
+// min(npg, tail_pg) pages go to short items of kShortItemPages, the rest to
+// long items of pps pages.
+struct SeqSplits {
+    int long_pages, n_long, n_short;
+};
+__host__ __device__ __forceinline__ SeqSplits seq_splits(int npg, int pps, int tail_pg) {
+    SeqSplits r;
+    const int short_pages = npg < tail_pg ? npg : tail_pg;
+    r.long_pages = npg - short_pages;
+    r.n_long = (r.long_pages + pps - 1) / pps;
+    r.n_short = (short_pages + kShortItemPages - 1) / kShortItemPages;
+    return r;
+}
 
 cudaError_t launch_evict(const EvictParams& p, cudaStream_t st);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st, cudaEvent_t ev_int2_start,
