@@ -1310,15 +1310,21 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(DecodeParams p) {
     asm volatile("cp.async.wait_group 0;" ::: "memory");
     __syncthreads();
     if (!lead) return;
-    // o[a] = sum_j w[j] U_V[a][j] for a = lane + 32 c
+    // o[a] = sum_j w[j] U_V[a][j] for a = lane + 32 c, four j per load (the
+    // lanes start at rotated float4 columns, so each quarter-warp's 16-byte
+    // reads fall on distinct banks); two partial sums per output
     const float* w = Ws + (size_t)warp * kMergeRow;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-    for (int j = 0; j < kD; ++j) {
-        const int jj = (j + lane) & (kD - 1);
-        const float wj = w[jj];
+    float acc[4][2] = {};
+#pragma unroll 4
+    for (int j4 = 0; j4 < kD / 4; ++j4) {
+        const int jj = 4 * ((j4 + lane) & (kD / 4 - 1));
+        const float4 wv = *reinterpret_cast<const float4*>(w + jj);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) acc[c] = fmaf(wj, Us[(lane + 32 * c) * kD + jj], acc[c]);
+        for (int c = 0; c < 4; ++c) {
+            const float4 u = *reinterpret_cast<const float4*>(Us + (lane + 32 * c) * kD + jj);
+            float& a = acc[c][j4 & 1];
+            a = fmaf(wv.w, u.w, fmaf(wv.z, u.z, fmaf(wv.y, u.y, fmaf(wv.x, u.x, a))));
+        }
     }
     // BF16 segment: log-sum-exp merge of its item partials (unrotated domain)
     const float* bp = p.bf_part + (size_t)(b * p.hk + kv) * p.bf_items * p.part_stride;
@@ -1349,7 +1355,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(DecodeParams p) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
         const int a2 = lane + 32 * c;
-        o[a2] = (wi * acc[c] + wb * ob[c]) * inv;
+        o[a2] = (wi * (acc[c][0] + acc[c][1]) + wb * ob[c]) * inv;
     }
 }
 
