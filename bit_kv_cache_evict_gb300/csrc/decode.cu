@@ -1190,8 +1190,10 @@ constexpr int kMergeWarps = 8;
 constexpr int kMergeThreads = 32 * kMergeWarps;
 constexpr int kMergeRow = kD + 4;  // floats per warp row (y[128], M, L; a multiple of 4 for float4 access)
 constexpr int kMergeSmem = (kD * kD + kMergeWarps * kMergeRow) * 4;
+constexpr int kMergeBatch = 12;   // split-K partials per batch of loads
+constexpr int kMaxBfItems = 5;    // BF16 segment blocks per row: ceil(320 / 64)
 
-__global__ void __launch_bounds__(kMergeThreads) merge_kernel(DecodeParams p) {
+__global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(DecodeParams p) {
     extern __shared__ __align__(16) float msm[];
     float* Us = msm;                  // [a][j] = U_V[a][j]
     float* Ws = msm + kD * kD;        // [warp][kMergeRow]: a warp's share (y, M, L), then the row's w
@@ -1213,6 +1215,27 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(DecodeParams p) {
     const int r5 = bitrev5(lane);
     // lane handles Hadamard indices j = 4 lane + k, stored at bitrev7(j)
     float M = -INFINITY, L = 0.f, y[4] = {0.f, 0.f, 0.f, 0.f};
+    // the BF16 segment's partials of the row (unrotated domain), loaded now
+    // so that their latency overlaps the split-K merge; used by the row's
+    // first warp after the un-rotation
+    float bm[kMaxBfItems], bl[kMaxBfItems], bo[kMaxBfItems][4];
+    {
+        const float* bp = p.bf_part + (size_t)(b * p.hk + kv) * p.bf_items * p.part_stride;
+#pragma unroll
+        for (int it = 0; it < kMaxBfItems; ++it) {
+            bm[it] = -INFINITY;
+            bl[it] = 0.f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) bo[it][c] = 0.f;
+            if (active && sub == 0 && it < p.bf_items) {
+                const float* pt = bp + (size_t)it * p.part_stride;
+                bm[it] = pt[(size_t)p.G * kD + hh];
+                bl[it] = pt[(size_t)p.G * kD + p.G + hh];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) bo[it][c] = pt[(size_t)hh * kD + lane + 32 * c];
+            }
+        }
+    }
     if (active) {
         // the (sequence, KV head)'s partials: n_long long items, then n_short short ones
         const int s0 = __ldg(p.item_start + b), t0 = __ldg(p.item_start2 + b);
@@ -1221,34 +1244,47 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(DecodeParams p) {
         const int splits = n_long + n_short;
         const int first = s0 + kv * n_long;
         const int first2 = __ldg(p.item_start + p.B) + t0 + kv * n_short - n_long;
-        auto part_of = [&](int s) { return (size_t)(s < n_long ? first + s : first2 + s); };
-        // this warp's splits: sub, sub + wpr, ...; statistics lane-parallel
-        for (int s = sub + wpr * lane; s < splits; s += 32 * wpr)
-            M = fmaxf(M, p.part[part_of(s) * p.part_stride + (size_t)p.G * kD + hh]);
+        // this warp's splits sub, sub + wpr, ..., merged by online log-sum-exp
+        // in batches whose loads (statistics and this lane's four values of
+        // each split) are all issued before any is used
+        const int nmine = splits > sub ? (splits - sub + wpr - 1) / wpr : 0;
+        for (int i0 = 0; i0 < nmine; i0 += kMergeBatch) {
+            float ms[kMergeBatch], ls[kMergeBatch], ov[kMergeBatch][4];
 #pragma unroll
-        for (int mm = 16; mm > 0; mm >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, mm));
-        for (int s0b = sub; s0b < splits; s0b += 32 * wpr) {
-            float sc = 0.f;
-            const int sl = s0b + wpr * lane;
-            if (sl < splits) {
-                const float* pt = p.part + part_of(sl) * p.part_stride + (size_t)p.G * kD;
-                const float ls = pt[p.G + hh];
-                if (ls > 0.f) {
-                    sc = ex2(pt[hh] - M);
-                    L += sc * ls;
+            for (int i = 0; i < kMergeBatch; ++i) {
+                ms[i] = -INFINITY;
+                ls[i] = 0.f;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) ov[i][k] = 0.f;
+                if (i0 + i < nmine) {
+                    const int sp = sub + wpr * (i0 + i);
+                    const float* pt =
+                        p.part + (size_t)(sp < n_long ? first + sp : first2 + sp) * p.part_stride;
+                    ms[i] = pt[(size_t)p.G * kD + hh];
+                    ls[i] = pt[(size_t)p.G * kD + p.G + hh];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) ov[i][k] = pt[(size_t)hh * kD + 32 * bitrev2(k) + r5];
                 }
             }
-            const int cnt = min(32, (splits - s0b + wpr - 1) / wpr);
-#pragma unroll 8
-            for (int i = 0; i < cnt; ++i) {
-                const float w = __shfl_sync(kFull, sc, i);
-                const float* o = p.part + part_of(s0b + wpr * i) * p.part_stride + (size_t)hh * kD;
+            float mb = M;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) y[k] = fmaf(w, o[32 * bitrev2(k) + r5], y[k]);
+            for (int i = 0; i < kMergeBatch; ++i)
+                if (ls[i] > 0.f) mb = fmaxf(mb, ms[i]);
+            if (mb != -INFINITY) {
+                const float a = (M == -INFINITY) ? 0.f : ex2(M - mb);
+                L *= a;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) y[k] *= a;
+#pragma unroll
+                for (int i = 0; i < kMergeBatch; ++i) {
+                    const float sc = (ls[i] > 0.f) ? ex2(ms[i] - mb) : 0.f;
+                    L = fmaf(sc, ls[i], L);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) y[k] = fmaf(sc, ov[i][k], y[k]);
+                }
+                M = mb;
             }
         }
-#pragma unroll
-        for (int mm = 16; mm > 0; mm >>= 1) L += __shfl_xor_sync(kFull, L, mm);
     }
     if (wpr > 1) {  // combine the row's shares in its first warp
         float* ws = Ws + (size_t)warp * kMergeRow;
@@ -1327,22 +1363,19 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(DecodeParams p) {
         }
     }
     // BF16 segment: log-sum-exp merge of its item partials (unrotated domain)
-    const float* bp = p.bf_part + (size_t)(b * p.hk + kv) * p.bf_items * p.part_stride;
     float mb = -INFINITY;
-    for (int it = 0; it < p.bf_items; ++it) {
-        const float* pt = bp + (size_t)it * p.part_stride + (size_t)p.G * kD;
-        if (pt[p.G + hh] > 0.f) mb = fmaxf(mb, pt[hh]);
-    }
+#pragma unroll
+    for (int it = 0; it < kMaxBfItems; ++it)
+        if (bl[it] > 0.f) mb = fmaxf(mb, bm[it]);
     float lb = 0.f, ob[4] = {0.f, 0.f, 0.f, 0.f};
     if (mb != -INFINITY) {
-        for (int it = 0; it < p.bf_items; ++it) {
-            const float* pt = bp + (size_t)it * p.part_stride;
-            const float li = pt[(size_t)p.G * kD + p.G + hh];
-            if (li > 0.f) {
-                const float sc = ex2(pt[(size_t)p.G * kD + hh] - mb);
-                lb = fmaf(sc, li, lb);
 #pragma unroll
-                for (int c = 0; c < 4; ++c) ob[c] = fmaf(sc, pt[(size_t)hh * kD + lane + 32 * c], ob[c]);
+        for (int it = 0; it < kMaxBfItems; ++it) {
+            if (bl[it] > 0.f) {
+                const float sc = ex2(bm[it] - mb);
+                lb = fmaf(sc, bl[it], lb);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) ob[c] = fmaf(sc, bo[it][c], ob[c]);
             }
         }
     }
