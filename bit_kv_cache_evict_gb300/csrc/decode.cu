@@ -976,7 +976,8 @@ constexpr int kBfThreads = 32 * kBfWarps;
 constexpr int kBfItemTok = 16 * kBfWarps;          // tokens per block
 constexpr int kBfPitch = 528;                      // bytes per staged token row (512 + 16)
 constexpr int kBfWarpBytes = 16 * kBfPitch;        // also holds the warp's state [G][kD + 2] at the end
-constexpr int kBfSmem = kBfWarps * kBfWarpBytes;
+constexpr int kBfQBytes = 8 * kD * 2;                 // query rows of one KV group (up to 8 heads)
+constexpr int kBfSmem = 2 * kBfWarps * kBfWarpBytes + 2 * kBfQBytes;  // two buffers
 static_assert(8 * (kD + 2) * 4 <= kBfWarpBytes, "warp state must fit in the warp's row tile");
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
@@ -993,8 +994,28 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], const void* p) {
                  : "r"(smem_u32(p)));
 }
 
+// Copy one 16-token tile of (b, kv)'s BF16 rows (K | V, 512 B each) into
+// rows with cp.async and zero the rows past the valid tokens; the caller
+// commits the group.
+__device__ __forceinline__ void bf16_stage_rows(const DecodeParams& p, int b, int kv, int t0, int nvalid,
+                                                uint8_t* rows) {
+    if (nvalid <= 0) return;
+    const int lane = threadIdx.x & 31;
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(p.bf16_kv) +
+                         (((size_t)b * p.nslot + t0) * p.hk + kv) * (2 * kD * 2);
+    const size_t row_stride = (size_t)p.hk * 2 * kD * 2;
+#pragma unroll 4
+    for (int r = 0; r < 16; ++r) {
+        if (r < nvalid) cp_async16(rows + r * kBfPitch + 16 * lane, src + r * row_stride + 16 * lane);
+        else *reinterpret_cast<uint4*>(rows + r * kBfPitch + 16 * lane) = make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+// One warp's 16-token tile from staged rows and the staged query rows of
+// its KV group (qsm: [G][kD] bf16); leaves the warp's state (o, m, l) per
+// head in rows.
 template <int G>
-__device__ void bf16_tile(const DecodeParams& p, int b, int kv, int t0, int nvalid, uint8_t* rows) {
+__device__ void bf16_tile(int nvalid, uint8_t* rows, const __nv_bfloat16* qsm, float qscale) {
     const int lane = threadIdx.x & 31, gID = lane >> 2, tq = lane & 3;
     float* st = reinterpret_cast<float*>(rows);  // [G][kD + 2] at the end
     if (nvalid <= 0) {
@@ -1004,22 +1025,11 @@ __device__ void bf16_tile(const DecodeParams& p, int b, int kv, int t0, int nval
         }
         return;
     }
-    // stage the valid rows (K | V, 512 B each); zero the rest of the tile
-    const uint8_t* src = reinterpret_cast<const uint8_t*>(p.bf16_kv) +
-                         (((size_t)b * p.nslot + t0) * p.hk + kv) * (2 * kD * 2);
-    const size_t row_stride = (size_t)p.hk * 2 * kD * 2;
-#pragma unroll 4
-    for (int r = 0; r < 16; ++r) {
-        if (r < nvalid) cp_async16(rows + r * kBfPitch + 16 * lane, src + r * row_stride + 16 * lane);
-        else *reinterpret_cast<uint4*>(rows + r * kBfPitch + 16 * lane) = make_uint4(0u, 0u, 0u, 0u);
-    }
-    asm volatile("cp.async.commit_group;" ::: "memory");
-
     // A = query rows: row r < 2G holds head r/2, the rest are zero
     constexpr bool kHigh = (G == 8);                  // rows gID + 8 in use
     const bool row_lo_on = gID < 2 * G;
-    const __nv_bfloat16* qa = p.q + ((size_t)b * p.hq + kv * G + (gID >> 1)) * kD;
-    const __nv_bfloat16* qb = p.q + ((size_t)b * p.hq + kv * G + ((gID + 8) >> 1)) * kD;
+    const __nv_bfloat16* qa = qsm + (row_lo_on ? (gID >> 1) : 0) * kD;
+    const __nv_bfloat16* qb = qsm + (kHigh ? ((gID + 8) >> 1) : 0) * kD;
     uint32_t qf[8][4];
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
@@ -1029,8 +1039,6 @@ __device__ void bf16_tile(const DecodeParams& p, int b, int kv, int t0, int nval
         qf[ks][1] = kHigh ? *reinterpret_cast<const uint32_t*>(qb + d0) : 0u;
         qf[ks][3] = kHigh ? *reinterpret_cast<const uint32_t*>(qb + d0 + 8) : 0u;
     }
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
-    __syncwarp();
 
     // S = Q.K^T for tokens 8nt .. 8nt+7 (B via ldmatrix: matrix i/8 = dims
     // 16ks + 8(i/8) of token row i%8, covering k-steps ks and ks+1)
@@ -1055,7 +1063,7 @@ __device__ void bf16_tile(const DecodeParams& p, int b, int kv, int t0, int nval
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int tok = 8 * nt + 2 * tq + (e & 1);
-            sacc[nt][e] = (tok < nvalid) ? sacc[nt][e] * p.qscale : -INFINITY;
+            sacc[nt][e] = (tok < nvalid) ? sacc[nt][e] * qscale : -INFINITY;
             if (e < 2) ma = fmaxf(ma, sacc[nt][e]);
             else mb = fmaxf(mb, sacc[nt][e]);
         }
@@ -1129,49 +1137,83 @@ __device__ void bf16_tile(const DecodeParams& p, int b, int kv, int t0, int nval
     }
 }
 
-// Launched as a programmatic dependent of int2_kernel, whose results it does
-// not read; it waits for int2_kernel's completion before it exits, so that
-// the merge after it sees both.
-__global__ void __launch_bounds__(kBfThreads) bf16_kernel(DecodeParams p) {
+// Persistent: 3 blocks per SM loop over the (sequence, KV head, 64-slot
+// block) items with two buffers per warp, so that the next item's rows (and
+// its query rows, staged by warp 0) are in flight while the current item is
+// attended.  Launched as a programmatic dependent of int2_kernel, whose
+// results it does not read; it waits for int2_kernel's completion before it
+// exits, so that the merge after it sees both.
+__global__ void __launch_bounds__(kBfThreads, 3) bf16_kernel(DecodeParams p) {
     extern __shared__ __align__(128) uint8_t bsm[];
     pdl_trigger();
-    const int item = blockIdx.x, bk = blockIdx.y;
-    const int b = bk / p.hk, kv = bk % p.hk;
-    const int warp = threadIdx.x >> 5;
-    const int n = min(max(__ldg(p.bf16_len + b), 0), p.nslot);
-    const int t0 = item * kBfItemTok + 16 * warp;
-    uint8_t* rows = bsm + warp * kBfWarpBytes;
-    switch (p.G) {
-        case 1: bf16_tile<1>(p, b, kv, t0, n - t0, rows); break;
-        case 2: bf16_tile<2>(p, b, kv, t0, n - t0, rows); break;
-        case 4: bf16_tile<4>(p, b, kv, t0, n - t0, rows); break;
-        default: bf16_tile<8>(p, b, kv, t0, n - t0, rows); break;
-    }
-    __syncthreads();
-    // merge the four warps: thread -> dimension
-    float* part = p.bf_part + ((size_t)bk * p.bf_items + item) * p.part_stride;
-    const int d = threadIdx.x;
-    for (int h = 0; h < p.G; ++h) {
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kBfWarps; ++w)
-            M = fmaxf(M, reinterpret_cast<const float*>(bsm + w * kBfWarpBytes)[h * (kD + 2) + kD]);
-        float acc = 0.f, L = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-            for (int w = 0; w < kBfWarps; ++w) {
-                const float* src = reinterpret_cast<const float*>(bsm + w * kBfWarpBytes) + h * (kD + 2);
-                const float sc = ex2(src[kD] - M);
-                acc = fmaf(sc, src[d], acc);
-                L = fmaf(sc, src[kD + 1], L);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int total = p.bf_items * p.B * p.hk;
+    auto rows_of = [&](int buf, int w) { return bsm + (buf * kBfWarps + w) * kBfWarpBytes; };
+    auto q_of = [&](int buf) { return bsm + 2 * kBfWarps * kBfWarpBytes + buf * kBfQBytes; };
+    auto stage = [&](int it, int buf) {
+        if (it < total) {
+            const int bk = it / p.bf_items, item = it % p.bf_items;
+            const int b = bk / p.hk, kv = bk % p.hk;
+            const int n = min(max(__ldg(p.bf16_len + b), 0), p.nslot);
+            const int t0 = item * kBfItemTok + 16 * warp;
+            bf16_stage_rows(p, b, kv, t0, n - t0, rows_of(buf, warp));
+            if (warp == 0) {  // the KV group's query rows (the query is only 8-byte aligned)
+                const uint8_t* qsrc = reinterpret_cast<const uint8_t*>(p.q + ((size_t)b * p.hq + kv * p.G) * kD);
+                uint8_t* qdst = q_of(buf);
+                for (int c = lane; c < p.G * (kD * 2 / 8); c += 32)
+                    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(qdst + 8 * c)),
+                                 "l"(qsrc + 8 * c)
+                                 : "memory");
             }
         }
-        part[(size_t)h * kD + d] = acc;
-        if (d == 0) {
-            part[(size_t)p.G * kD + h] = M;
-            part[(size_t)p.G * kD + p.G + h] = L;
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    int buf = 0;
+    stage(blockIdx.x, 0);
+    for (int it = blockIdx.x; it < total; it += gridDim.x, buf ^= 1) {
+        stage(it + gridDim.x, buf ^ 1);
+        asm volatile("cp.async.wait_group 1;" ::: "memory");
+        __syncthreads();  // this item's rows and query rows have landed
+        const int bk = it / p.bf_items, item = it % p.bf_items;
+        const int b = bk / p.hk;
+        const int n = min(max(__ldg(p.bf16_len + b), 0), p.nslot);
+        const int t0 = item * kBfItemTok + 16 * warp;
+        uint8_t* rows = rows_of(buf, warp);
+        const __nv_bfloat16* qsm = reinterpret_cast<const __nv_bfloat16*>(q_of(buf));
+        switch (p.G) {
+            case 1: bf16_tile<1>(n - t0, rows, qsm, p.qscale); break;
+            case 2: bf16_tile<2>(n - t0, rows, qsm, p.qscale); break;
+            case 4: bf16_tile<4>(n - t0, rows, qsm, p.qscale); break;
+            default: bf16_tile<8>(n - t0, rows, qsm, p.qscale); break;
         }
+        __syncthreads();
+        // merge the four warps: thread -> dimension
+        float* part = p.bf_part + ((size_t)bk * p.bf_items + item) * p.part_stride;
+        const int d = threadIdx.x;
+        for (int h = 0; h < p.G; ++h) {
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kBfWarps; ++w)
+                M = fmaxf(M, reinterpret_cast<const float*>(rows_of(buf, w))[h * (kD + 2) + kD]);
+            float acc = 0.f, L = 0.f;
+            if (M != -INFINITY) {
+#pragma unroll
+                for (int w = 0; w < kBfWarps; ++w) {
+                    const float* src = reinterpret_cast<const float*>(rows_of(buf, w)) + h * (kD + 2);
+                    const float sc = ex2(src[kD] - M);
+                    acc = fmaf(sc, src[d], acc);
+                    L = fmaf(sc, src[kD + 1], L);
+                }
+            }
+            part[(size_t)h * kD + d] = acc;
+            if (d == 0) {
+                part[(size_t)p.G * kD + h] = M;
+                part[(size_t)p.G * kD + p.G + h] = L;
+            }
+        }
+        __syncthreads();  // states read before this buffer is refilled
     }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
     if (threadIdx.x == 0) pdl_wait();
 }
 
@@ -1465,7 +1507,8 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st, cudaEvent_t ev
         if (e != cudaSuccess) return e;
         at.setb = true;
     }
-    e = launch_pdl(bf16_kernel, dim3(p.bf_items, p.B * p.hk), dim3(kBfThreads), kBfSmem, st, p);
+    const int bf_total = p.bf_items * p.B * p.hk;
+    e = launch_pdl(bf16_kernel, dim3(min(bf_total, 3 * at.sms)), dim3(kBfThreads), kBfSmem, st, p);
     if (e != cudaSuccess) return e;
     if (!at.setm) {
         e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMergeSmem);
