@@ -307,4 +307,43 @@ oscar_status oscar_decode_attn(const oscar_shape* shape, int32_t batch, const vo
     return e == cudaSuccess ? OSCAR_OK : cuda_fail(e);
 }
 
+oscar_status oscar_calibrate_rotation(const oscar_shape* shape, int32_t n_q, const void* q, int32_t n_t,
+                                      const void* kv, float sm_scale, float* U, float* eigvals,
+                                      void* workspace, size_t* ws_bytes, int32_t* dev_status, void* stream) {
+    const oscar_status sst = check_shape(shape);
+    if (sst != OSCAR_OK) return sst;
+    if (n_q < 1 || n_t < 1 || !ws_bytes) return OSCAR_ERR_INVALID_ARG;
+    const int hq = shape->num_q_heads, hk = shape->num_kv_heads;
+    // covariance sums [2][Hk][d][d], then the attention outputs [n_q][Hq][d]
+    const size_t c_bytes = round_up((size_t)2 * hk * kD * kD * 4, 256);
+    const size_t total = c_bytes + round_up((size_t)n_q * hq * kD * 4, 256);
+    if (!workspace) {
+        *ws_bytes = total;
+        return OSCAR_OK;
+    }
+    if (*ws_bytes < total) return OSCAR_ERR_WORKSPACE;
+    if (!q || !kv || !U) return OSCAR_ERR_INVALID_ARG;
+    if (!aligned(q, 8) || !aligned(kv, 16) || !aligned(U, 16) || !aligned(eigvals, 4) || !aligned(workspace, 16) ||
+        !aligned(dev_status, 4))
+        return OSCAR_ERR_INVALID_ARG;
+    if (!(sm_scale > 0.f) || !(sm_scale < 3.0e38f)) return OSCAR_ERR_INVALID_ARG;
+    if ((double)n_q * hq > 2.0e9 || (double)n_t * hk * 2 * kD > 2.0e9) return OSCAR_ERR_INVALID_ARG;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    CalibParams p{};
+    p.q = static_cast<const __nv_bfloat16*>(q);
+    p.kv = static_cast<const __nv_bfloat16*>(kv);
+    p.C = reinterpret_cast<float*>(ws);
+    p.o = reinterpret_cast<float*>(ws + c_bytes);
+    p.U = U;
+    p.lam = eigvals;
+    p.status = dev_status;
+    p.n_q = n_q;
+    p.n_t = n_t;
+    p.hq = hq;
+    p.hk = hk;
+    p.sm_scale = sm_scale;
+    const cudaError_t e = launch_calibrate(p, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? OSCAR_OK : cuda_fail(e);
+}
+
 }  // extern "C"

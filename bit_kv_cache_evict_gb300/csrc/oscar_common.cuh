@@ -317,6 +317,20 @@ __host__ __device__ __forceinline__ SeqSplits seq_splits(int npg, int pps, int t
     return r;
 }
 
+// offline rotation calibration (calibrate.cu)
+struct CalibParams {
+    const __nv_bfloat16* q;    // [n_q][hq][kD] calibration queries
+    const __nv_bfloat16* kv;   // [n_t][hk][2][kD] calibration tokens
+    float* o;                  // [n_q][hq][kD] attention outputs (scratch)
+    float* C;                  // [2][hk][kD][kD] covariance sums (scratch): K, then V
+    float* U;                  // [hk][2][kD][kD] out
+    float* lam;                // [hk][2][kD] out, nullable
+    int* status;
+    int n_q, n_t, hq, hk;
+    float sm_scale;
+};
+cudaError_t launch_calibrate(const CalibParams& p, cudaStream_t st);
+
 cudaError_t launch_evict(const EvictParams& p, cudaStream_t st);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st, cudaEvent_t ev_int2_start,
                           cudaEvent_t ev_int2_stop);

@@ -70,6 +70,9 @@ def lib() -> ctypes.CDLL:
                                                 ctypes.c_int32, _P, _P, ctypes.c_float, _P, _P, _P]
         L.oscar_time_next_int2.restype = None
         L.oscar_time_next_int2.argtypes = [_P, _P]
+        L.oscar_calibrate_rotation.restype = ctypes.c_int
+        L.oscar_calibrate_rotation.argtypes = [S, ctypes.c_int32, _P, ctypes.c_int32, _P, ctypes.c_float, _P, _P,
+                                               _P, ctypes.POINTER(ctypes.c_size_t), _P, _P]
         _LIB = L
     return _LIB
 
@@ -201,3 +204,26 @@ def oscar_decode_attn_noalloc(shape: oscar_shape, q, bf16_kv, bf16_len, pool, pa
         _dptr(U, "U", torch.float32), ctypes.c_float(sm_scale), _dptr(out, "out", torch.float32),
         _dptr(dev_status, "dev_status", torch.int32), _stream_ptr(stream))
     _check("oscar_decode_attn_noalloc", st)
+
+
+def oscar_calibrate_workspace_bytes(shape: oscar_shape, n_q: int) -> int:
+    ws = ctypes.c_size_t(0)
+    st = lib().oscar_calibrate_rotation(ctypes.byref(shape), n_q, None, 1, None, ctypes.c_float(1.0), None, None,
+                                        None, ctypes.byref(ws), None, None)
+    _check("oscar_calibrate_rotation", st)
+    return int(ws.value)
+
+
+def oscar_calibrate_rotation(shape: oscar_shape, q, kv, sm_scale: float, U, workspace, eigvals=None,
+                             dev_status=None, stream=None) -> None:
+    """Offline calibration of U from calibration queries q [n_q][Hq][d] and
+    tokens kv [n_t][Hk][2][d] (bf16 CUDA tensors) into U [Hk][2][d][d]
+    (fp32); see include/oscar.h."""
+    import torch
+    ws = ctypes.c_size_t(int(workspace.numel()))
+    st = lib().oscar_calibrate_rotation(
+        ctypes.byref(shape), int(q.shape[0]), _dptr(q, "q", torch.bfloat16), int(kv.shape[0]),
+        _dptr(kv, "kv", torch.bfloat16), ctypes.c_float(sm_scale), _dptr(U, "U", torch.float32),
+        _dptr(eigvals, "eigvals", torch.float32), _dptr(workspace, "workspace", torch.uint8), ctypes.byref(ws),
+        _dptr(dev_status, "dev_status", torch.int32), _stream_ptr(stream))
+    _check("oscar_calibrate_rotation", st)

@@ -197,3 +197,36 @@ def kv_tokens_torch(w: Workload, n: int, gen, profile_t, device):
         c = torch.randn((n, w.hk, 2, D, 3), generator=gen, device=device, dtype=torch.float32)
         x = z / torch.sqrt((c * c).sum(-1) / 3.0)
     return (x * profile_t).to(torch.bfloat16)
+
+
+# ---------------------------------------------------------------------------
+# offline rotation calibration
+# ---------------------------------------------------------------------------
+
+CALIB_SPECTRUM_SCALE = 24.0   # eigenvalue i of each drawn covariance: exp(-i / 24)
+
+
+def calibration_inputs(seed: int, n_q: int, n_t: int, hq: int, hk: int):
+    """Seeded calibration activations for the offline rotation calibration:
+    query tokens q [n_q][hq][D] and K/V tokens [n_t][hk][2][D], as bf16 bit
+    patterns.  Each KV head draws three orthogonal bases (queries of its
+    group, keys, values) and the values are Gaussian along them with the
+    spectrum exp(-i / 24) (every eigenvalue distinct), scaled so that the
+    attention of a query over the tokens is selective (logits of a few
+    units), as the pages' calibration on real activations would be.  They
+    stand in for model activations, which this build has none of."""
+    rng = np.random.Generator(np.random.PCG64([seed, 7]))
+    g = hq // hk
+    sd = np.sqrt(np.exp(-np.arange(D) / CALIB_SPECTRUM_SCALE))
+    q = np.empty((n_q, hq, D))
+    kv = np.empty((n_t, hk, 2, D))
+    for h in range(hk):
+        bases = []
+        for _ in range(3):
+            a, r = np.linalg.qr(rng.standard_normal((D, D)))
+            bases.append(a * np.sign(np.diag(r))[None, :])
+        for j in range(g):
+            q[:, h * g + j, :] = 3.0 * (rng.standard_normal((n_q, D)) * sd) @ bases[0].T
+        kv[:, h, 0, :] = 3.0 * (rng.standard_normal((n_t, D)) * sd) @ bases[1].T
+        kv[:, h, 1, :] = 2.0 * (rng.standard_normal((n_t, D)) * sd) @ bases[2].T
+    return bf16_bits(q), bf16_bits(kv)

@@ -91,6 +91,7 @@ typedef enum {
 #define OSCAR_STATUS_BAD_PAGE 1 /* a page id outside [0, num_pages) */
 #define OSCAR_STATUS_BAD_POS 2  /* a position, row or sequence index out of range */
 #define OSCAR_STATUS_TIMEOUT 4  /* a bounded wait for a page copy gave up */
+#define OSCAR_STATUS_NO_CONVERGENCE 8 /* the calibration eigensolver stopped before converging */
 
 #define OSCAR_BLOCK_BYTES 6144  /* bytes per (page, KV head) block, d=128, g=32, page 64 */
 
@@ -247,6 +248,43 @@ oscar_status oscar_decode_attn_noalloc(const oscar_shape* shape, int32_t batch, 
                                        int32_t max_pages, int32_t num_pages, const int32_t* hist_len,
                                        const float* U, float sm_scale, float* out, int32_t* dev_status,
                                        void* stream);
+
+/*
+ * oscar_calibrate_rotation -- offline calibration of U ([NEWS] sec. B: U is
+ * fixed offline per layer and KV head, for K from the covariance of the
+ * queries that read the keys, for V from the covariance of the values as
+ * weighted by the attention scores).  The pages give no formula; this call
+ * takes the plainest reading:
+ *   U_K[kv] = eigenvectors of mean(q q^T) over every calibration query token
+ *             of every query head h with h / G = kv;
+ *   U_V[kv] = eigenvectors of mean(o o^T) over the same samples, o the
+ *             output of that query head's full (non-causal) softmax
+ *             attention, scale sm_scale, over the calibration tokens:
+ *             sum o o^T = V^T S^T S V with S the attention probabilities;
+ * columns in order of decreasing eigenvalue, each column's entry of largest
+ * magnitude positive; the result feeds oscar_evict_quantize and
+ * oscar_decode_attn as U.  Arithmetic is fp32 (attention, covariance sums,
+ * cyclic Jacobi eigensolver), so U is orthogonal to about 1e-6.  It runs
+ * once per layer, offline; it is not part of a decode step.
+ *
+ *   q        (device) bf16 [n_q][Hq][d] calibration queries, 8-byte aligned
+ *   kv       (device) bf16 [n_t][Hk][2][d] calibration keys and values,
+ *            16-byte aligned
+ *   U        (device) fp32 [Hk][2][d][d] out (layout of the U argument above)
+ *   eigvals  (device) fp32 [Hk][2][d] out, the eigenvalues in U's column
+ *            order, or NULL
+ *   workspace, *ws_bytes: as oscar_decode_attn (workspace == NULL returns
+ *            the size, which depends on shape and n_q); 16-byte aligned.
+ *   dev_status: OSCAR_STATUS_NO_CONVERGENCE if a matrix's off-diagonal mass
+ *            stayed above 1e-6 of its diagonal after the sweep limit (U is
+ *            then the last iterate).
+ * Errors: OSCAR_ERR_INVALID_ARG for n_q < 1, n_t < 1, null or misaligned
+ * pointers, a non-finite or non-positive sm_scale; OSCAR_ERR_UNSUPPORTED as
+ * for the other calls; OSCAR_ERR_WORKSPACE for a short workspace.
+ */
+oscar_status oscar_calibrate_rotation(const oscar_shape* shape, int32_t n_q, const void* q, int32_t n_t,
+                                      const void* kv, float sm_scale, float* U, float* eigvals,
+                                      void* workspace, size_t* ws_bytes, int32_t* dev_status, void* stream);
 
 #ifdef __cplusplus
 }
