@@ -89,6 +89,9 @@ def parse_args():
                     help="oracle steps timed for cpu_baseline (about 10 s of host work)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--calibrate", action="store_true",
+                    help="time the offline rotation calibration (oscar_calibrate_rotation) instead of a decode "
+                         "step: one JSON line, the float64 oracle timed on the same inputs")
     ap.add_argument("--quant-group", type=int, default=32, choices=[32, 64, 128],
                     help="stored positions per fp16 scale/zero pair (32 is the configured format)")
     return ap.parse_args()
@@ -617,9 +620,70 @@ def run_oscar(args, rank: int, world: int, local: int) -> None:
         dist.destroy_process_group()
 
 
+CALIB_CONFIG = {"workload": "qwen3_8b_calibration", "query_tokens": 1024, "query_heads": 32, "kv_heads": 8,
+                "tokens": 2048, "head_dim": S.D}
+
+
+def run_calibrate(args, rank: int) -> None:
+    """Offline rotation calibration of one layer (Qwen3-8B heads): attention
+    outputs of 1024 calibration query tokens x 32 heads over 2048 tokens,
+    the K and V covariances of the 8 KV groups and their eigenvectors.  The
+    metric is the time of one calibration; the float64 oracle runs once on
+    the same inputs for cpu_baseline."""
+    import torch
+    from bit_kv_cache_evict_gb300 import build as B
+    from bit_kv_cache_evict_gb300 import oscar as O
+    if rank != 0:
+        return
+    B.build()
+    cfg = CALIB_CONFIG
+    nq, nt, hq, hk = cfg["query_tokens"], cfg["tokens"], cfg["query_heads"], cfg["kv_heads"]
+    qb, kvb = S.calibration_inputs(1800, nq, nt, hq, hk)
+    sh = O.make_shape(hq, hk)
+    dev = torch.device("cuda", 0)
+    q_t = torch.from_numpy(qb.view(np.int16)).to(dev).view(torch.bfloat16)
+    kv_t = torch.from_numpy(kvb.view(np.int16)).to(dev).view(torch.bfloat16)
+    U_t = torch.empty((hk, 2, S.D, S.D), dtype=torch.float32, device=dev)
+    ws = torch.zeros(O.oscar_calibrate_workspace_bytes(sh, nq), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    scale = 1.0 / math.sqrt(S.D)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(args.warmup, 3)):
+        O.oscar_calibrate_rotation(sh, q_t, kv_t, scale, U_t, ws, dev_status=status, stream=stream)
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(0)
+    clocks.start()
+    for a, b in ev:
+        a.record(stream)
+        O.oscar_calibrate_rotation(sh, q_t, kv_t, scale, U_t, ws, dev_status=status, stream=stream)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    flops = 2.0 * nq * hq * nt * S.D * 2          # logits and weighted sum of the attention outputs
+    from oracle import calibrate as OC
+    q64 = S.bf16_to_f32(qb).astype(np.float64)
+    kv64 = S.bf16_to_f32(kvb).astype(np.float64)
+    t0 = time.perf_counter()
+    OC.calibrate(q64, kv64, scale)
+    cpu_s = time.perf_counter() - t0
+    print(json.dumps({
+        "metric": "offline rotation calibration time per layer", "value": ms, "unit": "ms",
+        "higher_is_better": False, "n_gpus": 1, "steps": args.steps, "warmup": max(args.warmup, 3),
+        "dtype": "f32", "data": "synthetic", "config": cfg, "vs_baseline": None,
+        "status": int(status.item()), "attention_tflops": flops / (ms * 1e-3) / 1e12,
+        "cpu_baseline": {"value": cpu_s * 1e3, "unit": "ms", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": "the same calibration, float64 numpy (BLAS threads)"},
+        "clocks": clk}))
+
+
 def main():
     args = parse_args()
     rank, world, local = dist_info()
+    if args.calibrate:
+        run_calibrate(args, rank)
+        return
     if args.gpus != world and world > 1:
         print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
     if args.impl == "reference":
