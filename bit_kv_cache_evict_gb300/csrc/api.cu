@@ -346,4 +346,37 @@ oscar_status oscar_calibrate_rotation(const oscar_shape* shape, int32_t n_q, con
     return e == cudaSuccess ? OSCAR_OK : cuda_fail(e);
 }
 
+oscar_status oscar_calibrate_clip(const oscar_shape* shape, int32_t n_t, const void* kv, const float* U,
+                                  const float* grid, int32_t n_grid, float* clip, float* mse, void* workspace,
+                                  size_t* ws_bytes, void* stream) {
+    const oscar_status sst = check_shape(shape);
+    if (sst != OSCAR_OK) return sst;
+    if (n_t < 1 || n_grid < 1 || n_grid > kMaxClipGrid || !ws_bytes) return OSCAR_ERR_INVALID_ARG;
+    const int hk = shape->num_kv_heads;
+    const size_t total = round_up((size_t)hk * 2 * kMaxClipGrid * sizeof(double), 256);
+    if (!workspace) {
+        *ws_bytes = total;
+        return OSCAR_OK;
+    }
+    if (*ws_bytes < total) return OSCAR_ERR_WORKSPACE;
+    if (!kv || !U || !grid || !clip) return OSCAR_ERR_INVALID_ARG;
+    if (!aligned(kv, 16) || !aligned(U, 16) || !aligned(grid, 4) || !aligned(clip, 4) || !aligned(mse, 4) ||
+        !aligned(workspace, 16))
+        return OSCAR_ERR_INVALID_ARG;
+    if ((double)n_t * hk * 2 * kD > 2.0e9) return OSCAR_ERR_INVALID_ARG;
+    ClipParams p{};
+    p.kv = static_cast<const __nv_bfloat16*>(kv);
+    p.U = U;
+    p.grid = grid;
+    p.err = static_cast<double*>(workspace);
+    p.clip = clip;
+    p.mse = mse;
+    p.n_t = n_t;
+    p.hk = hk;
+    p.n_grid = n_grid;
+    p.gshift = gshift_of(shape);
+    const cudaError_t e = launch_calibrate_clip(p, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? OSCAR_OK : cuda_fail(e);
+}
+
 }  // extern "C"

@@ -325,8 +325,157 @@ __global__ void __launch_bounds__(kEigThreads) calib_eig_kernel(const float* C, 
 }
 
 // ---------------------------------------------------------------------------
+// clip-threshold search
+// ---------------------------------------------------------------------------
+// Block = (chunk of calibration tokens, (KV head, K/V)): U of the matrix is
+// staged in shared memory; each warp rotates one token at a time,
+// y = x . U . H (fp32, Hadamard by warp shuffles, scaled 1/sqrt(d)), with
+// lane l holding Hadamard outputs j = 4l + k whose stored positions
+// bitrev7(j) put value k of every lane in 32-position block bitrev2(k) -- so
+// a block's statistics are warp reductions, as in the eviction.  For every
+// candidate ratio c the token is quantised as the eviction does (clip to
+// +-c max|y| per group, fp16 s = (max - min) / 3 and z = min, codes from the
+// stored s, z) and sum (y - y^)^2 is added to the candidate's total.
+constexpr int kClipWarps = 8;
+constexpr int kClipTokens = 64;       // tokens per block
+
+__global__ void __launch_bounds__(32 * kClipWarps) calib_clip_kernel(ClipParams p) {
+    extern __shared__ __align__(16) float csm[];
+    float* Us = csm;                                   // [kD][kD]
+    float* errs = Us + kD * kD;                        // [kMaxClipGrid]
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int mat = blockIdx.y;                        // kv * 2 + which
+    const int kv = mat >> 1, which = mat & 1;
+    const float* Ug = p.U + (size_t)mat * kD * kD;
+    for (int i = threadIdx.x; i < kD * kD / 4; i += 32 * kClipWarps)
+        reinterpret_cast<float4*>(Us)[i] = reinterpret_cast<const float4*>(Ug)[i];
+    if (threadIdx.x < kMaxClipGrid) errs[threadIdx.x] = 0.f;
+    __syncthreads();
+    const int gshift = p.gshift;
+    const int t_end = min(p.n_t, (blockIdx.x + 1) * kClipTokens);
+    for (int t = blockIdx.x * kClipTokens + warp; t < t_end; t += kClipWarps) {
+        const uint2 xr = *reinterpret_cast<const uint2*>(p.kv + ((size_t)t * p.hk * 2 + mat) * kD + 4 * lane);
+        const float x[4] = {bf16_lo(xr.x), bf16_hi(xr.x), bf16_lo(xr.y), bf16_hi(xr.y)};
+        float y[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int a = 0; a < kD; ++a) {
+            const float xa = __shfl_sync(kFull, x[a & 3], a >> 2);
+            const float4 u = *reinterpret_cast<const float4*>(Us + a * kD + 4 * lane);
+            y[0] = fmaf(xa, u.x, y[0]);
+            y[1] = fmaf(xa, u.y, y[1]);
+            y[2] = fmaf(xa, u.z, y[2]);
+            y[3] = fmaf(xa, u.w, y[3]);
+        }
+        {  // Hadamard: in-lane stages, then lanes
+            const float t0 = y[0] + y[1], t1 = y[0] - y[1], t2 = y[2] + y[3], t3 = y[2] - y[3];
+            y[0] = t0 + t2;
+            y[2] = t0 - t2;
+            y[1] = t1 + t3;
+            y[3] = t1 - t3;
+        }
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1) {
+            const bool upper = (lane & m) != 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float o = __shfl_xor_sync(kFull, y[k], m);
+                y[k] = upper ? o - y[k] : y[k] + o;
+            }
+        }
+        float amax[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            y[k] *= (float)kInvSqrtD;
+            amax[k] = fabsf(y[k]);
+        }
+#pragma unroll
+        for (int m = 16; m > 0; m >>= 1)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) amax[k] = fmaxf(amax[k], __shfl_xor_sync(kFull, amax[k], m));
+        if (gshift >= 1) {  // groups of 64 (128) stored positions: values k = {0,2}, {1,3} (all)
+            amax[0] = amax[2] = fmaxf(amax[0], amax[2]);
+            amax[1] = amax[3] = fmaxf(amax[1], amax[3]);
+        }
+        if (gshift >= 2) amax[0] = amax[1] = amax[2] = amax[3] = fmaxf(amax[0], amax[1]);
+        for (int c = 0; c < p.n_grid; ++c) {
+            const float cr = p.grid[c];
+            float yc[4], lo[4], hi[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float tt = cr * amax[k];
+                yc[k] = cr < 1.f ? fminf(fmaxf(y[k], -tt), tt) : y[k];
+                lo[k] = hi[k] = yc[k];
+            }
+#pragma unroll
+            for (int m = 16; m > 0; m >>= 1)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    lo[k] = fminf(lo[k], __shfl_xor_sync(kFull, lo[k], m));
+                    hi[k] = fmaxf(hi[k], __shfl_xor_sync(kFull, hi[k], m));
+                }
+            if (gshift >= 1) {
+                lo[0] = lo[2] = fminf(lo[0], lo[2]);
+                lo[1] = lo[3] = fminf(lo[1], lo[3]);
+                hi[0] = hi[2] = fmaxf(hi[0], hi[2]);
+                hi[1] = hi[3] = fmaxf(hi[1], hi[3]);
+            }
+            if (gshift >= 2) {
+                lo[0] = lo[1] = lo[2] = lo[3] = fminf(lo[0], lo[1]);
+                hi[0] = hi[1] = hi[2] = hi[3] = fmaxf(hi[0], hi[1]);
+            }
+            float e = 0.f;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float sf = __half2float(__float2half_rn((hi[k] - lo[k]) / 3.f));
+                const float zf = __half2float(__float2half_rn(lo[k]));
+                float code = 0.f;
+                if (sf != 0.f) code = fminf(fmaxf(rintf((yc[k] - zf) / sf), 0.f), 3.f);
+                const float d = y[k] - fmaf(sf, code, zf);
+                e = fmaf(d, d, e);
+            }
+#pragma unroll
+            for (int m = 16; m > 0; m >>= 1) e += __shfl_xor_sync(kFull, e, m);
+            if (lane == 0) atomicAdd(&errs[c], e);
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x < p.n_grid) atomicAdd(p.err + (size_t)mat * kMaxClipGrid + threadIdx.x, (double)errs[threadIdx.x]);
+}
+
+// the ratio with the least error per matrix (the larger ratio on ties)
+__global__ void calib_clip_pick_kernel(ClipParams p) {
+    const int mat = threadIdx.x;
+    if (mat >= p.hk * 2) return;
+    const double* e = p.err + (size_t)mat * kMaxClipGrid;
+    const double denom = (double)p.n_t * kD;
+    int best = 0;
+    for (int c = 1; c < p.n_grid; ++c)
+        if (e[c] < e[best] || (e[c] == e[best] && p.grid[c] > p.grid[best])) best = c;
+    p.clip[mat] = p.grid[best];
+    if (p.mse)
+        for (int c = 0; c < p.n_grid; ++c) p.mse[(size_t)mat * p.n_grid + c] = (float)(e[c] / denom);
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
+cudaError_t launch_calibrate_clip(const ClipParams& p, cudaStream_t st) {
+    cudaError_t e = cudaMemsetAsync(p.err, 0, (size_t)p.hk * 2 * kMaxClipGrid * sizeof(double), st);
+    if (e != cudaSuccess) return e;
+    const int smem = (kD * kD + kMaxClipGrid) * 4;
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    static bool attr_set[64] = {};
+    if (!attr_set[dev & 63]) {
+        e = cudaFuncSetAttribute(calib_clip_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        attr_set[dev & 63] = true;
+    }
+    dim3 grid((p.n_t + kClipTokens - 1) / kClipTokens, p.hk * 2);
+    calib_clip_kernel<<<grid, 32 * kClipWarps, smem, st>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    calib_clip_pick_kernel<<<1, 32 * ((p.hk * 2 + 31) / 32), 0, st>>>(p);
+    return cudaGetLastError();
+}
 cudaError_t launch_calibrate(const CalibParams& p, cudaStream_t st) {
     const size_t mat = (size_t)kD * kD;
     cudaError_t e = cudaMemsetAsync(p.C, 0, (size_t)p.hk * 2 * mat * sizeof(float), st);

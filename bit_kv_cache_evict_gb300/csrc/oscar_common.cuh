@@ -331,6 +331,18 @@ struct CalibParams {
 };
 cudaError_t launch_calibrate(const CalibParams& p, cudaStream_t st);
 
+constexpr int kMaxClipGrid = 32;   // candidate clip ratios per search
+struct ClipParams {
+    const __nv_bfloat16* kv;   // [n_t][hk][2][kD] calibration tokens
+    const float* U;            // [hk][2][kD][kD]
+    const float* grid;         // [n_grid] candidate ratios (device)
+    double* err;               // [hk * 2][kMaxClipGrid] squared-error sums (scratch)
+    float* clip;               // [hk][2] out
+    float* mse;                // [hk][2][n_grid] out, nullable
+    int n_t, hk, n_grid, gshift;
+};
+cudaError_t launch_calibrate_clip(const ClipParams& p, cudaStream_t st);
+
 cudaError_t launch_evict(const EvictParams& p, cudaStream_t st);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st, cudaEvent_t ev_int2_start,
                           cudaEvent_t ev_int2_stop);

@@ -70,6 +70,9 @@ def lib() -> ctypes.CDLL:
                                                 ctypes.c_int32, _P, _P, ctypes.c_float, _P, _P, _P]
         L.oscar_time_next_int2.restype = None
         L.oscar_time_next_int2.argtypes = [_P, _P]
+        L.oscar_calibrate_clip.restype = ctypes.c_int
+        L.oscar_calibrate_clip.argtypes = [S, ctypes.c_int32, _P, _P, _P, ctypes.c_int32, _P, _P, _P,
+                                           ctypes.POINTER(ctypes.c_size_t), _P]
         L.oscar_calibrate_rotation.restype = ctypes.c_int
         L.oscar_calibrate_rotation.argtypes = [S, ctypes.c_int32, _P, ctypes.c_int32, _P, ctypes.c_float, _P, _P,
                                                _P, ctypes.POINTER(ctypes.c_size_t), _P, _P]
@@ -227,3 +230,25 @@ def oscar_calibrate_rotation(shape: oscar_shape, q, kv, sm_scale: float, U, work
         _dptr(eigvals, "eigvals", torch.float32), _dptr(workspace, "workspace", torch.uint8), ctypes.byref(ws),
         _dptr(dev_status, "dev_status", torch.int32), _stream_ptr(stream))
     _check("oscar_calibrate_rotation", st)
+
+
+def oscar_calibrate_clip(shape: oscar_shape, kv, U, grid, clip, workspace=None, mse=None, stream=None) -> None:
+    """Offline clip-ratio search: for each (KV head, K/V) the ratio of grid
+    (fp32 CUDA tensor) with the least reconstruction error of the rotated
+    calibration tokens kv [n_t][Hk][2][d] under the eviction's quantiser;
+    see include/oscar.h.  ``workspace`` defaults to a fresh tensor."""
+    import torch
+    n_grid = int(grid.numel())
+    need = ctypes.c_size_t(0)
+    st = lib().oscar_calibrate_clip(ctypes.byref(shape), int(kv.shape[0]), None, None, None, n_grid, None, None,
+                                    None, ctypes.byref(need), None)
+    _check("oscar_calibrate_clip", st)
+    if workspace is None:
+        workspace = torch.zeros(int(need.value), dtype=torch.uint8, device=kv.device)
+    ws = ctypes.c_size_t(int(workspace.numel()))
+    st = lib().oscar_calibrate_clip(
+        ctypes.byref(shape), int(kv.shape[0]), _dptr(kv, "kv", torch.bfloat16), _dptr(U, "U", torch.float32),
+        _dptr(grid, "grid", torch.float32), n_grid, _dptr(clip, "clip", torch.float32),
+        _dptr(mse, "mse", torch.float32), _dptr(workspace, "workspace", torch.uint8), ctypes.byref(ws),
+        _stream_ptr(stream))
+    _check("oscar_calibrate_clip", st)

@@ -286,6 +286,30 @@ oscar_status oscar_calibrate_rotation(const oscar_shape* shape, int32_t n_q, con
                                       const void* kv, float sm_scale, float* U, float* eigvals,
                                       void* workspace, size_t* ws_bytes, int32_t* dev_status, void* stream);
 
+/*
+ * oscar_calibrate_clip -- offline choice of the clip ratios ([NEWS] sec. B:
+ * the clip thresholds are fixed offline together with U).  Reading: for each
+ * (KV head, K/V) the ratio c of the candidate list with the least mean
+ * squared error sum (y - y^)^2 / (n_t d) over the calibration tokens, y = x . R
+ * the rotated vector and y^ its dequantised value under the eviction's
+ * quantiser with clip ratio c (values clipped to +-c max|y| per group, the
+ * error measured against the unclipped y); ties go to the larger ratio.
+ * fp32 arithmetic (rotation x . U in fp32, not the eviction's compensated
+ * form; the error totals in fp64).
+ *
+ *   kv       (device) bf16 [n_t][Hk][2][d] calibration tokens, 16-byte aligned
+ *   U        (device) fp32 [Hk][2][d][d] (e.g. from oscar_calibrate_rotation)
+ *   grid     (device) fp32 [n_grid] candidate ratios in (0, 1], 1 <= n_grid <= 32
+ *   clip     (device) fp32 [Hk][2] out: the chosen ratios (the eviction's clip)
+ *   mse      (device) fp32 [Hk][2][n_grid] out, the mean squared error of every
+ *            candidate, or NULL
+ *   workspace, *ws_bytes: as oscar_decode_attn (workspace == NULL returns the
+ *            size), 16-byte aligned.
+ */
+oscar_status oscar_calibrate_clip(const oscar_shape* shape, int32_t n_t, const void* kv, const float* U,
+                                  const float* grid, int32_t n_grid, float* clip, float* mse, void* workspace,
+                                  size_t* ws_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

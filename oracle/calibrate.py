@@ -91,3 +91,37 @@ def calibrate(q: np.ndarray, kv: np.ndarray, sm_scale: float):
         U[h, 0], lam[h, 0] = rotation_from_covariance(ck[h])
         U[h, 1], lam[h, 1] = rotation_from_covariance(cv[h])
     return U, lam
+
+
+def clip_search(kv: np.ndarray, U: np.ndarray, grid, group: int = 32):
+    """Clip ratios chosen offline with U ([NEWS] sec. B fixes the clip
+    thresholds offline together with U; the criterion is a reading): for
+    each (KV head, K/V) the candidate c with the least mean squared error
+    sum (y - y^)^2 / (n_t d) over the calibration tokens, y = x . R the rotated
+    vector (float64) and y^ its dequantised value under the eviction's
+    quantiser (the C oracle's quantize_vec / dequantize_vec) with clip c,
+    measured against the unclipped y; ties go to the larger c.
+
+    kv: float64 [n_t][Hk][2][d]; U: [Hk][2][d][d].  Returns (clip [Hk][2],
+    mse [Hk][2][len(grid)])."""
+    from oracle import get
+    orc = get()
+    n_t, hk, _, d = kv.shape
+    grid = [float(c) for c in grid]
+    mse = np.zeros((hk, 2, len(grid)))
+    clip = np.zeros((hk, 2))
+    for h in range(hk):
+        for w in range(2):
+            Y = np.asarray(kv[:, h, w, :], np.float64) @ orc.build_R(U[h, w])
+            for ci, c in enumerate(grid):
+                err = 0.0
+                for y in Y:
+                    codes, s16, z16 = orc.quantize_vec(y, group, c)[:3]
+                    err += float(((y - orc.dequantize_vec(codes, s16, z16, group)) ** 2).sum())
+                mse[h, w, ci] = err / (n_t * d)
+            best = 0
+            for ci in range(1, len(grid)):
+                if mse[h, w, ci] < mse[h, w, best] or (mse[h, w, ci] == mse[h, w, best] and grid[ci] > grid[best]):
+                    best = ci
+            clip[h, w] = grid[best]
+    return clip, mse

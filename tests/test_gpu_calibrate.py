@@ -74,3 +74,30 @@ def test_calibration_matches_oracle(n_q, n_t, hq, hk):
                 mags = np.sort(np.abs(U_r[:, j]))
                 if mags[-1] - mags[-2] > 10 * bound:  # the sign convention's pivot entry is unambiguous
                     assert dot > 0, (h, w, j, dot)
+
+
+@pytest.mark.parametrize("n_t,hk,qg", [(300, 2, 32), (130, 1, 128)])
+def test_clip_search_matches_oracle(n_t, hk, qg):
+    """Per-candidate mean squared errors within 2e-4 (relative) of the
+    oracle's, and the chosen ratio equal to the oracle's unless the oracle's
+    two best candidates are that close."""
+    _, kvb = S.calibration_inputs(90 + n_t, 8, n_t, 4 * hk, hk)
+    w = S.Workload(77, "clip", batch=1, hq=4 * hk, hk=hk)
+    U = S.rotation_U(w).astype(np.float32)
+    grid = np.round(np.arange(0.80, 1.0001, 0.02), 4).astype(np.float32)
+    sh = O.oscar_shape(128, qg, 64, 256, 64, 4 * hk, hk)
+    kv_t = torch.from_numpy(kvb.view(np.int16)).cuda().view(torch.bfloat16)
+    U_t = torch.from_numpy(U).cuda()
+    grid_t = torch.from_numpy(grid).cuda()
+    clip_t = torch.zeros((hk, 2), dtype=torch.float32, device="cuda")
+    mse_t = torch.zeros((hk, 2, grid.size), dtype=torch.float32, device="cuda")
+    O.oscar_calibrate_clip(sh, kv_t, U_t, grid_t, clip_t, mse=mse_t)
+    torch.cuda.synchronize()
+    clip_r, mse_r = OC.clip_search(S.bf16_to_f32(kvb).astype(np.float64), U.astype(np.float64), grid, qg)
+    mse_g, clip_g = mse_t.cpu().numpy(), clip_t.cpu().numpy()
+    assert np.abs(mse_g - mse_r).max() <= 2e-4 * mse_r.max()
+    for h in range(hk):
+        for wv in range(2):
+            srt = np.sort(mse_r[h, wv])
+            if srt[1] - srt[0] > 2e-4 * srt[0]:
+                assert clip_g[h, wv] == clip_r[h, wv], (h, wv, clip_g[h, wv], clip_r[h, wv], mse_r[h, wv])

@@ -96,3 +96,43 @@ def test_calibrate_end_to_end_on_a_small_case():
     assert np.abs(ck @ U[0, 0] - U[0, 0] * lam[0, 0]).max() < 1e-9 * lam[0, 0, 0]
     for w in range(2):
         assert np.abs(U[0, w].T @ U[0, w] - np.eye(D)).max() < 1e-12
+
+
+def _minmax_mse(Y: np.ndarray, g: int) -> float:
+    """Textbook min-max asymmetric INT2 (fp16 scale/zero, round half to even)
+    computed with numpy alone."""
+    err = 0.0
+    for y in Y:
+        for k in range(0, y.size, g):
+            v = y[k:k + g]
+            lo, hi = v.min(), v.max()
+            s = float(np.float16((hi - lo) / 3))
+            z = float(np.float16(lo))
+            codes = np.zeros(g) if s == 0 else np.clip(np.rint((v - z) / s), 0, 3)
+            err += float(((v - (s * codes + z)) ** 2).sum())
+    return err / Y.size
+
+
+def test_clip_search_without_clipping_is_textbook_minmax():
+    from oracle import get
+    rng = np.random.default_rng(12)
+    kv = rng.standard_normal((20, 1, 2, D))
+    U = np.stack([_orthogonal(1), _orthogonal(2)])[None]
+    clip, mse = C.clip_search(kv, U, [1.0])
+    assert clip[0, 0] == 1.0 and clip[0, 1] == 1.0
+    Y = kv[:, 0, 0, :] @ get().build_R(U[0, 0])
+    assert np.isclose(mse[0, 0, 0], _minmax_mse(Y, 32), rtol=1e-12)
+
+
+def test_clip_search_prefers_clipping_a_lone_outlier():
+    # after the rotation every group holds N(0, 1)-like values; add one large
+    # value per group in the rotated domain through U = identity-like setup
+    from oracle import get
+    rng = np.random.default_rng(13)
+    R = get().build_R(np.eye(D))
+    Y = rng.standard_normal((40, D))
+    Y[:, ::32] = 12.0                                    # one value per 32-position group far out
+    kv = (Y @ R.T)[:, None, None, :].repeat(2, axis=2)   # x with x . R = Y
+    clip, mse = C.clip_search(kv, np.eye(D)[None, None].repeat(2, axis=1), [0.3, 0.6, 1.0])
+    assert clip[0, 0] < 1.0
+    assert mse[0, 0, 2] > mse[0, 0, list([0.3, 0.6, 1.0]).index(clip[0, 0])]
