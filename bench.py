@@ -628,8 +628,9 @@ def run_calibrate(args, rank: int) -> None:
     """Offline rotation calibration of one layer (Qwen3-8B heads): attention
     outputs of 1024 calibration query tokens x 32 heads over 2048 tokens,
     the K and V covariances of the 8 KV groups and their eigenvectors.  The
-    metric is the time of one calibration; the float64 oracle runs once on
-    the same inputs for cpu_baseline."""
+    metric is the time of one calibration; the clip-ratio search with the
+    calibrated U is timed beside it, and the float64 oracle's rotation
+    calibration runs once on the same inputs for cpu_baseline."""
     import torch
     from bit_kv_cache_evict_gb300 import build as B
     from bit_kv_cache_evict_gb300 import oscar as O
@@ -661,6 +662,21 @@ def run_calibrate(args, rank: int) -> None:
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
     ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    # clip-ratio search with the calibrated U (11 candidates, 0.50 .. 1.00)
+    grid_np = np.round(np.arange(0.50, 1.0001, 0.05), 4).astype(np.float32)
+    grid_t = torch.from_numpy(grid_np).to(dev)
+    clip_t = torch.empty((hk, 2), dtype=torch.float32, device=dev)
+    cws = torch.zeros(O.oscar_calibrate_clip_workspace_bytes(sh, nt, int(grid_np.size)), dtype=torch.uint8,
+                      device=dev)
+    for _ in range(3):
+        O.oscar_calibrate_clip(sh, kv_t, U_t, grid_t, clip_t, workspace=cws, stream=stream)
+    cev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in cev:
+        a.record(stream)
+        O.oscar_calibrate_clip(sh, kv_t, U_t, grid_t, clip_t, workspace=cws, stream=stream)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    clip_ms = statistics.median(a.elapsed_time(b) for a, b in cev)
     flops = 2.0 * nq * hq * nt * S.D * 2          # logits and weighted sum of the attention outputs
     from oracle import calibrate as OC
     q64 = S.bf16_to_f32(qb).astype(np.float64)
@@ -673,6 +689,8 @@ def run_calibrate(args, rank: int) -> None:
         "higher_is_better": False, "n_gpus": 1, "steps": args.steps, "warmup": max(args.warmup, 3),
         "dtype": "f32", "data": "synthetic", "config": cfg, "vs_baseline": None,
         "status": int(status.item()), "attention_tflops": flops / (ms * 1e-3) / 1e12,
+        "clip_search_ms": clip_ms, "clip_candidates": int(grid_np.size),
+        "clips_chosen": sorted(set(float(c) for c in clip_t.cpu().numpy().ravel())),
         "cpu_baseline": {"value": cpu_s * 1e3, "unit": "ms", "cores": os.cpu_count(), "kind": "oracle",
                          "sample": "the same calibration, float64 numpy (BLAS threads)"},
         "clocks": clk}))

@@ -232,6 +232,14 @@ def oscar_calibrate_rotation(shape: oscar_shape, q, kv, sm_scale: float, U, work
     _check("oscar_calibrate_rotation", st)
 
 
+def oscar_calibrate_clip_workspace_bytes(shape: oscar_shape, n_t: int = 1, n_grid: int = 1) -> int:
+    need = ctypes.c_size_t(0)
+    st = lib().oscar_calibrate_clip(ctypes.byref(shape), n_t, None, None, None, n_grid, None, None, None,
+                                    ctypes.byref(need), None)
+    _check("oscar_calibrate_clip", st)
+    return int(need.value)
+
+
 def oscar_calibrate_clip(shape: oscar_shape, kv, U, grid, clip, workspace=None, mse=None, stream=None) -> None:
     """Offline clip-ratio search: for each (KV head, K/V) the ratio of grid
     (fp32 CUDA tensor) with the least reconstruction error of the rotated
@@ -239,12 +247,9 @@ def oscar_calibrate_clip(shape: oscar_shape, kv, U, grid, clip, workspace=None, 
     see include/oscar.h.  ``workspace`` defaults to a fresh tensor."""
     import torch
     n_grid = int(grid.numel())
-    need = ctypes.c_size_t(0)
-    st = lib().oscar_calibrate_clip(ctypes.byref(shape), int(kv.shape[0]), None, None, None, n_grid, None, None,
-                                    None, ctypes.byref(need), None)
-    _check("oscar_calibrate_clip", st)
     if workspace is None:
-        workspace = torch.zeros(int(need.value), dtype=torch.uint8, device=kv.device)
+        workspace = torch.zeros(oscar_calibrate_clip_workspace_bytes(shape, int(kv.shape[0]), n_grid),
+                                dtype=torch.uint8, device=kv.device)
     ws = ctypes.c_size_t(int(workspace.numel()))
     st = lib().oscar_calibrate_clip(
         ctypes.byref(shape), int(kv.shape[0]), _dptr(kv, "kv", torch.bfloat16), _dptr(U, "U", torch.float32),
