@@ -200,12 +200,11 @@ oscar_status oscar_pool_layout(const oscar_shape* shape, int32_t batch, const in
     return OSCAR_OK;
 }
 
-oscar_status oscar_evict_quantize(const oscar_shape* shape, int32_t n_tok, const void* src_kv,
-                                  int32_t src_rows, const int32_t* src_row, const int32_t* dst_seq,
-                                  const int32_t* dst_pos, const void* new_kv, const float* U,
-                                  const float* clip, uint8_t* pool, const int32_t* page_table,
-                                  int32_t batch, int32_t max_pages, int32_t num_pages,
-                                  int32_t* dev_status, void* stream) {
+static oscar_status evict_impl(const oscar_shape* shape, int32_t n_tok, const void* src_kv, int32_t src_rows,
+                               const int32_t* src_row, const int32_t* dst_seq, const int32_t* dst_pos,
+                               const void* new_kv, const float* U, const float* clip, const float* codebook,
+                               uint8_t* pool, const int32_t* page_table, int32_t batch, int32_t max_pages,
+                               int32_t num_pages, int32_t* dev_status, void* stream) {
     const oscar_status sst = check_shape(shape);
     if (sst != OSCAR_OK) return sst;
     if (n_tok < 0 || src_rows < 0 || batch < 0 || max_pages <= 0 || num_pages < 0) return OSCAR_ERR_INVALID_ARG;
@@ -224,6 +223,7 @@ oscar_status oscar_evict_quantize(const oscar_shape* shape, int32_t n_tok, const
     p.new_kv = static_cast<const __nv_bfloat16*>(new_kv);
     p.U = U;
     p.clip = clip;
+    p.codebook = codebook;
     p.pool = pool;
     p.page_table = page_table;
     p.status = dev_status;
@@ -239,11 +239,32 @@ oscar_status oscar_evict_quantize(const oscar_shape* shape, int32_t n_tok, const
     return e == cudaSuccess ? OSCAR_OK : cuda_fail(e);
 }
 
-oscar_status oscar_decode_attn(const oscar_shape* shape, int32_t batch, const void* q, const void* bf16_kv,
-                               const int32_t* bf16_len, const uint8_t* pool, const int32_t* page_table,
-                               int32_t max_pages, int32_t num_pages, const int32_t* hist_len, const float* U,
-                               float sm_scale, float* out, void* workspace, size_t* ws_bytes,
-                               int32_t* dev_status, void* stream) {
+oscar_status oscar_evict_quantize(const oscar_shape* shape, int32_t n_tok, const void* src_kv,
+                                  int32_t src_rows, const int32_t* src_row, const int32_t* dst_seq,
+                                  const int32_t* dst_pos, const void* new_kv, const float* U,
+                                  const float* clip, uint8_t* pool, const int32_t* page_table,
+                                  int32_t batch, int32_t max_pages, int32_t num_pages,
+                                  int32_t* dev_status, void* stream) {
+    return evict_impl(shape, n_tok, src_kv, src_rows, src_row, dst_seq, dst_pos, new_kv, U, clip, nullptr, pool,
+                      page_table, batch, max_pages, num_pages, dev_status, stream);
+}
+
+oscar_status oscar_evict_quantize_codebook(const oscar_shape* shape, int32_t n_tok, const void* src_kv,
+                                           int32_t src_rows, const int32_t* src_row, const int32_t* dst_seq,
+                                           const int32_t* dst_pos, const void* new_kv, const float* U,
+                                           const float* clip, const float* codebook, uint8_t* pool,
+                                           const int32_t* page_table, int32_t batch, int32_t max_pages,
+                                           int32_t num_pages, int32_t* dev_status, void* stream) {
+    if (!codebook || !aligned(codebook, 4)) return OSCAR_ERR_INVALID_ARG;
+    return evict_impl(shape, n_tok, src_kv, src_rows, src_row, dst_seq, dst_pos, new_kv, U, clip, codebook, pool,
+                      page_table, batch, max_pages, num_pages, dev_status, stream);
+}
+
+static oscar_status decode_impl(const oscar_shape* shape, int32_t batch, const void* q, const void* bf16_kv,
+                                const int32_t* bf16_len, const uint8_t* pool, const int32_t* page_table,
+                                int32_t max_pages, int32_t num_pages, const int32_t* hist_len, const float* U,
+                                const float* codebook, float sm_scale, float* out, void* workspace,
+                                size_t* ws_bytes, int32_t* dev_status, void* stream) {
     const oscar_status sst = check_shape(shape);
     if (sst != OSCAR_OK) return sst;
     if (batch < 0 || max_pages <= 0 || num_pages < 0 || !ws_bytes) return OSCAR_ERR_INVALID_ARG;
@@ -300,11 +321,34 @@ oscar_status oscar_decode_attn(const oscar_shape* shape, int32_t batch, const vo
     p.tail_pg = w.tail_pg;
     p.part_stride = w.part_stride;
     p.qscale = sm_scale * kLog2e;
+    p.codebook = codebook;
     cudaEvent_t ev0 = g_int2_ev_start, ev1 = g_int2_ev_stop;
     g_int2_ev_start = g_int2_ev_stop = nullptr;
     if (!ev0 || !ev1) ev0 = ev1 = nullptr;
     const cudaError_t e = launch_decode(p, static_cast<cudaStream_t>(stream), ev0, ev1);
     return e == cudaSuccess ? OSCAR_OK : cuda_fail(e);
+}
+
+oscar_status oscar_decode_attn(const oscar_shape* shape, int32_t batch, const void* q, const void* bf16_kv,
+                               const int32_t* bf16_len, const uint8_t* pool, const int32_t* page_table,
+                               int32_t max_pages, int32_t num_pages, const int32_t* hist_len, const float* U,
+                               float sm_scale, float* out, void* workspace, size_t* ws_bytes,
+                               int32_t* dev_status, void* stream) {
+    return decode_impl(shape, batch, q, bf16_kv, bf16_len, pool, page_table, max_pages, num_pages, hist_len, U,
+                       nullptr, sm_scale, out, workspace, ws_bytes, dev_status, stream);
+}
+
+oscar_status oscar_decode_attn_codebook(const oscar_shape* shape, int32_t batch, const void* q, const void* bf16_kv,
+                                        const int32_t* bf16_len, const uint8_t* pool, const int32_t* page_table,
+                                        int32_t max_pages, int32_t num_pages, const int32_t* hist_len,
+                                        const float* U, const float* codebook, float sm_scale, float* out,
+                                        void* workspace, size_t* ws_bytes, int32_t* dev_status, void* stream) {
+    const oscar_status sst = check_shape(shape);
+    if (sst != OSCAR_OK) return sst;
+    if (shape->num_q_heads / shape->num_kv_heads > 4) return OSCAR_ERR_UNSUPPORTED;
+    if (workspace && (!codebook || !aligned(codebook, 4))) return OSCAR_ERR_INVALID_ARG;
+    return decode_impl(shape, batch, q, bf16_kv, bf16_len, pool, page_table, max_pages, num_pages, hist_len, U,
+                       codebook, sm_scale, out, workspace, ws_bytes, dev_status, stream);
 }
 
 oscar_status oscar_calibrate_rotation(const oscar_shape* shape, int32_t n_q, const void* q, int32_t n_t,

@@ -313,7 +313,7 @@ constexpr int kPvRow = 72;  // floats per probability / V-scale row (64 + 8: con
 // token, and s~ in the P.V token order (pv_pos).
 template <bool FULL, int GS>
 __device__ __forceinline__ void page_scales_g(const uint8_t* blk, int valid, float4* ksS, float4* kzS, float4* vzS,
-                                              float* vsS) {
+                                              float* vsS, float kmul, float vmul) {
     constexpr int NG = 4 >> GS;  // (s, z) pairs per token vector
     const int lane = threadIdx.x & 31;
 #pragma unroll
@@ -340,7 +340,7 @@ __device__ __forceinline__ void page_scales_g(const uint8_t* blk, int valid, flo
             }
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
-                sv[b] = s_g[b >> GS] * (which ? v_scale_up(b) : k_scale_up(b));
+                sv[b] = s_g[b >> GS] * (which ? v_scale_up(b) * vmul : k_scale_up(b) * kmul);
                 zz[b] = z_g[b >> GS];
             }
         } else {
@@ -359,14 +359,46 @@ __device__ __forceinline__ void page_scales_g(const uint8_t* blk, int valid, flo
     }
 }
 
+// kmul / vmul multiply the K / V scales (the Lloyd-Max inner level a; 1 for
+// the uniform levels)
 template <bool FULL>
 __device__ __forceinline__ void page_scales(const uint8_t* blk, int valid, int gshift, float4* ksS, float4* kzS,
-                                            float4* vzS, float* vsS) {
+                                            float4* vzS, float* vsS, float kmul = 1.f, float vmul = 1.f) {
     switch (gshift) {  // warp-uniform, once per page
-        case 0: page_scales_g<FULL, 0>(blk, valid, ksS, kzS, vzS, vsS); break;
-        case 1: page_scales_g<FULL, 1>(blk, valid, ksS, kzS, vzS, vsS); break;
-        default: page_scales_g<FULL, 2>(blk, valid, ksS, kzS, vzS, vsS); break;
+        case 0: page_scales_g<FULL, 0>(blk, valid, ksS, kzS, vzS, vsS, kmul, vmul); break;
+        case 1: page_scales_g<FULL, 1>(blk, valid, ksS, kzS, vzS, vsS, kmul, vmul); break;
+        default: page_scales_g<FULL, 2>(blk, valid, ksS, kzS, vzS, vsS, kmul, vmul); break;
     }
+}
+
+// Lloyd-Max codebook of an item: levels {0, a, 3 - a, 3} in units of s above
+// z.  With c = b0 + 2 b1 the level is a c + (3 - 3a) b1, so a codebook
+// product is a times the code product plus (3 - 3a) / 2 times the product
+// of the high-bit plane (the plane's operand reads 2 b1 in the code's units).
+// The factor a goes into the scales, kappa = (3 - 3a) / (2a) weighs the
+// plane.  a <= 0 selects the uniform levels (kappa = 0).
+struct Codebook {
+    float ka, va, kk, vk;  // a and kappa for K and V
+};
+__device__ __forceinline__ Codebook codebook_of(const float* cb, int kv) {
+    float a[2];
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+        const float x = cb ? __ldg(cb + kv * 2 + w) : 0.f;
+        a[w] = x > 0.f ? x : 1.f;
+    }
+    return {a[0], a[1], (3.f - 3.f * a[0]) / (2.f * a[0]), (3.f - 3.f * a[1]) / (2.f * a[1])};
+}
+// high-bit plane of a code operand register (codes at bits P, P + 1 of each half)
+template <int SLOT>
+__device__ __forceinline__ uint32_t high_plane(uint32_t a) { return a & (0x00020002u << slot_bit(SLOT)); }
+template <int SLOT>
+__device__ __forceinline__ void high_planes(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t& c0,
+                                            uint32_t& c1, uint32_t& c2, uint32_t& c3) {
+    c0 = high_plane<SLOT>(a0);
+    c1 = high_plane<SLOT>(a1);
+    c2 = high_plane<SLOT>(a2);
+    c3 = high_plane<SLOT>(a3);
 }
 
 
@@ -375,11 +407,11 @@ __device__ __forceinline__ void page_scales(const uint8_t* blk, int valid, int g
 // products.  FULL (all 64 tokens valid, the common case) removes the
 // per-tile conditions of the logit phase so that the four tiles' work can
 // interleave.
-template <int NT, bool FULL>
+template <int NT, bool FULL, bool LM = false>
 __device__ __forceinline__ void attend_page(const uint8_t* blk, int valid, uint8_t* wbuf, const uint2* qfS,
                                             const float4 (&qsv)[NT], float (&m_run)[NT], float (&l_run)[NT],
                                             float (&zacc)[NT][4], float (&acc_o)[NT][8][4],
-                                            const SplitSel& take_lo, int gshift) {
+                                            const SplitSel& take_lo, int gshift, const Codebook& cbk = {}) {
     using SM = Int2Smem<NT>;
     const int lane = threadIdx.x & 31, gID = lane >> 2, tq = lane & 3;
     if (FULL) valid = kPage;
@@ -390,7 +422,8 @@ __device__ __forceinline__ void attend_page(const uint8_t* blk, int valid, uint8
     float* pS = reinterpret_cast<float*>(wbuf + SM::kWP);       // [G4][kPvRow] P at pv_pos
     const int ntile = FULL ? 4 : (valid + 15) >> 4;             // warp-uniform, 1..4
 
-    page_scales<FULL>(blk, valid, gshift, ksS, kzS, vzS, vsS);
+    if constexpr (LM) page_scales<FULL>(blk, valid, gshift, ksS, kzS, vzS, vsS, cbk.ka, cbk.va);
+    else page_scales<FULL>(blk, valid, gshift, ksS, kzS, vzS, vsS);
     __syncwarp();
 
     // -- logits of the page's tiles: A rows gID / gID+8 = tokens 16m+gID /
@@ -407,27 +440,44 @@ __device__ __forceinline__ void attend_page(const uint8_t* blk, int valid, uint8
             const uint32_t wa[2] = {x.x, x.y}, wb[2] = {y.x, y.y};
             const uint32_t wa8[2] = {wa[0] >> 8, wa[1] >> 8}, wb8[2] = {wb[0] >> 8, wb[1] >> 8};
             float acc[4][NT][4];
+            float acc1[LM ? 4 : 1][NT][4];   // high-bit plane (Lloyd-Max levels)
 #pragma unroll
             for (int g = 0; g < 4; ++g)
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) acc[g][nt][e] = 0.f;
+                    for (int e = 0; e < 4; ++e) {
+                        acc[g][nt][e] = 0.f;
+                        if (LM) acc1[LM ? g : 0][nt][e] = 0.f;
+                    }
 #pragma unroll
             for (int it = 0; it < 8; ++it) {
                 // half-major order: the four groups' accumulation chains interleave
                 const int h = it >> 2, g = it & 3, ks = 2 * g + h;
-                uint32_t a0, a1, a2, a3;
+                uint32_t a0, a1, a2, a3, c0 = 0, c1 = 0, c2 = 0, c3 = 0;
                 switch (g) {  // compile-time after unrolling
-                    case 0: k_operands<0>(wa[h], wb[h], wa8[h], wb8[h], a0, a1, a2, a3); break;
-                    case 1: k_operands<1>(wa[h], wb[h], wa8[h], wb8[h], a0, a1, a2, a3); break;
-                    case 2: k_operands<2>(wa[h], wb[h], wa8[h], wb8[h], a0, a1, a2, a3); break;
-                    default: k_operands<3>(wa[h], wb[h], wa8[h], wb8[h], a0, a1, a2, a3); break;
+                    case 0:
+                        k_operands<0>(wa[h], wb[h], wa8[h], wb8[h], a0, a1, a2, a3);
+                        if (LM) high_planes<0>(a0, a1, a2, a3, c0, c1, c2, c3);
+                        break;
+                    case 1:
+                        k_operands<1>(wa[h], wb[h], wa8[h], wb8[h], a0, a1, a2, a3);
+                        if (LM) high_planes<1>(a0, a1, a2, a3, c0, c1, c2, c3);
+                        break;
+                    case 2:
+                        k_operands<2>(wa[h], wb[h], wa8[h], wb8[h], a0, a1, a2, a3);
+                        if (LM) high_planes<2>(a0, a1, a2, a3, c0, c1, c2, c3);
+                        break;
+                    default:
+                        k_operands<3>(wa[h], wb[h], wa8[h], wb8[h], a0, a1, a2, a3);
+                        if (LM) high_planes<3>(a0, a1, a2, a3, c0, c1, c2, c3);
+                        break;
                 }
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     const uint2 qb = qfS[(nt * 8 + ks) * 32 + lane];
                     mma_bf16_16816(acc[g][nt], a0, a1, a2, a3, qb.x, qb.y);
+                    if (LM) mma_bf16_16816(acc1[LM ? g : 0][nt], c0, c1, c2, c3, qb.x, qb.y);
                 }
             }
             const float4 sA = ksS[ta], sB = ksS[ta + 8], zA = kzS[ta], zB = kzS[ta + 8];
@@ -440,9 +490,14 @@ __device__ __forceinline__ void attend_page(const uint8_t* blk, int valid, uint8
                 float xa = 0.f, xb = 0.f;
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
-                    xa = fmaf(sa[g], acc[g][nt][0] + acc[g][nt][1], xa);
+                    float da = acc[g][nt][0] + acc[g][nt][1], db = acc[g][nt][2] + acc[g][nt][3];
+                    if (LM) {
+                        da = fmaf(cbk.kk, acc1[LM ? g : 0][nt][0] + acc1[LM ? g : 0][nt][1], da);
+                        db = fmaf(cbk.kk, acc1[LM ? g : 0][nt][2] + acc1[LM ? g : 0][nt][3], db);
+                    }
+                    xa = fmaf(sa[g], da, xa);
                     xa = fmaf(za[g], qg[g], xa);
-                    xb = fmaf(sb[g], acc[g][nt][2] + acc[g][nt][3], xb);
+                    xb = fmaf(sb[g], db, xb);
                     xb = fmaf(zb[g], qg[g], xb);
                 }
                 la[m][nt] = va ? xa : -INFINITY;
@@ -513,26 +568,51 @@ __device__ __forceinline__ void attend_page(const uint8_t* blk, int valid, uint8
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
             const float4 sg = *reinterpret_cast<const float4*>(vsS + g * kPvRow + chunk);
-            uint32_t bb0[NT], bb1[NT];
+            uint32_t bb0[NT], bb1[NT], cc0[LM ? NT : 1], cc1[LM ? NT : 1];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                bb0[nt] = split_w_pair(make_float2(pp[nt].x, pp[nt].y), make_float2(sg.x, sg.y), take_lo);
-                bb1[nt] = split_w_pair(make_float2(pp[nt].z, pp[nt].w), make_float2(sg.z, sg.w), take_lo);
+                if constexpr (LM) {
+                    const float2 w0 = mul2(make_float2(pp[nt].x, pp[nt].y), make_float2(sg.x, sg.y));
+                    const float2 w1 = mul2(make_float2(pp[nt].z, pp[nt].w), make_float2(sg.z, sg.w));
+                    bb0[nt] = split_pair(w0, take_lo);
+                    bb1[nt] = split_pair(w1, take_lo);
+                    // the high-bit plane's weights kappa * W
+                    const float2 kv2 = make_float2(cbk.vk, cbk.vk);
+                    cc0[nt] = split_pair(mul2(w0, kv2), take_lo);
+                    cc1[nt] = split_pair(mul2(w1, kv2), take_lo);
+                } else {
+                    bb0[nt] = split_w_pair(make_float2(pp[nt].x, pp[nt].y), make_float2(sg.x, sg.y), take_lo);
+                    bb1[nt] = split_w_pair(make_float2(pp[nt].z, pp[nt].w), make_float2(sg.z, sg.w), take_lo);
+                }
             }
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 const uint32_t r0 = pw[2 * half], r1 = pw[2 * half + 1];
                 const uint32_t r08 = pw8[2 * half], r18 = pw8[2 * half + 1];
-                uint32_t a0, a1, a2, a3;
+                uint32_t a0, a1, a2, a3, c0 = 0, c1 = 0, c2 = 0, c3 = 0;
                 switch (g) {
-                    case 0: v_operands<0>(r0, r1, r08, r18, a0, a1, a2, a3); break;
-                    case 1: v_operands<1>(r0, r1, r08, r18, a0, a1, a2, a3); break;
-                    case 2: v_operands<2>(r0, r1, r08, r18, a0, a1, a2, a3); break;
-                    default: v_operands<3>(r0, r1, r08, r18, a0, a1, a2, a3); break;
+                    case 0:
+                        v_operands<0>(r0, r1, r08, r18, a0, a1, a2, a3);
+                        if (LM) high_planes<0>(a0, a1, a2, a3, c0, c1, c2, c3);
+                        break;
+                    case 1:
+                        v_operands<1>(r0, r1, r08, r18, a0, a1, a2, a3);
+                        if (LM) high_planes<1>(a0, a1, a2, a3, c0, c1, c2, c3);
+                        break;
+                    case 2:
+                        v_operands<2>(r0, r1, r08, r18, a0, a1, a2, a3);
+                        if (LM) high_planes<2>(a0, a1, a2, a3, c0, c1, c2, c3);
+                        break;
+                    default:
+                        v_operands<3>(r0, r1, r08, r18, a0, a1, a2, a3);
+                        if (LM) high_planes<3>(a0, a1, a2, a3, c0, c1, c2, c3);
+                        break;
                 }
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
+                for (int nt = 0; nt < NT; ++nt) {
                     mma_bf16_16816(acc_o[nt][2 * g + half], a0, a1, a2, a3, bb0[nt], bb1[nt]);
+                    if (LM) mma_bf16_16816(acc_o[nt][2 * g + half], c0, c1, c2, c3, cc0[LM ? nt : 0], cc1[LM ? nt : 0]);
+                }
             }
         }
     }
@@ -700,7 +780,7 @@ __device__ __forceinline__ void attend_page_g8(const uint8_t* blk, int valid, ui
     }
 }
 
-template <int NT>
+template <int NT, bool LM = false>
 __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(DecodeParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     using SM = Int2Smem<NT>;
@@ -825,6 +905,7 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
     uint2* qfS = reinterpret_cast<uint2*>(smem + SM::kQf);
     float4 qsv[NT];
     float m_run[NT], l_run[NT], zacc[NT][4], acc_o[NT][8][4];
+    Codebook cbk{1.f, 1.f, 0.f, 0.f};  // Lloyd-Max levels of the current item's KV head
 
     for (uint32_t n = warp;; n += kConsumerWarps) {
         const uint32_t s = n % kStages;
@@ -840,6 +921,7 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
 
         if (flags & kFlagFirst) {
             const int bk = sraw.y * p.hk + sraw.z;
+            if (LM) cbk = codebook_of(p.codebook, sraw.z);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 const uint32_t* fr = p.qfrag + ((size_t)bk * NT + nt) * 8 * 32 * 2;
@@ -868,9 +950,11 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
                     attend_page_g8<false>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o[0], p.gshift);
             } else {
                 if (valid == kPage)
-                    attend_page<NT, true>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o, take_lo, p.gshift);
+                    attend_page<NT, true, LM>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o, take_lo,
+                                              p.gshift, cbk);
                 else
-                    attend_page<NT, false>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o, take_lo, p.gshift);
+                    attend_page<NT, false, LM>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o, take_lo,
+                                               p.gshift, cbk);
             }
         }
         __syncwarp();
@@ -1439,7 +1523,7 @@ __global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(DecodeParams p)
 // ---------------------------------------------------------------------------
 struct Int2Attr {
     int sms = 0;
-    bool set1 = false, set2 = false, setm = false, setp = false, setb = false;
+    bool set1 = false, set2 = false, setl = false, setm = false, setp = false, setb = false;
 };
 
 static Int2Attr& attr_for_device(int dev) {
@@ -1447,11 +1531,11 @@ static Int2Attr& attr_for_device(int dev) {
     return attrs[dev & 63];
 }
 
-template <int NT>
+template <int NT, bool LM = false>
 static cudaError_t launch_int2(const DecodeParams& p, cudaStream_t st, int sms, bool& attr_set) {
     const int smem = Int2Smem<NT>::kBytes;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(int2_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaError_t e = cudaFuncSetAttribute(int2_kernel<NT, LM>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -1459,7 +1543,7 @@ static cudaError_t launch_int2(const DecodeParams& p, cudaStream_t st, int sms, 
     const int max_items = p.B * p.hk * ((p.max_pages + p.pps - 1) / p.pps + p.tail_pg / kShortItemPages);
     int blocks = min(per_sm * sms, max_items);
     if (blocks < 1) blocks = 1;
-    cudaError_t e = launch_pdl(int2_kernel<NT>, dim3(blocks), dim3(kInt2Threads), smem, st, p);
+    cudaError_t e = launch_pdl(int2_kernel<NT, LM>, dim3(blocks), dim3(kInt2Threads), smem, st, p);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -1499,7 +1583,10 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st, cudaEvent_t ev
     dim3 pg((p.B + kPrepSeqs - 1) / kPrepSeqs + 1, p.hk);
     if ((e = launch_pdl(prep_kernel, pg, dim3(kPrepThreads), kPrepSmem, st, p)) != cudaSuccess) return e;
     if (ev_int2_start && (e = cudaEventRecord(ev_int2_start, st)) != cudaSuccess) return e;
-    e = (p.NT == 1) ? launch_int2<1>(p, st, at.sms, at.set1) : launch_int2<2>(p, st, at.sms, at.set2);
+    if (p.codebook)  // Lloyd-Max levels (up to four query heads per KV head)
+        e = launch_int2<1, true>(p, st, at.sms, at.setl);
+    else
+        e = (p.NT == 1) ? launch_int2<1>(p, st, at.sms, at.set1) : launch_int2<2>(p, st, at.sms, at.set2);
     if (e != cudaSuccess) return e;
     if (ev_int2_stop && (e = cudaEventRecord(ev_int2_stop, st)) != cudaSuccess) return e;
     if (!at.setb) {

@@ -142,6 +142,7 @@ __global__ void __launch_bounds__(32 * kEvictWarps) evict_kernel(EvictParams p) 
     // pair's fp32 value, and the code decision u = (y_c - z) / s is evaluated
     // from the exact pair difference, so its error is below 4e-7 code units.
     const float cr = __ldg(p.clip + kv * 2 + which);
+    const float cb_a = p.codebook ? __ldg(p.codebook + kv * 2 + which) : 0.f;
     const float kc_hi = __uint_as_float(0x3db504f3u), kc_lo = __uint_as_float(0x30cfe77au);
     df yn[4];
     float amax[4];
@@ -222,7 +223,10 @@ __global__ void __launch_bounds__(32 * kEvictWarps) evict_kernel(EvictParams p) 
         if (sf != 0.f) {
             const df yz = df_add(yn[k], df{-zf, 0.f});
             const float u = __fdiv_rn(__fadd_rn(yz.hi, yz.lo), sf);
-            code = (int)fminf(fmaxf(rintf(u), 0.f), 3.f);
+            if (cb_a > 0.f)  // Lloyd-Max levels {0, a, 3 - a, 3}: the nearest one
+                code = (u >= 0.5f * cb_a) + (u >= 1.5f) + (u >= 3.f - 0.5f * cb_a);
+            else
+                code = (int)fminf(fmaxf(rintf(u), 0.f), 3.f);
         }
         byte |= (uint32_t)code << (2 * bitrev2(k));
     }

@@ -262,6 +262,7 @@ struct EvictParams {
     const __nv_bfloat16* new_kv;
     const float* U;
     const float* clip;
+    const float* codebook;   // [hk][2] inner level a of the Lloyd-Max codebook, or null (uniform levels)
     uint8_t* pool;
     const int32_t* page_table;
     int32_t* status;
@@ -300,6 +301,7 @@ struct DecodeParams {
     int gshift;    // log2(quant_group / 32)
     int block_bytes;
     float qscale;  // sm_scale * log2(e)
+    const float* codebook;  // [hk][2] Lloyd-Max inner level a, or null (uniform levels)
 };
 
 // Split-K geometry of one sequence with npg history pages: the last

@@ -70,6 +70,14 @@ def lib() -> ctypes.CDLL:
                                                 ctypes.c_int32, _P, _P, ctypes.c_float, _P, _P, _P]
         L.oscar_time_next_int2.restype = None
         L.oscar_time_next_int2.argtypes = [_P, _P]
+        L.oscar_evict_quantize_codebook.restype = ctypes.c_int
+        L.oscar_evict_quantize_codebook.argtypes = [S, ctypes.c_int32, _P, ctypes.c_int32, _P, _P, _P, _P, _P, _P,
+                                                    _P, _P, _P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P,
+                                                    _P]
+        L.oscar_decode_attn_codebook.restype = ctypes.c_int
+        L.oscar_decode_attn_codebook.argtypes = [S, ctypes.c_int32, _P, _P, _P, _P, _P, ctypes.c_int32,
+                                                 ctypes.c_int32, _P, _P, _P, ctypes.c_float, _P, _P,
+                                                 ctypes.POINTER(ctypes.c_size_t), _P, _P]
         L.oscar_calibrate_clip.restype = ctypes.c_int
         L.oscar_calibrate_clip.argtypes = [S, ctypes.c_int32, _P, _P, _P, ctypes.c_int32, _P, _P, _P,
                                            ctypes.POINTER(ctypes.c_size_t), _P]
@@ -257,3 +265,40 @@ def oscar_calibrate_clip(shape: oscar_shape, kv, U, grid, clip, workspace=None, 
         _dptr(mse, "mse", torch.float32), _dptr(workspace, "workspace", torch.uint8), ctypes.byref(ws),
         _stream_ptr(stream))
     _check("oscar_calibrate_clip", st)
+
+
+def oscar_evict_quantize_codebook(shape: oscar_shape, src_kv, dst_seq, dst_pos, U, clip, codebook, pool, page_table,
+                                  batch: int, max_pages: int, num_pages: int, src_row=None, new_kv=None,
+                                  dev_status=None, stream=None) -> None:
+    """oscar_evict_quantize with the Lloyd-Max levels {0, a, 3 - a, 3}
+    (codebook: fp32 [Hk][2] inner levels a); see include/oscar.h."""
+    import torch
+    n_tok = int(dst_seq.numel())
+    st = lib().oscar_evict_quantize_codebook(
+        ctypes.byref(shape), n_tok, _dptr(src_kv, "src_kv", torch.bfloat16), int(src_kv.shape[0]),
+        _dptr(src_row, "src_row", torch.int32), _dptr(dst_seq, "dst_seq", torch.int32),
+        _dptr(dst_pos, "dst_pos", torch.int32), _dptr(new_kv, "new_kv", torch.bfloat16),
+        _dptr(U, "U", torch.float32), _dptr(clip, "clip", torch.float32),
+        _dptr(codebook, "codebook", torch.float32), _dptr(pool, "pool", torch.uint8),
+        _dptr(page_table, "page_table", torch.int32), batch, max_pages, num_pages,
+        _dptr(dev_status, "dev_status", torch.int32), _stream_ptr(stream))
+    _check("oscar_evict_quantize_codebook", st)
+
+
+def oscar_decode_attn_codebook(shape: oscar_shape, q, bf16_kv, bf16_len, pool, page_table, max_pages: int,
+                               num_pages: int, hist_len, U, codebook, sm_scale: float, out, workspace,
+                               dev_status=None, stream=None) -> None:
+    """oscar_decode_attn reading the history with the Lloyd-Max levels
+    (codebook: fp32 [Hk][2]); G <= 4.  The workspace size is
+    oscar_decode_workspace_bytes's."""
+    import torch
+    B = int(q.shape[0])
+    ws = ctypes.c_size_t(int(workspace.numel()))
+    st = lib().oscar_decode_attn_codebook(
+        ctypes.byref(shape), B, _dptr(q, "q", torch.bfloat16), _dptr(bf16_kv, "bf16_kv", torch.bfloat16),
+        _dptr(bf16_len, "bf16_len", torch.int32), _dptr(pool, "pool", torch.uint8),
+        _dptr(page_table, "page_table", torch.int32), max_pages, num_pages, _dptr(hist_len, "hist_len", torch.int32),
+        _dptr(U, "U", torch.float32), _dptr(codebook, "codebook", torch.float32), ctypes.c_float(sm_scale),
+        _dptr(out, "out", torch.float32), _dptr(workspace, "workspace", torch.uint8), ctypes.byref(ws),
+        _dptr(dev_status, "dev_status", torch.int32), _stream_ptr(stream))
+    _check("oscar_decode_attn_codebook", st)

@@ -250,6 +250,40 @@ oscar_status oscar_decode_attn_noalloc(const oscar_shape* shape, int32_t batch, 
                                        void* stream);
 
 /*
+ * Lloyd-Max codebook variant ([NEWS] sec. E: OSCAR's code repository pairs
+ * the rotation with a Lloyd-Max codebook; the pages give no format).
+ * Reading: the stored format is unchanged (codes, fp16 scale s and zero z
+ * per group, z = clipped minimum, s = range / 3) and only the four levels
+ * move: in units of s above z they are {0, a, 3 - a, 3} instead of
+ * {0, 1, 2, 3}, with one inner level a per (KV head, K/V), fixed offline
+ * (oscar_calibrate_codebook).  A code is the nearest level to
+ * u = (y_clipped - z) / s (u reaching a threshold a/2, 3/2 or 3 - a/2 moves
+ * it up); a value dequantises to z + s * level[code].  a = 1 gives the
+ * uniform levels; a <= 0 is read as 1.
+ *
+ *   codebook (device) fp32 [Hk][2] the inner levels a (K, V of each KV head)
+ *
+ * oscar_evict_quantize_codebook: oscar_evict_quantize with the codebook's
+ *   nearest-level codes.
+ * oscar_decode_attn_codebook: oscar_decode_attn reading the history with
+ *   the codebook's levels; query groups G = Hq/Hk of at most 4
+ *   (OSCAR_ERR_UNSUPPORTED otherwise).  About 1.5x the INT2 arithmetic of
+ *   the uniform levels: one more tensor-core product on the codes' high-bit
+ *   plane for K and for V.
+ */
+oscar_status oscar_evict_quantize_codebook(const oscar_shape* shape, int32_t n_tok, const void* src_kv,
+                                           int32_t src_rows, const int32_t* src_row, const int32_t* dst_seq,
+                                           const int32_t* dst_pos, const void* new_kv, const float* U,
+                                           const float* clip, const float* codebook, uint8_t* pool,
+                                           const int32_t* page_table, int32_t batch, int32_t max_pages,
+                                           int32_t num_pages, int32_t* dev_status, void* stream);
+oscar_status oscar_decode_attn_codebook(const oscar_shape* shape, int32_t batch, const void* q, const void* bf16_kv,
+                                        const int32_t* bf16_len, const uint8_t* pool, const int32_t* page_table,
+                                        int32_t max_pages, int32_t num_pages, const int32_t* hist_len,
+                                        const float* U, const float* codebook, float sm_scale, float* out,
+                                        void* workspace, size_t* ws_bytes, int32_t* dev_status, void* stream);
+
+/*
  * oscar_calibrate_rotation -- offline calibration of U ([NEWS] sec. B: U is
  * fixed offline per layer and KV head, for K from the covariance of the
  * queries that read the keys, for V from the covariance of the values as
