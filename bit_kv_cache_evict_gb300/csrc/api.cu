@@ -390,6 +390,36 @@ oscar_status oscar_calibrate_rotation(const oscar_shape* shape, int32_t n_q, con
     return e == cudaSuccess ? OSCAR_OK : cuda_fail(e);
 }
 
+oscar_status oscar_calibrate_codebook(const oscar_shape* shape, int32_t n_t, const void* kv, const float* U,
+                                      const float* clip, float* codebook, void* workspace, size_t* ws_bytes,
+                                      void* stream) {
+    const oscar_status sst = check_shape(shape);
+    if (sst != OSCAR_OK) return sst;
+    if (n_t < 1 || !ws_bytes) return OSCAR_ERR_INVALID_ARG;
+    const int hk = shape->num_kv_heads;
+    if ((double)n_t * hk * 2 * kD > 1.0e9) return OSCAR_ERR_INVALID_ARG;
+    const size_t total = round_up((size_t)hk * 2 * n_t * kD * 4, 256);
+    if (!workspace) {
+        *ws_bytes = total;
+        return OSCAR_OK;
+    }
+    if (*ws_bytes < total) return OSCAR_ERR_WORKSPACE;
+    if (!kv || !U || !clip || !codebook) return OSCAR_ERR_INVALID_ARG;
+    if (!aligned(kv, 16) || !aligned(U, 16) || !aligned(clip, 4) || !aligned(codebook, 4) || !aligned(workspace, 16))
+        return OSCAR_ERR_INVALID_ARG;
+    FitParams p{};
+    p.kv = static_cast<const __nv_bfloat16*>(kv);
+    p.U = U;
+    p.clip = clip;
+    p.v = static_cast<float*>(workspace);
+    p.a = codebook;
+    p.n_t = n_t;
+    p.hk = hk;
+    p.gshift = gshift_of(shape);
+    const cudaError_t e = launch_calibrate_codebook(p, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? OSCAR_OK : cuda_fail(e);
+}
+
 oscar_status oscar_calibrate_clip(const oscar_shape* shape, int32_t n_t, const void* kv, const float* U,
                                   const float* grid, int32_t n_grid, float* clip, float* mse, void* workspace,
                                   size_t* ws_bytes, void* stream) {

@@ -456,8 +456,176 @@ __global__ void calib_clip_pick_kernel(ClipParams p) {
 }
 
 // ---------------------------------------------------------------------------
+// Lloyd-Max codebook fit
+// ---------------------------------------------------------------------------
+// Folded code coordinates of the calibration tokens: for every element, u =
+// (y_c - z) / s under the eviction's quantiser with the matrix's clip ratio
+// (rotation in fp32 as in the clip search), folded to v = min(u, 3 - u)
+// clamped to [0, 3/2] (the codebook is symmetric); groups with s = 0 give
+// no samples (v = -1, skipped by the fit).
+__global__ void __launch_bounds__(32 * kClipWarps) calib_fold_kernel(FitParams p) {
+    extern __shared__ __align__(16) float fsm[];
+    float* Us = fsm;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int mat = blockIdx.y;
+    const float* Ug = p.U + (size_t)mat * kD * kD;
+    for (int i = threadIdx.x; i < kD * kD / 4; i += 32 * kClipWarps)
+        reinterpret_cast<float4*>(Us)[i] = reinterpret_cast<const float4*>(Ug)[i];
+    __syncthreads();
+    const float cr = p.clip[mat];
+    const int gshift = p.gshift;
+    const int t_end = min(p.n_t, (blockIdx.x + 1) * kClipTokens);
+    for (int t = blockIdx.x * kClipTokens + warp; t < t_end; t += kClipWarps) {
+        const uint2 xr = *reinterpret_cast<const uint2*>(p.kv + ((size_t)t * p.hk * 2 + mat) * kD + 4 * lane);
+        const float x[4] = {bf16_lo(xr.x), bf16_hi(xr.x), bf16_lo(xr.y), bf16_hi(xr.y)};
+        float y[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int a = 0; a < kD; ++a) {
+            const float xa = __shfl_sync(kFull, x[a & 3], a >> 2);
+            const float4 u = *reinterpret_cast<const float4*>(Us + a * kD + 4 * lane);
+            y[0] = fmaf(xa, u.x, y[0]);
+            y[1] = fmaf(xa, u.y, y[1]);
+            y[2] = fmaf(xa, u.z, y[2]);
+            y[3] = fmaf(xa, u.w, y[3]);
+        }
+        {
+            const float t0 = y[0] + y[1], t1 = y[0] - y[1], t2 = y[2] + y[3], t3 = y[2] - y[3];
+            y[0] = t0 + t2;
+            y[2] = t0 - t2;
+            y[1] = t1 + t3;
+            y[3] = t1 - t3;
+        }
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1) {
+            const bool upper = (lane & m) != 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float o = __shfl_xor_sync(kFull, y[k], m);
+                y[k] = upper ? o - y[k] : y[k] + o;
+            }
+        }
+        float amax[4], lo[4], hi[4], yc[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            y[k] *= (float)kInvSqrtD;
+            amax[k] = fabsf(y[k]);
+        }
+#pragma unroll
+        for (int m = 16; m > 0; m >>= 1)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) amax[k] = fmaxf(amax[k], __shfl_xor_sync(kFull, amax[k], m));
+        if (gshift >= 1) {
+            amax[0] = amax[2] = fmaxf(amax[0], amax[2]);
+            amax[1] = amax[3] = fmaxf(amax[1], amax[3]);
+        }
+        if (gshift >= 2) amax[0] = amax[1] = amax[2] = amax[3] = fmaxf(amax[0], amax[1]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float tt = cr * amax[k];
+            yc[k] = cr < 1.f ? fminf(fmaxf(y[k], -tt), tt) : y[k];
+            lo[k] = hi[k] = yc[k];
+        }
+#pragma unroll
+        for (int m = 16; m > 0; m >>= 1)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                lo[k] = fminf(lo[k], __shfl_xor_sync(kFull, lo[k], m));
+                hi[k] = fmaxf(hi[k], __shfl_xor_sync(kFull, hi[k], m));
+            }
+        if (gshift >= 1) {
+            lo[0] = lo[2] = fminf(lo[0], lo[2]);
+            lo[1] = lo[3] = fminf(lo[1], lo[3]);
+            hi[0] = hi[2] = fmaxf(hi[0], hi[2]);
+            hi[1] = hi[3] = fmaxf(hi[1], hi[3]);
+        }
+        if (gshift >= 2) {
+            lo[0] = lo[1] = lo[2] = lo[3] = fminf(lo[0], lo[1]);
+            hi[0] = hi[1] = hi[2] = hi[3] = fmaxf(hi[0], hi[1]);
+        }
+        float v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float sf = __half2float(__float2half_rn((hi[k] - lo[k]) / 3.f));
+            const float zf = __half2float(__float2half_rn(lo[k]));
+            if (sf == 0.f) {
+                v[k] = -1.f;
+            } else {
+                const float u = (yc[k] - zf) / sf;
+                v[k] = fminf(fmaxf(fminf(u, 3.f - u), 0.f), 1.5f);
+            }
+        }
+        *reinterpret_cast<float4*>(p.v + ((size_t)mat * p.n_t + t) * kD + 4 * lane) = make_float4(v[0], v[1], v[2], v[3]);
+    }
+}
+
+// One block per matrix: Lloyd's iteration a <- mean{v : v >= a/2} from a = 1
+// until a moves by less than 1e-6 (at most kFitIters rounds).
+constexpr int kFitThreads = 512, kFitIters = 200;
+__global__ void __launch_bounds__(kFitThreads) calib_lloyd_kernel(FitParams p) {
+    __shared__ float rs[kFitThreads / 32], rc[kFitThreads / 32];
+    __shared__ float a_sh;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, mat = blockIdx.x;
+    const float* v = p.v + (size_t)mat * p.n_t * kD;
+    const size_t n = (size_t)p.n_t * kD;
+    float a = 1.f;
+    for (int it = 0; it < kFitIters; ++it) {
+        const float th = 0.5f * a;
+        float sum = 0.f, cnt = 0.f;
+        for (size_t i = tid; i < n; i += kFitThreads) {
+            const float x = v[i];
+            if (x >= th) {
+                sum += x;
+                cnt += 1.f;
+            }
+        }
+#pragma unroll
+        for (int m = 16; m > 0; m >>= 1) {
+            sum += __shfl_xor_sync(kFull, sum, m);
+            cnt += __shfl_xor_sync(kFull, cnt, m);
+        }
+        if (lane == 0) {
+            rs[warp] = sum;
+            rc[warp] = cnt;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            float S = 0.f, C = 0.f;
+            for (int w = 0; w < kFitThreads / 32; ++w) {
+                S += rs[w];
+                C += rc[w];
+            }
+            a_sh = C > 0.f ? S / C : a;
+        }
+        __syncthreads();
+        const float a_new = a_sh;
+        __syncthreads();
+        const bool done = fabsf(a_new - a) < 1e-6f;
+        a = a_new;
+        if (done) break;
+    }
+    if (tid == 0) p.a[mat] = a;
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
+cudaError_t launch_calibrate_codebook(const FitParams& p, cudaStream_t st) {
+    const int smem = kD * kD * 4;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static bool attr_set[64] = {};
+    if (!attr_set[dev & 63]) {
+        e = cudaFuncSetAttribute(calib_fold_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        attr_set[dev & 63] = true;
+    }
+    dim3 grid((p.n_t + kClipTokens - 1) / kClipTokens, p.hk * 2);
+    calib_fold_kernel<<<grid, 32 * kClipWarps, smem, st>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    calib_lloyd_kernel<<<p.hk * 2, kFitThreads, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_calibrate_clip(const ClipParams& p, cudaStream_t st) {
     cudaError_t e = cudaMemsetAsync(p.err, 0, (size_t)p.hk * 2 * kMaxClipGrid * sizeof(double), st);
     if (e != cudaSuccess) return e;

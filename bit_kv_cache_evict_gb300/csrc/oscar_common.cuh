@@ -345,6 +345,16 @@ struct ClipParams {
 };
 cudaError_t launch_calibrate_clip(const ClipParams& p, cudaStream_t st);
 
+struct FitParams {
+    const __nv_bfloat16* kv;   // [n_t][hk][2][kD] calibration tokens
+    const float* U;            // [hk][2][kD][kD]
+    const float* clip;         // [hk][2]
+    float* v;                  // [hk * 2][n_t][kD] folded code coordinates (scratch)
+    float* a;                  // [hk][2] out: the inner level of each codebook
+    int n_t, hk, gshift;
+};
+cudaError_t launch_calibrate_codebook(const FitParams& p, cudaStream_t st);
+
 cudaError_t launch_evict(const EvictParams& p, cudaStream_t st);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st, cudaEvent_t ev_int2_start,
                           cudaEvent_t ev_int2_stop);

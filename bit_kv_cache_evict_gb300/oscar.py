@@ -78,6 +78,9 @@ def lib() -> ctypes.CDLL:
         L.oscar_decode_attn_codebook.argtypes = [S, ctypes.c_int32, _P, _P, _P, _P, _P, ctypes.c_int32,
                                                  ctypes.c_int32, _P, _P, _P, ctypes.c_float, _P, _P,
                                                  ctypes.POINTER(ctypes.c_size_t), _P, _P]
+        L.oscar_calibrate_codebook.restype = ctypes.c_int
+        L.oscar_calibrate_codebook.argtypes = [S, ctypes.c_int32, _P, _P, _P, _P, _P, ctypes.POINTER(ctypes.c_size_t),
+                                               _P]
         L.oscar_calibrate_clip.restype = ctypes.c_int
         L.oscar_calibrate_clip.argtypes = [S, ctypes.c_int32, _P, _P, _P, ctypes.c_int32, _P, _P, _P,
                                            ctypes.POINTER(ctypes.c_size_t), _P]
@@ -302,3 +305,22 @@ def oscar_decode_attn_codebook(shape: oscar_shape, q, bf16_kv, bf16_len, pool, p
         _dptr(out, "out", torch.float32), _dptr(workspace, "workspace", torch.uint8), ctypes.byref(ws),
         _dptr(dev_status, "dev_status", torch.int32), _stream_ptr(stream))
     _check("oscar_decode_attn_codebook", st)
+
+
+def oscar_calibrate_codebook(shape: oscar_shape, kv, U, clip, codebook, workspace=None, stream=None) -> None:
+    """Lloyd-Max fit of the codebook inner levels a [Hk][2] (fp32 CUDA tensor,
+    out) from calibration tokens kv [n_t][Hk][2][d]; see include/oscar.h."""
+    import torch
+    n_t = int(kv.shape[0])
+    if workspace is None:
+        need = ctypes.c_size_t(0)
+        st = lib().oscar_calibrate_codebook(ctypes.byref(shape), n_t, None, None, None, None, None,
+                                            ctypes.byref(need), None)
+        _check("oscar_calibrate_codebook", st)
+        workspace = torch.zeros(int(need.value), dtype=torch.uint8, device=kv.device)
+    ws = ctypes.c_size_t(int(workspace.numel()))
+    st = lib().oscar_calibrate_codebook(
+        ctypes.byref(shape), n_t, _dptr(kv, "kv", torch.bfloat16), _dptr(U, "U", torch.float32),
+        _dptr(clip, "clip", torch.float32), _dptr(codebook, "codebook", torch.float32),
+        _dptr(workspace, "workspace", torch.uint8), ctypes.byref(ws), _stream_ptr(stream))
+    _check("oscar_calibrate_codebook", st)

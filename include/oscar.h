@@ -284,6 +284,22 @@ oscar_status oscar_decode_attn_codebook(const oscar_shape* shape, int32_t batch,
                                         void* workspace, size_t* ws_bytes, int32_t* dev_status, void* stream);
 
 /*
+ * oscar_calibrate_codebook -- offline Lloyd-Max fit of the inner level a of
+ * each (KV head, K/V) codebook from calibration tokens: every element's
+ * u = (y_clipped - z) / s under the eviction's quantiser (given U and clip,
+ * rotation in fp32), folded by the symmetry to v = min(u, 3 - u) in
+ * [0, 3/2]; Lloyd's iteration a <- mean{v : v >= a/2} from a = 1 until a
+ * moves by less than 1e-6 (at most 200 rounds).  Groups with s = 0 give no
+ * samples.
+ *   kv (device) bf16 [n_t][Hk][2][d]; U fp32 [Hk][2][d][d]; clip fp32 [Hk][2]
+ *   codebook (device) fp32 [Hk][2] out; workspace as oscar_decode_attn
+ *   (workspace == NULL returns the size: 4 * Hk * 2 * n_t * d bytes).
+ */
+oscar_status oscar_calibrate_codebook(const oscar_shape* shape, int32_t n_t, const void* kv, const float* U,
+                                      const float* clip, float* codebook, void* workspace, size_t* ws_bytes,
+                                      void* stream);
+
+/*
  * oscar_calibrate_rotation -- offline calibration of U ([NEWS] sec. B: U is
  * fixed offline per layer and KV head, for K from the covariance of the
  * queries that read the keys, for V from the covariance of the values as

@@ -122,3 +122,24 @@ def decode(q_bits, bf16_kv_bits, bf16_len, pool, table, hist_len, U, R_of, a, sm
                 p = np.exp(lg - lg.max())
                 out[b, hh] = p @ Vc / p.sum()
     return out
+
+
+def fit_from_tokens(kv: np.ndarray, U: np.ndarray, clip: np.ndarray, group: int = 32) -> np.ndarray:
+    """a [Hk][2] fitted on calibration tokens kv (float64 [n_t][Hk][2][d]):
+    the u of every element of the groups whose stored s is non-zero, from
+    the C oracle's quantiser (rotation y = x . R in float64), folded and
+    passed to fit_a."""
+    from oracle import get
+    orc = get()
+    n_t, hk, _, d = kv.shape
+    out = np.zeros((hk, 2))
+    for h in range(hk):
+        for w in range(2):
+            R = orc.build_R(U[h, w])
+            samples = []
+            for x in kv[:, h, w, :]:
+                codes, s16, z16, u = orc.quantize_vec(x @ R, group, float(clip[h, w]))[:4]
+                keep = np.repeat(s16 != 0, group)
+                samples.append(u[keep])
+            out[h, w] = fit_a(np.concatenate(samples))
+    return out

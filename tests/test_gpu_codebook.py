@@ -140,3 +140,24 @@ def test_codebook_one_is_the_uniform_path():
         torch.cuda.synchronize()
         outs.append(out.cpu().numpy().astype(np.float64))
     assert np.abs(outs[0] - outs[1]).max() <= 1e-5 * max(1.0, np.abs(outs[0]).max())
+
+
+@pytest.mark.parametrize("g", [32, 128])
+def test_codebook_fit_matches_oracle(g):
+    """The Lloyd-Max fit of a on calibration tokens (fp32 rotation on the
+    GPU, float64 in the oracle) agrees within 1e-4."""
+    hk, n_t = 2, 400
+    w = S.Workload(47, "fit", batch=1, hq=4 * hk, hk=hk)
+    rng = S.rng_for(w, 5)
+    kvb = S.kv_tokens(w, n_t, rng, S.channel_profile(w))
+    U = S.rotation_U(w).astype(np.float32)
+    clip = S.clip_ratios(w)
+    sh = O.oscar_shape(128, g, 64, 256, 64, 4 * hk, hk)
+    a_t = torch.zeros((hk, 2), dtype=torch.float32, device="cuda")
+    O.oscar_calibrate_codebook(sh, H.bf16_t(kvb), H.f32_t(U), H.f32_t(clip), a_t)
+    torch.cuda.synchronize()
+    a_ref = L.fit_from_tokens(S.bf16_to_f32(kvb).astype(np.float64), U.astype(np.float64), clip, g)
+    a_g = a_t.cpu().numpy().astype(np.float64)
+    print(f"codebook fit g={g}: gpu {a_g.ravel()} oracle {a_ref.ravel()}")
+    assert np.abs(a_g - a_ref).max() <= 1e-4, (a_g, a_ref)
+    assert np.all(a_ref > 0.3) and np.all(a_ref < 1.5)
