@@ -92,6 +92,9 @@ def parse_args():
     ap.add_argument("--calibrate", action="store_true",
                     help="time the offline rotation calibration (oscar_calibrate_rotation) instead of a decode "
                          "step: one JSON line, the float64 oracle timed on the same inputs")
+    ap.add_argument("--codebook", type=float, default=None, metavar="A",
+                    help="Lloyd-Max levels {0, A, 3-A, 3} for every head (up to four query heads per KV head) "
+                         "instead of the uniform grid")
     ap.add_argument("--quant-group", type=int, default=32, choices=[32, 64, 128],
                     help="stored positions per fp16 scale/zero pair (32 is the configured format)")
     return ap.parse_args()
@@ -229,7 +232,8 @@ def load_peaks() -> dict:
 class GpuState:
     """Pools, BF16 segments, queries and per-step metadata for every layer."""
 
-    def __init__(self, w: S.Workload, layers: int, steps_total: int, rank: int, quant_group: int = 32):
+    def __init__(self, w: S.Workload, layers: int, steps_total: int, rank: int, quant_group: int = 32,
+                 codebook: float | None = None):
         import torch
         from bit_kv_cache_evict_gb300 import oscar as O
         self.O, self.torch = O, torch
@@ -266,6 +270,9 @@ class GpuState:
         self.sm_scale = 1.0 / math.sqrt(d)
         self.ws = torch.empty(O.oscar_decode_workspace_bytes(self.shape, B, self.max_pages), dtype=torch.uint8,
                               device=dev)
+        # Lloyd-Max levels {0, a, 3 - a, 3} with one a for every head (None: uniform levels)
+        self.cb = None if codebook is None else torch.full((Hk, 2), float(codebook), dtype=torch.float32,
+                                                           device=dev)
         self.layers = []
         gen = torch.Generator(device=dev)
         for layer in range(layers):
@@ -303,20 +310,37 @@ class GpuState:
         for i in range(0, seq.size, chunk):
             n = min(chunk, seq.size - i)
             toks = S.kv_tokens_torch(self.w, n, gen, prof, self.dev).contiguous()
-            self.O.oscar_evict_quantize(self.shape, toks, torch.from_numpy(seq[i:i + n]).to(self.dev),
-                                        torch.from_numpy(pos[i:i + n]).to(self.dev), U, clip, pool, self.table,
-                                        self.B, self.max_pages, self.num_pages)
+            sq = torch.from_numpy(seq[i:i + n]).to(self.dev)
+            ps = torch.from_numpy(pos[i:i + n]).to(self.dev)
+            if self.cb is None:
+                self.O.oscar_evict_quantize(self.shape, toks, sq, ps, U, clip, pool, self.table, self.B,
+                                            self.max_pages, self.num_pages)
+            else:
+                self.O.oscar_evict_quantize_codebook(self.shape, toks, sq, ps, U, clip, self.cb, pool, self.table,
+                                                     self.B, self.max_pages, self.num_pages)
 
     def layer_step(self, layer: int, s: int, int2_events=None):
         O = self.O
         st = self.layers[layer]
-        O.oscar_evict_quantize(self.shape, st["kv"].view(self.B * S.NSLOT, self.Hk, 2, S.D), self.seqs,
-                               self.hist_before[s], st["U"], st["clip"], st["pool"], self.table, self.B,
-                               self.max_pages, self.num_pages, src_row=self.src_row[s], new_kv=st["new_kv"])
+        flat = st["kv"].view(self.B * S.NSLOT, self.Hk, 2, S.D)
+        if self.cb is None:
+            O.oscar_evict_quantize(self.shape, flat, self.seqs, self.hist_before[s], st["U"], st["clip"], st["pool"],
+                                   self.table, self.B, self.max_pages, self.num_pages, src_row=self.src_row[s],
+                                   new_kv=st["new_kv"])
+        else:
+            O.oscar_evict_quantize_codebook(self.shape, flat, self.seqs, self.hist_before[s], st["U"], st["clip"],
+                                            self.cb, st["pool"], self.table, self.B, self.max_pages, self.num_pages,
+                                            src_row=self.src_row[s], new_kv=st["new_kv"])
         if int2_events is not None:
             O.oscar_time_next_int2(*int2_events)
-        O.oscar_decode_attn(self.shape, st["q"], st["kv"], self.bf16_len, st["pool"], self.table, self.max_pages,
-                            self.num_pages, self.hist_after[s], st["U"], self.sm_scale, st["out"], self.ws)
+        if self.cb is None:
+            O.oscar_decode_attn(self.shape, st["q"], st["kv"], self.bf16_len, st["pool"], self.table,
+                                self.max_pages, self.num_pages, self.hist_after[s], st["U"], self.sm_scale,
+                                st["out"], self.ws)
+        else:
+            O.oscar_decode_attn_codebook(self.shape, st["q"], st["kv"], self.bf16_len, st["pool"], self.table,
+                                         self.max_pages, self.num_pages, self.hist_after[s], st["U"], self.cb,
+                                         self.sm_scale, st["out"], self.ws)
 
     # algorithmic bytes (per layer) of the step with index s
     def hist_tokens_after(self, s: int) -> int:
@@ -451,7 +475,7 @@ def run_reference(args, rank: int, world: int) -> None:
     print(json.dumps(line), flush=True)
 
 
-def config_of(w: S.Workload, layers: int, quant_group: int = 32) -> dict:
+def config_of(w: S.Workload, layers: int, quant_group: int = 32, codebook: float | None = None) -> dict:
     ctx = {"fixed": f"{w.ctx_lo}", "uniform": f"uniform[{w.ctx_lo},{w.ctx_hi}]",
            "loguniform": f"loguniform[{w.ctx_lo},{w.ctx_hi}]"}[w.ctx_kind]
     cfg = {"workload": w.name, "batch_per_gpu": w.batch, "layers": layers, "q_heads": w.hq, "kv_heads": w.hk,
@@ -459,6 +483,8 @@ def config_of(w: S.Workload, layers: int, quant_group: int = 32) -> dict:
            "page": S.PAGE, "page_table": "shuffled" if w.shuffled else "contiguous",
            "kv_values": w.dist, "l2": "inputs larger than L2 (a distinct pool per layer)",
            "parallelism": "replicas (independent sequences per GPU)"}
+    if codebook is not None:
+        cfg["levels"] = f"Lloyd-Max {{0, {codebook:g}, {3 - codebook:g}, 3}}"
     if w.prefix_seqs:
         cfg["prefix_sharing"] = f"{w.prefix_seqs} sequences share a {w.prefix_tokens}-token prefix"
     return cfg
@@ -477,7 +503,7 @@ def run_oscar(args, rank: int, world: int, local: int) -> None:
     e2e_steps = 0 if args.no_e2e else K
     total_steps = W + K + e2e_steps
     t0 = time.time()
-    st = GpuState(w, L, total_steps, rank, args.quant_group)
+    st = GpuState(w, L, total_steps, rank, args.quant_group, args.codebook)
     setup_s = time.time() - t0
     stream = torch.cuda.current_stream()
 
@@ -598,7 +624,7 @@ def run_oscar(args, rank: int, world: int, local: int) -> None:
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
             "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "int2 codes x bf16 hi/lo on tensor cores, fp32 accumulate", "data": "synthetic",
-            "config": config_of(w, L, args.quant_group),
+            "config": config_of(w, L, args.quant_group, args.codebook),
             "decode_tokens_per_s": world * w.batch * K / (t_ms_max / 1e3),
             "bits_per_element": st.bits_per_element(W + K - 1),
             "step_algorithmic_gbs": step_bytes / (ms_per_step * 1e-3) / 1e9,

@@ -258,6 +258,8 @@ struct Int2Smem {
     // (all four are inside the same item between two item-end merges)
     static constexpr int kQf = kWarp + kConsumerWarps * kWarpBytes;       // [NT][8][32] uint2
     static constexpr int kBytes = kQf + NT * 8 * 32 * 8;
+    // Lloyd-Max levels: kappa q' fragments of the high-bit plane follow q'
+    static constexpr int kBytesLM = kBytes + NT * 8 * 32 * 8;
 };
 
 __device__ __forceinline__ int find_seq(const int32_t* item_start, int B, int item) {
@@ -402,6 +404,24 @@ __device__ __forceinline__ void high_planes(uint32_t a0, uint32_t a1, uint32_t a
 }
 
 
+// B fragment of kappa q' from one of q': column n of a head's column pair
+// holds its hi (n even) or lo (n odd) part, the partner column sits in lane
+// ^ 4.  q' = hi + lo is rebuilt, scaled and split again.
+__device__ __forceinline__ uint2 scaled_fragment(uint2 f, float kappa, int is_lo) {
+    const uint32_t ox = __shfl_xor_sync(kFull, f.x, 4), oy = __shfl_xor_sync(kFull, f.y, 4);
+    const uint32_t hx = is_lo ? ox : f.x, hy = is_lo ? oy : f.y, lx = is_lo ? f.x : ox, ly = is_lo ? f.y : oy;
+    const float y[4] = {kappa * (bf16_lo(hx) + bf16_lo(lx)), kappa * (bf16_hi(hx) + bf16_hi(lx)),
+                        kappa * (bf16_lo(hy) + bf16_lo(ly)), kappa * (bf16_hi(hy) + bf16_hi(ly))};
+    float h[4], l[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        h[i] = __bfloat162float(__float2bfloat16_rn(y[i]));
+        l[i] = __bfloat162float(__float2bfloat16_rn(y[i] - h[i]));
+    }
+    return is_lo ? make_uint2(pack_bf16x2_rn(l[0], l[1]), pack_bf16x2_rn(l[2], l[3]))
+                 : make_uint2(pack_bf16x2_rn(h[0], h[1]), pack_bf16x2_rn(h[2], h[3]));
+}
+
 // One page of INT2 history for one consumer warp: the page's scales, the
 // logits of its four 16-token tiles, one online-softmax update, and the P.V
 // products.  FULL (all 64 tokens valid, the common case) removes the
@@ -440,16 +460,12 @@ __device__ __forceinline__ void attend_page(const uint8_t* blk, int valid, uint8
             const uint32_t wa[2] = {x.x, x.y}, wb[2] = {y.x, y.y};
             const uint32_t wa8[2] = {wa[0] >> 8, wa[1] >> 8}, wb8[2] = {wb[0] >> 8, wb[1] >> 8};
             float acc[4][NT][4];
-            float acc1[LM ? 4 : 1][NT][4];   // high-bit plane (Lloyd-Max levels)
 #pragma unroll
             for (int g = 0; g < 4; ++g)
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        acc[g][nt][e] = 0.f;
-                        if (LM) acc1[LM ? g : 0][nt][e] = 0.f;
-                    }
+                    for (int e = 0; e < 4; ++e) acc[g][nt][e] = 0.f;
 #pragma unroll
             for (int it = 0; it < 8; ++it) {
                 // half-major order: the four groups' accumulation chains interleave
@@ -477,7 +493,10 @@ __device__ __forceinline__ void attend_page(const uint8_t* blk, int valid, uint8
                 for (int nt = 0; nt < NT; ++nt) {
                     const uint2 qb = qfS[(nt * 8 + ks) * 32 + lane];
                     mma_bf16_16816(acc[g][nt], a0, a1, a2, a3, qb.x, qb.y);
-                    if (LM) mma_bf16_16816(acc1[LM ? g : 0][nt], c0, c1, c2, c3, qb.x, qb.y);
+                    if (LM) {  // high-bit plane against kappa q'
+                        const uint2 qk = qfS[((NT + nt) * 8 + ks) * 32 + lane];
+                        mma_bf16_16816(acc[g][nt], c0, c1, c2, c3, qk.x, qk.y);
+                    }
                 }
             }
             const float4 sA = ksS[ta], sB = ksS[ta + 8], zA = kzS[ta], zB = kzS[ta + 8];
@@ -490,11 +509,7 @@ __device__ __forceinline__ void attend_page(const uint8_t* blk, int valid, uint8
                 float xa = 0.f, xb = 0.f;
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
-                    float da = acc[g][nt][0] + acc[g][nt][1], db = acc[g][nt][2] + acc[g][nt][3];
-                    if (LM) {
-                        da = fmaf(cbk.kk, acc1[LM ? g : 0][nt][0] + acc1[LM ? g : 0][nt][1], da);
-                        db = fmaf(cbk.kk, acc1[LM ? g : 0][nt][2] + acc1[LM ? g : 0][nt][3], db);
-                    }
+                    const float da = acc[g][nt][0] + acc[g][nt][1], db = acc[g][nt][2] + acc[g][nt][3];
                     xa = fmaf(sa[g], da, xa);
                     xa = fmaf(za[g], qg[g], xa);
                     xb = fmaf(sb[g], db, xb);
@@ -926,8 +941,11 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
             for (int nt = 0; nt < NT; ++nt) {
                 const uint32_t* fr = p.qfrag + ((size_t)bk * NT + nt) * 8 * 32 * 2;
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks)  // every warp writes the same values
-                    qfS[(nt * 8 + ks) * 32 + lane] = *reinterpret_cast<const uint2*>(fr + ((size_t)ks * 32 + lane) * 2);
+                for (int ks = 0; ks < 8; ++ks) {  // every warp writes the same values
+                    const uint2 f = *reinterpret_cast<const uint2*>(fr + ((size_t)ks * 32 + lane) * 2);
+                    qfS[(nt * 8 + ks) * 32 + lane] = f;
+                    if (LM) qfS[((NT + nt) * 8 + ks) * 32 + lane] = scaled_fragment(f, cbk.kk, (lane >> 2) & 1);
+                }
                 // head of the lane's column: 4nt + tq (up to four heads), 2tq + nt (eight)
                 const int hq = (NT == 2) ? 2 * tq + nt : 4 * nt + tq;
                 qsv[nt] = *reinterpret_cast<const float4*>(p.qsum + ((size_t)bk * NT * 4 + hq) * 4);
@@ -1533,7 +1551,7 @@ static Int2Attr& attr_for_device(int dev) {
 
 template <int NT, bool LM = false>
 static cudaError_t launch_int2(const DecodeParams& p, cudaStream_t st, int sms, bool& attr_set) {
-    const int smem = Int2Smem<NT>::kBytes;
+    const int smem = LM ? Int2Smem<NT>::kBytesLM : Int2Smem<NT>::kBytes;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(int2_kernel<NT, LM>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
