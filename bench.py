@@ -38,6 +38,7 @@ from bit_kv_cache_evict_gb300 import synth as S  # noqa: E402
 METRIC = "decode context-tokens/s attended"
 UNIT = "tokens/s"
 HIST_BYTES_PER_TOKEN_HEAD = 96      # 2 x 32 B codes + 2 x 4 x (fp16 s, fp16 z) at 32 positions per group
+BOOST_RECORD_BYTES = 16             # K channel boost: 8 x (position, 4-bit code) entries per K token-vector
 
 
 def hist_bytes_per_token_head(g: int) -> int:
@@ -95,6 +96,9 @@ def parse_args():
     ap.add_argument("--codebook", type=float, default=None, metavar="A",
                     help="Lloyd-Max levels {0, A, 3-A, 3} for every head (up to four query heads per KV head) "
                          "instead of the uniform grid")
+    ap.add_argument("--boost", action="store_true",
+                    help="K channel precision boost: eight positions per K token-vector at 4 bits (up to four "
+                         "query heads per KV head)")
     ap.add_argument("--quant-group", type=int, default=32, choices=[32, 64, 128],
                     help="stored positions per fp16 scale/zero pair (32 is the configured format)")
     return ap.parse_args()
@@ -233,7 +237,7 @@ class GpuState:
     """Pools, BF16 segments, queries and per-step metadata for every layer."""
 
     def __init__(self, w: S.Workload, layers: int, steps_total: int, rank: int, quant_group: int = 32,
-                 codebook: float | None = None):
+                 codebook: float | None = None, boost: bool = False):
         import torch
         from bit_kv_cache_evict_gb300 import oscar as O
         self.O, self.torch = O, torch
@@ -242,7 +246,9 @@ class GpuState:
         self.dev = dev
         B, Hq, Hk, d = w.batch, w.hq, w.hk, S.D
         self.shape = O.make_shape(Hq, Hk, quant_group=quant_group)
-        self.hist_tok_bytes = hist_bytes_per_token_head(quant_group)
+        # K channel boost: one 16-byte record per K token-vector beside the pool
+        self.boost = boost
+        self.hist_tok_bytes = hist_bytes_per_token_head(quant_group) + (BOOST_RECORD_BYTES if boost else 0)
         ctx = S.context_lengths(w)
         self.ctx0 = ctx
         hist0 = np.maximum(ctx - S.NSLOT, 0).astype(np.int64)
@@ -281,15 +287,17 @@ class GpuState:
             clip = torch.from_numpy(S.clip_ratios(w).astype(np.float32)).to(dev)
             prof = torch.from_numpy(S.channel_profile(w, layer).astype(np.float32)).to(dev)
             pool = torch.empty(self.pool_bytes, dtype=torch.uint8, device=dev)
-            self._fill_history(pool, U, clip, prof, gen, hist0, grp)
+            brec = (torch.empty(self.num_pages * Hk * O.BOOST_BLOCK_BYTES, dtype=torch.uint8, device=dev)
+                    if boost else None)
+            self._fill_history(pool, brec, U, clip, prof, gen, hist0, grp)
             kv = S.kv_tokens_torch(w, B * S.NSLOT, gen, prof, dev).view(B, S.NSLOT, Hk, 2, d).contiguous()
             q = torch.randn((B, Hq, d), generator=gen, device=dev).to(torch.bfloat16)
             new_kv = S.kv_tokens_torch(w, B, gen, prof, dev).contiguous()
             out = torch.empty((B, Hq, d), dtype=torch.float32, device=dev)
-            self.layers.append(dict(U=U, clip=clip, pool=pool, kv=kv, q=q, new_kv=new_kv, out=out))
+            self.layers.append(dict(U=U, clip=clip, pool=pool, boost=brec, kv=kv, q=q, new_kv=new_kv, out=out))
         torch.cuda.synchronize()
 
-    def _fill_history(self, pool, U, clip, prof, gen, hist0, grp):
+    def _fill_history(self, pool, brec, U, clip, prof, gen, hist0, grp):
         """Bulk-evict each sequence's initial history (shared prefix pages
         once, by the first sharer) in chunks."""
         torch = self.torch
@@ -312,7 +320,10 @@ class GpuState:
             toks = S.kv_tokens_torch(self.w, n, gen, prof, self.dev).contiguous()
             sq = torch.from_numpy(seq[i:i + n]).to(self.dev)
             ps = torch.from_numpy(pos[i:i + n]).to(self.dev)
-            if self.cb is None:
+            if brec is not None:
+                self.O.oscar_evict_quantize_boost(self.shape, toks, sq, ps, U, clip, pool, brec, self.table, self.B,
+                                                  self.max_pages, self.num_pages)
+            elif self.cb is None:
                 self.O.oscar_evict_quantize(self.shape, toks, sq, ps, U, clip, pool, self.table, self.B,
                                             self.max_pages, self.num_pages)
             else:
@@ -323,7 +334,11 @@ class GpuState:
         O = self.O
         st = self.layers[layer]
         flat = st["kv"].view(self.B * S.NSLOT, self.Hk, 2, S.D)
-        if self.cb is None:
+        if self.boost:
+            O.oscar_evict_quantize_boost(self.shape, flat, self.seqs, self.hist_before[s], st["U"], st["clip"],
+                                         st["pool"], st["boost"], self.table, self.B, self.max_pages,
+                                         self.num_pages, src_row=self.src_row[s], new_kv=st["new_kv"])
+        elif self.cb is None:
             O.oscar_evict_quantize(self.shape, flat, self.seqs, self.hist_before[s], st["U"], st["clip"], st["pool"],
                                    self.table, self.B, self.max_pages, self.num_pages, src_row=self.src_row[s],
                                    new_kv=st["new_kv"])
@@ -333,7 +348,11 @@ class GpuState:
                                             src_row=self.src_row[s], new_kv=st["new_kv"])
         if int2_events is not None:
             O.oscar_time_next_int2(*int2_events)
-        if self.cb is None:
+        if self.boost:
+            O.oscar_decode_attn_boost(self.shape, st["q"], st["kv"], self.bf16_len, st["pool"], st["boost"],
+                                      self.table, self.max_pages, self.num_pages, self.hist_after[s], st["U"],
+                                      self.sm_scale, st["out"], self.ws)
+        elif self.cb is None:
             O.oscar_decode_attn(self.shape, st["q"], st["kv"], self.bf16_len, st["pool"], self.table,
                                 self.max_pages, self.num_pages, self.hist_after[s], st["U"], self.sm_scale,
                                 st["out"], self.ws)
@@ -475,7 +494,8 @@ def run_reference(args, rank: int, world: int) -> None:
     print(json.dumps(line), flush=True)
 
 
-def config_of(w: S.Workload, layers: int, quant_group: int = 32, codebook: float | None = None) -> dict:
+def config_of(w: S.Workload, layers: int, quant_group: int = 32, codebook: float | None = None,
+              boost: bool = False) -> dict:
     ctx = {"fixed": f"{w.ctx_lo}", "uniform": f"uniform[{w.ctx_lo},{w.ctx_hi}]",
            "loguniform": f"loguniform[{w.ctx_lo},{w.ctx_hi}]"}[w.ctx_kind]
     cfg = {"workload": w.name, "batch_per_gpu": w.batch, "layers": layers, "q_heads": w.hq, "kv_heads": w.hk,
@@ -485,6 +505,8 @@ def config_of(w: S.Workload, layers: int, quant_group: int = 32, codebook: float
            "parallelism": "replicas (independent sequences per GPU)"}
     if codebook is not None:
         cfg["levels"] = f"Lloyd-Max {{0, {codebook:g}, {3 - codebook:g}, 3}}"
+    if boost:
+        cfg["k_boost"] = "8 of 128 K positions per token at 4 bits (16-byte record)"
     if w.prefix_seqs:
         cfg["prefix_sharing"] = f"{w.prefix_seqs} sequences share a {w.prefix_tokens}-token prefix"
     return cfg
@@ -503,7 +525,7 @@ def run_oscar(args, rank: int, world: int, local: int) -> None:
     e2e_steps = 0 if args.no_e2e else K
     total_steps = W + K + e2e_steps
     t0 = time.time()
-    st = GpuState(w, L, total_steps, rank, args.quant_group, args.codebook)
+    st = GpuState(w, L, total_steps, rank, args.quant_group, args.codebook, args.boost)
     setup_s = time.time() - t0
     stream = torch.cuda.current_stream()
 
@@ -624,14 +646,15 @@ def run_oscar(args, rank: int, world: int, local: int) -> None:
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
             "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "int2 codes x bf16 hi/lo on tensor cores, fp32 accumulate", "data": "synthetic",
-            "config": config_of(w, L, args.quant_group, args.codebook),
+            "config": config_of(w, L, args.quant_group, args.codebook, args.boost),
             "decode_tokens_per_s": world * w.batch * K / (t_ms_max / 1e3),
             "bits_per_element": st.bits_per_element(W + K - 1),
             "step_algorithmic_gbs": step_bytes / (ms_per_step * 1e-3) / 1e9,
             "roofline": {"kernel": "int2_kernel (split-K INT2 history attention)", "bound": "hbm",
                          "achieved": achieved, "peak": peaks["hbm_gbs"], "peak_source": peaks["source"],
                          "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                         "traffic": int2_traffic(w.name if args.quant_group == 32 else "", int2_bytes),
+                         "traffic": int2_traffic(w.name if args.quant_group == 32 and args.codebook is None and not args.boost
+                                                else "", int2_bytes),
                          "bytes_per_launch": int2_bytes, "launch_ms": int2_avg_ms,
                          "share_of_step": int2_avg_ms * L / ms_per_step,
                          "launches_timed": len(int2_ms)},

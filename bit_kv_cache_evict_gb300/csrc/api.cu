@@ -66,7 +66,7 @@ static int block_bytes_of(const oscar_shape* s) { return 4096 + 512 * (kD / s->q
 static int tail_pages_of(int pps) { return pps > kShortItemPages ? 2 * kShortItemPages : 0; }
 
 struct WsLayout {
-    size_t counter, item_start, item_start2, qfrag, qsum, part, bf_part, total;
+    size_t counter, item_start, item_start2, qfrag, qsum, qrot, part, bf_part, total;
     int NT, pps, tail_pg, part_stride, max_items;
 };
 
@@ -89,6 +89,8 @@ static WsLayout ws_layout(const oscar_shape* s, int batch, int max_pages) {
     off = round_up(off + (size_t)batch * hk * w.NT * 8 * 32 * 2 * 4, 256);
     w.qsum = off;
     off = round_up(off + (size_t)batch * hk * w.NT * 4 * 4 * 4, 256);
+    w.qrot = off;
+    off = round_up(off + (size_t)batch * hk * 4 * kD * 4, 256);
     w.part = off;
     off = round_up(off + (size_t)w.max_items * w.part_stride * 4, 256);
     w.bf_part = off;
@@ -203,8 +205,8 @@ oscar_status oscar_pool_layout(const oscar_shape* shape, int32_t batch, const in
 static oscar_status evict_impl(const oscar_shape* shape, int32_t n_tok, const void* src_kv, int32_t src_rows,
                                const int32_t* src_row, const int32_t* dst_seq, const int32_t* dst_pos,
                                const void* new_kv, const float* U, const float* clip, const float* codebook,
-                               uint8_t* pool, const int32_t* page_table, int32_t batch, int32_t max_pages,
-                               int32_t num_pages, int32_t* dev_status, void* stream) {
+                               uint8_t* pool, uint8_t* boost, const int32_t* page_table, int32_t batch,
+                               int32_t max_pages, int32_t num_pages, int32_t* dev_status, void* stream) {
     const oscar_status sst = check_shape(shape);
     if (sst != OSCAR_OK) return sst;
     if (n_tok < 0 || src_rows < 0 || batch < 0 || max_pages <= 0 || num_pages < 0) return OSCAR_ERR_INVALID_ARG;
@@ -225,6 +227,7 @@ static oscar_status evict_impl(const oscar_shape* shape, int32_t n_tok, const vo
     p.clip = clip;
     p.codebook = codebook;
     p.pool = pool;
+    p.boost = boost;
     p.page_table = page_table;
     p.status = dev_status;
     p.n_tok = n_tok;
@@ -246,7 +249,18 @@ oscar_status oscar_evict_quantize(const oscar_shape* shape, int32_t n_tok, const
                                   int32_t batch, int32_t max_pages, int32_t num_pages,
                                   int32_t* dev_status, void* stream) {
     return evict_impl(shape, n_tok, src_kv, src_rows, src_row, dst_seq, dst_pos, new_kv, U, clip, nullptr, pool,
-                      page_table, batch, max_pages, num_pages, dev_status, stream);
+                      nullptr, page_table, batch, max_pages, num_pages, dev_status, stream);
+}
+
+oscar_status oscar_evict_quantize_boost(const oscar_shape* shape, int32_t n_tok, const void* src_kv,
+                                        int32_t src_rows, const int32_t* src_row, const int32_t* dst_seq,
+                                        const int32_t* dst_pos, const void* new_kv, const float* U,
+                                        const float* clip, uint8_t* pool, uint8_t* boost,
+                                        const int32_t* page_table, int32_t batch, int32_t max_pages,
+                                        int32_t num_pages, int32_t* dev_status, void* stream) {
+    if (n_tok > 0 && (!boost || !aligned(boost, 16))) return OSCAR_ERR_INVALID_ARG;
+    return evict_impl(shape, n_tok, src_kv, src_rows, src_row, dst_seq, dst_pos, new_kv, U, clip, nullptr, pool,
+                      boost, page_table, batch, max_pages, num_pages, dev_status, stream);
 }
 
 oscar_status oscar_evict_quantize_codebook(const oscar_shape* shape, int32_t n_tok, const void* src_kv,
@@ -257,14 +271,14 @@ oscar_status oscar_evict_quantize_codebook(const oscar_shape* shape, int32_t n_t
                                            int32_t num_pages, int32_t* dev_status, void* stream) {
     if (!codebook || !aligned(codebook, 4)) return OSCAR_ERR_INVALID_ARG;
     return evict_impl(shape, n_tok, src_kv, src_rows, src_row, dst_seq, dst_pos, new_kv, U, clip, codebook, pool,
-                      page_table, batch, max_pages, num_pages, dev_status, stream);
+                      nullptr, page_table, batch, max_pages, num_pages, dev_status, stream);
 }
 
 static oscar_status decode_impl(const oscar_shape* shape, int32_t batch, const void* q, const void* bf16_kv,
                                 const int32_t* bf16_len, const uint8_t* pool, const int32_t* page_table,
                                 int32_t max_pages, int32_t num_pages, const int32_t* hist_len, const float* U,
-                                const float* codebook, float sm_scale, float* out, void* workspace,
-                                size_t* ws_bytes, int32_t* dev_status, void* stream) {
+                                const float* codebook, const uint8_t* boost, float sm_scale, float* out,
+                                void* workspace, size_t* ws_bytes, int32_t* dev_status, void* stream) {
     const oscar_status sst = check_shape(shape);
     if (sst != OSCAR_OK) return sst;
     if (batch < 0 || max_pages <= 0 || num_pages < 0 || !ws_bytes) return OSCAR_ERR_INVALID_ARG;
@@ -297,6 +311,7 @@ static oscar_status decode_impl(const oscar_shape* shape, int32_t batch, const v
     p.item_start2 = reinterpret_cast<int32_t*>(ws + w.item_start2);
     p.qfrag = reinterpret_cast<uint32_t*>(ws + w.qfrag);
     p.qsum = reinterpret_cast<float*>(ws + w.qsum);
+    p.qrot = reinterpret_cast<float*>(ws + w.qrot);
     p.part = reinterpret_cast<float*>(ws + w.part);
     p.bf_part = reinterpret_cast<float*>(ws + w.bf_part);
     p.B = batch;
@@ -322,6 +337,7 @@ static oscar_status decode_impl(const oscar_shape* shape, int32_t batch, const v
     p.part_stride = w.part_stride;
     p.qscale = sm_scale * kLog2e;
     p.codebook = codebook;
+    p.boost = boost;
     cudaEvent_t ev0 = g_int2_ev_start, ev1 = g_int2_ev_stop;
     g_int2_ev_start = g_int2_ev_stop = nullptr;
     if (!ev0 || !ev1) ev0 = ev1 = nullptr;
@@ -335,7 +351,20 @@ oscar_status oscar_decode_attn(const oscar_shape* shape, int32_t batch, const vo
                                float sm_scale, float* out, void* workspace, size_t* ws_bytes,
                                int32_t* dev_status, void* stream) {
     return decode_impl(shape, batch, q, bf16_kv, bf16_len, pool, page_table, max_pages, num_pages, hist_len, U,
-                       nullptr, sm_scale, out, workspace, ws_bytes, dev_status, stream);
+                       nullptr, nullptr, sm_scale, out, workspace, ws_bytes, dev_status, stream);
+}
+
+oscar_status oscar_decode_attn_boost(const oscar_shape* shape, int32_t batch, const void* q, const void* bf16_kv,
+                                     const int32_t* bf16_len, const uint8_t* pool, const uint8_t* boost,
+                                     const int32_t* page_table, int32_t max_pages, int32_t num_pages,
+                                     const int32_t* hist_len, const float* U, float sm_scale, float* out,
+                                     void* workspace, size_t* ws_bytes, int32_t* dev_status, void* stream) {
+    const oscar_status sst = check_shape(shape);
+    if (sst != OSCAR_OK) return sst;
+    if (shape->num_q_heads / shape->num_kv_heads > 4) return OSCAR_ERR_UNSUPPORTED;
+    if (workspace && batch > 0 && num_pages > 0 && (!boost || !aligned(boost, 16))) return OSCAR_ERR_INVALID_ARG;
+    return decode_impl(shape, batch, q, bf16_kv, bf16_len, pool, page_table, max_pages, num_pages, hist_len, U,
+                       nullptr, boost, sm_scale, out, workspace, ws_bytes, dev_status, stream);
 }
 
 oscar_status oscar_decode_attn_codebook(const oscar_shape* shape, int32_t batch, const void* q, const void* bf16_kv,
@@ -348,7 +377,7 @@ oscar_status oscar_decode_attn_codebook(const oscar_shape* shape, int32_t batch,
     if (shape->num_q_heads / shape->num_kv_heads > 4) return OSCAR_ERR_UNSUPPORTED;
     if (workspace && (!codebook || !aligned(codebook, 4))) return OSCAR_ERR_INVALID_ARG;
     return decode_impl(shape, batch, q, bf16_kv, bf16_len, pool, page_table, max_pages, num_pages, hist_len, U,
-                       codebook, sm_scale, out, workspace, ws_bytes, dev_status, stream);
+                       codebook, nullptr, sm_scale, out, workspace, ws_bytes, dev_status, stream);
 }
 
 oscar_status oscar_calibrate_rotation(const oscar_shape* shape, int32_t n_q, const void* q, int32_t n_t,

@@ -135,6 +135,8 @@ __device__ __forceinline__ void prep_body(const DecodeParams& p) {
                 *reinterpret_cast<uint2*>(frag + ((size_t)ks * 32 + L) * 2) = make_uint2(0u, 0u);
             }
             if (lane < 4) qsum[lane] = 0.f;
+            if (p.boost)
+                *reinterpret_cast<float4*>(p.qrot + ((size_t)bk * 4 + hl) * kD + 4 * lane) = make_float4(0.f, 0.f, 0.f, 0.f);
             continue;
         }
         const int h = kv * p.G + hl;
@@ -175,6 +177,9 @@ __device__ __forceinline__ void prep_body(const DecodeParams& p) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) qs[32 * bitrev2(k) + r5] = y[k] * scale;  // stored order
         __syncwarp();
+        if (p.boost)  // q' itself for the boost corrections (NT = 1: heads 0..3)
+            *reinterpret_cast<float4*>(p.qrot + ((size_t)bk * 4 + hl) * kD + 4 * lane) =
+                *reinterpret_cast<const float4*>(qs + 4 * lane);
 
         // group sums of the split values (exactly what the MMA multiplies)
         float gs = 0.f;
@@ -237,6 +242,7 @@ constexpr int kFlagFirst = 1, kFlagLast = 2, kFlagPad = 4;
 
 struct StageInfo {
     int item, b, kv, valid_flags;  // valid tokens in bits 0-7, flags above
+    int pid, pad[3];               // page id (read by the boost variant)
 };
 
 template <int NT>
@@ -258,8 +264,10 @@ struct Int2Smem {
     // (all four are inside the same item between two item-end merges)
     static constexpr int kQf = kWarp + kConsumerWarps * kWarpBytes;       // [NT][8][32] uint2
     static constexpr int kBytes = kQf + NT * 8 * 32 * 8;
-    // Lloyd-Max levels: kappa q' fragments of the high-bit plane follow q'
+    // Lloyd-Max levels: kappa q' fragments of the high-bit plane follow q';
+    // channel boost: q' [kD] float4 (four heads) there instead
     static constexpr int kBytesLM = kBytes + NT * 8 * 32 * 8;
+    static_assert(NT * 8 * 32 * 8 >= kD * 16, "room for the boost's q'");
 };
 
 __device__ __forceinline__ int find_seq(const int32_t* item_start, int B, int item) {
@@ -427,11 +435,12 @@ __device__ __forceinline__ uint2 scaled_fragment(uint2 f, float kappa, int is_lo
 // products.  FULL (all 64 tokens valid, the common case) removes the
 // per-tile conditions of the logit phase so that the four tiles' work can
 // interleave.
-template <int NT, bool FULL, bool LM = false>
+template <int NT, bool FULL, bool LM = false, bool BOOST = false>
 __device__ __forceinline__ void attend_page(const uint8_t* blk, int valid, uint8_t* wbuf, const uint2* qfS,
                                             const float4 (&qsv)[NT], float (&m_run)[NT], float (&l_run)[NT],
                                             float (&zacc)[NT][4], float (&acc_o)[NT][8][4],
-                                            const SplitSel& take_lo, int gshift, const Codebook& cbk = {}) {
+                                            const SplitSel& take_lo, int gshift, const Codebook& cbk = {},
+                                            const float4* qbS = nullptr, const uint8_t* brec = nullptr) {
     using SM = Int2Smem<NT>;
     const int lane = threadIdx.x & 31, gID = lane >> 2, tq = lane & 3;
     if (FULL) valid = kPage;
@@ -441,6 +450,11 @@ __device__ __forceinline__ void attend_page(const uint8_t* blk, int valid, uint8
     float* vsS = reinterpret_cast<float*>(wbuf + SM::kWVs);     // [4][kPvRow] V s at pv_pos
     float* pS = reinterpret_cast<float*>(wbuf + SM::kWP);       // [G4][kPvRow] P at pv_pos
     const int ntile = FULL ? 4 : (valid + 15) >> 4;             // warp-uniform, 1..4
+    uint4 br0 = make_uint4(0u, 0u, 0u, 0u), br1 = br0;         // boost records of tokens 2 lane, 2 lane + 1
+    if constexpr (BOOST) {
+        br0 = __ldg(reinterpret_cast<const uint4*>(brec) + 2 * lane);
+        br1 = __ldg(reinterpret_cast<const uint4*>(brec) + 2 * lane + 1);
+    }
 
     if constexpr (LM) page_scales<FULL>(blk, valid, gshift, ksS, kzS, vzS, vsS, cbk.ka, cbk.va);
     else page_scales<FULL>(blk, valid, gshift, ksS, kzS, vzS, vsS);
@@ -519,6 +533,46 @@ __device__ __forceinline__ void attend_page(const uint8_t* blk, int valid, uint8
                 lb[m][nt] = vb ? xb : -INFINITY;
             }
         }
+    }
+
+    // -- channel boost: logit corrections q'[pos] s (q4 / 5 - c) of the
+    //    boosted positions; lane l computes tokens 2l, 2l + 1 for the four
+    //    heads into the P scratch (free until the softmax below)
+    if constexpr (BOOST) {
+        float4* cS = reinterpret_cast<float4*>(pS);
+        const int ng = 4 >> gshift;
+#pragma unroll
+        for (int tt = 0; tt < 2; ++tt) {
+            const int t = 2 * lane + tt;
+            const uint4 rr = tt ? br1 : br0;
+            float4 c = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (t < valid) {
+                const uint32_t* szw = reinterpret_cast<const uint32_t*>(blk + kKScale + t * 4 * ng);
+                const uint32_t wv[4] = {rr.x, rr.y, rr.z, rr.w};
+#pragma unroll
+                for (int e = 0; e < kBoostN; ++e) {
+                    const uint32_t ent = wv[e >> 1] >> (16 * (e & 1));
+                    const int pos = ent & 127;
+                    const float sg = __half2float(__ushort_as_half((unsigned short)(szw[pos >> (5 + gshift)] & 0xffffu)));
+                    const float d = sg * fmaf((float)((ent >> 8) & 15u), 0.2f, -(float)((ent >> 12) & 3u));
+                    const float4 qv = qbS[pos];
+                    c.x = fmaf(d, qv.x, c.x);
+                    c.y = fmaf(d, qv.y, c.y);
+                    c.z = fmaf(d, qv.z, c.z);
+                    c.w = fmaf(d, qv.w, c.w);
+                }
+            }
+            cS[t] = c;
+        }
+        __syncwarp();
+        const float* cf = reinterpret_cast<const float*>(pS);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int ta = 16 * m + gID;
+            la[m][0] += cf[ta * 4 + tq];
+            lb[m][0] += cf[(ta + 8) * 4 + tq];
+        }
+        __syncwarp();
     }
 
     // -- online softmax (base 2), once per page; every token's p is written
@@ -795,7 +849,7 @@ __device__ __forceinline__ void attend_page_g8(const uint8_t* blk, int valid, ui
     }
 }
 
-template <int NT, bool LM = false>
+template <int NT, bool LM = false, bool BOOST = false>
 __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(DecodeParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     using SM = Int2Smem<NT>;
@@ -841,12 +895,15 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
                     flags |= kFlagPad;
                 }
                 si.valid_flags = valid | (flags << 8);
+                si.pid = pid;
                 if (item < 0 || (flags & kFlagPad)) {
                     mbar_arrive(&full[s]);
                 } else {
                     mbar_arrive_expect_tx(&full[s], p.block_bytes);
                     bulk_g2s(stages + s * kBlock, p.pool + ((size_t)pid * p.hk + kv) * p.block_bytes,
                              p.block_bytes, &full[s]);
+                    // the consumer loads the page's boost records itself: have them in L2
+                    if constexpr (BOOST) bulk_prefetch_l2(p.boost + ((size_t)pid * p.hk + kv) * kBoostBlock, kBoostBlock);
                 }
             }
             __syncwarp();
@@ -918,6 +975,7 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
     };
 
     uint2* qfS = reinterpret_cast<uint2*>(smem + SM::kQf);
+    float4* qbS = reinterpret_cast<float4*>(smem + SM::kQf + NT * 8 * 32 * 8);  // boost: q' of the four heads
     float4 qsv[NT];
     float m_run[NT], l_run[NT], zacc[NT][4], acc_o[NT][8][4];
     Codebook cbk{1.f, 1.f, 0.f, 0.f};  // Lloyd-Max levels of the current item's KV head
@@ -946,6 +1004,16 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
                     qfS[(nt * 8 + ks) * 32 + lane] = f;
                     if (LM) qfS[((NT + nt) * 8 + ks) * 32 + lane] = scaled_fragment(f, cbk.kk, (lane >> 2) & 1);
                 }
+                if constexpr (BOOST) {  // q'[j] of heads 0..3 as one float4 per stored position j
+                    const float* qr = p.qrot + (size_t)bk * 4 * kD + 4 * lane;
+                    const float4 a0 = *reinterpret_cast<const float4*>(qr), a1 = *reinterpret_cast<const float4*>(qr + kD);
+                    const float4 a2 = *reinterpret_cast<const float4*>(qr + 2 * kD);
+                    const float4 a3 = *reinterpret_cast<const float4*>(qr + 3 * kD);
+                    qbS[4 * lane + 0] = make_float4(a0.x, a1.x, a2.x, a3.x);
+                    qbS[4 * lane + 1] = make_float4(a0.y, a1.y, a2.y, a3.y);
+                    qbS[4 * lane + 2] = make_float4(a0.z, a1.z, a2.z, a3.z);
+                    qbS[4 * lane + 3] = make_float4(a0.w, a1.w, a2.w, a3.w);
+                }
                 // head of the lane's column: 4nt + tq (up to four heads), 2tq + nt (eight)
                 const int hq = (NT == 2) ? 2 * tq + nt : 4 * nt + tq;
                 qsv[nt] = *reinterpret_cast<const float4*>(p.qsum + ((size_t)bk * NT * 4 + hq) * 4);
@@ -967,12 +1035,14 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
                 else
                     attend_page_g8<false>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o[0], p.gshift);
             } else {
+                const uint8_t* brec = nullptr;
+                if constexpr (BOOST) brec = p.boost + ((size_t)info[s].pid * p.hk + sraw.z) * kBoostBlock;
                 if (valid == kPage)
-                    attend_page<NT, true, LM>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o, take_lo,
-                                              p.gshift, cbk);
+                    attend_page<NT, true, LM, BOOST>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o,
+                                                     take_lo, p.gshift, cbk, qbS, brec);
                 else
-                    attend_page<NT, false, LM>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o, take_lo,
-                                               p.gshift, cbk);
+                    attend_page<NT, false, LM, BOOST>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o,
+                                                      take_lo, p.gshift, cbk, qbS, brec);
             }
         }
         __syncwarp();
@@ -1541,7 +1611,7 @@ __global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(DecodeParams p)
 // ---------------------------------------------------------------------------
 struct Int2Attr {
     int sms = 0;
-    bool set1 = false, set2 = false, setl = false, setm = false, setp = false, setb = false;
+    bool set1 = false, set2 = false, setl = false, setk = false, setm = false, setp = false, setb = false;
 };
 
 static Int2Attr& attr_for_device(int dev) {
@@ -1549,11 +1619,12 @@ static Int2Attr& attr_for_device(int dev) {
     return attrs[dev & 63];
 }
 
-template <int NT, bool LM = false>
+template <int NT, bool LM = false, bool BOOST = false>
 static cudaError_t launch_int2(const DecodeParams& p, cudaStream_t st, int sms, bool& attr_set) {
-    const int smem = LM ? Int2Smem<NT>::kBytesLM : Int2Smem<NT>::kBytes;
+    const int smem = (LM || BOOST) ? Int2Smem<NT>::kBytesLM : Int2Smem<NT>::kBytes;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(int2_kernel<NT, LM>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaError_t e =
+            cudaFuncSetAttribute(int2_kernel<NT, LM, BOOST>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -1561,7 +1632,7 @@ static cudaError_t launch_int2(const DecodeParams& p, cudaStream_t st, int sms, 
     const int max_items = p.B * p.hk * ((p.max_pages + p.pps - 1) / p.pps + p.tail_pg / kShortItemPages);
     int blocks = min(per_sm * sms, max_items);
     if (blocks < 1) blocks = 1;
-    cudaError_t e = launch_pdl(int2_kernel<NT, LM>, dim3(blocks), dim3(kInt2Threads), smem, st, p);
+    cudaError_t e = launch_pdl(int2_kernel<NT, LM, BOOST>, dim3(blocks), dim3(kInt2Threads), smem, st, p);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -1603,6 +1674,8 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st, cudaEvent_t ev
     if (ev_int2_start && (e = cudaEventRecord(ev_int2_start, st)) != cudaSuccess) return e;
     if (p.codebook)  // Lloyd-Max levels (up to four query heads per KV head)
         e = launch_int2<1, true>(p, st, at.sms, at.setl);
+    else if (p.boost)  // K channel boost (up to four query heads per KV head)
+        e = launch_int2<1, false, true>(p, st, at.sms, at.setk);
     else
         e = (p.NT == 1) ? launch_int2<1>(p, st, at.sms, at.set1) : launch_int2<2>(p, st, at.sms, at.set2);
     if (e != cudaSuccess) return e;

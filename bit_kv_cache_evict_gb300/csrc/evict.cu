@@ -212,6 +212,9 @@ __global__ void __launch_bounds__(32 * kEvictWarps) evict_kernel(EvictParams p) 
     // all four codes of code byte j = bitrev5(lane) are this lane's, group k in
     // bits 2k..2k+1
     uint32_t byte = 0;
+    const bool boost = p.boost != nullptr && which == 0;
+    float berr[4] = {0.f, 0.f, 0.f, 0.f};  // 2-bit rounding error (0 where s = 0)
+    int bq4[4] = {0, 0, 0, 0};             // 4-bit code on the group range
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         const df d = df_add(hi[k], df_neg(lo[k]));
@@ -227,6 +230,10 @@ __global__ void __launch_bounds__(32 * kEvictWarps) evict_kernel(EvictParams p) 
                 code = (u >= 0.5f * cb_a) + (u >= 1.5f) + (u >= 3.f - 0.5f * cb_a);
             else
                 code = (int)fminf(fmaxf(rintf(u), 0.f), 3.f);
+            if (boost) {
+                berr[k] = fabsf(u - (float)code);
+                bq4[k] = (int)fminf(fmaxf(rintf(__fmul_rn(5.f, u)), 0.f), 15.f);
+            }
         }
         byte |= (uint32_t)code << (2 * bitrev2(k));
     }
@@ -258,6 +265,51 @@ __global__ void __launch_bounds__(32 * kEvictWarps) evict_kernel(EvictParams p) 
         if (ng == 4) *reinterpret_cast<uint4*>(sz) = make_uint4(w[0], w[1], w[2], w[3]);
         else if (ng == 2) *reinterpret_cast<uint2*>(sz) = make_uint2(w[0], w[1]);
         else *reinterpret_cast<uint32_t*>(sz) = w[0];
+    }
+    if (boost) {
+        // kBoostN rounds of a warp arg-max over the 128 errors (ties to the
+        // lower stored position); value k of this lane is position 32
+        // bitrev2(k) + j
+        uint32_t sel = 0;  // bit k: value k chosen
+#pragma unroll 1
+        for (int r = 0; r < kBoostN; ++r) {
+            float be = -1.f;
+            int bp = 1 << 30;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int pos_k = 32 * bitrev2(k) + j;
+                if (!((sel >> k) & 1u) && (berr[k] > be || (berr[k] == be && pos_k < bp))) {
+                    be = berr[k];
+                    bp = pos_k;
+                }
+            }
+            float me = be;
+#pragma unroll
+            for (int m = 16; m > 0; m >>= 1) me = fmaxf(me, __shfl_xor_sync(kFull, me, m));
+            int mp = (be == me) ? bp : (1 << 30);
+#pragma unroll
+            for (int m = 16; m > 0; m >>= 1) mp = min(mp, __shfl_xor_sync(kFull, mp, m));
+            if ((mp & 31) == j) sel |= 1u << bitrev2(mp >> 5);
+        }
+        // rank of a chosen position = chosen positions below it: per 32-position
+        // block b, lane L gathers the flag of position 32 b + L (held by lane
+        // bitrev5(L)) and a ballot gives the block's mask in position order
+        uint32_t mask[4];
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+            mask[b] = __ballot_sync(kFull, (__shfl_sync(kFull, sel, bitrev5(lane)) >> bitrev2(b)) & 1u);
+        uint16_t* rec = reinterpret_cast<uint16_t*>(p.boost + ((size_t)page * p.hk + kv) * kBoostBlock +
+                                                    slot * kBoostRecord);
+        int below = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const int k = bitrev2(b);
+            if ((sel >> k) & 1u) {
+                const int rank = below + __popc(mask[b] & ((1u << j) - 1u));
+                rec[rank] = (uint16_t)((32 * b + j) | (bq4[k] << 8) | (((byte >> (2 * b)) & 3u) << 12));
+            }
+            below += __popc(mask[b]);
+        }
     }
 }
 

@@ -246,6 +246,11 @@ __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, u
         : "memory");
 }
 
+// Bulk prefetch of global memory into L2 (16-byte aligned address and size).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src_gmem, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src_gmem), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void report(int32_t* status, int32_t bits) {
     if (status) atomicOr(status, bits);
 }
@@ -254,6 +259,16 @@ __device__ __forceinline__ void report(int32_t* status, int32_t bits) {
 // ------------------------------------------------------------------
 // launch parameters (host <-> kernels)
 // ------------------------------------------------------------------
+// Channel precision boost of the K history: per token vector the kBoostN
+// stored positions with the largest 2-bit rounding error |u - c| also keep
+// a 4-bit code q4 = clamp(rint(5u), 0, 15) (levels z + s q4 / 5).  Record =
+// kBoostN 16-bit entries (position bits 0-6, q4 bits 8-11, a copy of the
+// position's 2-bit code in bits 12-13) in increasing position; records of a
+// (page, KV head) in one block, token t at 16 t.
+constexpr int kBoostN = 8;
+constexpr int kBoostRecord = 2 * kBoostN;
+constexpr int kBoostBlock = 64 * kBoostRecord;
+
 struct EvictParams {
     const __nv_bfloat16* src_kv;
     const int32_t* src_row;
@@ -264,6 +279,7 @@ struct EvictParams {
     const float* clip;
     const float* codebook;   // [hk][2] inner level a of the Lloyd-Max codebook, or null (uniform levels)
     uint8_t* pool;
+    uint8_t* boost;          // K boost records [num_pages][hk][kBoostBlock], or null (no boost)
     const int32_t* page_table;
     int32_t* status;
     int n_tok, hk, src_rows, batch, max_pages, num_pages;
@@ -292,6 +308,7 @@ struct DecodeParams {
     int32_t* item_start2; // [B + 1] short tail items before sequence b
     uint32_t* qfrag;      // [B*Hk][NT][8][32][2]
     float* qsum;          // [B*Hk][NT*4][4]
+    float* qrot;          // [B*Hk][4][kD] q' in stored order (fp32), written when boost is set
     float* part;          // [max_items][part_stride]
     float* bf_part;       // [B*Hk][bf_items][part_stride]
     int B, hq, hk, G, NT, nslot, max_pages, num_pages, pps, part_stride;
@@ -302,6 +319,7 @@ struct DecodeParams {
     int block_bytes;
     float qscale;  // sm_scale * log2(e)
     const float* codebook;  // [hk][2] Lloyd-Max inner level a, or null (uniform levels)
+    const uint8_t* boost;   // K boost records [num_pages][hk][kBoostBlock], or null (no boost)
 };
 
 // Split-K geometry of one sequence with npg history pages: the last

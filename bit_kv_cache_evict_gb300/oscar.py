@@ -78,6 +78,13 @@ def lib() -> ctypes.CDLL:
         L.oscar_decode_attn_codebook.argtypes = [S, ctypes.c_int32, _P, _P, _P, _P, _P, ctypes.c_int32,
                                                  ctypes.c_int32, _P, _P, _P, ctypes.c_float, _P, _P,
                                                  ctypes.POINTER(ctypes.c_size_t), _P, _P]
+        L.oscar_evict_quantize_boost.restype = ctypes.c_int
+        L.oscar_evict_quantize_boost.argtypes = [S, ctypes.c_int32, _P, ctypes.c_int32, _P, _P, _P, _P, _P, _P,
+                                                 _P, _P, _P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, _P]
+        L.oscar_decode_attn_boost.restype = ctypes.c_int
+        L.oscar_decode_attn_boost.argtypes = [S, ctypes.c_int32, _P, _P, _P, _P, _P, _P, ctypes.c_int32,
+                                              ctypes.c_int32, _P, _P, ctypes.c_float, _P, _P,
+                                              ctypes.POINTER(ctypes.c_size_t), _P, _P]
         L.oscar_calibrate_codebook.restype = ctypes.c_int
         L.oscar_calibrate_codebook.argtypes = [S, ctypes.c_int32, _P, _P, _P, _P, _P, ctypes.POINTER(ctypes.c_size_t),
                                                _P]
@@ -305,6 +312,45 @@ def oscar_decode_attn_codebook(shape: oscar_shape, q, bf16_kv, bf16_len, pool, p
         _dptr(out, "out", torch.float32), _dptr(workspace, "workspace", torch.uint8), ctypes.byref(ws),
         _dptr(dev_status, "dev_status", torch.int32), _stream_ptr(stream))
     _check("oscar_decode_attn_codebook", st)
+
+
+BOOST_N = 8
+BOOST_BLOCK_BYTES = 1024        # per (page, KV head): 64 tokens x 8 entries x 2 bytes
+
+
+def oscar_evict_quantize_boost(shape: oscar_shape, src_kv, dst_seq, dst_pos, U, clip, pool, boost, page_table,
+                               batch: int, max_pages: int, num_pages: int, src_row=None, new_kv=None,
+                               dev_status=None, stream=None) -> None:
+    """oscar_evict_quantize plus the K channel-boost records (boost: uint8
+    [num_pages * Hk * BOOST_BLOCK_BYTES]); see include/oscar.h."""
+    import torch
+    n_tok = int(dst_seq.numel())
+    st = lib().oscar_evict_quantize_boost(
+        ctypes.byref(shape), n_tok, _dptr(src_kv, "src_kv", torch.bfloat16), int(src_kv.shape[0]),
+        _dptr(src_row, "src_row", torch.int32), _dptr(dst_seq, "dst_seq", torch.int32),
+        _dptr(dst_pos, "dst_pos", torch.int32), _dptr(new_kv, "new_kv", torch.bfloat16),
+        _dptr(U, "U", torch.float32), _dptr(clip, "clip", torch.float32), _dptr(pool, "pool", torch.uint8),
+        _dptr(boost, "boost", torch.uint8), _dptr(page_table, "page_table", torch.int32), batch, max_pages,
+        num_pages, _dptr(dev_status, "dev_status", torch.int32), _stream_ptr(stream))
+    _check("oscar_evict_quantize_boost", st)
+
+
+def oscar_decode_attn_boost(shape: oscar_shape, q, bf16_kv, bf16_len, pool, boost, page_table, max_pages: int,
+                            num_pages: int, hist_len, U, sm_scale: float, out, workspace, dev_status=None,
+                            stream=None) -> None:
+    """oscar_decode_attn with the boosted K values; G <= 4.  The workspace
+    size is oscar_decode_workspace_bytes's."""
+    import torch
+    B = int(q.shape[0])
+    ws = ctypes.c_size_t(int(workspace.numel()))
+    st = lib().oscar_decode_attn_boost(
+        ctypes.byref(shape), B, _dptr(q, "q", torch.bfloat16), _dptr(bf16_kv, "bf16_kv", torch.bfloat16),
+        _dptr(bf16_len, "bf16_len", torch.int32), _dptr(pool, "pool", torch.uint8), _dptr(boost, "boost", torch.uint8),
+        _dptr(page_table, "page_table", torch.int32), max_pages, num_pages, _dptr(hist_len, "hist_len", torch.int32),
+        _dptr(U, "U", torch.float32), ctypes.c_float(sm_scale), _dptr(out, "out", torch.float32),
+        _dptr(workspace, "workspace", torch.uint8), ctypes.byref(ws), _dptr(dev_status, "dev_status", torch.int32),
+        _stream_ptr(stream))
+    _check("oscar_decode_attn_boost", st)
 
 
 def oscar_calibrate_codebook(shape: oscar_shape, kv, U, clip, codebook, workspace=None, stream=None) -> None:

@@ -284,6 +284,48 @@ oscar_status oscar_decode_attn_codebook(const oscar_shape* shape, int32_t batch,
                                         void* workspace, size_t* ws_bytes, int32_t* dev_status, void* stream);
 
 /*
+ * K channel precision boost (the "Zhongzhu (Charlie) Zhou" home page,
+ * Featured Projects, entry "KITTY: Accurate and Efficient 2-bit KV Cache
+ * Quantization with Dynamic Channel-wise Precision Boost": a small fraction
+ * of the K cache's channels is kept at 4 bits, the rest at 2 bits; the
+ * pages give no format).  Reading: the pool is written exactly as by
+ * oscar_evict_quantize; in addition, for every stored K token-vector the
+ * OSCAR_BOOST_N = 8 stored positions (rotated channels) with the largest
+ * 2-bit rounding error |u - c| (ties to the lower position; error 0 where
+ * s = 0) keep a 4-bit code q4 = clamp(rint(5 u), 0, 15) on the group's
+ * range: the K value there is z + s * q4 / 5 instead of z + s * c.  V is
+ * unchanged.
+ *
+ *   boost (device) uint8 [num_pages][Hk][OSCAR_BOOST_BLOCK_BYTES], 16-byte
+ *          aligned; caller-owned, indexed by the same page ids as the pool.
+ *          Token t of a page has its record at byte 16 t of the block:
+ *          eight little-endian uint16 entries, stored position in bits 0-6,
+ *          q4 in bits 8-11 and a copy of the position's 2-bit code c in
+ *          bits 12-13 (other bits 0), in increasing position.  A
+ *          record is written when its token is evicted; the decode reads
+ *          the records of the history tokens only.
+ *
+ * oscar_evict_quantize_boost: oscar_evict_quantize plus the K records.
+ * oscar_decode_attn_boost: oscar_decode_attn with the boosted K values;
+ *   query groups G = Hq/Hk of at most 4 (OSCAR_ERR_UNSUPPORTED otherwise).
+ *   The corrections q'[pos] * s * (q4 / 5 - c) are added to the logits of
+ *   the INT2 kernel; everything else is the uniform path.
+ */
+#define OSCAR_BOOST_N 8
+#define OSCAR_BOOST_BLOCK_BYTES 1024 /* 64 tokens x 8 entries x 2 bytes */
+oscar_status oscar_evict_quantize_boost(const oscar_shape* shape, int32_t n_tok, const void* src_kv,
+                                        int32_t src_rows, const int32_t* src_row, const int32_t* dst_seq,
+                                        const int32_t* dst_pos, const void* new_kv, const float* U,
+                                        const float* clip, uint8_t* pool, uint8_t* boost,
+                                        const int32_t* page_table, int32_t batch, int32_t max_pages,
+                                        int32_t num_pages, int32_t* dev_status, void* stream);
+oscar_status oscar_decode_attn_boost(const oscar_shape* shape, int32_t batch, const void* q, const void* bf16_kv,
+                                     const int32_t* bf16_len, const uint8_t* pool, const uint8_t* boost,
+                                     const int32_t* page_table, int32_t max_pages, int32_t num_pages,
+                                     const int32_t* hist_len, const float* U, float sm_scale, float* out,
+                                     void* workspace, size_t* ws_bytes, int32_t* dev_status, void* stream);
+
+/*
  * oscar_calibrate_codebook -- offline Lloyd-Max fit of the inner level a of
  * each (KV head, K/V) codebook from calibration tokens: every element's
  * u = (y_clipped - z) / s under the eviction's quantiser (given U and clip,

@@ -20,7 +20,9 @@ here keeps OSCAR's stored format and adds to it:
     the same group range, i.e. levels z + s * q4 / 5 (sixteen levels from z
     to z + 3 s, step s / 5; rint = round half to even);
   - the boost record of a token is NB little-endian 16-bit entries
-    (stored position in bits 0-6, q4 in bits 8-11), in increasing stored
+    (stored position in bits 0-6, q4 in bits 8-11, and a copy of the
+    position's 2-bit code c in bits 12-13, so that a reader finds the
+    correction q4 / 5 - c without the code bytes), in increasing stored
     position, 16 bytes; the records of a (page, KV head) form a 1024-byte
     block (token t at byte 16 t) of a separate array indexed like the pool;
   - a K value is z + s * q4 / 5 at a boosted position, z + s * c elsewhere;
@@ -52,19 +54,26 @@ def record(u: np.ndarray, codes: np.ndarray, s_nonzero: np.ndarray) -> np.ndarra
     """The 16-byte boost record of one vector."""
     pos = select(u, codes, s_nonzero)
     q4 = np.where(s_nonzero[pos], q4_of(u[pos]), 0)
-    ent = (pos | (q4 << 8)).astype("<u2")
+    ent = (pos | (q4 << 8) | (np.asarray(codes, np.int64)[pos] << 12)).astype("<u2")
     return ent.view(np.uint8)
 
 
 def parse(rec: np.ndarray):
+    """(positions, 4-bit codes) of a record."""
     ent = np.asarray(rec, np.uint8).view("<u2").astype(np.int64)
     return ent & 0x7F, (ent >> 8) & 0xF
 
 
+def parse_codes(rec: np.ndarray):
+    """The 2-bit code copies of a record's entries."""
+    return (np.asarray(rec, np.uint8).view("<u2").astype(np.int64) >> 12) & 3
+
+
 def evict(orc, shape, src, seq, pos, U, clip, pool, table, max_pages, boost):
     """The uniform eviction (the C oracle) plus the boost records of the K
-    vectors written into ``boost`` (uint8, num_pages * Hk * 1024)."""
-    u, _, _ = orc.evict(shape, src, seq, pos, U, clip, pool, table, max_pages, want_aux=True)
+    vectors written into ``boost`` (uint8, num_pages * Hk * 1024).  Returns
+    the C oracle's (u, s_pre, z_pre)."""
+    u, sp, zp = orc.evict(shape, src, seq, pos, U, clip, pool, table, max_pages, want_aux=True)
     hk, g = shape.num_kv_heads, shape.quant_group
     for i in range(len(seq)):
         b, p = int(seq[i]), int(pos[i])
@@ -74,7 +83,7 @@ def evict(orc, shape, src, seq, pos, U, clip, pool, table, max_pages, boost):
             nz = np.repeat(s != 0, g)
             off = (page * hk + kv) * BLOCK + (p % 64) * RECORD
             boost[off:off + RECORD] = record(u[i, kv, 0], codes, nz)
-    return u
+    return u, sp, zp
 
 
 def _f16(h) -> np.ndarray:

@@ -20,12 +20,13 @@ def test_record_bytes_of_a_hand_built_case():
     # the errors are 0.5 (pos 5: c 0, q4 rint(2.5) = 2), 0.45 (pos 100:
     # u 1.45, c 1, q4 rint(7.25) = 7), 0.4 (pos 31: u 2.6, c 3, q4 13),
     # 0.3 (pos 64: u 0.3, c 0, q4 rint(1.5) = 2); the other four entries are
-    # the lowest error-0 positions 0, 1, 2, 3 (q4 0)
+    # the lowest error-0 positions 0, 1, 2, 3 (q4 0); the code copy sits in
+    # bits 12-13 (c = 1 at pos 100, 3 at pos 31)
     u = np.zeros(D)
     u[5], u[100], u[31], u[64] = 0.5, 1.45, 2.6, 0.3
     codes = np.clip(np.rint(u), 0, 3).astype(np.uint8)
     rec = K.record(u, codes, np.ones(D, bool))
-    want = bytes([0, 0, 1, 0, 2, 0, 3, 0, 5, 2, 31, 13, 64, 2, 100, 7])
+    want = bytes([0, 0, 1, 0, 2, 0, 3, 0, 5, 2, 31, 0x3D, 64, 2, 100, 0x17])
     assert rec.tobytes() == want
 
 
@@ -36,8 +37,10 @@ def test_selected_errors_dominate_and_entries_are_sorted():
             y = rng.standard_normal(D) * rng.uniform(0.1, 5)
             codes, s16, z16, u, s, z = _quant(y, g, 0.9)
             nz = np.repeat(s != 0, g)
-            pos, q4 = K.parse(K.record(u, codes, nz))
+            rec = K.record(u, codes, nz)
+            pos, q4 = K.parse(rec)
             assert pos.size == K.NB and np.all(np.diff(pos) > 0)
+            assert np.array_equal(K.parse_codes(rec), codes[pos])
             err = np.abs(u - codes)
             others = np.setdiff1d(np.arange(D), pos)
             assert err[pos].min() >= err[others].max()
@@ -114,7 +117,7 @@ def test_decode_closed_form_of_one_changed_boost_code():
     pos, q4 = K.parse(rec1)
     p, dq = int(pos[0]), (1 if q4[0] < 15 else -1)
     ent = rec1.view("<u2").copy()
-    ent[0] = p | ((int(q4[0]) + dq) << 8)
+    ent[0] = (int(ent[0]) & ~0x0F00) | ((int(q4[0]) + dq) << 8)
     boost2 = boost.copy()
     boost2[K.RECORD:2 * K.RECORD] = ent.view(np.uint8)
     _, s, _ = K.read_k(pool, table, 0, 1, 0, 1, 32)
@@ -134,7 +137,8 @@ def test_decode_without_correction_is_the_plain_oracle():
         rec = boost[t * K.RECORD:(t + 1) * K.RECORD]
         pos, _ = K.parse(rec)
         codes, _, _ = K.read_k(pool, table, 0, t, 0, 1, 32)
-        ent = (pos | (5 * codes[pos].astype(np.int64) << 8)).astype("<u2")
+        c = codes[pos].astype(np.int64)
+        ent = (pos | (5 * c << 8) | (c << 12)).astype("<u2")
         boost[t * K.RECORD:(t + 1) * K.RECORD] = ent.view(np.uint8)
     rng = np.random.default_rng(3)
     bkv = S.bf16_bits(rng.standard_normal((1, 320, 1, 2, D)).astype(np.float32))
