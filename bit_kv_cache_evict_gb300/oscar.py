@@ -59,6 +59,22 @@ def lib() -> ctypes.CDLL:
         L.oscar_pool_layout.restype = ctypes.c_int
         L.oscar_pool_layout.argtypes = [S, ctypes.c_int32, _P, _P, ctypes.c_int32, ctypes.c_uint64, ctypes.c_int32,
                                         _P, _P, _P]
+        I32, PP = ctypes.c_int32, ctypes.POINTER(ctypes.c_void_p)
+        L.oscar_pages_create.restype = ctypes.c_int
+        L.oscar_pages_create.argtypes = [I32, PP]
+        L.oscar_pages_destroy.restype = None
+        L.oscar_pages_destroy.argtypes = [_P]
+        for fn in ("oscar_pages_alloc", "oscar_pages_retain", "oscar_pages_release"):
+            getattr(L, fn).restype = ctypes.c_int
+            getattr(L, fn).argtypes = [_P, I32, _P]
+        L.oscar_pages_refcount.restype = I32
+        L.oscar_pages_refcount.argtypes = [_P, I32]
+        L.oscar_pages_free_count.restype = I32
+        L.oscar_pages_free_count.argtypes = [_P]
+        L.oscar_pages_prepare_write.restype = ctypes.c_int
+        L.oscar_pages_prepare_write.argtypes = [_P, I32, _P, _P, _P, I32, I32, _P, _P, _P]
+        L.oscar_pages_copy.restype = ctypes.c_int
+        L.oscar_pages_copy.argtypes = [S, I32, _P, _P, _P, _P, I32, _P]
         L.oscar_evict_quantize.restype = ctypes.c_int
         L.oscar_evict_quantize.argtypes = [S, ctypes.c_int32, _P, ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P, _P,
                                            ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, _P]
@@ -312,6 +328,83 @@ def oscar_decode_attn_codebook(shape: oscar_shape, q, bf16_kv, bf16_len, pool, p
         _dptr(out, "out", torch.float32), _dptr(workspace, "workspace", torch.uint8), ctypes.byref(ws),
         _dptr(dev_status, "dev_status", torch.int32), _stream_ptr(stream))
     _check("oscar_decode_attn_codebook", st)
+
+
+def _host_i32(a):
+    import numpy as np
+    return np.ascontiguousarray(a, np.int32)
+
+
+def _np_ptr(a):
+    return a.ctypes.data_as(ctypes.c_void_p) if a is not None and a.size else None
+
+
+class Pages:
+    """Refcounted history pages with copy-on-write (host logic of the C ABI's
+    oscar_pages_* calls; see include/oscar.h)."""
+
+    def __init__(self, num_pages: int):
+        h = ctypes.c_void_p()
+        _check("oscar_pages_create", lib().oscar_pages_create(int(num_pages), ctypes.byref(h)))
+        self._h = h
+
+    def close(self) -> None:
+        if self._h:
+            lib().oscar_pages_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def alloc(self, n: int):
+        import numpy as np
+        out = np.zeros(max(int(n), 0), np.int32)
+        _check("oscar_pages_alloc", lib().oscar_pages_alloc(self._h, int(n), _np_ptr(out)))
+        return out
+
+    def retain(self, pages) -> None:
+        a = _host_i32(pages)
+        _check("oscar_pages_retain", lib().oscar_pages_retain(self._h, a.size, _np_ptr(a)))
+
+    def release(self, pages) -> None:
+        a = _host_i32(pages)
+        _check("oscar_pages_release", lib().oscar_pages_release(self._h, a.size, _np_ptr(a)))
+
+    def refcount(self, page: int) -> int:
+        return int(lib().oscar_pages_refcount(self._h, int(page)))
+
+    def free_count(self) -> int:
+        return int(lib().oscar_pages_free_count(self._h))
+
+    def prepare_write(self, seq, page_index, page_table):
+        """Make the target pages of page_table (numpy int32 [batch][max_pages],
+        updated in place) private; returns (copy_src, copy_dst)."""
+        import numpy as np
+        sq, pi = _host_i32(seq), _host_i32(page_index)
+        assert page_table.dtype == np.int32 and page_table.flags.c_contiguous
+        src = np.zeros(max(sq.size, 1), np.int32)
+        dst = np.zeros(max(sq.size, 1), np.int32)
+        n = ctypes.c_int32(0)
+        st = lib().oscar_pages_prepare_write(self._h, sq.size, _np_ptr(sq), _np_ptr(pi),
+                                             page_table.ctypes.data_as(ctypes.c_void_p), page_table.shape[0],
+                                             page_table.shape[1], _np_ptr(src), _np_ptr(dst), ctypes.byref(n))
+        _check("oscar_pages_prepare_write", st)
+        return src[:n.value].copy(), dst[:n.value].copy()
+
+
+def oscar_pages_copy(shape: oscar_shape, copy_src, copy_dst, pool, boost, num_pages: int, stream=None) -> None:
+    """Copy the pool blocks (and boost records) of copy_src pages to copy_dst
+    pages on the device (host index arrays)."""
+    import torch
+    src, dst = _host_i32(copy_src), _host_i32(copy_dst)
+    assert src.size == dst.size
+    st = lib().oscar_pages_copy(ctypes.byref(shape), src.size, _np_ptr(src), _np_ptr(dst),
+                                _dptr(pool, "pool", torch.uint8), _dptr(boost, "boost", torch.uint8), num_pages,
+                                _stream_ptr(stream))
+    _check("oscar_pages_copy", st)
 
 
 BOOST_N = 8

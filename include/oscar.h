@@ -284,6 +284,56 @@ oscar_status oscar_decode_attn_codebook(const oscar_shape* shape, int32_t batch,
                                         void* workspace, size_t* ws_bytes, int32_t* dev_status, void* stream);
 
 /*
+ * Refcounted history pages with copy-on-write (prefix sharing: [NEWS]
+ * sec. C, the pool works with paged KV and a radix prefix cache).  Host
+ * only, except oscar_pages_copy.  Not thread-safe: one host thread per
+ * allocator.
+ *
+ * Sequences that share a prefix hold the same page ids in their rows of
+ * the page table, one reference each (oscar_pages_retain when a sequence
+ * adopts another's pages; oscar_pages_release when it drops them).  A
+ * prefix need not end on a page boundary: before tokens are evicted into
+ * pages, oscar_pages_prepare_write makes each target page private to its
+ * row, and oscar_pages_copy copies the shared contents into the new pages;
+ * then the caller uploads the changed table rows and evicts as usual.
+ *
+ * oscar_pages_create: num_pages free pages, handed out lowest id first.
+ * oscar_pages_alloc: n fresh pages (one reference each) into pages_out;
+ *   OSCAR_ERR_OUT_OF_PAGES (nothing taken) if fewer than n are free.
+ * oscar_pages_retain / oscar_pages_release: one more / one less reference
+ *   per listed page (duplicates count once each); a page whose count drops
+ *   to 0 is free again.  OSCAR_ERR_INVALID_ARG (nothing changed) for a
+ *   free or out-of-range page, or more releases than references.
+ * oscar_pages_refcount: references of a page (-1 if out of range).
+ * oscar_pages_prepare_write: for each of the n write targets (seq[i],
+ *   page_index[i]) of page_table (host, [batch][max_pages], updated in
+ *   place): an empty entry (-1) gets a fresh page; a page with more than
+ *   one reference is replaced in that row by a fresh page, its reference
+ *   moves there and (old, new) is appended to copy_src / copy_dst (host,
+ *   room for n each; *n_copies = count); a private page is left as is.
+ *   Repeated targets count once.  OSCAR_ERR_OUT_OF_PAGES or
+ *   OSCAR_ERR_INVALID_ARG leave the allocator and the table unchanged.
+ * oscar_pages_copy: for each pair, the Hk pool blocks of page copy_src[i]
+ *   (and, when boost is not NULL, its Hk boost-record blocks) copied to
+ *   page copy_dst[i] on the device, one cudaMemcpyAsync per page and array
+ *   on `stream`; copy_src / copy_dst are host arrays.
+ */
+typedef struct oscar_pages oscar_pages;
+oscar_status oscar_pages_create(int32_t num_pages, oscar_pages** out);
+void oscar_pages_destroy(oscar_pages* pages);
+oscar_status oscar_pages_alloc(oscar_pages* pages, int32_t n, int32_t* pages_out);
+oscar_status oscar_pages_retain(oscar_pages* pages, int32_t n, const int32_t* page_ids);
+oscar_status oscar_pages_release(oscar_pages* pages, int32_t n, const int32_t* page_ids);
+int32_t oscar_pages_refcount(const oscar_pages* pages, int32_t page);
+int32_t oscar_pages_free_count(const oscar_pages* pages);
+oscar_status oscar_pages_prepare_write(oscar_pages* pages, int32_t n, const int32_t* seq, const int32_t* page_index,
+                                       int32_t* page_table, int32_t batch, int32_t max_pages, int32_t* copy_src,
+                                       int32_t* copy_dst, int32_t* n_copies);
+oscar_status oscar_pages_copy(const oscar_shape* shape, int32_t n_copies, const int32_t* copy_src,
+                              const int32_t* copy_dst, uint8_t* pool, uint8_t* boost, int32_t num_pages,
+                              void* stream);
+
+/*
  * K channel precision boost (the "Zhongzhu (Charlie) Zhou" home page,
  * Featured Projects, entry "KITTY: Accurate and Efficient 2-bit KV Cache
  * Quantization with Dynamic Channel-wise Precision Boost": a small fraction
