@@ -136,6 +136,31 @@ def test_boost_eviction_and_decode_match_oracle(g, hq, hk, perm):
     print(f"boost g={g} G={hq // hk}: max-abs {err:.3e} rel-L2 {rel:.3e} exempt records {n_ex}")
 
 
+@pytest.mark.parametrize("hist,hq,hk", [([0, 17, 64, 130], 2, 2), ([1, 63, 65], 4, 1)])
+def test_boost_edge_histories(hist, hq, hk):
+    """Empty, one-token, page-sized and ragged histories, G = 1 and G = 4."""
+    orc, shape, hist, table, npages, nbytes, src, seq, pos, U, clip, bf16_kv, q = _setup(hist, hq, hk, 32, 57)
+    sh, pool_t, boost_t = _evict_gpu(shape, src, seq, pos, U, clip, table, npages, nbytes, len(hist))
+    pool_g, boost_g = pool_t.cpu().numpy(), boost_t.cpu().numpy()
+    pool_o = np.zeros(max(nbytes, 16), np.uint8)
+    boost_o = np.zeros(max(npages * hk * K.BLOCK, 16), np.uint8)
+    aux = K.evict(orc, shape, src, seq, pos, U.astype(np.float64), clip, pool_o, table, table.shape[1], boost_o)
+    items = [(int(seq[i]), int(pos[i]), i) for i in range(seq.size)]
+    H.compare_evicted(pool_g, pool_o, table, items, aux, hk, 32)
+    _check_records(pool_g, pool_o, boost_g, table, seq, pos, aux[0], hk, 32)
+    B_ = len(hist)
+    bf16_len = np.array([S.NSLOT, 5, S.NSLOT, 200][:B_], np.int32)
+    out = torch.zeros((B_, hq, S.D), dtype=torch.float32, device="cuda")
+    ws = torch.zeros(O.oscar_decode_workspace_bytes(sh, B_, table.shape[1]), dtype=torch.uint8, device="cuda")
+    O.oscar_decode_attn_boost(sh, H.bf16_t(q), H.bf16_t(bf16_kv), H.i32_t(bf16_len), pool_t, boost_t,
+                              H.i32_t(table), table.shape[1], npages, H.i32_t(hist), H.f32_t(U), 1 / np.sqrt(S.D),
+                              out, ws)
+    torch.cuda.synchronize()
+    ref = K.decode(orc, shape, q, bf16_kv, bf16_len, pool_g, table, hist, U.astype(np.float64), boost_g,
+                   1 / np.sqrt(S.D))
+    H.assert_close(out.cpu().numpy(), ref)
+
+
 def test_records_without_correction_give_the_uniform_decode():
     """Records whose 4-bit codes equal 5c (written on the host from the
     GPU pool) make oscar_decode_attn_boost equal oscar_decode_attn."""

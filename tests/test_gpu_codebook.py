@@ -116,6 +116,25 @@ def test_codebook_eviction_and_decode_match_oracle(g):
     print(f"codebook g={g}: max-abs {err:.3e} rel-L2 {rel:.3e} exempt codes {exempt}")
 
 
+@pytest.mark.parametrize("hist,hq,hk", [([0, 17, 64, 130], 2, 2), ([1, 63, 65], 4, 1)])
+def test_codebook_edge_histories(hist, hq, hk):
+    """Empty, one-token, page-sized and ragged histories, G = 1 and G = 4."""
+    orc, shape, hist, table, max_pages, npages, nbytes, src, seq, pos, U, clip, bf16_kv, q = _setup(hist, hq, hk, 32, 59)
+    cb = np.array([[0.7, 1.3], [1.2, 0.9]], np.float32)[:hk]
+    sh, pool_t = _evict_gpu(shape, src, seq, pos, U, clip, cb, table, max_pages, npages, nbytes, len(hist))
+    pool_g = pool_t.cpu().numpy()
+    B_ = len(hist)
+    bf16_len = np.array([S.NSLOT, 5, S.NSLOT, 200][:B_], np.int32)
+    out = torch.zeros((B_, hq, S.D), dtype=torch.float32, device="cuda")
+    ws = torch.zeros(O.oscar_decode_workspace_bytes(sh, B_, max_pages), dtype=torch.uint8, device="cuda")
+    O.oscar_decode_attn_codebook(sh, H.bf16_t(q), H.bf16_t(bf16_kv), H.i32_t(bf16_len), pool_t, H.i32_t(table),
+                                 max_pages, npages, H.i32_t(hist), H.f32_t(U), H.f32_t(cb), 1 / np.sqrt(S.D), out, ws)
+    torch.cuda.synchronize()
+    ref = L.decode(q, bf16_kv, bf16_len, pool_g, table, hist, U.astype(np.float64), orc.build_R, cb.astype(np.float64),
+                   1 / np.sqrt(S.D), 32)
+    H.assert_close(out.cpu().numpy(), ref)
+
+
 def test_codebook_one_is_the_uniform_path():
     hist = [900, 400]
     hq, hk = 4, 1
