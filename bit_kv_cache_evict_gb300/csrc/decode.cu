@@ -248,7 +248,7 @@ struct StageInfo {
 template <int NT>
 struct Int2Smem {
     static constexpr int G4 = NT * 4;  // head columns (padded to 4 per n-tile)
-    // per-warp scratch: K s [64] float4 | K z-M s [64] float4 | V z-M s [64]
+    // per-warp scratch: K s [64] float4 | K z [64] float4 | V z [64]
     // float4 | V s [4][72] float (token order pv_pos) | P [G4][72] float
     // (same token order).  Reused at an item's end for
     // the warp's (o', m, l) state [G4][kD + 2].
@@ -445,8 +445,8 @@ __device__ __forceinline__ void attend_page(const uint8_t* blk, int valid, uint8
     const int lane = threadIdx.x & 31, gID = lane >> 2, tq = lane & 3;
     if (FULL) valid = kPage;
     float4* ksS = reinterpret_cast<float4*>(wbuf + SM::kWKs);   // [64] K s
-    float4* kzS = reinterpret_cast<float4*>(wbuf + SM::kWKz);   // [64] K z - M s
-    float4* vzS = reinterpret_cast<float4*>(wbuf + SM::kWVz);   // [64] V z - M s
+    float4* kzS = reinterpret_cast<float4*>(wbuf + SM::kWKz);   // [64] K z
+    float4* vzS = reinterpret_cast<float4*>(wbuf + SM::kWVz);   // [64] V z
     float* vsS = reinterpret_cast<float*>(wbuf + SM::kWVs);     // [4][kPvRow] V s at pv_pos
     float* pS = reinterpret_cast<float*>(wbuf + SM::kWP);       // [G4][kPvRow] P at pv_pos
     const int ntile = FULL ? 4 : (valid + 15) >> 4;             // warp-uniform, 1..4
