@@ -452,6 +452,14 @@ class OracleSample:
         dt = time.perf_counter() - t0
         return toks / dt, dt
 
+    def time_one_thread(self):
+        """One step on a single host thread (the same sample)."""
+        self.orc.set_num_threads(1)
+        try:
+            return self.time(1, 0)
+        finally:
+            self.orc.set_num_threads(self.threads)
+
     def describe(self) -> str:
         return (f"layer 0 of the workload: sequences 0..{self.n - 1} (history {int(self.hist.sum())} tokens, "
                 f"{self.shape.num_q_heads} query / {self.shape.num_kv_heads} KV heads), one eviction per "
@@ -638,8 +646,10 @@ def run_oscar(args, rank: int, world: int, local: int) -> None:
     if rank == 0 and not args.no_cpu:
         samp = OracleSample(w, args.cpu_tokens)
         tps, dt = samp.time(args.cpu_steps, 0)
+        tps1, dt1 = samp.time_one_thread()
         cpu = {"value": tps, "unit": UNIT, "cores": samp.threads, "kind": "oracle",
-               "sample": f"{args.cpu_steps} steps of " + samp.describe(), "seconds": dt, "cpu": cpu_info()}
+               "sample": f"{args.cpu_steps} steps of " + samp.describe(), "seconds": dt, "cpu": cpu_info(),
+               "value_1_thread": tps1, "seconds_1_thread": dt1}
 
     if rank == 0:
         line = {

@@ -8,10 +8,6 @@
 
 namespace oscar {
 
-
-
-// History pages per split-K work item: about 8192 items for the largest
-// request the table allows, between 4 and 64 pages.
 // Pages per split-K item: about 4096 items for the whole batch at most,
 // 16-64 pages each (an item ends with a merge of the four consumer warps'
 // states, so short items pay it per page or two; 16 pages is 4 per warp).
