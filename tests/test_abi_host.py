@@ -104,3 +104,29 @@ def test_argument_checks_before_launch(lib):
     bad = O.make_shape(32, 8, head_dim=96)
     assert lib.oscar_evict_quantize(ctypes.byref(bad), 3, fake, 3, None, fake, fake, None, fake, fake, fake, fake,
                                     1, 1, 1, None, None) == O.OSCAR_ERR_UNSUPPORTED
+
+
+def test_variant_calls_validate_before_launch(lib):
+    """The Lloyd-Max and channel-boost calls reject what they cannot run
+    before touching the GPU: G = 8, a missing codebook or boost array."""
+    fake = ctypes.c_void_p(4096)
+    ws = ctypes.c_size_t(1 << 30)
+    g8 = O.make_shape(64, 8)
+    for fn, extra in (("oscar_decode_attn_codebook", "codebook"), ("oscar_decode_attn_boost", "boost")):
+        f = getattr(lib, fn)
+        if extra == "codebook":
+            args = lambda sh, cb: (ctypes.byref(sh), 4, fake, fake, fake, fake, fake, 10, 1, fake, fake, cb,  # noqa: E731
+                                   ctypes.c_float(1.0), fake, fake, ctypes.byref(ws), None, None)
+        else:
+            args = lambda sh, cb: (ctypes.byref(sh), 4, fake, fake, fake, fake, cb, fake, 10, 1, fake, fake,  # noqa: E731
+                                   ctypes.c_float(1.0), fake, fake, ctypes.byref(ws), None, None)
+        assert f(*args(g8, fake)) == O.OSCAR_ERR_UNSUPPORTED
+        assert f(*args(O.make_shape(32, 8), None)) == O.OSCAR_ERR_INVALID_ARG
+        assert f(*args(O.make_shape(32, 8), ctypes.c_void_p(4098))) == O.OSCAR_ERR_INVALID_ARG   # misaligned
+    sh = O.make_shape(32, 8)
+    assert lib.oscar_evict_quantize_codebook(ctypes.byref(sh), 3, fake, 3, None, fake, fake, None, fake, fake, None,
+                                             fake, fake, 1, 1, 1, None, None) == O.OSCAR_ERR_INVALID_ARG
+    assert lib.oscar_evict_quantize_boost(ctypes.byref(sh), 3, fake, 3, None, fake, fake, None, fake, fake, fake,
+                                          None, fake, 1, 1, 1, None, None) == O.OSCAR_ERR_INVALID_ARG
+    assert lib.oscar_evict_quantize_boost(ctypes.byref(sh), 0, None, 0, None, None, None, None, None, None, None,
+                                          None, None, 1, 1, 1, None, None) == O.OSCAR_OK          # nothing to do
