@@ -46,12 +46,19 @@ using namespace oscar;
 
 extern "C" {
 
+// No C++ exception leaves the C ABI: a failed host allocation is reported as
+// OSCAR_ERR_OUT_OF_PAGES with nothing changed.
 oscar_status oscar_pages_create(int32_t num_pages, oscar_pages** out) {
     if (!out || num_pages < 0) return OSCAR_ERR_INVALID_ARG;
     oscar_pages* a = new (std::nothrow) oscar_pages;
-    if (!a) return OSCAR_ERR_INVALID_ARG;
-    a->ref.assign((size_t)num_pages, 0);
-    a->free.resize((size_t)num_pages);
+    if (!a) return OSCAR_ERR_OUT_OF_PAGES;
+    try {
+        a->ref.assign((size_t)num_pages, 0);
+        a->free.resize((size_t)num_pages);
+    } catch (...) {
+        delete a;
+        return OSCAR_ERR_OUT_OF_PAGES;
+    }
     for (int32_t i = 0; i < num_pages; ++i) a->free[(size_t)i] = num_pages - 1 - i;  // lowest id first
     *out = a;
     return OSCAR_OK;
@@ -80,7 +87,7 @@ oscar_status oscar_pages_retain(oscar_pages* a, int32_t n, const int32_t* pages)
     return OSCAR_OK;
 }
 
-oscar_status oscar_pages_release(oscar_pages* a, int32_t n, const int32_t* pages) {
+oscar_status oscar_pages_release(oscar_pages* a, int32_t n, const int32_t* pages) try {
     if (!a || n < 0 || (n > 0 && !pages)) return OSCAR_ERR_INVALID_ARG;
     std::vector<int32_t> need(a->ref.size(), 0);  // references this call drops, per page
     for (int32_t i = 0; i < n; ++i) {
@@ -89,11 +96,13 @@ oscar_status oscar_pages_release(oscar_pages* a, int32_t n, const int32_t* pages
     }
     for (int32_t i = 0; i < n; ++i) drop(a, pages[i]);
     return OSCAR_OK;
+} catch (...) {
+    return OSCAR_ERR_OUT_OF_PAGES;
 }
 
 oscar_status oscar_pages_prepare_write(oscar_pages* a, int32_t n, const int32_t* seq, const int32_t* page_index,
                                        int32_t* page_table, int32_t batch, int32_t max_pages, int32_t* copy_src,
-                                       int32_t* copy_dst, int32_t* n_copies) {
+                                       int32_t* copy_dst, int32_t* n_copies) try {
     if (!a || n < 0 || !n_copies || batch < 0 || max_pages <= 0) return OSCAR_ERR_INVALID_ARG;
     if (n > 0 && (!seq || !page_index || !page_table || !copy_src || !copy_dst)) return OSCAR_ERR_INVALID_ARG;
     // validate and count the fresh pages needed before changing anything
@@ -134,6 +143,8 @@ oscar_status oscar_pages_prepare_write(oscar_pages* a, int32_t n, const int32_t*
     }
     *n_copies = c;
     return OSCAR_OK;
+} catch (...) {  // the scratch vectors: before any change
+    return OSCAR_ERR_OUT_OF_PAGES;
 }
 
 oscar_status oscar_pages_copy(const oscar_shape* shape, int32_t n_copies, const int32_t* copy_src,

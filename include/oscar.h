@@ -297,7 +297,9 @@ oscar_status oscar_decode_attn_codebook(const oscar_shape* shape, int32_t batch,
  * row, and oscar_pages_copy copies the shared contents into the new pages;
  * then the caller uploads the changed table rows and evicts as usual.
  *
- * oscar_pages_create: num_pages free pages, handed out lowest id first.
+ * oscar_pages_create: num_pages free pages, handed out lowest id first
+ *   (OSCAR_ERR_OUT_OF_PAGES if host memory for the counts runs out; the
+ *   other calls report a failed host allocation the same way, unchanged).
  * oscar_pages_alloc: n fresh pages (one reference each) into pages_out;
  *   OSCAR_ERR_OUT_OF_PAGES (nothing taken) if fewer than n are free.
  * oscar_pages_retain / oscar_pages_release: one more / one less reference
