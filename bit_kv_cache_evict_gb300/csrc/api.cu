@@ -138,7 +138,7 @@ void oscar_time_next_int2(void* ev_start, void* ev_stop) {
 oscar_status oscar_pool_layout(const oscar_shape* shape, int32_t batch, const int32_t* hist_capacity,
                                const int32_t* prefix_group, int32_t shared_hist_tokens, uint64_t perm_seed,
                                int32_t max_pages, int32_t* page_table, int32_t* num_pages_out,
-                               uint64_t* pool_bytes_out) {
+                               uint64_t* pool_bytes_out) try {
     const oscar_status sst = check_shape(shape);
     if (sst != OSCAR_OK) return sst;
     if (batch < 0 || max_pages <= 0 || (batch > 0 && (!hist_capacity || !page_table)))
@@ -196,6 +196,8 @@ oscar_status oscar_pool_layout(const oscar_shape* shape, int32_t batch, const in
     if (pool_bytes_out)
         *pool_bytes_out = (uint64_t)next * (uint64_t)shape->num_kv_heads * (uint64_t)block_bytes_of(shape);
     return OSCAR_OK;
+} catch (...) {  // host scratch allocation: nothing was written
+    return OSCAR_ERR_OUT_OF_PAGES;
 }
 
 static oscar_status evict_impl(const oscar_shape* shape, int32_t n_tok, const void* src_kv, int32_t src_rows,
