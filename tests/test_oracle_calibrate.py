@@ -136,3 +136,34 @@ def test_clip_search_prefers_clipping_a_lone_outlier():
     clip, mse = C.clip_search(kv, np.eye(D)[None, None].repeat(2, axis=1), [0.3, 0.6, 1.0])
     assert clip[0, 0] < 1.0
     assert mse[0, 0, 2] > mse[0, 0, list([0.3, 0.6, 1.0]).index(clip[0, 0])]
+
+
+def test_two_token_attention_is_a_logistic_mix():
+    # two keys: the output is v0 + sigmoid(sm (q.k1 - q.k0)) (v1 - v0)
+    rng = np.random.default_rng(21)
+    q = rng.standard_normal((3, 1, D))
+    k = rng.standard_normal((2, 1, D))
+    v = rng.standard_normal((2, 1, D))
+    sm = 0.37
+    o = C.attention_outputs(q, k, v, sm)
+    for n in range(3):
+        lam = 1.0 / (1.0 + np.exp(-sm * (q[n, 0] @ k[1, 0] - q[n, 0] @ k[0, 0])))
+        assert np.allclose(o[n, 0], v[0, 0] + lam * (v[1, 0] - v[0, 0]), atol=1e-12)
+
+
+def test_value_rotation_of_uniform_attention_is_the_mean_value():
+    # identical keys: every output is the mean value m, so C_V = m m^T and the
+    # first column of U_V is m / |m| (sign convention: largest entry positive)
+    # with eigenvalue |m|^2
+    rng = np.random.default_rng(22)
+    n_t = 50
+    kv = np.zeros((n_t, 1, 2, D))
+    kv[:, 0, 0, :] = rng.standard_normal(D)             # the same key for every token
+    kv[:, 0, 1, :] = rng.standard_normal((n_t, D)) + 0.5
+    q = rng.standard_normal((7, 2, D))
+    U, lam = C.calibrate(q, kv, 0.2)
+    m = kv[:, 0, 1, :].mean(axis=0)
+    u0 = m / np.linalg.norm(m)
+    u0 = u0 if u0[np.argmax(np.abs(u0))] > 0 else -u0
+    assert np.allclose(U[0, 1, :, 0], u0, atol=1e-9)
+    assert np.isclose(lam[0, 1, 0], m @ m, rtol=1e-10)
