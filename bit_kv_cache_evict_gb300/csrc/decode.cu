@@ -236,7 +236,11 @@ __device__ __forceinline__ void prep_body(const DecodeParams& p) {
 // exits.
 constexpr int kConsumerWarps = 4;
 constexpr int kStages = 2 * kConsumerWarps;
-constexpr int kWaitPolls = 1 << 22;
+// Poll budget of every bounded mbarrier wait: a try_wait suspends about 4 us
+// when the phase is not complete (measured on GB300), so 2^18 polls give up
+// after about a second, far beyond any legitimate wait (a page copy, or the
+// other consumer warps finishing an item).
+constexpr int kWaitPolls = 1 << 18;
 constexpr int kInt2Threads = (kConsumerWarps + 1) * 32;
 constexpr int kFlagFirst = 1, kFlagLast = 2, kFlagPad = 4;
 
