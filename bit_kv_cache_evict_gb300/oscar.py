@@ -75,6 +75,18 @@ def lib() -> ctypes.CDLL:
         L.oscar_pages_prepare_write.argtypes = [_P, I32, _P, _P, _P, I32, I32, _P, _P, _P]
         L.oscar_pages_copy.restype = ctypes.c_int
         L.oscar_pages_copy.argtypes = [S, I32, _P, _P, _P, _P, I32, _P]
+        L.oscar_radix_create.restype = ctypes.c_int
+        L.oscar_radix_create.argtypes = [_P, PP]
+        L.oscar_radix_destroy.restype = None
+        L.oscar_radix_destroy.argtypes = [_P]
+        L.oscar_radix_insert.restype = ctypes.c_int
+        L.oscar_radix_insert.argtypes = [_P, _P, I32, _P, I32]
+        L.oscar_radix_match.restype = ctypes.c_int
+        L.oscar_radix_match.argtypes = [_P, _P, I32, I32, _P, _P]
+        L.oscar_radix_evict.restype = ctypes.c_int
+        L.oscar_radix_evict.argtypes = [_P, I32, _P]
+        L.oscar_radix_cached_pages.restype = I32
+        L.oscar_radix_cached_pages.argtypes = [_P]
         L.oscar_evict_quantize.restype = ctypes.c_int
         L.oscar_evict_quantize.argtypes = [S, ctypes.c_int32, _P, ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P, _P,
                                            ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, _P]
@@ -393,6 +405,49 @@ class Pages:
                                              page_table.shape[1], _np_ptr(src), _np_ptr(dst), ctypes.byref(n))
         _check("oscar_pages_prepare_write", st)
         return src[:n.value].copy(), dst[:n.value].copy()
+
+
+class Radix:
+    """Radix prefix cache over history pages (the C ABI's oscar_radix_*; see
+    include/oscar.h).  Keeps a reference to its Pages allocator."""
+
+    def __init__(self, pages: Pages):
+        h = ctypes.c_void_p()
+        _check("oscar_radix_create", lib().oscar_radix_create(pages._h, ctypes.byref(h)))
+        self._h, self.pages = h, pages
+
+    def close(self) -> None:
+        if self._h:
+            lib().oscar_radix_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def insert(self, tokens, pages) -> None:
+        t, p = _host_i32(tokens), _host_i32(pages)
+        _check("oscar_radix_insert", lib().oscar_radix_insert(self._h, _np_ptr(t), t.size, _np_ptr(p), p.size))
+
+    def match(self, tokens, max_pages: int):
+        """Page ids of the longest cached prefix (one reference each for the caller)."""
+        import numpy as np
+        t = _host_i32(tokens)
+        out = np.zeros(max(int(max_pages), 1), np.int32)
+        n = ctypes.c_int32(0)
+        _check("oscar_radix_match", lib().oscar_radix_match(self._h, _np_ptr(t), t.size, int(max_pages),
+                                                            _np_ptr(out), ctypes.byref(n)))
+        return out[:n.value].copy()
+
+    def evict(self, n_pages: int) -> int:
+        n = ctypes.c_int32(0)
+        _check("oscar_radix_evict", lib().oscar_radix_evict(self._h, int(n_pages), ctypes.byref(n)))
+        return int(n.value)
+
+    def cached_pages(self) -> int:
+        return int(lib().oscar_radix_cached_pages(self._h))
 
 
 def oscar_pages_copy(shape: oscar_shape, copy_src, copy_dst, pool, boost, num_pages: int, stream=None) -> None:

@@ -336,6 +336,42 @@ oscar_status oscar_pages_copy(const oscar_shape* shape, int32_t n_copies, const 
                               void* stream);
 
 /*
+ * Radix prefix cache over history pages ([NEWS] sec. C: the pool works with
+ * a radix prefix cache; sec. D: the decode gain is largest at a full prefix
+ * hit).  Host only, on top of an oscar_pages allocator (not owned; it must
+ * outlive the cache).  Not thread-safe.
+ *
+ * A context (token ids) is cut into 64-token chunks: chunk 0 is the BF16
+ * sink (no page), chunk i >= 1 is INT2 history page i - 1.  A token's K/V
+ * depend on every token before it, so a page is reused only under the same
+ * chain of chunks from the start: the tree's paths are token sequences and
+ * each node below the sink level holds the page of its chunk, with one page
+ * reference of its own.  Only whole chunks are cached.
+ *
+ * oscar_radix_insert: caches the first n_pages history pages of a context
+ *   (tokens[n_tokens], n_tokens >= 64 * (1 + n_pages); pages[i] = the page
+ *   holding history page i, allocated).  Chunks already cached keep their
+ *   page; new nodes take one reference each.
+ * oscar_radix_match: the longest cached prefix of tokens, in whole chunks:
+ *   up to max_pages page ids of history pages 0, 1, ... into pages_out,
+ *   *n_pages_out = count (0 if even the sink chunk differs); the caller
+ *   receives one reference per returned page (release them when done).
+ * oscar_radix_evict: removes least-recently-used leaves whose page nobody
+ *   but the cache holds, freeing up to n_pages pages; *n_freed = count.
+ * oscar_radix_cached_pages: pages held by the cache.
+ * oscar_radix_destroy: drops the cache's references.
+ */
+typedef struct oscar_radix oscar_radix;
+oscar_status oscar_radix_create(oscar_pages* pages, oscar_radix** out);
+void oscar_radix_destroy(oscar_radix* radix);
+oscar_status oscar_radix_insert(oscar_radix* radix, const int32_t* tokens, int32_t n_tokens, const int32_t* pages,
+                                int32_t n_pages);
+oscar_status oscar_radix_match(oscar_radix* radix, const int32_t* tokens, int32_t n_tokens, int32_t max_pages,
+                               int32_t* pages_out, int32_t* n_pages_out);
+oscar_status oscar_radix_evict(oscar_radix* radix, int32_t n_pages, int32_t* n_freed);
+int32_t oscar_radix_cached_pages(const oscar_radix* radix);
+
+/*
  * K channel precision boost (the "Zhongzhu (Charlie) Zhou" home page,
  * Featured Projects, entry "KITTY: Accurate and Efficient 2-bit KV Cache
  * Quantization with Dynamic Channel-wise Precision Boost": a small fraction
