@@ -747,7 +747,7 @@ def run_calibrate(args, rank: int) -> None:
         "metric": "offline rotation calibration time per layer", "value": ms, "unit": "ms",
         "higher_is_better": False, "n_gpus": 1, "steps": args.steps, "warmup": max(args.warmup, 3),
         "dtype": "f32", "data": "synthetic", "config": cfg, "vs_baseline": None,
-        "status": int(status.item()), "attention_tflops": flops / (ms * 1e-3) / 1e12,
+        "status": int(status.item()), "attention_gflop": flops / 1e9,
         "clip_search_ms": clip_ms, "clip_candidates": int(grid_np.size),
         "clips_chosen": sorted(set(float(c) for c in clip_t.cpu().numpy().ravel())),
         "cpu_baseline": {"value": cpu_s * 1e3, "unit": "ms", "cores": os.cpu_count(), "kind": "oracle",

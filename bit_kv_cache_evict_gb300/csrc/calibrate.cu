@@ -182,13 +182,14 @@ __device__ __forceinline__ void rr_pair(int r, int k, int& pp, int& qq) {
     }
 }
 
-// C: [nmat][kD][kD] sums, scaled by inv_count.  Matrix m of the launch is
-// C + m * kD * kD; its eigenvectors go to U + m * ustride (column j =
-// eigenvector j, row-major kD x kD) and its eigenvalues to lam + m * lstride
-// (lam may be null).
+// C: sums of kD x kD matrices, scaled by inv_count.  Block (x, y) takes
+// matrix C + x * kD * kD + y * c_y; its eigenvectors go to U + x * ustride +
+// y * u_y (column j = eigenvector j, row-major kD x kD) and its eigenvalues
+// to lam + x * lstride + y * l_y (lam may be null).  One launch serves the K
+// (y = 0) and V (y = 1) matrices of every KV head.
 __global__ void __launch_bounds__(kEigThreads) calib_eig_kernel(const float* C, float inv_count, float* U,
                                                                 size_t ustride, float* lam, size_t lstride,
-                                                                int* status) {
+                                                                int* status, size_t c_y, size_t u_y, size_t l_y) {
     extern __shared__ __align__(16) float esm[];
     float* A = esm;                      // [kD][kEigLd]
     float* V = A + kD * kEigLd;          // [kD][kEigLd]
@@ -201,7 +202,7 @@ __global__ void __launch_bounds__(kEigThreads) calib_eig_kernel(const float* C, 
     float* red = d2 + 64;                // [kD] reduction scratch
     int* rank = reinterpret_cast<int*>(red + kD);   // [kD]
     const int tid = threadIdx.x;
-    const size_t mo = (size_t)blockIdx.x * kD * kD;
+    const size_t mo = (size_t)blockIdx.x * kD * kD + blockIdx.y * c_y;
     for (int e = tid; e < kD * kD; e += kEigThreads) {
         const int i = e / kD, j = e % kD;
         // symmetrise the accumulated sums (the atomics add in any order)
@@ -318,9 +319,9 @@ __global__ void __launch_bounds__(kEigThreads) calib_eig_kernel(const float* C, 
         }
         const float sg = V[imax * kEigLd + tid] < 0.f ? -1.f : 1.f;
         const int col = rank[tid];
-        float* Um = U + blockIdx.x * ustride;
+        float* Um = U + blockIdx.x * ustride + blockIdx.y * u_y;
         for (int i = 0; i < kD; ++i) Um[(size_t)i * kD + col] = sg * V[i * kEigLd + tid];
-        if (lam) lam[blockIdx.x * lstride + col] = A[tid * kEigLd + tid];
+        if (lam) lam[blockIdx.x * lstride + blockIdx.y * l_y + col] = A[tid * kEigLd + tid];
     }
 }
 
@@ -668,10 +669,8 @@ cudaError_t launch_calibrate(const CalibParams& p, cudaStream_t st) {
     }
     // outputs in the [hk][2] (K, V) layout of U and lam
     const float inv = 1.f / (float)(p.n_q * g);
-    calib_eig_kernel<<<p.hk, kEigThreads, kEigSmem, st>>>(p.C, inv, p.U, 2 * mat, p.lam, 2 * kD, p.status);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    calib_eig_kernel<<<p.hk, kEigThreads, kEigSmem, st>>>(p.C + (size_t)p.hk * mat, inv, p.U + mat, 2 * mat,
-                                                          p.lam ? p.lam + kD : nullptr, 2 * kD, p.status);
+    calib_eig_kernel<<<dim3(p.hk, 2), kEigThreads, kEigSmem, st>>>(p.C, inv, p.U, 2 * mat, p.lam, 2 * kD, p.status,
+                                                                   (size_t)p.hk * mat, mat, kD);
     return cudaGetLastError();
 }
 
