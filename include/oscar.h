@@ -38,6 +38,23 @@
  *   - Only head_dim 128, quant_group 32, 64 or 128, page_size 64 and
  *     query-per-KV-head groups G = Hq/Hk in {1, 2, 4, 8} are supported;
  *     other shapes return OSCAR_ERR_UNSUPPORTED.
+ *   - The host-side page allocator and prefix cache (oscar_pages,
+ *     oscar_radix) are opaque objects the caller creates and destroys; they
+ *     hold host memory only.  No C++ exception crosses this interface.
+ *
+ * Calls, in the order of this header
+ *   oscar_pool_layout                      static page layout (host)
+ *   oscar_evict_quantize                   fused rotate/clip/quantise/pack
+ *   oscar_decode_attn, _noalloc            decode attention over the pool
+ *   oscar_evict_quantize_codebook,
+ *   oscar_decode_attn_codebook             Lloyd-Max levels variant
+ *   oscar_pages_*                          refcounted copy-on-write pages
+ *   oscar_radix_*                          radix prefix cache over pages
+ *   oscar_evict_quantize_boost,
+ *   oscar_decode_attn_boost                K channel precision boost
+ *   oscar_calibrate_codebook               offline fit of the Lloyd-Max levels
+ *   oscar_calibrate_rotation               offline U_K, U_V
+ *   oscar_calibrate_clip                   offline clip ratios
  *
  * Data layouts (row-major, little-endian)
  *   K/V token rows   bf16 [rows][Hk][2][d]           (index 0 = K, 1 = V)
