@@ -97,8 +97,7 @@ def parse_args():
                     help="Lloyd-Max levels {0, A, 3-A, 3} for every head (up to four query heads per KV head) "
                          "instead of the uniform grid")
     ap.add_argument("--boost", action="store_true",
-                    help="K channel precision boost: eight positions per K token-vector at 4 bits (up to four "
-                         "query heads per KV head)")
+                    help="K channel precision boost: eight positions per K token-vector at 4 bits")
     ap.add_argument("--quant-group", type=int, default=32, choices=[32, 64, 128],
                     help="stored positions per fp16 scale/zero pair (32 is the configured format)")
     return ap.parse_args()

@@ -86,7 +86,7 @@ static WsLayout ws_layout(const oscar_shape* s, int batch, int max_pages) {
     w.qsum = off;
     off = round_up(off + (size_t)batch * hk * w.NT * 4 * 4 * 4, 256);
     w.qrot = off;
-    off = round_up(off + (size_t)batch * hk * 4 * kD * 4, 256);
+    off = round_up(off + (size_t)batch * hk * w.NT * 4 * kD * 4, 256);
     w.part = off;
     off = round_up(off + (size_t)w.max_items * w.part_stride * 4, 256);
     w.bf_part = off;
@@ -359,7 +359,6 @@ oscar_status oscar_decode_attn_boost(const oscar_shape* shape, int32_t batch, co
                                      void* workspace, size_t* ws_bytes, int32_t* dev_status, void* stream) {
     const oscar_status sst = check_shape(shape);
     if (sst != OSCAR_OK) return sst;
-    if (shape->num_q_heads / shape->num_kv_heads > 4) return OSCAR_ERR_UNSUPPORTED;
     if (workspace && batch > 0 && num_pages > 0 && (!boost || !aligned(boost, 16))) return OSCAR_ERR_INVALID_ARG;
     return decode_impl(shape, batch, q, bf16_kv, bf16_len, pool, page_table, max_pages, num_pages, hist_len, U,
                        nullptr, boost, sm_scale, out, workspace, ws_bytes, dev_status, stream);

@@ -136,7 +136,8 @@ __device__ __forceinline__ void prep_body(const DecodeParams& p) {
             }
             if (lane < 4) qsum[lane] = 0.f;
             if (p.boost)
-                *reinterpret_cast<float4*>(p.qrot + ((size_t)bk * 4 + hl) * kD + 4 * lane) = make_float4(0.f, 0.f, 0.f, 0.f);
+                *reinterpret_cast<float4*>(p.qrot + ((size_t)bk * p.NT * 4 + hl) * kD + 4 * lane) =
+                    make_float4(0.f, 0.f, 0.f, 0.f);
             continue;
         }
         const int h = kv * p.G + hl;
@@ -177,8 +178,8 @@ __device__ __forceinline__ void prep_body(const DecodeParams& p) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) qs[32 * bitrev2(k) + r5] = y[k] * scale;  // stored order
         __syncwarp();
-        if (p.boost)  // q' itself for the boost corrections (NT = 1: heads 0..3)
-            *reinterpret_cast<float4*>(p.qrot + ((size_t)bk * 4 + hl) * kD + 4 * lane) =
+        if (p.boost)  // q' itself for the boost corrections
+            *reinterpret_cast<float4*>(p.qrot + ((size_t)bk * p.NT * 4 + hl) * kD + 4 * lane) =
                 *reinterpret_cast<const float4*>(qs + 4 * lane);
 
         // group sums of the split values (exactly what the MMA multiplies)
@@ -271,7 +272,7 @@ struct Int2Smem {
     // Lloyd-Max levels: kappa q' fragments of the high-bit plane follow q';
     // channel boost: q' [kD] float4 (four heads) there instead
     static constexpr int kBytesLM = kBytes + NT * 8 * 32 * 8;
-    static_assert(NT * 8 * 32 * 8 >= kD * 16, "room for the boost's q'");
+    static_assert(NT * 8 * 32 * 8 >= kD * NT * 16, "room for the boost's q'");
 };
 
 __device__ __forceinline__ int find_seq(const int32_t* item_start, int B, int item) {
@@ -704,11 +705,12 @@ __device__ __forceinline__ void split_both(float2 w, uint32_t& hi, uint32_t& lo)
 // heads, and the hi / lo parts of q' and of P*s enter as two MMAs on the
 // same A fragment (accumulating into the same registers).  Lane (gID, tq)
 // holds heads 2tq and 2tq + 1.
-template <bool FULL>
+template <bool FULL, bool BOOST = false>
 __device__ __forceinline__ void attend_page_g8(const uint8_t* blk, int valid, uint8_t* wbuf, const uint2* qfS,
                                                const float4 (&qsv)[2], float (&m_run)[2], float (&l_run)[2],
                                                float (&zacc)[2][4], float (&acc_o)[8][4],
-                                               int gshift) {
+                                               int gshift, const float4* qbS = nullptr,
+                                               const uint8_t* brec = nullptr) {
     using SM = Int2Smem<2>;
     const int lane = threadIdx.x & 31, gID = lane >> 2, tq = lane & 3;
     if (FULL) valid = kPage;
@@ -718,6 +720,11 @@ __device__ __forceinline__ void attend_page_g8(const uint8_t* blk, int valid, ui
     float* vsS = reinterpret_cast<float*>(wbuf + SM::kWVs);
     float* pS = reinterpret_cast<float*>(wbuf + SM::kWP);       // [8 heads][kPvRow]
     const int ntile = FULL ? 4 : (valid + 15) >> 4;
+    uint4 br0 = make_uint4(0u, 0u, 0u, 0u), br1 = br0;         // boost records of tokens 2 lane, 2 lane + 1
+    if constexpr (BOOST) {
+        br0 = __ldg(reinterpret_cast<const uint4*>(brec) + 2 * lane);
+        br1 = __ldg(reinterpret_cast<const uint4*>(brec) + 2 * lane + 1);
+    }
 
     page_scales<FULL>(blk, valid, gshift, ksS, kzS, vzS, vsS);
     __syncwarp();
@@ -773,6 +780,53 @@ __device__ __forceinline__ void attend_page_g8(const uint8_t* blk, int valid, ui
             lg[m][2] = vb ? xb0 : -INFINITY;
             lg[m][3] = vb ? xb1 : -INFINITY;
         }
+    }
+
+    // -- channel boost: as attend_page, for eight heads (q' of a position is
+    //    two float4); corrections [64][8] in the P scratch
+    if constexpr (BOOST) {
+        float4* cS = reinterpret_cast<float4*>(pS);
+        const int ng = 4 >> gshift;
+#pragma unroll
+        for (int tt = 0; tt < 2; ++tt) {
+            const int t = 2 * lane + tt;
+            const uint4 rr = tt ? br1 : br0;
+            float4 c0 = make_float4(0.f, 0.f, 0.f, 0.f), c1 = c0;
+            if (t < valid) {
+                const uint32_t* szw = reinterpret_cast<const uint32_t*>(blk + kKScale + t * 4 * ng);
+                const uint32_t wv[4] = {rr.x, rr.y, rr.z, rr.w};
+#pragma unroll
+                for (int e = 0; e < kBoostN; ++e) {
+                    const uint32_t ent = wv[e >> 1] >> (16 * (e & 1));
+                    const int pos = ent & 127;
+                    const float sg = __half2float(__ushort_as_half((unsigned short)(szw[pos >> (5 + gshift)] & 0xffffu)));
+                    const float d = sg * fmaf((float)((ent >> 8) & 15u), 0.2f, -(float)((ent >> 12) & 3u));
+                    const float4 qa = qbS[2 * pos], qb = qbS[2 * pos + 1];
+                    c0.x = fmaf(d, qa.x, c0.x);
+                    c0.y = fmaf(d, qa.y, c0.y);
+                    c0.z = fmaf(d, qa.z, c0.z);
+                    c0.w = fmaf(d, qa.w, c0.w);
+                    c1.x = fmaf(d, qb.x, c1.x);
+                    c1.y = fmaf(d, qb.y, c1.y);
+                    c1.z = fmaf(d, qb.z, c1.z);
+                    c1.w = fmaf(d, qb.w, c1.w);
+                }
+            }
+            cS[2 * t] = c0;
+            cS[2 * t + 1] = c1;
+        }
+        __syncwarp();
+        const float2* cf = reinterpret_cast<const float2*>(pS);  // [64][4] pairs: heads (2tq, 2tq + 1) at index tq
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int ta = 16 * m + gID;
+            const float2 ca = cf[ta * 4 + tq], cb = cf[(ta + 8) * 4 + tq];
+            lg[m][0] += ca.x;
+            lg[m][1] += ca.y;
+            lg[m][2] += cb.x;
+            lg[m][3] += cb.y;
+        }
+        __syncwarp();
     }
 
     // -- online softmax per head (j: head 2tq + j)
@@ -1008,15 +1062,15 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
                     qfS[(nt * 8 + ks) * 32 + lane] = f;
                     if (LM) qfS[((NT + nt) * 8 + ks) * 32 + lane] = scaled_fragment(f, cbk.kk, (lane >> 2) & 1);
                 }
-                if constexpr (BOOST) {  // q'[j] of heads 0..3 as one float4 per stored position j
-                    const float* qr = p.qrot + (size_t)bk * 4 * kD + 4 * lane;
+                if constexpr (BOOST) {  // q'[j] of heads 4nt..4nt+3 as float4 NT * j + nt
+                    const float* qr = p.qrot + ((size_t)bk * NT + nt) * 4 * kD + 4 * lane;
                     const float4 a0 = *reinterpret_cast<const float4*>(qr), a1 = *reinterpret_cast<const float4*>(qr + kD);
                     const float4 a2 = *reinterpret_cast<const float4*>(qr + 2 * kD);
                     const float4 a3 = *reinterpret_cast<const float4*>(qr + 3 * kD);
-                    qbS[4 * lane + 0] = make_float4(a0.x, a1.x, a2.x, a3.x);
-                    qbS[4 * lane + 1] = make_float4(a0.y, a1.y, a2.y, a3.y);
-                    qbS[4 * lane + 2] = make_float4(a0.z, a1.z, a2.z, a3.z);
-                    qbS[4 * lane + 3] = make_float4(a0.w, a1.w, a2.w, a3.w);
+                    qbS[NT * (4 * lane + 0) + nt] = make_float4(a0.x, a1.x, a2.x, a3.x);
+                    qbS[NT * (4 * lane + 1) + nt] = make_float4(a0.y, a1.y, a2.y, a3.y);
+                    qbS[NT * (4 * lane + 2) + nt] = make_float4(a0.z, a1.z, a2.z, a3.z);
+                    qbS[NT * (4 * lane + 3) + nt] = make_float4(a0.w, a1.w, a2.w, a3.w);
                 }
                 // head of the lane's column: 4nt + tq (up to four heads), 2tq + nt (eight)
                 const int hq = (NT == 2) ? 2 * tq + nt : 4 * nt + tq;
@@ -1033,14 +1087,16 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
         }
 
         if (!(flags & kFlagPad)) {
+            const uint8_t* brec = nullptr;
+            if constexpr (BOOST) brec = p.boost + ((size_t)info[s].pid * p.hk + sraw.z) * kBoostBlock;
             if constexpr (NT == 2) {
                 if (valid == kPage)
-                    attend_page_g8<true>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o[0], p.gshift);
+                    attend_page_g8<true, BOOST>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o[0], p.gshift,
+                                                qbS, brec);
                 else
-                    attend_page_g8<false>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o[0], p.gshift);
+                    attend_page_g8<false, BOOST>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o[0],
+                                                 p.gshift, qbS, brec);
             } else {
-                const uint8_t* brec = nullptr;
-                if constexpr (BOOST) brec = p.boost + ((size_t)info[s].pid * p.hk + sraw.z) * kBoostBlock;
                 if (valid == kPage)
                     attend_page<NT, true, LM, BOOST>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o,
                                                      take_lo, p.gshift, cbk, qbS, brec);
@@ -1615,7 +1671,8 @@ __global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(DecodeParams p)
 // ---------------------------------------------------------------------------
 struct Int2Attr {
     int sms = 0;
-    bool set1 = false, set2 = false, setl = false, setk = false, setm = false, setp = false, setb = false;
+    bool set1 = false, set2 = false, setl = false, setk = false, setk2 = false, setm = false, setp = false,
+         setb = false;
 };
 
 static Int2Attr& attr_for_device(int dev) {
@@ -1678,8 +1735,9 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st, cudaEvent_t ev
     if (ev_int2_start && (e = cudaEventRecord(ev_int2_start, st)) != cudaSuccess) return e;
     if (p.codebook)  // Lloyd-Max levels (up to four query heads per KV head)
         e = launch_int2<1, true>(p, st, at.sms, at.setl);
-    else if (p.boost)  // K channel boost (up to four query heads per KV head)
-        e = launch_int2<1, false, true>(p, st, at.sms, at.setk);
+    else if (p.boost)  // K channel boost
+        e = (p.NT == 1) ? launch_int2<1, false, true>(p, st, at.sms, at.setk)
+                        : launch_int2<2, false, true>(p, st, at.sms, at.setk2);
     else
         e = (p.NT == 1) ? launch_int2<1>(p, st, at.sms, at.set1) : launch_int2<2>(p, st, at.sms, at.set2);
     if (e != cudaSuccess) return e;

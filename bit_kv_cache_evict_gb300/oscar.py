@@ -486,8 +486,8 @@ def oscar_evict_quantize_boost(shape: oscar_shape, src_kv, dst_seq, dst_pos, U, 
 def oscar_decode_attn_boost(shape: oscar_shape, q, bf16_kv, bf16_len, pool, boost, page_table, max_pages: int,
                             num_pages: int, hist_len, U, sm_scale: float, out, workspace, dev_status=None,
                             stream=None) -> None:
-    """oscar_decode_attn with the boosted K values; G <= 4.  The workspace
-    size is oscar_decode_workspace_bytes's."""
+    """oscar_decode_attn with the boosted K values.  The workspace size is
+    oscar_decode_workspace_bytes's."""
     import torch
     B = int(q.shape[0])
     ws = ctypes.c_size_t(int(workspace.numel()))

@@ -411,10 +411,10 @@ int32_t oscar_radix_cached_pages(const oscar_radix* radix);
  *          the records of the history tokens only.
  *
  * oscar_evict_quantize_boost: oscar_evict_quantize plus the K records.
- * oscar_decode_attn_boost: oscar_decode_attn with the boosted K values;
- *   query groups G = Hq/Hk of at most 4 (OSCAR_ERR_UNSUPPORTED otherwise).
- *   The corrections q'[pos] * s * (q4 / 5 - c) are added to the logits of
- *   the INT2 kernel; everything else is the uniform path.
+ * oscar_decode_attn_boost: oscar_decode_attn with the boosted K values
+ *   (every supported G).  The corrections q'[pos] * s * (q4 / 5 - c) are
+ *   added to the logits of the INT2 kernel; everything else is the uniform
+ *   path.
  */
 #define OSCAR_BOOST_N 8
 #define OSCAR_BOOST_BLOCK_BYTES 1024 /* 64 tokens x 8 entries x 2 bytes */

@@ -107,7 +107,7 @@ def _check_records(pool_g, pool_o, boost_g, table, seq, pos, u, hk, g):
     return exempt
 
 
-@pytest.mark.parametrize("g,hq,hk,perm", [(32, 8, 2, 0), (128, 8, 2, 7), (64, 4, 2, 0)])
+@pytest.mark.parametrize("g,hq,hk,perm", [(32, 8, 2, 0), (128, 8, 2, 7), (64, 4, 2, 0), (32, 16, 2, 3)])
 def test_boost_eviction_and_decode_match_oracle(g, hq, hk, perm):
     hist = [700, 1300, 2050]
     orc, shape, hist, table, npages, nbytes, src, seq, pos, U, clip, bf16_kv, q = _setup(hist, hq, hk, g, 51, perm)
