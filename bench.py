@@ -94,8 +94,7 @@ def parse_args():
                     help="time the offline rotation calibration (oscar_calibrate_rotation) instead of a decode "
                          "step: one JSON line, the float64 oracle timed on the same inputs")
     ap.add_argument("--codebook", type=float, default=None, metavar="A",
-                    help="Lloyd-Max levels {0, A, 3-A, 3} for every head (up to four query heads per KV head) "
-                         "instead of the uniform grid")
+                    help="Lloyd-Max levels {0, A, 3-A, 3} for every head instead of the uniform grid")
     ap.add_argument("--boost", action="store_true",
                     help="K channel precision boost: eight positions per K token-vector at 4 bits")
     ap.add_argument("--quant-group", type=int, default=32, choices=[32, 64, 128],

@@ -371,7 +371,6 @@ oscar_status oscar_decode_attn_codebook(const oscar_shape* shape, int32_t batch,
                                         void* workspace, size_t* ws_bytes, int32_t* dev_status, void* stream) {
     const oscar_status sst = check_shape(shape);
     if (sst != OSCAR_OK) return sst;
-    if (shape->num_q_heads / shape->num_kv_heads > 4) return OSCAR_ERR_UNSUPPORTED;
     if (workspace && (!codebook || !aligned(codebook, 4))) return OSCAR_ERR_INVALID_ARG;
     return decode_impl(shape, batch, q, bf16_kv, bf16_len, pool, page_table, max_pages, num_pages, hist_len, U,
                        codebook, nullptr, sm_scale, out, workspace, ws_bytes, dev_status, stream);

@@ -705,12 +705,12 @@ __device__ __forceinline__ void split_both(float2 w, uint32_t& hi, uint32_t& lo)
 // heads, and the hi / lo parts of q' and of P*s enter as two MMAs on the
 // same A fragment (accumulating into the same registers).  Lane (gID, tq)
 // holds heads 2tq and 2tq + 1.
-template <bool FULL, bool BOOST = false>
+template <bool FULL, bool BOOST = false, bool LM = false>
 __device__ __forceinline__ void attend_page_g8(const uint8_t* blk, int valid, uint8_t* wbuf, const uint2* qfS,
                                                const float4 (&qsv)[2], float (&m_run)[2], float (&l_run)[2],
                                                float (&zacc)[2][4], float (&acc_o)[8][4],
                                                int gshift, const float4* qbS = nullptr,
-                                               const uint8_t* brec = nullptr) {
+                                               const uint8_t* brec = nullptr, const Codebook& cbk = {}) {
     using SM = Int2Smem<2>;
     const int lane = threadIdx.x & 31, gID = lane >> 2, tq = lane & 3;
     if (FULL) valid = kPage;
@@ -726,7 +726,8 @@ __device__ __forceinline__ void attend_page_g8(const uint8_t* blk, int valid, ui
         br1 = __ldg(reinterpret_cast<const uint4*>(brec) + 2 * lane + 1);
     }
 
-    page_scales<FULL>(blk, valid, gshift, ksS, kzS, vzS, vsS);
+    if constexpr (LM) page_scales<FULL>(blk, valid, gshift, ksS, kzS, vzS, vsS, cbk.ka, cbk.va);
+    else page_scales<FULL>(blk, valid, gshift, ksS, kzS, vzS, vsS);
     __syncwarp();
 
     // -- logits: lg[m] = (token a, head 2tq), (a, 2tq+1), (b, 2tq), (b, 2tq+1)
@@ -750,16 +751,33 @@ __device__ __forceinline__ void attend_page_g8(const uint8_t* blk, int valid, ui
 #pragma unroll
             for (int it = 0; it < 8; ++it) {
                 const int h = it >> 2, g = it & 3, ks = 2 * g + h;
-                uint32_t a0, a1, a2, a3;
+                uint32_t a0, a1, a2, a3, c0 = 0, c1 = 0, c2 = 0, c3 = 0;
                 switch (g) {
-                    case 0: k_operands<0>(wa[h], wb[h], wa8[h], wb8[h], a0, a1, a2, a3); break;
-                    case 1: k_operands<1>(wa[h], wb[h], wa8[h], wb8[h], a0, a1, a2, a3); break;
-                    case 2: k_operands<2>(wa[h], wb[h], wa8[h], wb8[h], a0, a1, a2, a3); break;
-                    default: k_operands<3>(wa[h], wb[h], wa8[h], wb8[h], a0, a1, a2, a3); break;
+                    case 0:
+                        k_operands<0>(wa[h], wb[h], wa8[h], wb8[h], a0, a1, a2, a3);
+                        if (LM) high_planes<0>(a0, a1, a2, a3, c0, c1, c2, c3);
+                        break;
+                    case 1:
+                        k_operands<1>(wa[h], wb[h], wa8[h], wb8[h], a0, a1, a2, a3);
+                        if (LM) high_planes<1>(a0, a1, a2, a3, c0, c1, c2, c3);
+                        break;
+                    case 2:
+                        k_operands<2>(wa[h], wb[h], wa8[h], wb8[h], a0, a1, a2, a3);
+                        if (LM) high_planes<2>(a0, a1, a2, a3, c0, c1, c2, c3);
+                        break;
+                    default:
+                        k_operands<3>(wa[h], wb[h], wa8[h], wb8[h], a0, a1, a2, a3);
+                        if (LM) high_planes<3>(a0, a1, a2, a3, c0, c1, c2, c3);
+                        break;
                 }
                 const uint2 qh = qfS[(0 * 8 + ks) * 32 + lane], ql = qfS[(1 * 8 + ks) * 32 + lane];
                 mma_bf16_16816(acc[g], a0, a1, a2, a3, qh.x, qh.y);
                 mma_bf16_16816(acc[g], a0, a1, a2, a3, ql.x, ql.y);
+                if (LM) {  // high-bit plane against kappa q' (parts 2, 3: hi, lo)
+                    const uint2 kh = qfS[(2 * 8 + ks) * 32 + lane], kl = qfS[(3 * 8 + ks) * 32 + lane];
+                    mma_bf16_16816(acc[g], c0, c1, c2, c3, kh.x, kh.y);
+                    mma_bf16_16816(acc[g], c0, c1, c2, c3, kl.x, kl.y);
+                }
             }
             const float4 sA = ksS[ta], sB = ksS[ta + 8], zA = kzS[ta], zB = kzS[ta + 8];
             const float sa[4] = {sA.x, sA.y, sA.z, sA.w}, za[4] = {zA.x, zA.y, zA.z, zA.w};
@@ -886,22 +904,45 @@ __device__ __forceinline__ void attend_page_g8(const uint8_t* blk, int valid, ui
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
             const float4 sg = *reinterpret_cast<const float4*>(vsS + g * kPvRow + chunk);
-            uint32_t bh0, bl0, bh1, bl1;
-            split_both(mul2(make_float2(pp.x, pp.y), make_float2(sg.x, sg.y)), bh0, bl0);
-            split_both(mul2(make_float2(pp.z, pp.w), make_float2(sg.z, sg.w)), bh1, bl1);
+            uint32_t bh0, bl0, bh1, bl1, ch0 = 0, cl0 = 0, ch1 = 0, cl1 = 0;
+            const float2 w0 = mul2(make_float2(pp.x, pp.y), make_float2(sg.x, sg.y));
+            const float2 w1 = mul2(make_float2(pp.z, pp.w), make_float2(sg.z, sg.w));
+            split_both(w0, bh0, bl0);
+            split_both(w1, bh1, bl1);
+            if constexpr (LM) {  // the high-bit plane's weights kappa * W
+                const float2 kv2 = make_float2(cbk.vk, cbk.vk);
+                split_both(mul2(w0, kv2), ch0, cl0);
+                split_both(mul2(w1, kv2), ch1, cl1);
+            }
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 const uint32_t r0 = pw[2 * half], r1 = pw[2 * half + 1];
                 const uint32_t r08 = pw8[2 * half], r18 = pw8[2 * half + 1];
-                uint32_t a0, a1, a2, a3;
+                uint32_t a0, a1, a2, a3, c0 = 0, c1 = 0, c2 = 0, c3 = 0;
                 switch (g) {
-                    case 0: v_operands<0>(r0, r1, r08, r18, a0, a1, a2, a3); break;
-                    case 1: v_operands<1>(r0, r1, r08, r18, a0, a1, a2, a3); break;
-                    case 2: v_operands<2>(r0, r1, r08, r18, a0, a1, a2, a3); break;
-                    default: v_operands<3>(r0, r1, r08, r18, a0, a1, a2, a3); break;
+                    case 0:
+                        v_operands<0>(r0, r1, r08, r18, a0, a1, a2, a3);
+                        if (LM) high_planes<0>(a0, a1, a2, a3, c0, c1, c2, c3);
+                        break;
+                    case 1:
+                        v_operands<1>(r0, r1, r08, r18, a0, a1, a2, a3);
+                        if (LM) high_planes<1>(a0, a1, a2, a3, c0, c1, c2, c3);
+                        break;
+                    case 2:
+                        v_operands<2>(r0, r1, r08, r18, a0, a1, a2, a3);
+                        if (LM) high_planes<2>(a0, a1, a2, a3, c0, c1, c2, c3);
+                        break;
+                    default:
+                        v_operands<3>(r0, r1, r08, r18, a0, a1, a2, a3);
+                        if (LM) high_planes<3>(a0, a1, a2, a3, c0, c1, c2, c3);
+                        break;
                 }
                 mma_bf16_16816(acc_o[2 * g + half], a0, a1, a2, a3, bh0, bh1);
                 mma_bf16_16816(acc_o[2 * g + half], a0, a1, a2, a3, bl0, bl1);
+                if (LM) {
+                    mma_bf16_16816(acc_o[2 * g + half], c0, c1, c2, c3, ch0, ch1);
+                    mma_bf16_16816(acc_o[2 * g + half], c0, c1, c2, c3, cl0, cl1);
+                }
             }
         }
     }
@@ -1060,7 +1101,27 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
                 for (int ks = 0; ks < 8; ++ks) {  // every warp writes the same values
                     const uint2 f = *reinterpret_cast<const uint2*>(fr + ((size_t)ks * 32 + lane) * 2);
                     qfS[(nt * 8 + ks) * 32 + lane] = f;
-                    if (LM) qfS[((NT + nt) * 8 + ks) * 32 + lane] = scaled_fragment(f, cbk.kk, (lane >> 2) & 1);
+                    if (LM && NT == 1) qfS[((NT + nt) * 8 + ks) * 32 + lane] = scaled_fragment(f, cbk.kk, (lane >> 2) & 1);
+                }
+                if constexpr (LM && NT == 2) {  // eight heads: parts 0, 1 are q' hi, lo; kappa q' into parts 2, 3
+                    if (nt == 1) {
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks) {
+                            const uint2 hh = qfS[(0 * 8 + ks) * 32 + lane], ll = qfS[(1 * 8 + ks) * 32 + lane];
+                            const float y[4] = {cbk.kk * (bf16_lo(hh.x) + bf16_lo(ll.x)),
+                                                cbk.kk * (bf16_hi(hh.x) + bf16_hi(ll.x)),
+                                                cbk.kk * (bf16_lo(hh.y) + bf16_lo(ll.y)),
+                                                cbk.kk * (bf16_hi(hh.y) + bf16_hi(ll.y))};
+                            float yh[4], yl[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                yh[i] = __bfloat162float(__float2bfloat16_rn(y[i]));
+                                yl[i] = __bfloat162float(__float2bfloat16_rn(y[i] - yh[i]));
+                            }
+                            qfS[(2 * 8 + ks) * 32 + lane] = make_uint2(pack_bf16x2_rn(yh[0], yh[1]), pack_bf16x2_rn(yh[2], yh[3]));
+                            qfS[(3 * 8 + ks) * 32 + lane] = make_uint2(pack_bf16x2_rn(yl[0], yl[1]), pack_bf16x2_rn(yl[2], yl[3]));
+                        }
+                    }
                 }
                 if constexpr (BOOST) {  // q'[j] of heads 4nt..4nt+3 as float4 NT * j + nt
                     const float* qr = p.qrot + ((size_t)bk * NT + nt) * 4 * kD + 4 * lane;
@@ -1091,11 +1152,11 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
             if constexpr (BOOST) brec = p.boost + ((size_t)info[s].pid * p.hk + sraw.z) * kBoostBlock;
             if constexpr (NT == 2) {
                 if (valid == kPage)
-                    attend_page_g8<true, BOOST>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o[0], p.gshift,
-                                                qbS, brec);
+                    attend_page_g8<true, BOOST, LM>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o[0],
+                                                    p.gshift, qbS, brec, cbk);
                 else
-                    attend_page_g8<false, BOOST>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o[0],
-                                                 p.gshift, qbS, brec);
+                    attend_page_g8<false, BOOST, LM>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o[0],
+                                                     p.gshift, qbS, brec, cbk);
             } else {
                 if (valid == kPage)
                     attend_page<NT, true, LM, BOOST>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o,
@@ -1671,8 +1732,8 @@ __global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(DecodeParams p)
 // ---------------------------------------------------------------------------
 struct Int2Attr {
     int sms = 0;
-    bool set1 = false, set2 = false, setl = false, setk = false, setk2 = false, setm = false, setp = false,
-         setb = false;
+    bool set1 = false, set2 = false, setl = false, setl2 = false, setk = false, setk2 = false, setm = false,
+         setp = false, setb = false;
 };
 
 static Int2Attr& attr_for_device(int dev) {
@@ -1733,8 +1794,8 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st, cudaEvent_t ev
     dim3 pg((p.B + kPrepSeqs - 1) / kPrepSeqs + 1, p.hk);
     if ((e = launch_pdl(prep_kernel, pg, dim3(kPrepThreads), kPrepSmem, st, p)) != cudaSuccess) return e;
     if (ev_int2_start && (e = cudaEventRecord(ev_int2_start, st)) != cudaSuccess) return e;
-    if (p.codebook)  // Lloyd-Max levels (up to four query heads per KV head)
-        e = launch_int2<1, true>(p, st, at.sms, at.setl);
+    if (p.codebook)  // Lloyd-Max levels
+        e = (p.NT == 1) ? launch_int2<1, true>(p, st, at.sms, at.setl) : launch_int2<2, true>(p, st, at.sms, at.setl2);
     else if (p.boost)  // K channel boost
         e = (p.NT == 1) ? launch_int2<1, false, true>(p, st, at.sms, at.setk)
                         : launch_int2<2, false, true>(p, st, at.sms, at.setk2);

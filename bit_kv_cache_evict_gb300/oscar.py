@@ -327,7 +327,7 @@ def oscar_decode_attn_codebook(shape: oscar_shape, q, bf16_kv, bf16_len, pool, p
                                num_pages: int, hist_len, U, codebook, sm_scale: float, out, workspace,
                                dev_status=None, stream=None) -> None:
     """oscar_decode_attn reading the history with the Lloyd-Max levels
-    (codebook: fp32 [Hk][2]); G <= 4.  The workspace size is
+    (codebook: fp32 [Hk][2]).  The workspace size is
     oscar_decode_workspace_bytes's."""
     import torch
     B = int(q.shape[0])

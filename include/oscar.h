@@ -283,10 +283,9 @@ oscar_status oscar_decode_attn_noalloc(const oscar_shape* shape, int32_t batch, 
  * oscar_evict_quantize_codebook: oscar_evict_quantize with the codebook's
  *   nearest-level codes.
  * oscar_decode_attn_codebook: oscar_decode_attn reading the history with
- *   the codebook's levels; query groups G = Hq/Hk of at most 4
- *   (OSCAR_ERR_UNSUPPORTED otherwise).  About 1.6x the INT2 instructions
- *   (and time) of the uniform levels: one more tensor-core product on the
- *   codes' high-bit plane for K and for V.
+ *   the codebook's levels (every supported G).  About 1.6x the INT2
+ *   instructions (and time) of the uniform levels at G <= 4: one more
+ *   tensor-core product on the codes' high-bit plane for K and for V.
  */
 oscar_status oscar_evict_quantize_codebook(const oscar_shape* shape, int32_t n_tok, const void* src_kv,
                                            int32_t src_rows, const int32_t* src_row, const int32_t* dst_seq,

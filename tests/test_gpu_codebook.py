@@ -68,10 +68,10 @@ def _evict_gpu(shape, src, seq, pos, U, clip, cb, table, max_pages, npages, nbyt
     return sh, pool
 
 
-@pytest.mark.parametrize("g", [32, 64])
-def test_codebook_eviction_and_decode_match_oracle(g):
+@pytest.mark.parametrize("g,hq", [(32, 8), (64, 8), (32, 16)])
+def test_codebook_eviction_and_decode_match_oracle(g, hq):
     hist = [700, 1300, 2050]
-    hq, hk = 8, 2
+    hk = 2
     orc, shape, hist, table, max_pages, npages, nbytes, src, seq, pos, U, clip, bf16_kv, q = _setup(hist, hq, hk, g, 41)
     cb = np.array([[1.2, 0.8], [1.1, 1.3]], np.float32)[:hk]
     sh, pool_t = _evict_gpu(shape, src, seq, pos, U, clip, cb, table, max_pages, npages, nbytes, len(hist))
@@ -113,7 +113,7 @@ def test_codebook_eviction_and_decode_match_oracle(g):
     ref = L.decode(q, bf16_kv, bf16_len, pool_g, table, hist, U.astype(np.float64), orc.build_R, cb.astype(np.float64),
                    1 / np.sqrt(S.D), g)
     err, rel = H.assert_close(out.cpu().numpy(), ref)
-    print(f"codebook g={g}: max-abs {err:.3e} rel-L2 {rel:.3e} exempt codes {exempt}")
+    print(f"codebook g={g} G={hq // hk}: max-abs {err:.3e} rel-L2 {rel:.3e} exempt codes {exempt}")
 
 
 @pytest.mark.parametrize("hist,hq,hk", [([0, 17, 64, 130], 2, 2), ([1, 63, 65], 4, 1)])

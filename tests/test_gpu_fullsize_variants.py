@@ -40,7 +40,7 @@ def _bits(t):
 
 
 @pytest.mark.parametrize("name,mode", [("gate", "codebook"), ("gate", "boost"), ("qwen3_8b_36l", "codebook"),
-                                       ("qwen3_8b_36l", "boost"), ("qwen3_32b", "boost")])
+                                       ("qwen3_8b_36l", "boost"), ("qwen3_32b", "codebook"), ("qwen3_32b", "boost")])
 def test_variant_full_size_sampled(name, mode):
     w = S.WORKLOADS[name]
     st = bench.GpuState(w, 1, 1, 0, 32, CB_A if mode == "codebook" else None, mode == "boost")
