@@ -524,6 +524,9 @@ def run_oscar(args, rank: int, world: int, local: int) -> None:
     dev = torch.device("cuda", local)
     dist_init(world, "nccl")
     from bit_kv_cache_evict_gb300 import build as Bld
+    if rank == 0:      # one rank compiles (if the library is stale); the others then find it built
+        Bld.build()
+    barrier(world)
     Bld.build()
     w = S.WORKLOADS[args.workload]
     L = args.layers or w.layers
