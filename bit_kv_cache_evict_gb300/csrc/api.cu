@@ -9,13 +9,16 @@
 namespace oscar {
 
 // Pages per split-K item: about 4096 items for the whole batch at most,
-// 16-64 pages each (an item ends with a merge of the four consumer warps'
+// 16-256 pages each (an item ends with a merge of the four consumer warps'
 // states, so short items pay it per page or two; 16 pages is 4 per warp).
+// Long items on large requests (batch 256 up to 128K tokens, batch 128 at
+// 32K) measured 2-5 % faster steps than a 64-page cap; the short tail items
+// keep the last wave balanced.
 static int pages_per_split(int batch, int hk, int max_pages) {
     const int64_t cap = (int64_t)batch * hk * max_pages;
     int64_t pps = (cap + 4095) / 4096;
     if (pps < 16) pps = 16;
-    if (pps > 64) pps = 64;
+    if (pps > 256) pps = 256;
     return (int)pps;
 }
 
