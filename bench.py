@@ -48,8 +48,9 @@ BF16_BYTES_PER_TOKEN_HEAD = 2 * 128 * 2
 DEFAULT_WORKLOAD = "qwen3_8b_36l"
 
 # DRAM traffic of int2_kernel from one ncu capture (dram__bytes_read.sum +
-# dram__bytes_write.sum of one launch; the capture's summary and command are
-# in profiles/int2_kernel_qwen3_8b_1layer.md), with the algorithmic bytes of
+# dram__bytes_write.sum of one launch: the one-layer version of the
+# workload, the bench's own launch configuration, captured with
+# `ncu --set full -k regex:int2_kernel -c 1`), with the algorithmic bytes of
 # the captured launch.  Reported, scaled to the bench's mean launch by the
 # units processed, only while the kernel source is the one captured.
 INT2_TRAFFIC_CAPTURE = {
@@ -524,7 +525,7 @@ def run_oscar(args, rank: int, world: int, local: int) -> None:
     dev = torch.device("cuda", local)
     dist_init(world, "nccl")
     from bit_kv_cache_evict_gb300 import build as Bld
-    if rank == 0:      # one rank compiles (if the library is stale); the others then find it built
+    if local == 0:     # one rank per node compiles (if the library is stale); the others then find it built
         Bld.build()
     barrier(world)
     Bld.build()

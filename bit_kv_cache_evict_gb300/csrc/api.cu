@@ -66,7 +66,8 @@ static int tail_pages_of(int pps) { return pps > kShortItemPages ? 2 * kShortIte
 
 struct WsLayout {
     size_t counter, item_start, item_start2, qfrag, qsum, qrot, part, bf_part, total;
-    int NT, pps, tail_pg, part_stride, max_items;
+    int NT, pps, tail_pg, part_stride;
+    int64_t max_items;   // split-K items at most (int64: batch x KV heads x splits can exceed int32)
 };
 
 static WsLayout ws_layout(const oscar_shape* s, int batch, int max_pages) {
@@ -76,7 +77,7 @@ static WsLayout ws_layout(const oscar_shape* s, int batch, int max_pages) {
     w.pps = pages_per_split(batch, hk, max_pages);
     w.part_stride = (int)round_up((size_t)G * (kD + 2), 4);
     w.tail_pg = tail_pages_of(w.pps);
-    w.max_items = batch * hk * ((max_pages + w.pps - 1) / w.pps + w.tail_pg / kShortItemPages);
+    w.max_items = (int64_t)batch * hk * ((max_pages + w.pps - 1) / w.pps + w.tail_pg / kShortItemPages);
     size_t off = 0;
     w.counter = off;
     off += 256;
@@ -284,6 +285,8 @@ static oscar_status decode_impl(const oscar_shape* shape, int32_t batch, const v
     if (sst != OSCAR_OK) return sst;
     if (batch < 0 || max_pages <= 0 || num_pages < 0 || !ws_bytes) return OSCAR_ERR_INVALID_ARG;
     const WsLayout w = ws_layout(shape, batch, max_pages);
+    // item counts, item offsets and partial indices are int32 on the device
+    if (w.max_items > INT32_MAX || (double)w.max_items * w.part_stride > 4.0e9) return OSCAR_ERR_INVALID_ARG;
     if (!workspace) {
         *ws_bytes = w.total;
         return OSCAR_OK;
@@ -295,7 +298,7 @@ static oscar_status decode_impl(const oscar_shape* shape, int32_t batch, const v
     if (!aligned(q, 8) || !aligned(bf16_kv, 16) || !aligned(U, 16) || !aligned(pool, 16) || !aligned(out, 16) ||
         !aligned(workspace, 16) || !aligned(dev_status, 4))
         return OSCAR_ERR_INVALID_ARG;
-    if (!(sm_scale == sm_scale) || (double)w.max_items * w.part_stride > 4.0e9) return OSCAR_ERR_INVALID_ARG;
+    if (!(sm_scale == sm_scale)) return OSCAR_ERR_INVALID_ARG;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     DecodeParams p{};
     p.q = static_cast<const __nv_bfloat16*>(q);

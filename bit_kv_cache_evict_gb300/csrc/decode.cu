@@ -1751,8 +1751,9 @@ static cudaError_t launch_int2(const DecodeParams& p, cudaStream_t st, int sms, 
         attr_set = true;
     }
     const int per_sm = (NT == 1) ? 3 : 2;
-    const int max_items = p.B * p.hk * ((p.max_pages + p.pps - 1) / p.pps + p.tail_pg / kShortItemPages);
-    int blocks = min(per_sm * sms, max_items);
+    const int64_t max_items =
+        (int64_t)p.B * p.hk * ((p.max_pages + p.pps - 1) / p.pps + p.tail_pg / kShortItemPages);
+    int blocks = (int)std::min<int64_t>((int64_t)per_sm * sms, max_items);
     if (blocks < 1) blocks = 1;
     cudaError_t e = launch_pdl(int2_kernel<NT, LM, BOOST>, dim3(blocks), dim3(kInt2Threads), smem, st, p);
     return e != cudaSuccess ? e : cudaGetLastError();

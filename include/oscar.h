@@ -163,7 +163,8 @@ oscar_status oscar_pool_layout(const oscar_shape* shape, int32_t batch, const in
 /*
  * oscar_evict_quantize -- the fused eviction kernel ([NEWS] sec. C): for
  * each of n_tok tokens and each KV head, rotate the K and V vectors by
- * R = U . H . P ([NEWS] sec. B), clip each group of 32 stored positions to
+ * R = U . H . P ([NEWS] sec. B), clip each group of quant_group (32, 64 or
+ * 128) stored positions to
  * +-c*max|y|, quantise to 2-bit codes with fp16 scale s = (max-min)/3 and
  * zero z = min (codes from the stored fp16 s, z, round half to even,
  * clamped to 0..3; all codes 0 when s == 0), pack four codes per byte and
@@ -181,10 +182,15 @@ oscar_status oscar_pool_layout(const oscar_shape* shape, int32_t batch, const in
  *            positions and page ids are bounds-checked on the device; a
  *            token with a bad index is skipped and reported in dev_status.
  *   U, clip  (device fp32) as in the layouts above.
- * The arithmetic keeps y = x.U.H accurate to ~2^-44 relative (compensated
- * fp32 products and sums, group statistics and code decisions in fp64), so
- * codes and fp16 s/z match a float64 evaluation except for values within
- * ~1e-13 of a rounding boundary.
+ * Precision: no fp64 arithmetic runs on the GPU.  y = x.U is accumulated
+ * with compensated fp32 products and sums (Dot2), the Hadamard transform
+ * and the group statistics (max |y|, clamp, min, max) run on double-float
+ * (hi, lo) pairs, s and z are rounded to fp16 from a value within 2^-23
+ * (relative) of the exact one, and each code is decided from a u within
+ * 4e-7 code units of a float64 evaluation.  Codes and fp16 s/z therefore
+ * match a float64 evaluation except where u lies within 4e-7 of k + 0.5, or
+ * a pre-rounding s or z within 2^-23 (relative) of an fp16 rounding
+ * midpoint.
  */
 oscar_status oscar_evict_quantize(const oscar_shape* shape, int32_t n_tok, const void* src_kv,
                                   int32_t src_rows, const int32_t* src_row, const int32_t* dst_seq,
@@ -255,7 +261,10 @@ void oscar_time_next_int2(void* ev_start, void* ev_stop);
  *     reports the size a request needs.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture.
+ *     before any stream capture.  The address is kept for the life of the
+ *     process: after cudaDeviceReset (or anything else that destroys the
+ *     device's primary context) it is stale, so this call must not be used
+ *     on that device again in the same process.
  *   - All calls share the one array and it keeps the last call's contents;
  *     each call rebuilds what it reads, but calls that may overlap on the GPU
  *     (different streams, or different host threads) race on it: order them.

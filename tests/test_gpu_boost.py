@@ -118,7 +118,9 @@ def test_boost_eviction_and_decode_match_oracle(g, hq, hk, perm):
     aux = K.evict(orc, shape, src, seq, pos, U.astype(np.float64), clip, pool_o, table, table.shape[1], boost_o)
     u = aux[0]
     items = [(int(seq[i]), int(pos[i]), i) for i in range(seq.size)]
-    H.compare_evicted(pool_g, pool_o, table, items, aux, hk, g)
+    allowed = np.zeros_like(pool_o)
+    H.compare_evicted(pool_g, pool_o, table, items, aux, hk, g, allowed=allowed)
+    H.assert_pools_equal_except(pool_g, pool_o, allowed)
     n_ex = _check_records(pool_g, pool_o, boost_g, table, seq, pos, u, hk, g)
     assert n_ex <= max(2, 2e-3 * seq.size * hk), n_ex
 
@@ -146,7 +148,9 @@ def test_boost_edge_histories(hist, hq, hk):
     boost_o = np.zeros(max(npages * hk * K.BLOCK, 16), np.uint8)
     aux = K.evict(orc, shape, src, seq, pos, U.astype(np.float64), clip, pool_o, table, table.shape[1], boost_o)
     items = [(int(seq[i]), int(pos[i]), i) for i in range(seq.size)]
-    H.compare_evicted(pool_g, pool_o, table, items, aux, hk, 32)
+    allowed = np.zeros_like(pool_o)
+    H.compare_evicted(pool_g, pool_o, table, items, aux, hk, 32, allowed=allowed)
+    H.assert_pools_equal_except(pool_g, pool_o, allowed)
     _check_records(pool_g, pool_o, boost_g, table, seq, pos, aux[0], hk, 32)
     B_ = len(hist)
     bf16_len = np.array([S.NSLOT, 5, S.NSLOT, 200][:B_], np.int32)

@@ -37,14 +37,26 @@ def _lib():
     B.build()
 
 
+# sampled (sequence, KV head) units per workload: eight for the workloads
+# with the widest value ranges (Student-t values) and length mixes (1K-128K
+# with a shared prefix), three or four elsewhere
+N_UNITS = {"qwen3_32b": 8, "stress": 8}
+
+
 def pick_units(w: S.Workload, ctx: np.ndarray):
     """Sampled (sequence, KV head) units: the shortest and the longest
-    sequence, one in the middle (and a prefix sharer for the stress mix)."""
-    order = np.argsort(ctx)
+    sequence, one in the middle (and two prefix sharers for the stress mix),
+    then sequences at evenly spaced length ranks up to N_UNITS."""
+    order = np.argsort(ctx, kind="stable")
     seqs = [int(order[0]), int(order[-1]), int(order[len(order) // 2])]
     if w.prefix_seqs:
-        seqs.append(1)
-    seqs = list(dict.fromkeys(seqs))
+        seqs += [1, w.prefix_seqs - 1]
+    n = N_UNITS.get(w.name, len(seqs))
+    for r in np.linspace(0, len(order) - 1, n + 2)[1:-1]:
+        if len(dict.fromkeys(seqs)) >= n:
+            break
+        seqs.append(int(order[int(round(r))]))
+    seqs = list(dict.fromkeys(seqs))[:max(n, 3)]
     if len(seqs) == 1:  # one sequence: two of its KV heads
         return [(seqs[0], 1), (seqs[0], w.hk - 2)]
     return [(b, (3 * i + 1) % w.hk) for i, b in enumerate(seqs)]

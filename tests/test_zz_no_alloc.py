@@ -3,11 +3,12 @@ allocate device memory (for instance code inside a runtime that owns all
 device memory, or a plugin limited to the buffers it is handed).  Its
 scratch is the library's fixed device array instead of a caller workspace.
 
-Checked through the C ABI against oscar_decode_attn with a workspace, on two
-calls in a row with different inputs (the second call must not see anything
-the first one left in the shared array), within the attention tolerance the
-other GPU tests use; requests larger than the array are rejected before any
-launch.  This file is collected last on purpose."""
+Checked through the C ABI against oscar_decode_attn with a workspace and
+against the float64 oracle on the same inputs, on two calls in a row with
+different inputs (the second call must not see anything the first one left
+in the shared array), within the attention tolerance the other GPU tests
+use; requests larger than the array are rejected before any launch.  This
+file is collected last on purpose."""
 import ctypes
 
 import numpy as np
@@ -69,10 +70,14 @@ def test_noalloc_matches_workspace_entry_twice(orc):
     got2 = without_workspace(sc2, d2, status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
-    for got, ref in ((got1, ref1), (got2, ref2)):
+    for sc, got, ref in ((sc1, got1, ref1), (sc2, got2, ref2)):
         g, r = got.cpu().numpy(), ref.cpu().numpy().astype(np.float64)
         assert np.isfinite(g).all()
         H.assert_close(g, r)
+        # and against the oracle's decode of the same pool and BF16 segment
+        o = orc.decode(sc.shape, sc.q, sc.bf16_kv, sc.bf16_len, sc.pool, sc.page_table, sc.max_pages, sc.hist_len,
+                       sc.U, sc.sm_scale)
+        H.assert_close(g, o)
 
 
 def test_noalloc_rejects_requests_beyond_the_array():
