@@ -91,6 +91,8 @@ def parse_args():
                     help="oracle steps timed for cpu_baseline (about 10 s of host work)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-side", action="store_true",
+                    help="skip the one-layer side records (gate, frac_by_workload) of a 1-GPU run")
     ap.add_argument("--calibrate", action="store_true",
                     help="time the offline rotation calibration (oscar_calibrate_rotation) instead of a decode "
                          "step: one JSON line, the float64 oracle timed on the same inputs")
@@ -519,6 +521,52 @@ def config_of(w: S.Workload, layers: int, quant_group: int = 32, codebook: float
     return cfg
 
 
+# One-layer side records of a 1-GPU run: the INT2 kernel's roofline fraction
+# on the other single-GPU workloads, measured in the same process after the
+# main timed region.  Each pool is larger than L2 (qwen3_4b's 0.2 GB layer
+# is rotated over four layers, so consecutive steps read different pools).
+SIDE_RECORDS = (("gate", 1), ("qwen3_4b", 4), ("qwen3_32b", 1), ("stress", 1))
+
+
+def side_record(name: str, layers: int, steps: int, warmup: int, peak_gbs: float) -> dict:
+    """INT2 launch time (CUDA events on the launching stream, every launch)
+    and whole-step time of a short run of workload ``name``."""
+    import torch
+    w = S.WORKLOADS[name]
+    st = GpuState(w, layers, warmup + steps, 0)
+    stream = torch.cuda.current_stream()
+    for s in range(warmup):
+        for layer in range(layers):
+            st.layer_step(layer, s)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps * layers)]
+    for a, b in evs:   # materialise the events (torch creates them at their first record)
+        a.record(stream)
+        b.record(stream)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for k in range(steps):
+        for layer in range(layers):
+            st.layer_step(layer, warmup + k, evs[k * layers + layer])
+    stop.record(stream)
+    torch.cuda.synchronize()
+    int2_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    step_ms = start.elapsed_time(stop) / steps
+    int2_bytes = statistics.mean(st.hist_tokens_after(warmup + k) * st.Hk * st.hist_tok_bytes for k in range(steps))
+    step_bytes = statistics.mean(st.step_bytes(warmup + k) for k in range(steps)) * layers
+    att = statistics.mean(st.attended_tokens(warmup + k) for k in range(steps)) * layers
+    del st
+    torch.cuda.empty_cache()
+    int2_gbs = int2_bytes / (int2_ms * 1e-3) / 1e9
+    step_gbs = step_bytes / (step_ms * 1e-3) / 1e9
+    return {"workload": name, "layers": layers, "batch": w.batch, "q_heads": w.hq, "kv_heads": w.hk,
+            "int2_launch_ms": int2_ms, "int2_bytes_per_launch": int2_bytes, "int2_gbs": int2_gbs,
+            "int2_frac": int2_gbs / peak_gbs, "step_ms": step_ms, "step_algorithmic_gbs": step_gbs,
+            "step_frac": step_gbs / peak_gbs, "context_tokens_per_s": att / (step_ms * 1e-3),
+            "steps": steps, "warmup": warmup}
+
+
 def run_oscar(args, rank: int, world: int, local: int) -> None:
     import torch
     torch.cuda.set_device(local)
@@ -545,15 +593,19 @@ def run_oscar(args, rank: int, world: int, local: int) -> None:
     torch.cuda.synchronize()
     barrier(world)
 
-    # int2-kernel events around the launches of every `stride`-th layer in the
+    # int2-kernel events around the launches of three layers per step in the
     # timed region (an event between two kernels ends their programmatic
     # overlap, so the other layers run without them; every layer carries the
-    # same history lengths)
-    stride = max(1, L // 6)
-    timed_layers = [layer for layer in range(L) if layer % stride == 0]
+    # same history lengths).  The end-to-end region records the same events
+    # on the same layers, so that the two regions carry the same
+    # instrumentation.
+    stride = max(1, L // 3)
+    timed_layers = [layer for layer in range(L) if layer % stride == 0][:3]
     evs = {(k, layer): (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for k in range(K) for layer in timed_layers}
-    for a, b in evs.values():   # materialise the events
+    e2e_evs = {(k, layer): (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for k in range(e2e_steps) for layer in timed_layers}
+    for a, b in list(evs.values()) + list(e2e_evs.values()):   # materialise the events
         a.record(stream)
         b.record(stream)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -580,6 +632,7 @@ def run_oscar(args, rank: int, world: int, local: int) -> None:
     step_bytes = sum(st.step_bytes(W + k) for k in range(K)) * L / K
     hist_bytes = [st.hist_tokens_after(W + k) * st.Hk * st.hist_tok_bytes for k in range(K)]
     int2_avg_ms = statistics.mean(int2_ms)
+    int2_median_ms = statistics.median(int2_ms)
     int2_bytes = statistics.mean(hist_bytes)
     peaks = load_peaks()
     achieved = int2_bytes / (int2_avg_ms * 1e-3) / 1e9
@@ -617,7 +670,7 @@ def run_oscar(args, rank: int, world: int, local: int) -> None:
                 if not overlap_copies:
                     lay["q"].copy_(hq[layer], non_blocking=True)
                     lay["new_kv"].copy_(hn[layer], non_blocking=True)
-                    st.layer_step(layer, s)
+                    st.layer_step(layer, s, e2e_evs.get((k, layer)))
                     ho[layer].copy_(lay["out"], non_blocking=True)
                     continue
                 with torch.cuda.stream(h2d_s):
@@ -627,7 +680,7 @@ def run_oscar(args, rank: int, world: int, local: int) -> None:
                     ev_in[layer].record(h2d_s)
                 stream.wait_event(ev_in[layer])
                 stream.wait_event(ev_out[layer])
-                st.layer_step(layer, s)
+                st.layer_step(layer, s, e2e_evs.get((k, layer)))
                 ev_done[layer].record(stream)
                 with torch.cuda.stream(d2h_s):
                     d2h_s.wait_event(ev_done[layer])
@@ -653,6 +706,18 @@ def run_oscar(args, rank: int, world: int, local: int) -> None:
                "sample": f"{args.cpu_steps} steps of " + samp.describe(), "seconds": dt, "cpu": cpu_info(),
                "value_1_thread": tps1, "seconds_1_thread": dt1}
 
+    # one-layer side records (1-GPU runs only): the 32K batch-64 layer the
+    # INT2 roofline target is stated on, and the other single-GPU shapes
+    bpe = st.bits_per_element(W + K - 1)
+    side = None
+    if world == 1 and not args.no_side:
+        del st
+        torch.cuda.empty_cache()
+        side = {}
+        for name, layers in SIDE_RECORDS:
+            if name != w.name:
+                side[name] = side_record(name, layers, 20, 3, peaks["hbm_gbs"])
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
@@ -660,17 +725,23 @@ def run_oscar(args, rank: int, world: int, local: int) -> None:
             "dtype": "int2 codes x bf16 hi/lo on tensor cores, fp32 accumulate", "data": "synthetic",
             "config": config_of(w, L, args.quant_group, args.codebook, args.boost),
             "decode_tokens_per_s": world * w.batch * K / (t_ms_max / 1e3),
-            "bits_per_element": st.bits_per_element(W + K - 1),
+            "bits_per_element": bpe,
             "step_algorithmic_gbs": step_bytes / (ms_per_step * 1e-3) / 1e9,
+            "step_frac": step_bytes / (ms_per_step * 1e-3) / 1e9 / peaks["hbm_gbs"],
             "roofline": {"kernel": "int2_kernel (split-K INT2 history attention)", "bound": "hbm",
                          "achieved": achieved, "peak": peaks["hbm_gbs"], "peak_source": peaks["source"],
                          "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                          "traffic": int2_traffic(w.name if args.quant_group == 32 and args.codebook is None and not args.boost
                                                 else "", int2_bytes),
                          "bytes_per_launch": int2_bytes, "launch_ms": int2_avg_ms,
+                         "launch_ms_median": int2_median_ms,
                          "share_of_step": int2_avg_ms * L / ms_per_step,
                          "launches_timed": len(int2_ms)},
             "cpu_baseline": cpu, "e2e": e2e,
+            "gate": side.get("gate") if side else None,
+            "frac_by_workload": ({w.name: achieved / peaks["hbm_gbs"],
+                                  **{k: v["int2_frac"] for k, v in side.items()}} if side else None),
+            "side_records": side,
             "gpu_launches": K * L * 5,
             "clocks": clk, "setup_s": setup_s,
         }

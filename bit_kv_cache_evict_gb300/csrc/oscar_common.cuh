@@ -136,6 +136,12 @@ __device__ __forceinline__ float2 sub2(float2 a, float2 b) {
         : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
     return r;
 }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    float2 r;
+    asm("{.reg .b64 A, B, C; mov.b64 A, {%2, %3}; mov.b64 B, {%4, %5}; add.rn.f32x2 C, A, B; mov.b64 {%0, %1}, C;}"
+        : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
     float2 r;
     asm("{.reg .b64 A, B, C, D; mov.b64 A, {%2, %3}; mov.b64 B, {%4, %5}; mov.b64 C, {%6, %7}; "
@@ -184,6 +190,15 @@ __device__ __forceinline__ uint32_t split_w_pair(float2 p, float2 s, const Split
 // tile: bits 0 and 1 swapped, so tokens (4a, 4a+2) and (4a+1, 4a+3) are
 // adjacent pairs (the two token pairs of a PV B-operand register).
 __device__ __forceinline__ int pv_slot(int t) { return (t & ~3) | ((t & 1) << 1) | ((t >> 1) & 1); }
+
+// D += A(16x16 f16, row) * B(16x8 f16, col), fp32 accumulate
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
 
 // D += A(16x16 bf16, row) * B(16x8 bf16, col), fp32 accumulate
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
@@ -306,7 +321,7 @@ struct DecodeParams {
     int32_t* counter;     // [1]
     int32_t* item_start;  // [B + 1] long items before sequence b (prefix sums)
     int32_t* item_start2; // [B + 1] short tail items before sequence b
-    uint32_t* qfrag;      // [B*Hk][NT][8][32][2]
+    uint32_t* qfrag;      // [B*Hk][NT * 1024] words: up to four heads [8][32] uint4, eight heads [3][8][32] uint2
     float* qsum;          // [B*Hk][NT*4][4]
     float* qrot;          // [B*Hk][4][kD] q' in stored order (fp32), written when boost is set
     float* part;          // [max_items][part_stride]
@@ -320,7 +335,20 @@ struct DecodeParams {
     float qscale;  // sm_scale * log2(e)
     const float* codebook;  // [hk][2] Lloyd-Max inner level a, or null (uniform levels)
     const uint8_t* boost;   // K boost records [num_pages][hk][kBoostBlock], or null (no boost)
+    // tensor-memory INT2 kernel (int2_tc_kernel, up to four heads, uniform levels)
+    uint8_t* kimg;          // [B*Hk][kTcKImg] q' B-operand images of int2_tc_kernel, or null
+    int tc;                 // 1: the INT2 segment runs int2_tc_kernel
+    int part_shift;         // log2(partials per split-K item): 1 with int2_tc_kernel (one per math group), else 0
 };
+
+// q' B-operand image of int2_tc_kernel, per (sequence, KV head): for each
+// of the eight k-steps (16 stored positions of one 32-position block, in the
+// A-operand column order), a 16 (k) x 16 (n = 4 part + head: bf16 high, low
+// and third part of q' 2^64 for up to four heads; columns 12-15 zero) bf16
+// matrix in the no-swizzle core-matrix layout (element (n, k) at
+// 2 (n % 8) + 16 (k % 8) + 256 (n / 8) + 128 (k / 8)), 512 bytes each.
+constexpr int kTcKStep = 512;
+constexpr int kTcKImg = 8 * kTcKStep;
 
 // Split-K geometry of one sequence with npg history pages: the last
 // min(npg, tail_pg) pages go to short items of kShortItemPages, the rest to
@@ -374,6 +402,7 @@ struct FitParams {
 cudaError_t launch_calibrate_codebook(const FitParams& p, cudaStream_t st);
 
 cudaError_t launch_evict(const EvictParams& p, cudaStream_t st);
+cudaError_t launch_int2_tc(const DecodeParams& p, cudaStream_t st, int sms);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st, cudaEvent_t ev_int2_start,
                           cudaEvent_t ev_int2_stop);
 
