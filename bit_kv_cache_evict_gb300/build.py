@@ -10,7 +10,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 OUT = os.path.join(PKG, "liboscar.so")
 BUILD = os.path.join(PKG, "_build")
-SOURCES = ["api.cu", "evict.cu", "decode.cu", "decode_tc.cu", "noalloc.cu", "calibrate.cu", "pages.cu", "radix.cu"]
+SOURCES = ["api.cu", "evict.cu", "decode.cu", "noalloc.cu", "calibrate.cu", "pages.cu", "radix.cu"]
 HEADERS = ["oscar_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

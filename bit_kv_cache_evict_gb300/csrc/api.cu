@@ -65,7 +65,7 @@ static int block_bytes_of(const oscar_shape* s) { return 4096 + 512 * (kD / s->q
 static int tail_pages_of(int pps) { return pps > kShortItemPages ? 2 * kShortItemPages : 0; }
 
 struct WsLayout {
-    size_t counter, item_start, item_start2, qfrag, qsum, qrot, kimg, part, bf_part, total;
+    size_t counter, item_start, item_start2, qfrag, qsum, qkinv, qrot, part, bf_part, total;
     int NT, pps, tail_pg, part_stride;
     int64_t max_items;   // split-K items at most (int64: batch x KV heads x splits can exceed int32)
 };
@@ -86,14 +86,14 @@ static WsLayout ws_layout(const oscar_shape* s, int batch, int max_pages) {
     w.item_start2 = off;
     off = round_up(off + (size_t)(batch + 1) * 4, 256);
     w.qfrag = off;
-    off = round_up(off + (size_t)batch * hk * w.NT * 4096, 256);  // q' fragments: NT x 4 KB per (b, kv)
+    off = round_up(off + (size_t)batch * hk * w.NT * 8 * 32 * 2 * 4, 256);
     w.qsum = off;
     off = round_up(off + (size_t)batch * hk * w.NT * 4 * 4 * 4, 256);
+    w.qkinv = off;
+    off = round_up(off + (size_t)batch * hk * 4, 256);
     w.qrot = off;
     off = round_up(off + (size_t)batch * hk * w.NT * 4 * kD * 4, 256);
-    w.kimg = off;   // q' B-operand images of the tensor-memory INT2 kernel (up to four heads)
-    off = round_up(off + (w.NT == 1 ? (size_t)batch * hk * kTcKImg : 0), 256);
-    w.part = off;   // split-K partials, one per item
+    w.part = off;
     off = round_up(off + (size_t)w.max_items * w.part_stride * 4, 256);
     w.bf_part = off;
     off = round_up(off + (size_t)batch * hk * bf16_items(s) * w.part_stride * 4, 256);
@@ -317,6 +317,7 @@ static oscar_status decode_impl(const oscar_shape* shape, int32_t batch, const v
     p.item_start2 = reinterpret_cast<int32_t*>(ws + w.item_start2);
     p.qfrag = reinterpret_cast<uint32_t*>(ws + w.qfrag);
     p.qsum = reinterpret_cast<float*>(ws + w.qsum);
+    p.qkinv = reinterpret_cast<float*>(ws + w.qkinv);
     p.qrot = reinterpret_cast<float*>(ws + w.qrot);
     p.part = reinterpret_cast<float*>(ws + w.part);
     p.bf_part = reinterpret_cast<float*>(ws + w.bf_part);
@@ -344,11 +345,6 @@ static oscar_status decode_impl(const oscar_shape* shape, int32_t batch, const v
     p.qscale = sm_scale * kLog2e;
     p.codebook = codebook;
     p.boost = boost;
-    // up to four query heads per KV head with the uniform levels: the INT2
-    // segment runs on the tensor-memory kernel
-    p.tc = (w.NT == 1 && !codebook && !boost) ? 1 : 0;
-    p.kimg = p.tc ? reinterpret_cast<uint8_t*>(ws + w.kimg) : nullptr;
-    p.part_shift = 0;
     cudaEvent_t ev0 = g_int2_ev_start, ev1 = g_int2_ev_stop;
     g_int2_ev_start = g_int2_ev_stop = nullptr;
     if (!ev0 || !ev1) ev0 = ev1 = nullptr;

@@ -7,29 +7,31 @@
 //
 // Kernels, in launch order:
 //   prep_kernel       q' = q . U_K . H . P scaled by sm_scale*log2(e), split
-//                     into bf16 hi+lo MMA fragments; work plan (split-K items).
+//                     into fp16 hi+lo MMA fragments; work plan (split-K items).
 //   int2_kernel<NT>   persistent warps; each takes split-K items (a run of
 //                     history pages of one (sequence, KV head)), streams the
 //                     6 KB page blocks into shared memory with bulk async
 //                     copies, and runs both products on tensor cores
-//                     (mma.sync m16n8k16 bf16 -> fp32) straight from the
-//                     packed codes.
+//                     (mma.sync m16n8k16, fp16 for the logits and bf16
+//                     for P.V, fp32 accumulate) straight from the packed
+//                     codes.
 //   bf16_kernel       sink + recent window per (sequence, KV head).
 //   merge_kernel      log-sum-exp merge of the INT2 splits, un-rotation by
 //                     R_V^T (bit-reversal, Hadamard, U_V^T), merge with the
 //                     BF16 partial.
 //
 // Exact factoring used by int2_kernel.  With codes c, per-(token, group)
-// fp16 scale s and zero z, and A-operand values c * 2^(P_b - 133) for the
-// 32-position block b (the code left in an otherwise clear bf16 pattern at
-// bit P_b, see code_pair_lo):
+// fp16 scale s and zero z, and the code left in an otherwise clear 16-bit
+// pattern at bit P_b for the 32-position block b (see code_pair_lo), which
+// reads c * 2^(P_b - 24) as fp16 and c * 2^(P_b - 133) as bf16:
 //   logit_t = sum_b s~_tb * D_tb + z_tb * Q_b,
-//       D_tb = sum_{j in b} c_tj 2^(P_b - 133) q'_j 2^kQUp  (MMA, tokens x heads),
-//       s~_tb = s_tb 2^(133 - kQUp - P_b),  Q_b = sum_{j in b} q'_j;
+//       D_tb = sum_{j in b} c_tj 2^(P_b - 24) q'_j 2^e   (fp16 MMA, tokens x heads),
+//       s~_tb = s_tb 2^(24 - P_b - e),  Q_b = sum_{j in b} q'_j,
+//       e one power of two per (sequence, KV head) from prep;
 //   o'_j   = 2^(133 - kVUp) sum_t W_t,b(j) c_tj 2^(P_b - 133) + sum_t p_t z_tb,
-//       W_tb = p_t s_tb 2^(kVUp - P_b)                  (MMA, dims x heads).
-// q' and W are split into bf16 hi + lo, so the products keep ~2^-17 relative
-// precision; codes are exact in bf16 and carry no offset.
+//       W_tb = p_t s_tb 2^(kVUp - P_b)                  (bf16 MMA, dims x heads).
+// q' 2^e is split into fp16 hi + lo (22 bits), W into bf16 hi + lo (~17
+// bits); codes are exact in both formats and carry no offset.
 #include "oscar_common.cuh"
 
 namespace oscar {
@@ -44,7 +46,8 @@ namespace oscar {
 // y = 0) builds the plan.
 constexpr int kPrepSeqs = 2;
 constexpr int kPrepThreads = 256;
-constexpr int kPrepSmem = kD * kD * 4 + (kPrepThreads / 32) * kD * 4;
+constexpr int kPrepUnits = kPrepSeqs * 2 * 4;  // (b, nt, hh) units of a block at most
+constexpr int kPrepSmem = kD * kD * 4 + kPrepUnits * kD * 4 + kPrepUnits * 4;
 
 __device__ __forceinline__ void prep_body(const DecodeParams& p);
 
@@ -62,7 +65,6 @@ __device__ __forceinline__ void prep_body(const DecodeParams& p) {
     extern __shared__ __align__(16) float psm[];
     float* Us = psm;                       // [a][k] = U_K[a][k]
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    float* qs = psm + kD * kD + warp * kD;
 
     if (blockIdx.x == gridDim.x - 1) {  // plan
         if (blockIdx.y != 0 || warp != 0) return;
@@ -118,23 +120,22 @@ __device__ __forceinline__ void prep_body(const DecodeParams& p) {
     }
     __syncthreads();
 
+    // Two passes over the block's (b, nt, hh) units.  Pass 1: q' of every
+    // unit into shared memory and its largest |q'|.  Pass 2: one power of
+    // two 2^e per (sequence, KV head), from the largest |q'| over the KV
+    // group's heads (times the Lloyd-Max plane weight kappa when it is
+    // above 1), put into [2^13, 2^14); the fp16 fragments of q' 2^e, the
+    // group sums of q' and 2^-e (which int2_kernel folds into the K scales).
     const int units = nseq * p.NT * 4;
+    float* qU = psm + kD * kD;               // [unit][kD] q' in stored order
+    float* mxU = qU + kPrepUnits * kD;       // [unit] largest |q'| (0 for padding)
     for (int u = warp; u < units; u += kPrepThreads / 32) {
-        const int hh = u & 3;
-        const int nt = (u >> 2) % p.NT;
+        const int hl = 4 * ((u >> 2) % p.NT) + (u & 3);  // head within the KV group
         const int b = b0 + (u >> 2) / p.NT;
         const int bk = b * p.hk + kv;
-        const int hl = 4 * nt + hh;  // head within the KV group
-        uint32_t* frag = p.qfrag + (size_t)bk * p.NT * 1024;  // up to four heads: [ks][32] uint4
-        float* qsum = p.qsum + ((size_t)bk * p.NT * 4 + hl) * 4;
-        const int ks = lane >> 2, tq = lane & 3;
-        if (hl >= p.G) {  // padding column pair: zeros
-#pragma unroll
-            for (int par = 0; par < 2; ++par) {
-                const int L = (2 * hh + par) * 4 + tq;
-                *reinterpret_cast<uint4*>(frag + ((size_t)ks * 32 + L) * 4) = make_uint4(0u, 0u, 0u, 0u);
-            }
-            if (lane < 4) qsum[lane] = 0.f;
+        float* qs = qU + u * kD;
+        if (hl >= p.G) {  // padding column pair
+            if (lane == 0) mxU[u] = 0.f;
             if (p.boost)
                 *reinterpret_cast<float4*>(p.qrot + ((size_t)bk * p.NT * 4 + hl) * kD + 4 * lane) =
                     make_float4(0.f, 0.f, 0.f, 0.f);
@@ -174,16 +175,58 @@ __device__ __forceinline__ void prep_body(const DecodeParams& p) {
         }
         const float scale = (float)kInvSqrtD * p.qscale;
         const int r5 = bitrev5(lane);
-        __syncwarp();
+        float mx = 0.f;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) qs[32 * bitrev2(k) + r5] = y[k] * scale;  // stored order
+        for (int k = 0; k < 4; ++k) {
+            const float v = y[k] * scale;
+            qs[32 * bitrev2(k) + r5] = v;  // stored order
+            mx = fmaxf(mx, fabsf(v));
+        }
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, m));
+        if (lane == 0) mxU[u] = mx;
         __syncwarp();
         if (p.boost)  // q' itself for the boost corrections
             *reinterpret_cast<float4*>(p.qrot + ((size_t)bk * p.NT * 4 + hl) * kD + 4 * lane) =
                 *reinterpret_cast<const float4*>(qs + 4 * lane);
+    }
+    __syncthreads();
 
-        // group sums of q' (the three split parts the MMAs multiply add up to
-        // q' within 2^-24 relative)
+    float kappa = 1.f;  // Lloyd-Max plane weight bound of this KV head's K levels
+    if (p.codebook) {
+        const float a = __ldg(p.codebook + kv * 2);
+        kappa = fmaxf(1.f, fabsf(a > 0.f ? (3.f - 3.f * a) / (2.f * a) : 0.f));
+    }
+    for (int u = warp; u < units; u += kPrepThreads / 32) {
+        const int hh = u & 3;
+        const int nt = (u >> 2) % p.NT;
+        const int b = b0 + (u >> 2) / p.NT;
+        const int bk = b * p.hk + kv;
+        const int hl = 4 * nt + hh;
+        const int u0 = u - (u % (p.NT * 4));     // first unit of this (sequence, KV head)
+        float mx = mxU[u0];
+        for (int i = 1; i < p.NT * 4; ++i) mx = fmaxf(mx, mxU[u0 + i]);
+        mx *= kappa;
+        const int ex = mx > 0.f ? (int)((__float_as_uint(mx) >> 23) & 0xffu) - 127 : 0;
+        const int e = min(126, max(-126, kQTopExp - ex));
+        const float up = __uint_as_float((uint32_t)(127 + e) << 23);
+        if (u == u0 && lane == 0) p.qkinv[bk] = __uint_as_float((uint32_t)(127 - e) << 23);
+        uint32_t* frag = p.qfrag + ((size_t)bk * p.NT + nt) * 8 * 32 * 2;
+        float* qsum = p.qsum + ((size_t)bk * p.NT * 4 + hl) * 4;
+        const int ks = lane >> 2, tq = lane & 3;
+        if (hl >= p.G) {  // padding column pair: zeros
+#pragma unroll
+            for (int par = 0; par < 2; ++par) {
+                const int L = (2 * hh + par) * 4 + tq;
+                *reinterpret_cast<uint2*>(frag + ((size_t)ks * 32 + L) * 2) = make_uint2(0u, 0u);
+            }
+            if (lane < 4) qsum[lane] = 0.f;
+            continue;
+        }
+        const float* qs = qU + u * kD;
+
+        // group sums of q' (the two fp16 parts add up to q' 2^e within
+        // 2^-22 relative)
         float gs = 0.f;
 #pragma unroll
         for (int k = 0; k < 4; ++k) gs += qs[4 * lane + k];
@@ -193,72 +236,20 @@ __device__ __forceinline__ void prep_body(const DecodeParams& p) {
 
         // fragments: lane -> (ks, tq), k-step ks = (group g = ks/2, half h = ks%2)
         // covers in-group indices 8tq + 4h + {0,2} (b0) and + {1,3} (b1), the
-        // four codes of bytes 4(2tq+h)..4(2tq+h)+3 of group g's slot.  q' is
-        // split into three bf16 parts (round to nearest each: high, low and
-        // third part carry ~24 bits together); up to four heads: column
-        // 2hh = high part, 2hh+1 = low part, and a second fragment set with
-        // the third part in column 2hh (zeros in 2hh+1)
+        // four codes of bytes 4(2tq+h)..4(2tq+h)+3 of group g's slot; column
+        // 2hh = hi, 2hh+1 = lo
         const int base = 32 * (ks >> 1) + 8 * tq + 4 * (ks & 1);
-        constexpr float up = pow2f(kQUp);  // exact; see the scalings in oscar_common.cuh
         const float v[4] = {qs[base] * up, qs[base + 2] * up, qs[base + 1] * up, qs[base + 3] * up};
-        float hv[4], lv[4], ev[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            hv[i] = __bfloat162float(__float2bfloat16_rn(v[i]));
-            lv[i] = __bfloat162float(__float2bfloat16_rn(v[i] - hv[i]));
-            ev[i] = (v[i] - hv[i]) - lv[i];  // exact in fp32
-        }
-        const uint32_t h01 = pack_bf16x2_rn(hv[0], hv[1]), h23 = pack_bf16x2_rn(hv[2], hv[3]);
-        const uint32_t l01 = pack_bf16x2_rn(lv[0], lv[1]), l23 = pack_bf16x2_rn(lv[2], lv[3]);
-        const uint32_t e01 = pack_bf16x2_rn(ev[0], ev[1]), e23 = pack_bf16x2_rn(ev[2], ev[3]);
+        uint32_t h01, h23, l01, l23;
+        split_f16(v, h01, h23, l01, l23);
         if (p.NT == 2) {
-            // eight heads: column = head, the three parts in three fragment sets
-            uint32_t* fr = p.qfrag + (size_t)bk * 2 * 1024;  // [part][ks][32] uint2
+            // eight heads: column = head, hi and lo parts in two fragment sets
+            uint32_t* fr = p.qfrag + (size_t)bk * 2 * 8 * 32 * 2;  // [part][ks][32] uint2
             *reinterpret_cast<uint2*>(fr + ((size_t)(0 * 8 + ks) * 32 + 4 * hl + tq) * 2) = make_uint2(h01, h23);
             *reinterpret_cast<uint2*>(fr + ((size_t)(1 * 8 + ks) * 32 + 4 * hl + tq) * 2) = make_uint2(l01, l23);
-            *reinterpret_cast<uint2*>(fr + ((size_t)(2 * 8 + ks) * 32 + 4 * hl + tq) * 2) = make_uint2(e01, e23);
         } else {
-            *reinterpret_cast<uint4*>(frag + ((size_t)ks * 32 + (2 * hh) * 4 + tq) * 4) = make_uint4(h01, h23, e01, e23);
-            *reinterpret_cast<uint4*>(frag + ((size_t)ks * 32 + (2 * hh + 1) * 4 + tq) * 4) = make_uint4(l01, l23, 0u, 0u);
-        }
-    }
-
-    if (p.kimg) {
-        // q' B-operand images of int2_tc_kernel (up to four heads, one warp per
-        // (sequence, head) above: warp 4 sq + h holds head h's q' in stored
-        // order).  Row k (0..15) of k-step ks is A-operand column c = 8 ks +
-        // k / 2 of the K codes: column c = 16 blk + 2 i + s of a token's row
-        // holds the codes of bytes 4i + s (low half) and 4i + s + 2 (high
-        // half) in slot blk, i.e. stored position 32 blk + 4 i + s + 2 (k & 1).
-        // Column n = 4 part + head: the three bf16 parts of q' 2^kTcQUp.
-        __syncthreads();
-        for (int idx = threadIdx.x; idx < nseq * 8 * 32; idx += kPrepThreads) {
-            const int sq = idx >> 8, rem = idx & 255, ks = rem >> 5, ch = rem & 31;
-            const int nb = ch >> 4, kb = (ch >> 3) & 1, kr = ch & 7;
-            const int k = 8 * kb + kr, c = 8 * ks + (k >> 1), blk = c >> 4;
-            const int pos = 32 * blk + 4 * ((c & 15) >> 1) + (c & 1) + 2 * (k & 1);
-            uint32_t wv[4];
-#pragma unroll
-            for (int e2 = 0; e2 < 4; ++e2) {
-                float v2[2];
-#pragma unroll
-                for (int e1 = 0; e1 < 2; ++e1) {
-                    const int n = 8 * nb + 2 * e2 + e1, part = n >> 2, h = n & 3;
-                    float x = 0.f;
-                    if (part < 3 && h < p.G) {
-                        constexpr float up = pow2f(kQUp);
-                        const float v = psm[kD * kD + (sq * 4 + h) * kD + pos] * up;
-                        const float hi = __bfloat162float(__float2bfloat16_rn(v));
-                        const float lo = __bfloat162float(__float2bfloat16_rn(v - hi));
-                        x = part == 0 ? hi : part == 1 ? lo : (v - hi) - lo;
-                    }
-                    v2[e1] = x;
-                }
-                wv[e2] = pack_bf16x2_rn(v2[0], v2[1]);
-            }
-            uint8_t* dst = p.kimg + (size_t)((b0 + sq) * p.hk + kv) * kTcKImg + ks * kTcKStep + nb * 256 + kb * 128 +
-                           kr * 16;
-            *reinterpret_cast<uint4*>(dst) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+            *reinterpret_cast<uint2*>(frag + ((size_t)ks * 32 + (2 * hh) * 4 + tq) * 2) = make_uint2(h01, h23);
+            *reinterpret_cast<uint2*>(frag + ((size_t)ks * 32 + (2 * hh + 1) * 4 + tq) * 2) = make_uint2(l01, l23);
         }
     }
 }
@@ -295,41 +286,27 @@ struct StageInfo {
     int pid, pad[3];               // page id (read by the boost variant)
 };
 
-template <int NT, bool V2 = false>
+template <int NT>
 struct Int2Smem {
     static constexpr int G4 = NT * 4;  // head columns (padded to 4 per n-tile)
-    // per-warp scratch (attend_page, attend_page_g8): K s [64] float4 | K z
-    // [64] float4 | V z [64] float4 | V s [4][72] float (token order pv_pos)
-    // | P [G4][72] float (same token order).
+    // per-warp scratch: K s [64] float4 | K z [64] float4 | V z [64]
+    // float4 | V s [4][72] float (token order pv_pos) | P [G4][72] float
+    // (same token order).  Reused at an item's end for
+    // the warp's (o', m, l) state [G4][kD + 2].
     static constexpr int kWKs = 0, kWKz = 1024, kWVz = 2048, kWVs = 3072, kWP = 3072 + 4 * 72 * 4;
-    // per-warp scratch (attend_page_v2): K s~ pairs [64 tokens][4 blocks]
-    // float2, overlaid once the logits are done by the P.V weights [256] x
-    // 16 B (w_chunk); V s~ pairs and V z pairs [32 token pairs][4 blocks]
-    // float2 each.
-    static constexpr int kW2Ks = 0, kW2W = 0, kW2Vs = 4096, kW2Vz = 5120;
-    static constexpr int kWarpBytes0 = V2 ? 6144 : kWP + G4 * 72 * 4;
-    // Reused at an item's end for the warp's (o', m, l) state [G4][kD + 2].
+    static constexpr int kWarpBytes0 = kWP + G4 * 72 * 4;
     static constexpr int kMergeBytes = G4 * (kD + 2) * 4;
     static constexpr int kWarpBytes = kWarpBytes0 > kMergeBytes ? kWarpBytes0 : kMergeBytes;
-    // ring stages: seven for up to four heads (room for the larger q'
-    // fragments at three blocks per SM), eight for eight heads
-    static constexpr int NS = NT == 1 ? kStages - 1 : kStages;
     static constexpr int kStage = 0;
-    static constexpr int kInfo = kStage + NS * kBlock;
-    static constexpr int kBars = kInfo + NS * (int)sizeof(StageInfo);
-    static constexpr int kWarp = kBars + (2 * NS + 2) * 8;
+    static constexpr int kInfo = kStage + kStages * kBlock;
+    static constexpr int kBars = kInfo + kStages * (int)sizeof(StageInfo);
+    static constexpr int kWarp = kBars + (2 * kStages + 2) * 8;
     // q' fragments of the current item, shared by the four consumer warps
-    // (all four are inside the same item between two item-end merges).  Up
-    // to four heads: [8 k-steps][32 lanes] uint4, the B registers of the
-    // (high part | low part) columns, then those of the third part (in the
-    // high-part columns; the low-part columns are zero).  Eight heads:
-    // [3 parts: high, low, third][8][32] uint2.
-    static constexpr int kQf = kWarp + kConsumerWarps * kWarpBytes;
-    static constexpr int kQfBytes = NT == 1 ? 8 * 32 * 16 : 3 * 8 * 32 * 8;
-    static constexpr int kBytes = kQf + kQfBytes;
-    // Lloyd-Max levels: kappa q' fragments of the high-bit plane follow
-    // ([NT][8][32] uint2, high and low parts); channel boost: q' [kD] float4
-    // (four heads) there instead
+    // (all four are inside the same item between two item-end merges)
+    static constexpr int kQf = kWarp + kConsumerWarps * kWarpBytes;       // [NT][8][32] uint2
+    static constexpr int kBytes = kQf + NT * 8 * 32 * 8;
+    // Lloyd-Max levels: kappa q' fragments of the high-bit plane follow q';
+    // channel boost: q' [kD] float4 (four heads) there instead
     static constexpr int kBytesLM = kBytes + NT * 8 * 32 * 8;
     static_assert(NT * 8 * 32 * 8 >= kD * NT * 16, "room for the boost's q'");
 };
@@ -433,8 +410,8 @@ __device__ __forceinline__ void page_scales_g(const uint8_t* blk, int valid, flo
     }
 }
 
-// kmul / vmul multiply the K / V scales (the Lloyd-Max inner level a; 1 for
-// the uniform levels)
+// kmul / vmul multiply the K / V scales (K: the item's 2^-e, times the
+// Lloyd-Max inner level a; V: a; 1 for the uniform levels)
 template <bool FULL>
 __device__ __forceinline__ void page_scales(const uint8_t* blk, int valid, int gshift, float4* ksS, float4* kzS,
                                             float4* vzS, float* vsS, float kmul = 1.f, float vmul = 1.f) {
@@ -476,22 +453,18 @@ __device__ __forceinline__ void high_planes(uint32_t a0, uint32_t a1, uint32_t a
 }
 
 
-// B fragment of kappa q' from one of q': column n of a head's column pair
-// holds its hi (n even) or lo (n odd) part, the partner column sits in lane
-// ^ 4.  q' = hi + lo is rebuilt, scaled and split again.
+// fp16 B fragment of kappa q' from one of q': column n of a head's column
+// pair holds its hi (n even) or lo (n odd) part, the partner column sits in
+// lane ^ 4.  q' = hi + lo is rebuilt, scaled and split again (prep's power
+// of two leaves room for kappa).
 __device__ __forceinline__ uint2 scaled_fragment(uint2 f, float kappa, int is_lo) {
     const uint32_t ox = __shfl_xor_sync(kFull, f.x, 4), oy = __shfl_xor_sync(kFull, f.y, 4);
     const uint32_t hx = is_lo ? ox : f.x, hy = is_lo ? oy : f.y, lx = is_lo ? f.x : ox, ly = is_lo ? f.y : oy;
-    const float y[4] = {kappa * (bf16_lo(hx) + bf16_lo(lx)), kappa * (bf16_hi(hx) + bf16_hi(lx)),
-                        kappa * (bf16_lo(hy) + bf16_lo(ly)), kappa * (bf16_hi(hy) + bf16_hi(ly))};
-    float h[4], l[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        h[i] = __bfloat162float(__float2bfloat16_rn(y[i]));
-        l[i] = __bfloat162float(__float2bfloat16_rn(y[i] - h[i]));
-    }
-    return is_lo ? make_uint2(pack_bf16x2_rn(l[0], l[1]), pack_bf16x2_rn(l[2], l[3]))
-                 : make_uint2(pack_bf16x2_rn(h[0], h[1]), pack_bf16x2_rn(h[2], h[3]));
+    const float y[4] = {kappa * (half_lo(hx) + half_lo(lx)), kappa * (half_hi(hx) + half_hi(lx)),
+                        kappa * (half_lo(hy) + half_lo(ly)), kappa * (half_hi(hy) + half_hi(ly))};
+    uint32_t h01, h23, l01, l23;
+    split_f16(y, h01, h23, l01, l23);
+    return is_lo ? make_uint2(l01, l23) : make_uint2(h01, h23);
 }
 
 // One page of INT2 history for one consumer warp: the page's scales, the
@@ -500,13 +473,11 @@ __device__ __forceinline__ uint2 scaled_fragment(uint2 f, float kappa, int is_lo
 // per-tile conditions of the logit phase so that the four tiles' work can
 // interleave.
 template <int NT, bool FULL, bool LM = false, bool BOOST = false>
-__device__ __forceinline__ void attend_page(const uint8_t* blk, int valid, uint8_t* wbuf, const uint4* qf4,
-                                            const uint2* qkS,
-                                            const float4 (&qsv)[NT], float (&m_run)[NT], float (&l_run)[NT],
-                                            float (&zacc)[NT][4], float (&acc_o)[NT][8][4],
+__device__ __forceinline__ void attend_page(const uint8_t* blk, int valid, uint8_t* wbuf, const uint2* qfS,
+                                            const float4 (&qsv)[NT], float kq, float (&m_run)[NT],
+                                            float (&l_run)[NT], float (&zacc)[NT][4], float (&acc_o)[NT][8][4],
                                             const SplitSel& take_lo, int gshift, const Codebook& cbk = {},
                                             const float4* qbS = nullptr, const uint8_t* brec = nullptr) {
-    static_assert(NT == 1, "attend_page serves up to four heads");
     using SM = Int2Smem<NT>;
     const int lane = threadIdx.x & 31, gID = lane >> 2, tq = lane & 3;
     if (FULL) valid = kPage;
@@ -522,8 +493,9 @@ __device__ __forceinline__ void attend_page(const uint8_t* blk, int valid, uint8
         br1 = __ldg(reinterpret_cast<const uint4*>(brec) + 2 * lane + 1);
     }
 
-    if constexpr (LM) page_scales<FULL>(blk, valid, gshift, ksS, kzS, vzS, vsS, cbk.ka, cbk.va);
-    else page_scales<FULL>(blk, valid, gshift, ksS, kzS, vzS, vsS);
+    // K scales times 2^-e (the power of two of the q' fragments)
+    if constexpr (LM) page_scales<FULL>(blk, valid, gshift, ksS, kzS, vzS, vsS, cbk.ka * kq, cbk.va);
+    else page_scales<FULL>(blk, valid, gshift, ksS, kzS, vzS, vsS, kq);
     __syncwarp();
 
     // -- logits of the page's tiles: A rows gID / gID+8 = tokens 16m+gID /
@@ -571,12 +543,11 @@ __device__ __forceinline__ void attend_page(const uint8_t* blk, int valid, uint8
                 }
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    const uint4 qb = qf4[ks * 32 + lane];
-                    mma_bf16_16816(acc[g][nt], a0, a1, a2, a3, qb.x, qb.y);
-                    mma_bf16_16816(acc[g][nt], a0, a1, a2, a3, qb.z, qb.w);  // third part of q'
+                    const uint2 qb = qfS[(nt * 8 + ks) * 32 + lane];
+                    mma_f16_16816(acc[g][nt], a0, a1, a2, a3, qb.x, qb.y);
                     if (LM) {  // high-bit plane against kappa q'
-                        const uint2 qk = qkS[ks * 32 + lane];
-                        mma_bf16_16816(acc[g][nt], c0, c1, c2, c3, qk.x, qk.y);
+                        const uint2 qk = qfS[((NT + nt) * 8 + ks) * 32 + lane];
+                        mma_f16_16816(acc[g][nt], c0, c1, c2, c3, qk.x, qk.y);
                     }
                 }
             }
@@ -754,315 +725,6 @@ __device__ __forceinline__ void attend_page(const uint8_t* blk, int valid, uint8
     }
 }
 
-// ---------------------------------------------------------------------------
-// attend_page_v2: the uniform-level page for up to four query heads per KV
-// head, with the P.V weights computed once per (token, block, head).
-// ---------------------------------------------------------------------------
-// Row i (0..7) of 16-token tile m of the logit products holds token
-// tile_token(m, i) and row i + 8 the token two places later: a lane's two
-// tokens (rows gID, gID + 8) are then the two tokens of one k-pair of the
-// P.V products, whose A operand pairs bytes 0 and 2 (or 1 and 3) of a
-// V code-plane word, i.e. tokens 4a + e and 4a + e + 2.
-__device__ __forceinline__ int tile_token(int m, int i) { return 16 * m + 4 * (i >> 1) + (i & 1); }
-
-// 16-byte chunk of the warp's P.V weights holding, for the token pair of
-// row i of tile m, head h and part (0: bf16 high parts, 1: rounded
-// remainders), the weight pairs of the four 32-position blocks.  The
-// swizzle keeps both the writes (one tile: lanes differ in i and h) and the
-// reads (one P.V k-step: lanes differ in m and part) on distinct banks
-// within each quarter warp.
-__device__ __forceinline__ int w_chunk(int m, int i, int h, int part) {
-    return (m * 8 + i) * 8 + (((h ^ m) << 1) | ((i & 1) ^ part));
-}
-
-// The page's scales for attend_page_v2.  K: per token t and 32-position
-// block b, s~ = s (of the block's group) * k_scale_up(b) * kmul, stored as
-// the pair (s~, s~): ksD[2t], ksD[2t + 1] = blocks (0, 1), (2, 3).  V: per
-// token pair p (tokens t = 4(p >> 1) + (p & 1) and t + 2, the pair of row
-// p & 7 of tile p >> 3), the pairs (s~_t, s~_t+2) with s~ = s *
-// v_scale_up(b), and (z_t, z_t+2): vsP / vzP[2p], [2p + 1].  Tokens past
-// the valid ones get zeros.
-template <bool FULL, int GS>
-__device__ __forceinline__ void page_scales_v2_g(const uint8_t* blk, int valid, float4* ksD, float4* vsP,
-                                                 float4* vzP, float kmul) {
-    constexpr int NG = 4 >> GS;  // (s, z) pairs per token vector
-    const int lane = threadIdx.x & 31;
-    auto load_row = [&](const uint8_t* base, float (&sg)[NG], float (&zg)[NG]) {
-        uint32_t w[NG];
-        if constexpr (NG == 4) {
-            const uint4 v = *reinterpret_cast<const uint4*>(base);
-            w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
-        } else if constexpr (NG == 2) {
-            const uint2 v = *reinterpret_cast<const uint2*>(base);
-            w[0] = v.x; w[1] = v.y;
-        } else {
-            w[0] = *reinterpret_cast<const uint32_t*>(base);
-        }
-#pragma unroll
-        for (int k = 0; k < NG; ++k) {
-            sg[k] = half_lo(w[k]);
-            zg[k] = half_hi(w[k]);
-        }
-    };
-    float kc[4];
-#pragma unroll
-    for (int b = 0; b < 4; ++b) kc[b] = k_scale_up(b) * kmul;
-#pragma unroll
-    for (int it = 0; it < 2; ++it) {
-        const int t = lane + 32 * it;
-        float sv[4] = {0.f, 0.f, 0.f, 0.f};
-        if (FULL || t < valid) {
-            float sg[NG], zg[NG];
-            load_row(blk + kKScale + t * 4 * NG, sg, zg);
-#pragma unroll
-            for (int b = 0; b < 4; ++b) sv[b] = sg[b >> GS] * kc[b];
-        }
-        ksD[2 * t] = make_float4(sv[0], sv[0], sv[1], sv[1]);
-        ksD[2 * t + 1] = make_float4(sv[2], sv[2], sv[3], sv[3]);
-    }
-    {
-        const int t0 = 4 * (lane >> 1) + (lane & 1);
-        float sv[2][4], zv[2][4];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int t = t0 + 2 * e;
-#pragma unroll
-            for (int b = 0; b < 4; ++b) sv[e][b] = zv[e][b] = 0.f;
-            if (FULL || t < valid) {
-                float sg[NG], zg[NG];
-                load_row(blk + v_scale_off(GS) + t * 4 * NG, sg, zg);
-#pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    sv[e][b] = sg[b >> GS] * v_scale_up(b);
-                    zv[e][b] = zg[b >> GS];
-                }
-            }
-        }
-        vsP[2 * lane] = make_float4(sv[0][0], sv[1][0], sv[0][1], sv[1][1]);
-        vsP[2 * lane + 1] = make_float4(sv[0][2], sv[1][2], sv[0][3], sv[1][3]);
-        vzP[2 * lane] = make_float4(zv[0][0], zv[1][0], zv[0][1], zv[1][1]);
-        vzP[2 * lane + 1] = make_float4(zv[0][2], zv[1][2], zv[0][3], zv[1][3]);
-    }
-}
-
-template <bool FULL>
-__device__ __forceinline__ void page_scales_v2(const uint8_t* blk, int valid, int gshift, float4* ksD, float4* vsP,
-                                               float4* vzP, float kmul) {
-    switch (gshift) {  // warp-uniform, once per page
-        case 0: page_scales_v2_g<FULL, 0>(blk, valid, ksD, vsP, vzP, kmul); break;
-        case 1: page_scales_v2_g<FULL, 1>(blk, valid, ksD, vsP, vzP, kmul); break;
-        default: page_scales_v2_g<FULL, 2>(blk, valid, ksD, vsP, vzP, kmul); break;
-    }
-}
-
-// Item-constant operands of attend_page_v2 for lane (gID, tq):
-//   bz    B fragment (f16x2, k-rows 2tq and 2tq + 1) of the zero-point
-//         product: 0 against the s entry of (s, z) word tq, and Q of group
-//         tq (sum of q' over the group's positions) of head gID >> 1, as its
-//         fp16 high part (gID even) or remainder (gID odd), scaled by 2^kq;
-//   kmul  2^kq, applied to the K scales as well, so that the logits come out
-//         scaled by 2^kq; kinv = 2^-kq undoes it.  kq puts the item's
-//         largest |Q| in [2^13, 2^14) (fp16 range, both parts normal).
-struct ZTerm {
-    uint32_t bz;
-    float kmul, kinv;
-};
-__device__ __forceinline__ ZTerm zterm_of(const float* qsum, int bk, int gshift) {
-    const int lane = threadIdx.x & 31, gID = lane >> 2, tq = lane & 3;
-    const float4 qb = *reinterpret_cast<const float4*>(qsum + ((size_t)bk * 4 + (gID >> 1)) * 4);
-    float qg;
-    if (gshift == 0) qg = tq == 0 ? qb.x : tq == 1 ? qb.y : tq == 2 ? qb.z : qb.w;
-    else if (gshift == 1) qg = tq == 0 ? qb.x + qb.y : tq == 1 ? qb.z + qb.w : 0.f;
-    else qg = tq == 0 ? (qb.x + qb.y) + (qb.z + qb.w) : 0.f;
-    float amax = fabsf(qg);
-#pragma unroll
-    for (int m = 1; m < 32; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, m));
-    int kq = 0;
-    if (amax > 0.f) {
-        const int e = (int)((__float_as_uint(amax) >> 23) & 0xffu) - 127;  // amax in [2^e, 2^(e+1))
-        kq = min(max(13 - e, -56), 40);
-    }
-    ZTerm r;
-    r.kmul = __uint_as_float((uint32_t)(127 + kq) << 23);
-    r.kinv = __uint_as_float((uint32_t)(127 - kq) << 23);
-    const float qs = qg * r.kmul;
-    const __half hi = __float2half_rn(qs);
-    const __half lo = __float2half_rn(qs - __half2float(hi));
-    r.bz = (uint32_t)__half_as_ushort((gID & 1) ? lo : hi) << 16;
-    return r;
-}
-
-// One page of INT2 history for one consumer warp, up to four query heads
-// (columns 2h, 2h + 1 = head h's q' high and low parts; a second MMA per
-// k-step adds the third part in the high column), uniform
-// levels.  Per tile: the code products as in attend_page, the zero-point
-// term sum_g z_g Q_g as one fp16 MMA on the raw (s, z) words, the scales by
-// paired FMAs.  Per page: one online-softmax update; each lane turns the p
-// of its two tokens into the P.V weights p * s~ of the four blocks (bf16
-// high part and rounded remainder) and stores them for the value products,
-// which then load their B fragments directly.  Logits are scaled by 2^kq
-// (ZTerm) until the softmax.
-template <bool FULL>
-__device__ __forceinline__ void attend_page_v2(const uint8_t* blk, int valid, uint8_t* wbuf, const uint4* qf4,
-                                               const ZTerm& zt, float& m_run, float2& l2, float2 (&zacc2)[4],
-                                               float (&acc_o)[8][4], int gshift) {
-    using SM = Int2Smem<1, true>;
-    const int lane = threadIdx.x & 31, gID = lane >> 2, tq = lane & 3;
-    if (FULL) valid = kPage;
-    float4* ksD = reinterpret_cast<float4*>(wbuf + SM::kW2Ks);
-    uint4* wS = reinterpret_cast<uint4*>(wbuf + SM::kW2W);
-    float4* vsP = reinterpret_cast<float4*>(wbuf + SM::kW2Vs);
-    float4* vzP = reinterpret_cast<float4*>(wbuf + SM::kW2Vz);
-    const int ntile = FULL ? 4 : (valid + 15) >> 4;  // warp-uniform, 1..4
-    const int ng = 4 >> gshift;
-
-    page_scales_v2<FULL>(blk, valid, gshift, ksD, vsP, vzP, zt.kmul);
-    __syncwarp();
-
-    // -- logits (scaled by 2^kq) of the page's tiles
-    float la[4], lb[4];
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        la[m] = lb[m] = -INFINITY;
-        if (m < ntile) {
-            const int ta = tile_token(m, gID), tb = ta + 2;
-            const uint2 x = *reinterpret_cast<const uint2*>(blk + kKCodes + ta * 32 + 8 * tq);
-            const uint2 y = *reinterpret_cast<const uint2*>(blk + kKCodes + tb * 32 + 8 * tq);
-            const uint32_t wa[2] = {x.x, x.y}, wb[2] = {y.x, y.y};
-            const uint32_t wa8[2] = {wa[0] >> 8, wa[1] >> 8}, wb8[2] = {wb[0] >> 8, wb[1] >> 8};
-            float acc[4][4];
-#pragma unroll
-            for (int g = 0; g < 4; ++g)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc[g][e] = 0.f;
-#pragma unroll
-            for (int it = 0; it < 8; ++it) {
-                const int h = it >> 2, g = it & 3, ks = 2 * g + h;
-                uint32_t a0, a1, a2, a3;
-                switch (g) {
-                    case 0: k_operands<0>(wa[h], wb[h], wa8[h], wb8[h], a0, a1, a2, a3); break;
-                    case 1: k_operands<1>(wa[h], wb[h], wa8[h], wb8[h], a0, a1, a2, a3); break;
-                    case 2: k_operands<2>(wa[h], wb[h], wa8[h], wb8[h], a0, a1, a2, a3); break;
-                    default: k_operands<3>(wa[h], wb[h], wa8[h], wb8[h], a0, a1, a2, a3); break;
-                }
-                const uint4 qb = qf4[ks * 32 + lane];
-                mma_bf16_16816(acc[g], a0, a1, a2, a3, qb.x, qb.y);
-                mma_bf16_16816(acc[g], a0, a1, a2, a3, qb.z, qb.w);  // third part of q' (high columns)
-            }
-            // zero-point term: A = (s, z) word tq of tokens ta, tb (f16; the s
-            // entries meet zeros in B), B = Q of group tq
-            const uint32_t za = tq < ng ? *reinterpret_cast<const uint32_t*>(blk + kKScale + ta * 4 * ng + 4 * tq) : 0u;
-            const uint32_t zb = tq < ng ? *reinterpret_cast<const uint32_t*>(blk + kKScale + tb * 4 * ng + 4 * tq) : 0u;
-            float dz[4] = {0.f, 0.f, 0.f, 0.f};
-            mma_f16_16816(dz, za, zb, 0u, 0u, zt.bz, 0u);
-            float2 XA = make_float2(dz[0], dz[1]), XB = make_float2(dz[2], dz[3]);
-            const float4 sa01 = ksD[2 * ta], sa23 = ksD[2 * ta + 1];
-            const float4 sb01 = ksD[2 * tb], sb23 = ksD[2 * tb + 1];
-            XA = fma2(make_float2(sa01.x, sa01.y), make_float2(acc[0][0], acc[0][1]), XA);
-            XB = fma2(make_float2(sb01.x, sb01.y), make_float2(acc[0][2], acc[0][3]), XB);
-            XA = fma2(make_float2(sa01.z, sa01.w), make_float2(acc[1][0], acc[1][1]), XA);
-            XB = fma2(make_float2(sb01.z, sb01.w), make_float2(acc[1][2], acc[1][3]), XB);
-            XA = fma2(make_float2(sa23.x, sa23.y), make_float2(acc[2][0], acc[2][1]), XA);
-            XB = fma2(make_float2(sb23.x, sb23.y), make_float2(acc[2][2], acc[2][3]), XB);
-            XA = fma2(make_float2(sa23.z, sa23.w), make_float2(acc[3][0], acc[3][1]), XA);
-            XB = fma2(make_float2(sb23.z, sb23.w), make_float2(acc[3][2], acc[3][3]), XB);
-            la[m] = (FULL || ta < valid) ? XA.x + XA.y : -INFINITY;
-            lb[m] = (FULL || tb < valid) ? XB.x + XB.y : -INFINITY;
-        }
-    }
-
-    // -- online softmax (base 2), once per page
-    float mx = fmaxf(la[0], lb[0]);
-#pragma unroll
-    for (int m = 1; m < 4; ++m) mx = fmaxf(mx, fmaxf(la[m], lb[m]));
-    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
-    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
-    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
-    const float m_new = fmaxf(m_run, mx * zt.kinv);
-    if (__any_sync(kFull, m_new > m_run)) {  // warp-uniform rescale
-        const float alpha = (m_new > m_run) ? ex2(m_run - m_new) : 1.f;
-        const float2 a2 = make_float2(alpha, alpha);
-        l2 = mul2(l2, a2);
-#pragma unroll
-        for (int g = 0; g < 4; ++g) zacc2[g] = mul2(zacc2[g], a2);
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-            const float2 u = mul2(make_float2(acc_o[mt][0], acc_o[mt][1]), a2);
-            const float2 v = mul2(make_float2(acc_o[mt][2], acc_o[mt][3]), a2);
-            acc_o[mt][0] = u.x;
-            acc_o[mt][1] = u.y;
-            acc_o[mt][2] = v.x;
-            acc_o[mt][3] = v.y;
-        }
-        m_run = m_new;
-    }
-    const float m_sub = (m_new == -INFINITY) ? 0.f : m_new;
-    __syncwarp();  // every lane's K scale reads are done before the weights overwrite them
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        const float2 P2 = make_float2(ex2(fmaf(la[m], zt.kinv, -m_sub)), ex2(fmaf(lb[m], zt.kinv, -m_sub)));
-        l2 = add2(l2, P2);
-        const int pr = 8 * m + gID;
-        const float4 z01 = vzP[2 * pr], z23 = vzP[2 * pr + 1];
-        const float4 s01 = vsP[2 * pr], s23 = vsP[2 * pr + 1];
-        zacc2[0] = fma2(P2, make_float2(z01.x, z01.y), zacc2[0]);
-        zacc2[1] = fma2(P2, make_float2(z01.z, z01.w), zacc2[1]);
-        zacc2[2] = fma2(P2, make_float2(z23.x, z23.y), zacc2[2]);
-        zacc2[3] = fma2(P2, make_float2(z23.z, z23.w), zacc2[3]);
-        const float2 w[4] = {mul2(P2, make_float2(s01.x, s01.y)), mul2(P2, make_float2(s01.z, s01.w)),
-                             mul2(P2, make_float2(s23.x, s23.y)), mul2(P2, make_float2(s23.z, s23.w))};
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-            const uint32_t wx = __float_as_uint(w[g].x), wy = __float_as_uint(w[g].y);
-            hi[g] = __byte_perm(wx, wy, 0x7632);  // bf16 high parts (truncation)
-            const float2 r = sub2(w[g], make_float2(__uint_as_float(wx & 0xffff0000u),
-                                                    __uint_as_float(wy & 0xffff0000u)));
-            lo[g] = pack_bf16x2_rn(r.x, r.y);     // remainders, rounded
-        }
-        const int c = w_chunk(m, gID, tq, 0);
-        wS[c] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        wS[c ^ 1] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    }
-    __syncwarp();
-
-    // -- values: A rows = dims (m-tile (g, half): in-group index 16 half +
-    //    row, code plane 16 half + row, slot g); k-step j covers tokens
-    //    16 tq + 4 j + {0, 2 | 1, 3} of each lane quad, i.e. the token pairs
-    //    of rows 2j, 2j + 1 of tile tq; columns = (head, part)
-    uint4 pv4[4];  // bytes 16 tq .. 16 tq + 15 of planes gID, 8 + gID, 16 + gID, 24 + gID
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-        pv4[k] = *reinterpret_cast<const uint4*>(blk + kVCodes + (gID + 8 * k) * kPage + 16 * tq);
-    const int rb = tq * 64 + (((gID >> 1) ^ tq) << 1);
-    const int r0 = rb + (gID & 1), r1 = rb + 8 + ((gID & 1) ^ 1);  // w_chunk(tq, 2j + e, gID >> 1, gID & 1) - 16 j
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const uint4 bw0 = wS[r0 + 16 * j], bw1 = wS[r1 + 16 * j];
-        const uint32_t b0[4] = {bw0.x, bw0.y, bw0.z, bw0.w}, b1[4] = {bw1.x, bw1.y, bw1.z, bw1.w};
-        uint32_t pw[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) pw[k] = j == 0 ? pv4[k].x : j == 1 ? pv4[k].y : j == 2 ? pv4[k].z : pv4[k].w;
-        const uint32_t pw8[4] = {pw[0] >> 8, pw[1] >> 8, pw[2] >> 8, pw[3] >> 8};
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                const uint32_t r0w = pw[2 * half], r1w = pw[2 * half + 1];
-                const uint32_t r08 = pw8[2 * half], r18 = pw8[2 * half + 1];
-                uint32_t a0, a1, a2, a3;
-                switch (g) {
-                    case 0: v_operands<0>(r0w, r1w, r08, r18, a0, a1, a2, a3); break;
-                    case 1: v_operands<1>(r0w, r1w, r08, r18, a0, a1, a2, a3); break;
-                    case 2: v_operands<2>(r0w, r1w, r08, r18, a0, a1, a2, a3); break;
-                    default: v_operands<3>(r0w, r1w, r08, r18, a0, a1, a2, a3); break;
-                }
-                mma_bf16_16816(acc_o[2 * g + half], a0, a1, a2, a3, b0[g], b1[g]);
-            }
-        }
-    }
-}
-
 // Split two fp32 values into bf16x2 registers of their high parts (the
 // values with the low 16 bits cleared) and of the rounded remainders.
 __device__ __forceinline__ void split_both(float2 w, uint32_t& hi, uint32_t& lo) {
@@ -1078,7 +740,8 @@ __device__ __forceinline__ void split_both(float2 w, uint32_t& hi, uint32_t& lo)
 // holds heads 2tq and 2tq + 1.
 template <bool FULL, bool BOOST = false, bool LM = false>
 __device__ __forceinline__ void attend_page_g8(const uint8_t* blk, int valid, uint8_t* wbuf, const uint2* qfS,
-                                               const float4 (&qsv)[2], float (&m_run)[2], float (&l_run)[2],
+                                               const float4 (&qsv)[2], float kq, float (&m_run)[2],
+                                               float (&l_run)[2],
                                                float (&zacc)[2][4], float (&acc_o)[8][4],
                                                int gshift, const float4* qbS = nullptr,
                                                const uint8_t* brec = nullptr, const Codebook& cbk = {}) {
@@ -1097,8 +760,9 @@ __device__ __forceinline__ void attend_page_g8(const uint8_t* blk, int valid, ui
         br1 = __ldg(reinterpret_cast<const uint4*>(brec) + 2 * lane + 1);
     }
 
-    if constexpr (LM) page_scales<FULL>(blk, valid, gshift, ksS, kzS, vzS, vsS, cbk.ka, cbk.va);
-    else page_scales<FULL>(blk, valid, gshift, ksS, kzS, vzS, vsS);
+    // K scales times 2^-e (the power of two of the q' fragments)
+    if constexpr (LM) page_scales<FULL>(blk, valid, gshift, ksS, kzS, vzS, vsS, cbk.ka * kq, cbk.va);
+    else page_scales<FULL>(blk, valid, gshift, ksS, kzS, vzS, vsS, kq);
     __syncwarp();
 
     // -- logits: lg[m] = (token a, head 2tq), (a, 2tq+1), (b, 2tq), (b, 2tq+1)
@@ -1142,14 +806,12 @@ __device__ __forceinline__ void attend_page_g8(const uint8_t* blk, int valid, ui
                         break;
                 }
                 const uint2 qh = qfS[(0 * 8 + ks) * 32 + lane], ql = qfS[(1 * 8 + ks) * 32 + lane];
-                const uint2 qe = qfS[(2 * 8 + ks) * 32 + lane];
-                mma_bf16_16816(acc[g], a0, a1, a2, a3, qh.x, qh.y);
-                mma_bf16_16816(acc[g], a0, a1, a2, a3, ql.x, ql.y);
-                mma_bf16_16816(acc[g], a0, a1, a2, a3, qe.x, qe.y);
-                if (LM) {  // high-bit plane against kappa q' (parts 3, 4: hi, lo)
-                    const uint2 kh = qfS[(3 * 8 + ks) * 32 + lane], kl = qfS[(4 * 8 + ks) * 32 + lane];
-                    mma_bf16_16816(acc[g], c0, c1, c2, c3, kh.x, kh.y);
-                    mma_bf16_16816(acc[g], c0, c1, c2, c3, kl.x, kl.y);
+                mma_f16_16816(acc[g], a0, a1, a2, a3, qh.x, qh.y);
+                mma_f16_16816(acc[g], a0, a1, a2, a3, ql.x, ql.y);
+                if (LM) {  // high-bit plane against kappa q' (parts 2, 3: hi, lo)
+                    const uint2 kh = qfS[(2 * 8 + ks) * 32 + lane], kl = qfS[(3 * 8 + ks) * 32 + lane];
+                    mma_f16_16816(acc[g], c0, c1, c2, c3, kh.x, kh.y);
+                    mma_f16_16816(acc[g], c0, c1, c2, c3, kl.x, kl.y);
                 }
             }
             const float4 sA = ksS[ta], sB = ksS[ta + 8], zA = kzS[ta], zB = kzS[ta + 8];
@@ -1324,19 +986,16 @@ __device__ __forceinline__ void attend_page_g8(const uint8_t* blk, int valid, ui
 template <int NT, bool LM = false, bool BOOST = false>
 __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(DecodeParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
-    // the uniform-level path for up to four heads runs attend_page_v2
-    constexpr bool V2 = (NT == 1 && !LM && !BOOST);
-    using SM = Int2Smem<NT, V2>;
+    using SM = Int2Smem<NT>;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint8_t* stages = smem + SM::kStage;
     StageInfo* info = reinterpret_cast<StageInfo*>(smem + SM::kInfo);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::kBars);
-    constexpr int NS = SM::NS;              // ring stages
-    uint64_t* empty = full + NS;
-    uint64_t* merge_bar = empty + NS;  // consumer-warp rendezvous at item ends
+    uint64_t* empty = full + kStages;
+    uint64_t* merge_bar = empty + kStages;  // consumer-warp rendezvous at item ends
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NS; ++s) {
+        for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
@@ -1351,13 +1010,13 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
         // ------------------------------ producer ------------------------------
         const int total_long = __ldg(p.item_start + p.B);
         const int total = total_long + __ldg(p.item_start2 + p.B);
-        uint32_t n = 0;      // slots issued so far (stage n % NS, warp n % 4)
+        uint32_t n = 0;      // slots issued so far (stage n % kStages, warp n % 4)
         bool ok = true;
         // one slot: wait for the stage, then publish its info (and copy)
         auto post = [&](int item, int b, int kv, int pid, int valid, int flags) -> bool {
-            const uint32_t s = n % NS;
-            if (n >= (uint32_t)NS) {
-                const bool w = mbar_wait_bounded(&empty[s], ((n / NS) - 1) & 1u, kWaitPolls);
+            const uint32_t s = n % kStages;
+            if (n >= (uint32_t)kStages) {
+                const bool w = mbar_wait_bounded(&empty[s], ((n / kStages) - 1) & 1u, kWaitPolls);
                 if (!__all_sync(kFull, w)) return false;
             }
             if (lane == 0) {
@@ -1426,9 +1085,9 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
         if (!ok) {
             if (lane == 0) report(p.status, OSCAR_STATUS_TIMEOUT);
             // let issued copies land before the block can exit
-            const uint32_t first = n > (uint32_t)NS ? n - NS : 0;
+            const uint32_t first = n > (uint32_t)kStages ? n - kStages : 0;
             for (uint32_t k = first; k < n; ++k)
-                (void)mbar_wait_bounded(&full[k % NS], (k / NS) & 1u, kWaitPolls);
+                (void)mbar_wait_bounded(&full[k % kStages], (k / kStages) & 1u, kWaitPolls);
         }
         return;
     }
@@ -1449,21 +1108,16 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
         return __all_sync(kFull, w);
     };
 
-    uint2* qfS = reinterpret_cast<uint2*>(smem + SM::kQf);            // eight heads: [3][8][32]
-    uint4* qf4 = reinterpret_cast<uint4*>(smem + SM::kQf);            // up to four heads: [8][32]
-    uint2* qkS = reinterpret_cast<uint2*>(smem + SM::kQf + SM::kQfBytes);  // Lloyd-Max, up to four heads: kappa q'
-    float4* qbS = reinterpret_cast<float4*>(smem + SM::kQf + SM::kQfBytes);  // boost: q' of the four heads
+    uint2* qfS = reinterpret_cast<uint2*>(smem + SM::kQf);
+    float4* qbS = reinterpret_cast<float4*>(smem + SM::kQf + NT * 8 * 32 * 8);  // boost: q' of the four heads
     float4 qsv[NT];
+    float kq = 1.f;  // the item's 2^-e (prep's power of two of q'), folded into the K scales
     float m_run[NT], l_run[NT], zacc[NT][4], acc_o[NT][8][4];
     Codebook cbk{1.f, 1.f, 0.f, 0.f};  // Lloyd-Max levels of the current item's KV head
-    ZTerm zt{0u, 1.f, 1.f};             // attend_page_v2: zero-point B fragment and logit scaling
-    float2 l2 = make_float2(0.f, 0.f), zacc2[4];  // attend_page_v2: softmax sums of the lane's two tokens
-#pragma unroll
-    for (int g = 0; g < 4; ++g) zacc2[g] = make_float2(0.f, 0.f);
 
     for (uint32_t n = warp;; n += kConsumerWarps) {
-        const uint32_t s = n % NS;
-        const bool w = mbar_wait_bounded(&full[s], (n / NS) & 1u, kWaitPolls);
+        const uint32_t s = n % kStages;
+        const bool w = mbar_wait_bounded(&full[s], (n / kStages) & 1u, kWaitPolls);
         if (!__all_sync(kFull, w)) {
             if (lane == 0) report(p.status, OSCAR_STATUS_TIMEOUT);
             return;
@@ -1476,41 +1130,32 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
         if (flags & kFlagFirst) {
             const int bk = sraw.y * p.hk + sraw.z;
             if (LM) cbk = codebook_of(p.codebook, sraw.z);
-            {   // q' fragments of the item (every warp writes the same values)
-                const uint32_t* fr = p.qfrag + (size_t)bk * NT * 1024;
-                if constexpr (NT == 1) {
+            kq = p.qkinv[bk];
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint4 f = *reinterpret_cast<const uint4*>(fr + ((size_t)ks * 32 + lane) * 4);
-                        qf4[ks * 32 + lane] = f;
-                        if (LM) qkS[ks * 32 + lane] = scaled_fragment(make_uint2(f.x, f.y), cbk.kk, (lane >> 2) & 1);
-                    }
-                } else {
+            for (int nt = 0; nt < NT; ++nt) {
+                const uint32_t* fr = p.qfrag + ((size_t)bk * NT + nt) * 8 * 32 * 2;
 #pragma unroll
-                    for (int i = 0; i < 3 * 8; ++i)
-                        qfS[i * 32 + lane] = *reinterpret_cast<const uint2*>(fr + ((size_t)i * 32 + lane) * 2);
-                    if constexpr (LM) {  // eight heads: kappa q' (from the high and low parts) into parts 3, 4
+                for (int ks = 0; ks < 8; ++ks) {  // every warp writes the same values
+                    const uint2 f = *reinterpret_cast<const uint2*>(fr + ((size_t)ks * 32 + lane) * 2);
+                    qfS[(nt * 8 + ks) * 32 + lane] = f;
+                    if (LM && NT == 1) qfS[((NT + nt) * 8 + ks) * 32 + lane] = scaled_fragment(f, cbk.kk, (lane >> 2) & 1);
+                }
+                if constexpr (LM && NT == 2) {  // eight heads: parts 0, 1 are q' hi, lo; kappa q' into parts 2, 3
+                    if (nt == 1) {
 #pragma unroll
                         for (int ks = 0; ks < 8; ++ks) {
                             const uint2 hh = qfS[(0 * 8 + ks) * 32 + lane], ll = qfS[(1 * 8 + ks) * 32 + lane];
-                            const float y[4] = {cbk.kk * (bf16_lo(hh.x) + bf16_lo(ll.x)),
-                                                cbk.kk * (bf16_hi(hh.x) + bf16_hi(ll.x)),
-                                                cbk.kk * (bf16_lo(hh.y) + bf16_lo(ll.y)),
-                                                cbk.kk * (bf16_hi(hh.y) + bf16_hi(ll.y))};
-                            float yh[4], yl[4];
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                yh[i] = __bfloat162float(__float2bfloat16_rn(y[i]));
-                                yl[i] = __bfloat162float(__float2bfloat16_rn(y[i] - yh[i]));
-                            }
-                            qfS[(3 * 8 + ks) * 32 + lane] = make_uint2(pack_bf16x2_rn(yh[0], yh[1]), pack_bf16x2_rn(yh[2], yh[3]));
-                            qfS[(4 * 8 + ks) * 32 + lane] = make_uint2(pack_bf16x2_rn(yl[0], yl[1]), pack_bf16x2_rn(yl[2], yl[3]));
+                            const float y[4] = {cbk.kk * (half_lo(hh.x) + half_lo(ll.x)),
+                                                cbk.kk * (half_hi(hh.x) + half_hi(ll.x)),
+                                                cbk.kk * (half_lo(hh.y) + half_lo(ll.y)),
+                                                cbk.kk * (half_hi(hh.y) + half_hi(ll.y))};
+                            uint32_t h01, h23, l01, l23;
+                            split_f16(y, h01, h23, l01, l23);
+                            qfS[(2 * 8 + ks) * 32 + lane] = make_uint2(h01, h23);
+                            qfS[(3 * 8 + ks) * 32 + lane] = make_uint2(l01, l23);
                         }
                     }
                 }
-            }
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
                 if constexpr (BOOST) {  // q'[j] of heads 4nt..4nt+3 as float4 NT * j + nt
                     const float* qr = p.qrot + ((size_t)bk * NT + nt) * 4 * kD + 4 * lane;
                     const float4 a0 = *reinterpret_cast<const float4*>(qr), a1 = *reinterpret_cast<const float4*>(qr + kD);
@@ -1533,35 +1178,24 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
 #pragma unroll
                     for (int e = 0; e < 4; ++e) acc_o[nt][mt][e] = 0.f;
             }
-            if constexpr (V2) {
-                zt = zterm_of(p.qsum, bk, p.gshift);
-                l2 = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int g = 0; g < 4; ++g) zacc2[g] = make_float2(0.f, 0.f);
-            }
         }
 
         if (!(flags & kFlagPad)) {
             const uint8_t* brec = nullptr;
             if constexpr (BOOST) brec = p.boost + ((size_t)info[s].pid * p.hk + sraw.z) * kBoostBlock;
-            if constexpr (V2) {
+            if constexpr (NT == 2) {
                 if (valid == kPage)
-                    attend_page_v2<true>(blk, valid, wbuf, qf4, zt, m_run[0], l2, zacc2, acc_o[0], p.gshift);
-                else
-                    attend_page_v2<false>(blk, valid, wbuf, qf4, zt, m_run[0], l2, zacc2, acc_o[0], p.gshift);
-            } else if constexpr (NT == 2) {
-                if (valid == kPage)
-                    attend_page_g8<true, BOOST, LM>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o[0],
+                    attend_page_g8<true, BOOST, LM>(blk, valid, wbuf, qfS, qsv, kq, m_run, l_run, zacc, acc_o[0],
                                                     p.gshift, qbS, brec, cbk);
                 else
-                    attend_page_g8<false, BOOST, LM>(blk, valid, wbuf, qfS, qsv, m_run, l_run, zacc, acc_o[0],
+                    attend_page_g8<false, BOOST, LM>(blk, valid, wbuf, qfS, qsv, kq, m_run, l_run, zacc, acc_o[0],
                                                      p.gshift, qbS, brec, cbk);
             } else {
                 if (valid == kPage)
-                    attend_page<NT, true, LM, BOOST>(blk, valid, wbuf, qf4, qkS, qsv, m_run, l_run, zacc, acc_o,
+                    attend_page<NT, true, LM, BOOST>(blk, valid, wbuf, qfS, qsv, kq, m_run, l_run, zacc, acc_o,
                                                      take_lo, p.gshift, cbk, qbS, brec);
                 else
-                    attend_page<NT, false, LM, BOOST>(blk, valid, wbuf, qf4, qkS, qsv, m_run, l_run, zacc, acc_o,
+                    attend_page<NT, false, LM, BOOST>(blk, valid, wbuf, qfS, qsv, kq, m_run, l_run, zacc, acc_o,
                                                       take_lo, p.gshift, cbk, qbS, brec);
             }
         }
@@ -1573,14 +1207,14 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
             float* mw = reinterpret_cast<float*>(wbuf);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                float l = V2 ? l2.x + l2.y : l_run[nt];
+                float l = l_run[nt];
                 l += __shfl_xor_sync(kFull, l, 4);
                 l += __shfl_xor_sync(kFull, l, 8);
                 l += __shfl_xor_sync(kFull, l, 16);
                 float z[4];
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
-                    z[g] = V2 ? zacc2[g].x + zacc2[g].y : zacc[nt][g];
+                    z[g] = zacc[nt][g];
                     z[g] += __shfl_xor_sync(kFull, z[g], 4);
                     z[g] += __shfl_xor_sync(kFull, z[g], 8);
                     z[g] += __shfl_xor_sync(kFull, z[g], 16);
@@ -1975,10 +1609,9 @@ __global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(DecodeParams p)
         const int s0 = __ldg(p.item_start + b), t0 = __ldg(p.item_start2 + b);
         const int n_long = (__ldg(p.item_start + b + 1) - s0) / p.hk;
         const int n_short = (__ldg(p.item_start2 + b + 1) - t0) / p.hk;
-        const int splits = (n_long + n_short) << p.part_shift;   // partials: one or two per item
+        const int splits = n_long + n_short;
         const int first = s0 + kv * n_long;
         const int first2 = __ldg(p.item_start + p.B) + t0 + kv * n_short - n_long;
-        const int pmask = (1 << p.part_shift) - 1;
         // this warp's splits sub, sub + wpr, ..., merged by online log-sum-exp
         // in batches whose loads (statistics and this lane's four values of
         // each split) are all issued before any is used
@@ -1992,9 +1625,9 @@ __global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(DecodeParams p)
 #pragma unroll
                 for (int k = 0; k < 4; ++k) ov[i][k] = 0.f;
                 if (i0 + i < nmine) {
-                    const int spp = sub + wpr * (i0 + i), sp = spp >> p.part_shift;
-                    const size_t row = (size_t)(sp < n_long ? first + sp : first2 + sp);
-                    const float* pt = p.part + ((row << p.part_shift) + (spp & pmask)) * p.part_stride;
+                    const int sp = sub + wpr * (i0 + i);
+                    const float* pt =
+                        p.part + (size_t)(sp < n_long ? first + sp : first2 + sp) * p.part_stride;
                     ms[i] = pt[(size_t)p.G * kD + hh];
                     ls[i] = pt[(size_t)p.G * kD + p.G + hh];
 #pragma unroll
@@ -2143,7 +1776,7 @@ static Int2Attr& attr_for_device(int dev) {
 
 template <int NT, bool LM = false, bool BOOST = false>
 static cudaError_t launch_int2(const DecodeParams& p, cudaStream_t st, int sms, bool& attr_set) {
-    const int smem = (LM || BOOST) ? Int2Smem<NT>::kBytesLM : Int2Smem<NT, NT == 1>::kBytes;
+    const int smem = (LM || BOOST) ? Int2Smem<NT>::kBytesLM : Int2Smem<NT>::kBytes;
     if (!attr_set) {
         cudaError_t e =
             cudaFuncSetAttribute(int2_kernel<NT, LM, BOOST>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -2195,9 +1828,7 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st, cudaEvent_t ev
     dim3 pg((p.B + kPrepSeqs - 1) / kPrepSeqs + 1, p.hk);
     if ((e = launch_pdl(prep_kernel, pg, dim3(kPrepThreads), kPrepSmem, st, p)) != cudaSuccess) return e;
     if (ev_int2_start && (e = cudaEventRecord(ev_int2_start, st)) != cudaSuccess) return e;
-    if (p.tc)  // up to four heads, uniform levels: tensor-memory kernel
-        e = launch_int2_tc(p, st, at.sms);
-    else if (p.codebook)  // Lloyd-Max levels
+    if (p.codebook)  // Lloyd-Max levels
         e = (p.NT == 1) ? launch_int2<1, true>(p, st, at.sms, at.setl) : launch_int2<2, true>(p, st, at.sms, at.setl2);
     else if (p.boost)  // K channel boost
         e = (p.NT == 1) ? launch_int2<1, false, true>(p, st, at.sms, at.setk)

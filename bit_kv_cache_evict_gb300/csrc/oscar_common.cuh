@@ -66,6 +66,22 @@ __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
 }
+// f16x2 with lo -> bits 0-15, hi -> bits 16-31, round to nearest even
+__device__ __forceinline__ uint32_t pack_f16x2_rn(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+// Split four fp32 values into two f16x2 pairs each: the values rounded to
+// fp16 (high parts) and the rounded remainders (low parts); together they
+// carry 22 significant bits of every value whose remainder is a normal fp16.
+__device__ __forceinline__ void split_f16(const float (&v)[4], uint32_t& h01, uint32_t& h23, uint32_t& l01,
+                                          uint32_t& l23) {
+    h01 = pack_f16x2_rn(v[0], v[1]);
+    h23 = pack_f16x2_rn(v[2], v[3]);
+    l01 = pack_f16x2_rn(v[0] - half_lo(h01), v[1] - half_hi(h01));
+    l23 = pack_f16x2_rn(v[2] - half_lo(h23), v[3] - half_hi(h23));
+}
 
 __device__ __forceinline__ uint32_t rotr(uint32_t x, uint32_t n) { return __funnelshift_r(x, x, n); }
 
@@ -102,24 +118,32 @@ __device__ __forceinline__ uint32_t code_pair_hi(uint32_t x, uint32_t x8) {
     else return x8 & (0x00030003u << (2 * SLOT));
 }
 
-// Fixed power-of-two scalings of the INT2 decode (all exact):
-//   q' enters the K products as q' * 2^kQUp;
-//   the K products of slot k are then c q' 2^(slot_bit(k) - 133 + kQUp), so
-//   the K scale s is stored as s * 2^(133 - kQUp - slot_bit(k));
-//   the V products use B = p * s * 2^(kVUp - slot_bit(k)), which puts every
-//   P.V accumulator at 2^(kVUp - 133) * sum(p s c);
-//   the item's output multiplies the accumulators back by 2^(133 - kVUp).
-// Ranges: |q'| < 2^64 and s <= 65504 keep every operand finite in bf16; a
-// product falls below the normal fp32 range only for |q'| < 2^-57 or
-// p * s < 2^-96, far below anything that moves a logit or an output.
-constexpr int kQUp = 64, kVUp = 103;
+// Power-of-two scalings of the INT2 decode (all exact):
+//   K products run in fp16 (mma kind f16): the same code bit pattern read
+//   as fp16 is c * 2^(slot_bit(k) - 24) (fp16 subnormals join the first
+//   normal binade without a gap as well), and q' enters as q' * 2^e, one e
+//   per (sequence, KV head) chosen by prep so that the largest |q'| of the
+//   KV group's heads (times the Lloyd-Max plane weight, where it is above
+//   1) lies in [2^13, 2^14): the fp16 high and low parts then hold q' to 22
+//   bits (to an absolute 2^-25 * 2^-e below 2^-3 * 2^-e);
+//   the K scale s is stored as s * 2^(24 - slot_bit(k) - e), which gives the
+//   logit's products their true scale;
+//   the V products (bf16) use B = p * s * 2^(kVUp - slot_bit(k)), which
+//   puts every P.V accumulator at 2^(kVUp - 133) * sum(p s c); the item's
+//   output multiplies the accumulators back by 2^(133 - kVUp).
+// Ranges: K operands are below 2^14 and K products above 2^-46 (normal
+// fp32); s <= 65504 keeps every V operand finite in bf16, and a V product
+// falls below the normal fp32 range only for p * s < 2^-96, far below
+// anything that moves an output.
+constexpr int kVUp = 103;
+constexpr int kQTopExp = 13;  // prep puts each head's largest |q'| in [2^13, 2^14)
 __host__ __device__ __forceinline__ constexpr float pow2f(int e) {
     float r = 1.f;
     for (int i = 0; i < e; ++i) r *= 2.f;
     for (int i = 0; i > e; --i) r *= 0.5f;
     return r;
 }
-__device__ __forceinline__ constexpr float k_scale_up(int slot) { return pow2f(133 - kQUp - slot_bit(slot)); }
+__device__ __forceinline__ constexpr float k_scale_up(int slot) { return pow2f(24 - slot_bit(slot)); }
 __device__ __forceinline__ constexpr float v_scale_up(int slot) { return pow2f(kVUp - slot_bit(slot)); }
 constexpr float kVOutScale = 1073741824.f;  // 2^(133 - kVUp) = 2^30
 
@@ -133,12 +157,6 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
 __device__ __forceinline__ float2 sub2(float2 a, float2 b) {
     float2 r;
     asm("{.reg .b64 A, B, C; mov.b64 A, {%2, %3}; mov.b64 B, {%4, %5}; sub.rn.f32x2 C, A, B; mov.b64 {%0, %1}, C;}"
-        : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return r;
-}
-__device__ __forceinline__ float2 add2(float2 a, float2 b) {
-    float2 r;
-    asm("{.reg .b64 A, B, C; mov.b64 A, {%2, %3}; mov.b64 B, {%4, %5}; add.rn.f32x2 C, A, B; mov.b64 {%0, %1}, C;}"
         : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
     return r;
 }
@@ -191,19 +209,18 @@ __device__ __forceinline__ uint32_t split_w_pair(float2 p, float2 s, const Split
 // adjacent pairs (the two token pairs of a PV B-operand register).
 __device__ __forceinline__ int pv_slot(int t) { return (t & ~3) | ((t & 1) << 1) | ((t >> 1) & 1); }
 
-// D += A(16x16 f16, row) * B(16x8 f16, col), fp32 accumulate
-__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                              uint32_t b0, uint32_t b1) {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
 // D += A(16x16 bf16, row) * B(16x8 bf16, col), fp32 accumulate
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                                uint32_t a3, uint32_t b0, uint32_t b1) {
     asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// The same product with fp16 operands (the K side of the INT2 decode).
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -321,8 +338,9 @@ struct DecodeParams {
     int32_t* counter;     // [1]
     int32_t* item_start;  // [B + 1] long items before sequence b (prefix sums)
     int32_t* item_start2; // [B + 1] short tail items before sequence b
-    uint32_t* qfrag;      // [B*Hk][NT * 1024] words: up to four heads [8][32] uint4, eight heads [3][8][32] uint2
-    float* qsum;          // [B*Hk][NT*4][4]
+    uint32_t* qfrag;      // [B*Hk][NT][8][32][2] fp16 q' fragments (times 2^e_h)
+    float* qsum;          // [B*Hk][NT*4][4] group sums of q' (times 2^e_h)
+    float* qkinv;         // [B*Hk] 2^-e of the (sequence, KV head)'s q' fragments
     float* qrot;          // [B*Hk][4][kD] q' in stored order (fp32), written when boost is set
     float* part;          // [max_items][part_stride]
     float* bf_part;       // [B*Hk][bf_items][part_stride]
@@ -335,20 +353,7 @@ struct DecodeParams {
     float qscale;  // sm_scale * log2(e)
     const float* codebook;  // [hk][2] Lloyd-Max inner level a, or null (uniform levels)
     const uint8_t* boost;   // K boost records [num_pages][hk][kBoostBlock], or null (no boost)
-    // tensor-memory INT2 kernel (int2_tc_kernel, up to four heads, uniform levels)
-    uint8_t* kimg;          // [B*Hk][kTcKImg] q' B-operand images of int2_tc_kernel, or null
-    int tc;                 // 1: the INT2 segment runs int2_tc_kernel
-    int part_shift;         // log2(partials per split-K item): 1 with int2_tc_kernel (one per math group), else 0
 };
-
-// q' B-operand image of int2_tc_kernel, per (sequence, KV head): for each
-// of the eight k-steps (16 stored positions of one 32-position block, in the
-// A-operand column order), a 16 (k) x 16 (n = 4 part + head: bf16 high, low
-// and third part of q' 2^64 for up to four heads; columns 12-15 zero) bf16
-// matrix in the no-swizzle core-matrix layout (element (n, k) at
-// 2 (n % 8) + 16 (k % 8) + 256 (n / 8) + 128 (k / 8)), 512 bytes each.
-constexpr int kTcKStep = 512;
-constexpr int kTcKImg = 8 * kTcKStep;
 
 // Split-K geometry of one sequence with npg history pages: the last
 // min(npg, tail_pg) pages go to short items of kShortItemPages, the rest to
@@ -402,7 +407,6 @@ struct FitParams {
 cudaError_t launch_calibrate_codebook(const FitParams& p, cudaStream_t st);
 
 cudaError_t launch_evict(const EvictParams& p, cudaStream_t st);
-cudaError_t launch_int2_tc(const DecodeParams& p, cudaStream_t st, int sms);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st, cudaEvent_t ev_int2_start,
                           cudaEvent_t ev_int2_stop);
 

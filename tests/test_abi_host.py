@@ -128,3 +128,23 @@ def test_variant_calls_validate_before_launch(lib):
                                           None, fake, 1, 1, 1, None, None) == O.OSCAR_ERR_INVALID_ARG
     assert lib.oscar_evict_quantize_boost(ctypes.byref(sh), 0, None, 0, None, None, None, None, None, None, None,
                                           None, None, 1, 1, 1, None, None) == O.OSCAR_OK          # nothing to do
+
+
+def test_workspace_query_rejects_int32_overflow(lib):
+    """Split-K item counts and partial offsets are int32 on the device: a
+    batch x pages shape whose item count (or partial-buffer word count) does
+    not fit is rejected by the workspace query itself, on the host, instead
+    of wrapping.  Items per (sequence, KV head) = ceil(max_pages / pps) + 2
+    short tail items, pps = 256 pages for these sizes."""
+    sh = O.make_shape(32, 8)                       # G = 4: a partial is 4 x 130 floats
+    ws = ctypes.c_size_t(0)
+
+    def query(batch, max_pages):
+        return lib.oscar_decode_attn(ctypes.byref(sh), batch, None, None, None, None, None, max_pages, 0, None,
+                                     None, ctypes.c_float(1.0), None, None, ctypes.byref(ws), None, None)
+
+    assert query(1024, 2048) == O.OSCAR_OK         # 8192 x (8 + 2) items
+    assert 81920 * 520 * 4 < ws.value < 2 * 81920 * 520 * 4 + (1 << 28)
+    assert query(1 << 20, 1 << 16) == O.OSCAR_ERR_INVALID_ARG    # 2^23 x 258 items > 2^31 - 1
+    assert query(1 << 16, 1 << 12) == O.OSCAR_ERR_INVALID_ARG    # 9.4e6 items x 520 words > 4e9 words
+    assert query(1 << 14, 1 << 12) == O.OSCAR_OK                 # 2.4e6 items x 520 words = 1.2e9 words
