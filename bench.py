@@ -722,7 +722,7 @@ def run_oscar(args, rank: int, world: int, local: int) -> None:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
             "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "int2 codes x fp16 hi/lo q' (logits), x bf16 hi/lo p*s (P.V) on tensor cores, fp32 accumulate", "data": "synthetic",
+            "dtype": "int2 codes x fp16 hi/lo operands (q', p*s) on tensor cores, fp32 accumulate", "data": "synthetic",
             "config": config_of(w, L, args.quant_group, args.codebook, args.boost),
             "decode_tokens_per_s": world * w.batch * K / (t_ms_max / 1e3),
             "bits_per_element": bpe,

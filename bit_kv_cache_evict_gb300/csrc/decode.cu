@@ -12,9 +12,8 @@
 //                     history pages of one (sequence, KV head)), streams the
 //                     6 KB page blocks into shared memory with bulk async
 //                     copies, and runs both products on tensor cores
-//                     (mma.sync m16n8k16, fp16 for the logits and bf16
-//                     for P.V, fp32 accumulate) straight from the packed
-//                     codes.
+//                     (mma.sync m16n8k16 fp16 -> fp32) straight from the
+//                     packed codes.
 //   bf16_kernel       sink + recent window per (sequence, KV head).
 //   merge_kernel      log-sum-exp merge of the INT2 splits, un-rotation by
 //                     R_V^T (bit-reversal, Hadamard, U_V^T), merge with the
@@ -28,10 +27,10 @@
 //       D_tb = sum_{j in b} c_tj 2^(P_b - 24) q'_j 2^e   (fp16 MMA, tokens x heads),
 //       s~_tb = s_tb 2^(24 - P_b - e),  Q_b = sum_{j in b} q'_j,
 //       e one power of two per (sequence, KV head) from prep;
-//   o'_j   = 2^(133 - kVUp) sum_t W_t,b(j) c_tj 2^(P_b - 133) + sum_t p_t z_tb,
-//       W_tb = p_t s_tb 2^(kVUp - P_b)                  (bf16 MMA, dims x heads).
-// q' 2^e is split into fp16 hi + lo (22 bits), W into bf16 hi + lo (~17
-// bits); codes are exact in both formats and carry no offset.
+//   o'_j   = 2^(24 - P_b) sum_t W_t,b(j) c_tj 2^(P_b - 24) + sum_t p_t z_tb,
+//       W_tb = p_t s_tb                                  (fp16 MMA, dims x heads).
+// q' 2^e and W are split into fp16 hi + lo (22 bits); codes are exact and
+// carry no offset.
 #include "oscar_common.cuh"
 
 namespace oscar {
@@ -324,23 +323,23 @@ __device__ __forceinline__ int find_seq(const int32_t* item_start, int B, int it
 // A-operand registers of one K k-step (slot g, word half h) from the
 // token-row words of rows gID and gID + 8 (w*) and their >> 8 copies (w*8).
 template <int G>
-__device__ __forceinline__ void k_operands(uint32_t wa, uint32_t wb, uint32_t wa8, uint32_t wb8, uint32_t& a0,
+__device__ __forceinline__ void k_operands(uint32_t wa, uint32_t wb, uint32_t was, uint32_t wbs, uint32_t& a0,
                                            uint32_t& a1, uint32_t& a2, uint32_t& a3) {
-    a0 = code_pair_lo<G>(wa);
-    a1 = code_pair_lo<G>(wb);
-    a2 = code_pair_hi<G>(wa, wa8);
-    a3 = code_pair_hi<G>(wb, wb8);
+    a0 = code_pair_lo<G>(wa, was);
+    a1 = code_pair_lo<G>(wb, wbs);
+    a2 = code_pair_hi<G>(wa, was);
+    a3 = code_pair_hi<G>(wb, wbs);
 }
 
 // A-operand registers of one V m-tile half (slot g): plane words r0, r1 and
 // their >> 8 copies.
 template <int G>
-__device__ __forceinline__ void v_operands(uint32_t r0, uint32_t r1, uint32_t r08, uint32_t r18, uint32_t& a0,
+__device__ __forceinline__ void v_operands(uint32_t r0, uint32_t r1, uint32_t r0s, uint32_t r1s, uint32_t& a0,
                                            uint32_t& a1, uint32_t& a2, uint32_t& a3) {
-    a0 = code_pair_lo<G>(r0);
-    a1 = code_pair_lo<G>(r1);
-    a2 = code_pair_hi<G>(r0, r08);
-    a3 = code_pair_hi<G>(r1, r18);
+    a0 = code_pair_lo<G>(r0, r0s);
+    a1 = code_pair_lo<G>(r1, r1s);
+    a2 = code_pair_hi<G>(r0, r0s);
+    a3 = code_pair_hi<G>(r1, r1s);
 }
 
 // Position of token t (0..63) in the warp's probability and V-scale rows.
@@ -359,7 +358,7 @@ constexpr int kPvRow = 72;  // floats per probability / V-scale row (64 + 8: con
 
 // The page's scales into the warp's scratch: for each token row and each
 // 32-position block b (quantisation group b >> GS), fp32 s scaled by the
-// block's fixed power of two (k_scale_up / v_scale_up) and z; rows past the
+// block's power of two (K: k_scale_up) and z; rows past the
 // valid tokens are zero.  K rows: s~ and z as float4 per token; V rows: z per
 // token, and s~ in the P.V token order (pv_pos).
 template <bool FULL, int GS>
@@ -391,7 +390,7 @@ __device__ __forceinline__ void page_scales_g(const uint8_t* blk, int valid, flo
             }
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
-                sv[b] = s_g[b >> GS] * (which ? v_scale_up(b) * vmul : k_scale_up(b) * kmul);
+                sv[b] = s_g[b >> GS] * (which ? vmul : k_scale_up(b) * kmul);
                 zz[b] = z_g[b >> GS];
             }
         } else {
@@ -494,7 +493,7 @@ __device__ __forceinline__ void attend_page(const uint8_t* blk, int valid, uint8
     }
 
     // K scales times 2^-e (the power of two of the q' fragments)
-    if constexpr (LM) page_scales<FULL>(blk, valid, gshift, ksS, kzS, vzS, vsS, cbk.ka * kq, cbk.va);
+    if constexpr (LM) page_scales<FULL>(blk, valid, gshift, ksS, kzS, vzS, vsS, cbk.ka * kq, cbk.va * kLmVDown);
     else page_scales<FULL>(blk, valid, gshift, ksS, kzS, vzS, vsS, kq);
     __syncwarp();
 
@@ -510,7 +509,7 @@ __device__ __forceinline__ void attend_page(const uint8_t* blk, int valid, uint8
             const uint2 x = *reinterpret_cast<const uint2*>(blk + kKCodes + ta * 32 + 8 * tq);
             const uint2 y = *reinterpret_cast<const uint2*>(blk + kKCodes + (ta + 8) * 32 + 8 * tq);
             const uint32_t wa[2] = {x.x, x.y}, wb[2] = {y.x, y.y};
-            const uint32_t wa8[2] = {wa[0] >> 8, wa[1] >> 8}, wb8[2] = {wb[0] >> 8, wb[1] >> 8};
+            const uint32_t wa8[2] = {code_swap(wa[0]), code_swap(wa[1])}, wb8[2] = {code_swap(wb[0]), code_swap(wb[1])};
             float acc[4][NT][4];
 #pragma unroll
             for (int g = 0; g < 4; ++g)
@@ -671,7 +670,7 @@ __device__ __forceinline__ void attend_page(const uint8_t* blk, int valid, uint8
         uint32_t pw[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) pw[k] = m == 0 ? pv4[k].x : m == 1 ? pv4[k].y : m == 2 ? pv4[k].z : pv4[k].w;
-        const uint32_t pw8[4] = {pw[0] >> 8, pw[1] >> 8, pw[2] >> 8, pw[3] >> 8};
+        const uint32_t pw8[4] = {code_swap(pw[0]), code_swap(pw[1]), code_swap(pw[2]), code_swap(pw[3])};
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
             const float4 sg = *reinterpret_cast<const float4*>(vsS + g * kPvRow + chunk);
@@ -681,15 +680,15 @@ __device__ __forceinline__ void attend_page(const uint8_t* blk, int valid, uint8
                 if constexpr (LM) {
                     const float2 w0 = mul2(make_float2(pp[nt].x, pp[nt].y), make_float2(sg.x, sg.y));
                     const float2 w1 = mul2(make_float2(pp[nt].z, pp[nt].w), make_float2(sg.z, sg.w));
-                    bb0[nt] = split_pair(w0, take_lo);
-                    bb1[nt] = split_pair(w1, take_lo);
+                    bb0[nt] = split_pair_f16(w0, take_lo);
+                    bb1[nt] = split_pair_f16(w1, take_lo);
                     // the high-bit plane's weights kappa * W
                     const float2 kv2 = make_float2(cbk.vk, cbk.vk);
-                    cc0[nt] = split_pair(mul2(w0, kv2), take_lo);
-                    cc1[nt] = split_pair(mul2(w1, kv2), take_lo);
+                    cc0[nt] = split_pair_f16(mul2(w0, kv2), take_lo);
+                    cc1[nt] = split_pair_f16(mul2(w1, kv2), take_lo);
                 } else {
-                    bb0[nt] = split_w_pair(make_float2(pp[nt].x, pp[nt].y), make_float2(sg.x, sg.y), take_lo);
-                    bb1[nt] = split_w_pair(make_float2(pp[nt].z, pp[nt].w), make_float2(sg.z, sg.w), take_lo);
+                    bb0[nt] = split_w_pair_f16(make_float2(pp[nt].x, pp[nt].y), make_float2(sg.x, sg.y), take_lo);
+                    bb1[nt] = split_w_pair_f16(make_float2(pp[nt].z, pp[nt].w), make_float2(sg.z, sg.w), take_lo);
                 }
             }
 #pragma unroll
@@ -717,21 +716,23 @@ __device__ __forceinline__ void attend_page(const uint8_t* blk, int valid, uint8
                 }
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    mma_bf16_16816(acc_o[nt][2 * g + half], a0, a1, a2, a3, bb0[nt], bb1[nt]);
-                    if (LM) mma_bf16_16816(acc_o[nt][2 * g + half], c0, c1, c2, c3, cc0[LM ? nt : 0], cc1[LM ? nt : 0]);
+                    mma_f16_16816(acc_o[nt][2 * g + half], a0, a1, a2, a3, bb0[nt], bb1[nt]);
+                    if (LM) mma_f16_16816(acc_o[nt][2 * g + half], c0, c1, c2, c3, cc0[LM ? nt : 0], cc1[LM ? nt : 0]);
                 }
             }
         }
     }
 }
 
-// Split two fp32 values into bf16x2 registers of their high parts (the
-// values with the low 16 bits cleared) and of the rounded remainders.
+// Split two fp32 values into f16x2 registers of their high parts (the
+// values with the low 13 bits cleared, see split_pair_f16) and of the
+// rounded remainders.
 __device__ __forceinline__ void split_both(float2 w, uint32_t& hi, uint32_t& lo) {
-    const uint32_t wx = __float_as_uint(w.x), wy = __float_as_uint(w.y);
-    hi = __byte_perm(wx, wy, 0x7632);
-    const float2 r = sub2(w, make_float2(__uint_as_float(wx & 0xffff0000u), __uint_as_float(wy & 0xffff0000u)));
-    lo = pack_bf16x2_rn(r.x, r.y);
+    const float2 h = make_float2(__uint_as_float(__float_as_uint(w.x) & 0xffffe000u),
+                                 __uint_as_float(__float_as_uint(w.y) & 0xffffe000u));
+    hi = pack_f16x2_rn(h.x, h.y);
+    const float2 r = sub2(w, h);
+    lo = pack_f16x2_rn(r.x, r.y);
 }
 
 // attend_page for eight query heads per KV head: the MMA columns are the
@@ -761,7 +762,7 @@ __device__ __forceinline__ void attend_page_g8(const uint8_t* blk, int valid, ui
     }
 
     // K scales times 2^-e (the power of two of the q' fragments)
-    if constexpr (LM) page_scales<FULL>(blk, valid, gshift, ksS, kzS, vzS, vsS, cbk.ka * kq, cbk.va);
+    if constexpr (LM) page_scales<FULL>(blk, valid, gshift, ksS, kzS, vzS, vsS, cbk.ka * kq, cbk.va * kLmVDown);
     else page_scales<FULL>(blk, valid, gshift, ksS, kzS, vzS, vsS, kq);
     __syncwarp();
 
@@ -777,7 +778,7 @@ __device__ __forceinline__ void attend_page_g8(const uint8_t* blk, int valid, ui
             const uint2 x = *reinterpret_cast<const uint2*>(blk + kKCodes + ta * 32 + 8 * tq);
             const uint2 y = *reinterpret_cast<const uint2*>(blk + kKCodes + (ta + 8) * 32 + 8 * tq);
             const uint32_t wa[2] = {x.x, x.y}, wb[2] = {y.x, y.y};
-            const uint32_t wa8[2] = {wa[0] >> 8, wa[1] >> 8}, wb8[2] = {wb[0] >> 8, wb[1] >> 8};
+            const uint32_t wa8[2] = {code_swap(wa[0]), code_swap(wa[1])}, wb8[2] = {code_swap(wb[0]), code_swap(wb[1])};
             float acc[4][4];
 #pragma unroll
             for (int g = 0; g < 4; ++g)
@@ -935,7 +936,7 @@ __device__ __forceinline__ void attend_page_g8(const uint8_t* blk, int valid, ui
         uint32_t pw[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) pw[k] = m == 0 ? pv4[k].x : m == 1 ? pv4[k].y : m == 2 ? pv4[k].z : pv4[k].w;
-        const uint32_t pw8[4] = {pw[0] >> 8, pw[1] >> 8, pw[2] >> 8, pw[3] >> 8};
+        const uint32_t pw8[4] = {code_swap(pw[0]), code_swap(pw[1]), code_swap(pw[2]), code_swap(pw[3])};
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
             const float4 sg = *reinterpret_cast<const float4*>(vsS + g * kPvRow + chunk);
@@ -972,11 +973,11 @@ __device__ __forceinline__ void attend_page_g8(const uint8_t* blk, int valid, ui
                         if (LM) high_planes<3>(a0, a1, a2, a3, c0, c1, c2, c3);
                         break;
                 }
-                mma_bf16_16816(acc_o[2 * g + half], a0, a1, a2, a3, bh0, bh1);
-                mma_bf16_16816(acc_o[2 * g + half], a0, a1, a2, a3, bl0, bl1);
+                mma_f16_16816(acc_o[2 * g + half], a0, a1, a2, a3, bh0, bh1);
+                mma_f16_16816(acc_o[2 * g + half], a0, a1, a2, a3, bl0, bl1);
                 if (LM) {
-                    mma_bf16_16816(acc_o[2 * g + half], c0, c1, c2, c3, ch0, ch1);
-                    mma_bf16_16816(acc_o[2 * g + half], c0, c1, c2, c3, cl0, cl1);
+                    mma_f16_16816(acc_o[2 * g + half], c0, c1, c2, c3, ch0, ch1);
+                    mma_f16_16816(acc_o[2 * g + half], c0, c1, c2, c3, cl0, cl1);
                 }
             }
         }
@@ -1205,6 +1206,10 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
         if (flags & kFlagLast) {
             // this warp's partial state -> its scratch (no longer needed)
             float* mw = reinterpret_cast<float*>(wbuf);
+            // P.V accumulator scales of the four slots (see v_out_scale)
+            constexpr float kLmUp = LM ? 1.f / kLmVDown : 1.f;
+            const float vout[4] = {v_out_scale(0) * kLmUp, v_out_scale(1) * kLmUp, v_out_scale(2) * kLmUp,
+                                   v_out_scale(3) * kLmUp};
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 float l = l_run[nt];
@@ -1225,8 +1230,8 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
                     for (int g = 0; g < 4; ++g)
 #pragma unroll
                         for (int half = 0; half < 2; ++half) {
-                            o[32 * g + 16 * half + gID] = fmaf(acc_o[0][2 * g + half][nt], kVOutScale, z[g]);
-                            o[32 * g + 16 * half + 8 + gID] = fmaf(acc_o[0][2 * g + half][2 + nt], kVOutScale, z[g]);
+                            o[32 * g + 16 * half + gID] = fmaf(acc_o[0][2 * g + half][nt], vout[g], z[g]);
+                            o[32 * g + 16 * half + 8 + gID] = fmaf(acc_o[0][2 * g + half][2 + nt], vout[g], z[g]);
                         }
                     if (gID == 0) {
                         o[kD] = m_run[nt];
@@ -1240,9 +1245,9 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         o[32 * g + 16 * half + gID] =
-                            fmaf(acc_o[nt][2 * g + half][0] + acc_o[nt][2 * g + half][1], kVOutScale, z[g]);
+                            fmaf(acc_o[nt][2 * g + half][0] + acc_o[nt][2 * g + half][1], vout[g], z[g]);
                         o[32 * g + 16 * half + 8 + gID] =
-                            fmaf(acc_o[nt][2 * g + half][2] + acc_o[nt][2 * g + half][3], kVOutScale, z[g]);
+                            fmaf(acc_o[nt][2 * g + half][2] + acc_o[nt][2 * g + half][3], vout[g], z[g]);
                     }
                 if (gID == 0) {
                     o[kD] = m_run[nt];

@@ -102,20 +102,25 @@ __device__ __forceinline__ uint32_t rotr(uint32_t x, uint32_t n) { return __funn
 // Slot k of a byte holds the code of stored position 32k + j of the byte's
 // vector (j = byte index); slot_bit(k) is the bit of that code inside the
 // operand half.
-__host__ __device__ __forceinline__ constexpr int slot_bit(int k) { return k == 1 ? 2 : k == 2 ? 4 : 6; }
+__host__ __device__ __forceinline__ constexpr int slot_bit(int k) { return k == 0 ? 8 : 2 * k; }
 
+// A code word with the two bytes of each 16-bit half swapped (bytes 1, 0,
+// 3, 2): slots 1-3 of bytes 1 and 3 land at bits 2-7 of the halves and slot
+// 0 of bytes 0 and 2 at bits 8-9, so that with the word itself every code
+// sits at bit 2, 4, 6 or 8 of a half in one of the two.
+__device__ __forceinline__ uint32_t code_swap(uint32_t x) { return __byte_perm(x, 0u, 0x2301u); }
 // Operand from the slot-k codes of bytes 0 and 2 of x (k-index 0 and 1 of
-// the register).
+// the register); xs = code_swap(x).
 template <int SLOT>
-__device__ __forceinline__ uint32_t code_pair_lo(uint32_t x) {
-    if constexpr (SLOT == 0) return (x << 6) & 0x00C000C0u;
+__device__ __forceinline__ uint32_t code_pair_lo(uint32_t x, uint32_t xs) {
+    if constexpr (SLOT == 0) return xs & 0x03000300u;
     else return x & (0x00030003u << (2 * SLOT));
 }
-// Operand from the slot-k codes of bytes 1 and 3 of x; x8 = x >> 8.
+// Operand from the slot-k codes of bytes 1 and 3 of x; xs = code_swap(x).
 template <int SLOT>
-__device__ __forceinline__ uint32_t code_pair_hi(uint32_t x, uint32_t x8) {
-    if constexpr (SLOT == 0) return (x >> 2) & 0x00C000C0u;
-    else return x8 & (0x00030003u << (2 * SLOT));
+__device__ __forceinline__ uint32_t code_pair_hi(uint32_t x, uint32_t xs) {
+    if constexpr (SLOT == 0) return x & 0x03000300u;
+    else return xs & (0x00030003u << (2 * SLOT));
 }
 
 // Power-of-two scalings of the INT2 decode (all exact):
@@ -128,14 +133,15 @@ __device__ __forceinline__ uint32_t code_pair_hi(uint32_t x, uint32_t x8) {
 //   bits (to an absolute 2^-25 * 2^-e below 2^-3 * 2^-e);
 //   the K scale s is stored as s * 2^(24 - slot_bit(k) - e), which gives the
 //   logit's products their true scale;
-//   the V products (bf16) use B = p * s * 2^(kVUp - slot_bit(k)), which
-//   puts every P.V accumulator at 2^(kVUp - 133) * sum(p s c); the item's
-//   output multiplies the accumulators back by 2^(133 - kVUp).
+//   the V products (fp16 too) use B = W = p * s (times the Lloyd-Max inner
+//   level a and 1/2 for the Lloyd-Max kernels), split into fp16 high and low
+//   parts, so the P.V accumulator of slot k holds 2^(slot_bit(k) - 24) *
+//   sum(W c), and the item's output multiplies it by v_out_scale(k).
 // Ranges: K operands are below 2^14 and K products above 2^-46 (normal
-// fp32); s <= 65504 keeps every V operand finite in bf16, and a V product
-// falls below the normal fp32 range only for p * s < 2^-96, far below
-// anything that moves an output.
-constexpr int kVUp = 103;
+// fp32); p <= 1 and s <= 65504 keep W <= 65504, finite in fp16 (the
+// Lloyd-Max levels' factors a <= 3/2 and kappa * a <= 3/2 are offset by the
+// 1/2); a W below 2^-14 keeps an absolute error of at most 2^-25, and V
+// products stay above 2^-46.
 constexpr int kQTopExp = 13;  // prep puts each head's largest |q'| in [2^13, 2^14)
 __host__ __device__ __forceinline__ constexpr float pow2f(int e) {
     float r = 1.f;
@@ -144,8 +150,8 @@ __host__ __device__ __forceinline__ constexpr float pow2f(int e) {
     return r;
 }
 __device__ __forceinline__ constexpr float k_scale_up(int slot) { return pow2f(24 - slot_bit(slot)); }
-__device__ __forceinline__ constexpr float v_scale_up(int slot) { return pow2f(kVUp - slot_bit(slot)); }
-constexpr float kVOutScale = 1073741824.f;  // 2^(133 - kVUp) = 2^30
+__device__ __forceinline__ constexpr float v_out_scale(int slot) { return pow2f(24 - slot_bit(slot)); }
+constexpr float kLmVDown = 0.5f;  // extra V-scale factor of the Lloyd-Max kernels (fp16 range)
 
 // ---- packed fp32x2 arithmetic (two lanes of fp32 per instruction) --------
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
@@ -204,6 +210,19 @@ __device__ __forceinline__ uint32_t split_w_pair(float2 p, float2 s, const Split
     return split_pair(mul2(p, s), sel);
 }
 
+// fp16 versions (the INT2 P.V products): hi = w with its low 13 bits
+// cleared, exact in fp16 for 2^-14 <= |hi| <= 65504 (below, its fp16
+// rounding moves the sum by at most 2^-25), lo = w - hi rounded to fp16.
+__device__ __forceinline__ uint32_t split_pair_f16(float2 w, const SplitSel& sel) {
+    const float2 hs = make_float2(__uint_as_float(lop3_and_xor(__float_as_uint(w.x), 0xffffe000u, sel.sign)),
+                                  __uint_as_float(lop3_and_xor(__float_as_uint(w.y), 0xffffe000u, sel.sign)));
+    const float2 x = fma2(sel.a, w, hs);  // hi, or w - hi
+    return pack_f16x2_rn(x.x, x.y);
+}
+__device__ __forceinline__ uint32_t split_w_pair_f16(float2 p, float2 s, const SplitSel& sel) {
+    return split_pair_f16(mul2(p, s), sel);
+}
+
 // Token order inside the shared probability / V-scale rows of a 16-token
 // tile: bits 0 and 1 swapped, so tokens (4a, 4a+2) and (4a+1, 4a+3) are
 // adjacent pairs (the two token pairs of a PV B-operand register).
@@ -217,7 +236,7 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-// The same product with fp16 operands (the K side of the INT2 decode).
+// The same product with fp16 operands (both products of the INT2 decode).
 __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                               uint32_t a3, uint32_t b0, uint32_t b1) {
     asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "

@@ -285,7 +285,9 @@ oscar_status oscar_decode_attn_noalloc(const oscar_shape* shape, int32_t batch, 
  * (oscar_calibrate_codebook).  A code is the nearest level to
  * u = (y_clipped - z) / s (u reaching a threshold a/2, 3/2 or 3 - a/2 moves
  * it up); a value dequantises to z + s * level[code].  a = 1 gives the
- * uniform levels; a <= 0 is read as 1.
+ * uniform levels; a <= 0 is read as 1.  The levels are in order for
+ * a <= 3/2, and the decode's fp16 products are sized for that range (a
+ * larger a can overflow them).
  *
  *   codebook (device) fp32 [Hk][2] the inner levels a (K, V of each KV head)
  *

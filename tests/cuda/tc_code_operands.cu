@@ -1,9 +1,9 @@
 // Test kernel: the INT2 decode's code operands on the tensor cores.  Each
-// case is one warp and one mma.sync.m16n8k16 (bf16 x bf16 or f16 x f16 ->
-// fp32, C = 0; the decode's P.V products use the first, its logits the
-// second):
+// case is one warp and one mma.sync.m16n8k16 (f16 x f16 -> fp32, C = 0, as
+// both of the decode's products; bf16 x bf16 for comparison on the slots
+// whose bit pattern is also a bf16 subnormal):
 // A is built from two 32-bit code words per lane with the library's own
-// operand helpers (code_pair_lo / code_pair_hi, exactly as the K and V
+// operand helpers (code_swap, code_pair_lo / code_pair_hi, exactly as the K and V
 // products build them: bytes 0 and 2 of a word give k-pair (2tq, 2tq+1),
 // bytes 1 and 3 give (2tq+8, 2tq+9), rows gID and gID+8 come from the two
 // words), B is given as bf16 or f16 bit patterns.  The A registers and D are
@@ -13,10 +13,11 @@
 
 template <int SLOT>
 __device__ __forceinline__ void operands(uint32_t w0, uint32_t w1, uint32_t (&a)[4]) {
-    a[0] = oscar::code_pair_lo<SLOT>(w0);
-    a[1] = oscar::code_pair_lo<SLOT>(w1);
-    a[2] = oscar::code_pair_hi<SLOT>(w0, w0 >> 8);
-    a[3] = oscar::code_pair_hi<SLOT>(w1, w1 >> 8);
+    const uint32_t s0 = oscar::code_swap(w0), s1 = oscar::code_swap(w1);
+    a[0] = oscar::code_pair_lo<SLOT>(w0, s0);
+    a[1] = oscar::code_pair_lo<SLOT>(w1, s1);
+    a[2] = oscar::code_pair_hi<SLOT>(w0, s0);
+    a[3] = oscar::code_pair_hi<SLOT>(w1, s1);
 }
 
 // words [case][32][2]; bmat [case][16 k][8 n] bf16 / f16 bits; aregs

@@ -1,31 +1,31 @@
 """The numeric property the INT2 decode's tensor-core products rest on.
 
-The decode feeds 2-bit codes to mma.sync without unpacking them into
-values: a code c left at bits P, P + 1 of an otherwise clear 16-bit half is
-the bit pattern c << P, whose value is c * 2^(P - 133) read as bf16 (the
-P.V products) and c * 2^(P - 24) read as fp16 (the logits), because in both
-formats the subnormals and the first normal binade join without a gap
-(patterns below 0x0100 / 0x0400).  The power of two is folded into the
-scales.  The tensor core keeps the products of such operands to a fixed
-number of bits below their nominal exponent, so the precision of a product
-depends on P: the kernel moves the codes of byte slot 0 up to bits 6-7 and
-uses slots 1, 2, 3 where they are (P = 2, 4, 6).
+The decode feeds 2-bit codes to mma.sync (fp16, both products) without
+unpacking them into values: a code c left at bits P, P + 1 of an otherwise
+clear 16-bit half is the bit pattern c << P, whose value read as fp16 is
+c * 2^(P - 24), because the fp16 subnormals and the first normal binade join
+without a gap (patterns below 0x0400; read as bf16 it is c * 2^(P - 133) for
+P <= 6).  The power of two is folded into the scales.  The tensor core keeps
+the products of such operands to a fixed number of bits below their nominal
+exponent, so the precision of a product depends on P: the kernel takes the
+codes of byte slot 0 at bits 8-9 (from the code word with the bytes of each
+half swapped) and slots 1, 2, 3 at bits 2, 4, 6.
 
 One warp and one MMA per case, A built by the library's operand helpers
 from random code words, B a sweep of magnitudes over the range the scale
-folding uses (bf16: 2^8 .. 2^125, p * s * 2^(103 - P) on the V side; fp16:
-2^-6 .. 2^14, q' * 2^e with the largest |q'| of a head at 2^13 .. 2^14 and
-its low parts and small elements below, down into the fp16 subnormals);
-checked here against exact float64 products:
+folding uses (fp16: 2^-6 .. 2^15: q' * 2^e with the largest |q'| of a KV
+group at 2^13 .. 2^14 and W = p * s up to 65504, low parts and small
+elements below, down into the fp16 subnormals; bf16, slots 1-3 only, for
+comparison: 2^8 .. 2^125); checked here against exact float64 products:
 
 - every A register is the expected bit pattern, and the pattern's value is
-  c * 2^(P - 133) (bf16) or c * 2^(P - 24) (fp16);
+  c * 2^(P - 24) (fp16) or c * 2^(P - 133) (bf16);
 - products of short-mantissa B values (exactly representable sums) come out
   exact for every slot;
 - for full-mantissa B with mixed magnitudes (hi and lo parts, tiny values),
-  |D - exact| <= 2^-r * sum |terms| with r = 22, 20, 18 retained bits for
-  P = 6, 4, 2 in both formats (a bit of margin over the bits each slot
-  keeps: P = 6 loses nothing, P = 4 two bits, P = 2 four bits).
+  |D - exact| <= 2^-r * sum |terms| with r = 22, 22, 20, 18 retained bits
+  for P = 8, 6, 4, 2 (a bit of margin over the bits each slot keeps: P = 8
+  and 6 lose nothing, P = 4 two bits, P = 2 four bits).
 """
 import ctypes
 import os
@@ -44,8 +44,8 @@ if not torch.cuda.is_available():
 from bit_kv_cache_evict_gb300 import build as B  # noqa: E402
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-SLOT_BIT = {0: 6, 1: 2, 2: 4, 3: 6}          # bit of the code inside its operand half, per byte slot
-RETAINED = {6: 22, 4: 20, 2: 18}             # bits kept relative to sum |terms|, with margin
+SLOT_BIT = {0: 8, 1: 2, 2: 4, 3: 6}          # bit of the code inside its operand half, per byte slot
+RETAINED = {8: 22, 6: 22, 4: 20, 2: 18}      # bits kept relative to sum |terms|, with margin
 
 
 @pytest.fixture(scope="module")
@@ -140,10 +140,10 @@ def test_code_operands_on_tensor_cores(probe, short, kind):
     rng = np.random.default_rng(20260 + int(short) + 2 * int(f16))
     # bf16 B magnitudes 2^8 .. 2^125 (the smallest mixed-in parts sit 2^-20
     # below 2^expo, so every product stays a normal fp32 number, as in the
-    # kernel); fp16 B magnitudes 2^-6 .. 2^14
-    expos = list(range(-6, 14, 2)) if f16 else list(range(28, 125, 6))
+    # kernel); fp16 B magnitudes 2^-6 .. 2^15
+    expos = list(range(-6, 16, 2)) if f16 else list(range(28, 125, 6))
     slots, words, bmats = [], [], []
-    for slot in range(4):
+    for slot in (range(4) if f16 else range(1, 4)):   # slot 0's bit 8 is an exponent bit in bf16
         for e in expos:
             for _ in range(3):
                 slots.append(slot)
