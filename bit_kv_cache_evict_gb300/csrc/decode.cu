@@ -285,7 +285,17 @@ struct StageInfo {
     int pid, pad[3];               // page id (read by the boost variant)
 };
 
-template <int NT>
+// Blocks per SM and ring stages of an int2_kernel instantiation: three
+// blocks (128 registers) with eight stages for up to four heads; for eight
+// heads three blocks with seven stages (the shared memory of three blocks),
+// except the Lloyd-Max and boost kernels, which keep two blocks (168
+// registers) and eight stages.
+template <int NT, bool LM, bool BOOST>
+__host__ __device__ constexpr int int2_blocks_per_sm() { return (NT == 1 || !(LM || BOOST)) ? 3 : 2; }
+template <int NT, bool LM, bool BOOST>
+__host__ __device__ constexpr int int2_stages() { return (NT == 2 && int2_blocks_per_sm<NT, LM, BOOST>() == 3) ? kStages - 1 : kStages; }
+
+template <int NT, int NS = kStages>
 struct Int2Smem {
     static constexpr int G4 = NT * 4;  // head columns (padded to 4 per n-tile)
     // per-warp scratch: K s [64] float4 | K z [64] float4 | V z [64]
@@ -297,9 +307,9 @@ struct Int2Smem {
     static constexpr int kMergeBytes = G4 * (kD + 2) * 4;
     static constexpr int kWarpBytes = kWarpBytes0 > kMergeBytes ? kWarpBytes0 : kMergeBytes;
     static constexpr int kStage = 0;
-    static constexpr int kInfo = kStage + kStages * kBlock;
-    static constexpr int kBars = kInfo + kStages * (int)sizeof(StageInfo);
-    static constexpr int kWarp = kBars + (2 * kStages + 2) * 8;
+    static constexpr int kInfo = kStage + NS * kBlock;
+    static constexpr int kBars = kInfo + NS * (int)sizeof(StageInfo);
+    static constexpr int kWarp = kBars + (2 * NS + 2) * 8;
     // q' fragments of the current item, shared by the four consumer warps
     // (all four are inside the same item between two item-end merges)
     static constexpr int kQf = kWarp + kConsumerWarps * kWarpBytes;       // [NT][8][32] uint2
@@ -985,18 +995,19 @@ __device__ __forceinline__ void attend_page_g8(const uint8_t* blk, int valid, ui
 }
 
 template <int NT, bool LM = false, bool BOOST = false>
-__global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(DecodeParams p) {
+__global__ void __launch_bounds__(kInt2Threads, (int2_blocks_per_sm<NT, LM, BOOST>())) int2_kernel(DecodeParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
-    using SM = Int2Smem<NT>;
+    constexpr int NS = int2_stages<NT, LM, BOOST>();  // ring stages
+    using SM = Int2Smem<NT, NS>;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint8_t* stages = smem + SM::kStage;
     StageInfo* info = reinterpret_cast<StageInfo*>(smem + SM::kInfo);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::kBars);
-    uint64_t* empty = full + kStages;
-    uint64_t* merge_bar = empty + kStages;  // consumer-warp rendezvous at item ends
+    uint64_t* empty = full + NS;
+    uint64_t* merge_bar = empty + NS;  // consumer-warp rendezvous at item ends
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < NS; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
@@ -1011,13 +1022,13 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
         // ------------------------------ producer ------------------------------
         const int total_long = __ldg(p.item_start + p.B);
         const int total = total_long + __ldg(p.item_start2 + p.B);
-        uint32_t n = 0;      // slots issued so far (stage n % kStages, warp n % 4)
+        uint32_t n = 0;      // slots issued so far (stage n % NS, warp n % 4)
         bool ok = true;
         // one slot: wait for the stage, then publish its info (and copy)
         auto post = [&](int item, int b, int kv, int pid, int valid, int flags) -> bool {
-            const uint32_t s = n % kStages;
-            if (n >= (uint32_t)kStages) {
-                const bool w = mbar_wait_bounded(&empty[s], ((n / kStages) - 1) & 1u, kWaitPolls);
+            const uint32_t s = n % NS;
+            if (n >= (uint32_t)NS) {
+                const bool w = mbar_wait_bounded(&empty[s], ((n / NS) - 1) & 1u, kWaitPolls);
                 if (!__all_sync(kFull, w)) return false;
             }
             if (lane == 0) {
@@ -1086,9 +1097,9 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
         if (!ok) {
             if (lane == 0) report(p.status, OSCAR_STATUS_TIMEOUT);
             // let issued copies land before the block can exit
-            const uint32_t first = n > (uint32_t)kStages ? n - kStages : 0;
+            const uint32_t first = n > (uint32_t)NS ? n - NS : 0;
             for (uint32_t k = first; k < n; ++k)
-                (void)mbar_wait_bounded(&full[k % kStages], (k / kStages) & 1u, kWaitPolls);
+                (void)mbar_wait_bounded(&full[k % NS], (k / NS) & 1u, kWaitPolls);
         }
         return;
     }
@@ -1117,8 +1128,8 @@ __global__ void __launch_bounds__(kInt2Threads, (NT == 1) ? 3 : 2) int2_kernel(D
     Codebook cbk{1.f, 1.f, 0.f, 0.f};  // Lloyd-Max levels of the current item's KV head
 
     for (uint32_t n = warp;; n += kConsumerWarps) {
-        const uint32_t s = n % kStages;
-        const bool w = mbar_wait_bounded(&full[s], (n / kStages) & 1u, kWaitPolls);
+        const uint32_t s = n % NS;
+        const bool w = mbar_wait_bounded(&full[s], (n / NS) & 1u, kWaitPolls);
         if (!__all_sync(kFull, w)) {
             if (lane == 0) report(p.status, OSCAR_STATUS_TIMEOUT);
             return;
@@ -1781,14 +1792,17 @@ static Int2Attr& attr_for_device(int dev) {
 
 template <int NT, bool LM = false, bool BOOST = false>
 static cudaError_t launch_int2(const DecodeParams& p, cudaStream_t st, int sms, bool& attr_set) {
-    const int smem = (LM || BOOST) ? Int2Smem<NT>::kBytesLM : Int2Smem<NT>::kBytes;
+    using SM = Int2Smem<NT, int2_stages<NT, LM, BOOST>()>;
+    constexpr int smem = (LM || BOOST) ? SM::kBytesLM : SM::kBytes;
+    // the blocks of one SM share its 228 KB (1 KB of it reserved per block)
+    static_assert(int2_blocks_per_sm<NT, LM, BOOST>() * (smem + 1024) <= 228 * 1024, "blocks per SM must fit");
     if (!attr_set) {
         cudaError_t e =
             cudaFuncSetAttribute(int2_kernel<NT, LM, BOOST>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    const int per_sm = (NT == 1) ? 3 : 2;
+    const int per_sm = int2_blocks_per_sm<NT, LM, BOOST>();
     const int64_t max_items =
         (int64_t)p.B * p.hk * ((p.max_pages + p.pps - 1) / p.pps + p.tail_pg / kShortItemPages);
     int blocks = (int)std::min<int64_t>((int64_t)per_sm * sms, max_items);
