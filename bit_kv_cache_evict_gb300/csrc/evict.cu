@@ -76,12 +76,16 @@ __global__ void __launch_bounds__(32 * kEvictWarps) evict_kernel(EvictParams p) 
         if (threadIdx.x == 0) report(p.status, OSCAR_STATUS_BAD_POS);
         return;
     }
+    // this warp's rows of U (kEvictTerms x 512 B) requested into L2 at once:
+    // after a decode launch has streamed the history through L2 they come
+    // from DRAM, and the term loop below reads them only a few rows ahead
+    const float* Um = p.U + ((size_t)kv * 2 + which) * kD * kD;
+    if (lane == 0) bulk_prefetch_l2(Um + (size_t)kEvictTerms * warp * kD, kEvictTerms * kD * 4);
     const size_t xoff = ((size_t)row * p.hk * 2 + (size_t)kv * 2 + which) * kD + 4 * lane;
     const uint2 xr = *reinterpret_cast<const uint2*>(p.src_kv + xoff);
     float x[4] = {bf16_lo(xr.x), bf16_hi(xr.x), bf16_lo(xr.y), bf16_hi(xr.y)};
 
     // ---- partial y = x . U over this warp's 32 terms, compensated -------------
-    const float* Um = p.U + ((size_t)kv * 2 + which) * kD * kD;
     float s[4] = {0.f, 0.f, 0.f, 0.f}, c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
     for (int aa = 0; aa < kEvictTerms; ++aa) {
