@@ -55,18 +55,26 @@ DEFAULT_WORKLOAD = "qwen3_8b_36l"
 # units processed, only while the kernel source is the one captured.
 INT2_TRAFFIC_CAPTURE = {
     "workload": "qwen3_8b_36l",
-    "source_sha256_16": "c694110dce766736",     # csrc/decode.cu + csrc/oscar_common.cuh
+    "source_sha256_16": "3acde18170d1e898",     # csrc/decode.cu + csrc/oscar_common.cuh, comments removed
     "traffic_bytes": 922.99e6 + 11.20e6,
     "algorithmic_bytes": 911.11e6,
 }
 
 
 def kernel_source_hash() -> str:
+    """sha256 prefix of the INT2 kernel's sources with comments and blank
+    lines removed (the captured counters depend on the code, not on its
+    comments)."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in ("decode.cu", "oscar_common.cuh"):
-        with open(os.path.join(ROOT, "bit_kv_cache_evict_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "bit_kv_cache_evict_gb300", "csrc", f), encoding="utf-8") as fh:
+            text = fh.read()
+        for line in text.splitlines():
+            code = re.sub(r"//.*$", "", line).rstrip()
+            if code:
+                h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

@@ -85,19 +85,21 @@ __device__ __forceinline__ void split_f16(const float (&v)[4], uint32_t& h01, ui
 
 __device__ __forceinline__ uint32_t rotr(uint32_t x, uint32_t n) { return __funnelshift_r(x, x, n); }
 
-// Code pairs -> bf16x2 MMA operands, with no offset and no arithmetic.
-// A 16-bit pattern below 0x0100 (exponent field 0 or 1) is a bf16 whose value
-// is exactly pattern * 2^-133: the subnormals and the first normal binade
-// join without a gap.  So a 2-bit code c left at bits P, P+1 of an otherwise
-// clear half reads as c * 2^(P-133), and one AND turns a code word into an
-// operand register.  The tensor core keeps the products of such subnormal
-// operands to a fixed number of bits below their nominal (biased) exponent,
-// so each leading zero of the 8-bit pattern costs one bit of the product:
-// codes at bits 6-7 lose nothing, at 4-5 two bits, at 2-3 four bits, at 0-1
-// six.  The codes of byte slot 0 (bits 0-1) are therefore moved up to bits
-// 6-7 first; slots 1-3 are used in place.  The power 2^(P-133) of each slot
-// is folded into the scales (and the query is scaled up so that every
-// product stays a normal fp32 number).
+// Code pairs -> f16x2 MMA operands, with no offset and no arithmetic.
+// A 16-bit pattern below 0x0400 (exponent field 0 or 1) is an fp16 whose
+// value is exactly pattern * 2^-24: the subnormals and the first normal
+// binade join without a gap.  So a 2-bit code c left at bits P, P+1 of an
+// otherwise clear half reads as c * 2^(P-24), and one AND turns a code word
+// into an operand register.  The tensor core keeps the products of such
+// subnormal operands to a fixed number of bits below their nominal (biased)
+// exponent, so each leading zero of the pattern below bit 9 costs one bit
+// of the product: codes at bits 8-9 and 6-7 lose nothing, at 4-5 two bits,
+// at 2-3 four bits, at 0-1 six.  The codes of byte slot 0 of bytes 0 and 2
+// (bits 0-1 of a half) are therefore taken at bits 8-9 from the word with
+// the two bytes of each half swapped (code_swap), which also brings slots
+// 1-3 of bytes 1 and 3 down to bits 2-7; slot 0 of bytes 1 and 3 sits at bits
+// 8-9 already and slots 1-3 of bytes 0 and 2 at bits 2-7.  The power
+// 2^(P-24) of each slot is folded into the scales.
 //
 // Slot k of a byte holds the code of stored position 32k + j of the byte's
 // vector (j = byte index); slot_bit(k) is the bit of that code inside the
@@ -181,8 +183,9 @@ __device__ __forceinline__ uint32_t lop3_and_xor(uint32_t x, uint32_t mask, uint
     return r;
 }
 
-// Selector of the bf16 hi / lo split below: a lane taking the hi parts uses
-// (a, sign) = (0, 0), a lane taking the lo parts (1, 0x80000000).
+// Selector of the hi / lo splits below (bf16 for the BF16 segment kernel's
+// P operand, fp16 for the INT2 kernel's P*s operand): a lane taking the hi
+// parts uses (a, sign) = (0, 0), a lane taking the lo parts (1, 0x80000000).
 struct SplitSel {
     float2 a;
     uint32_t sign;
