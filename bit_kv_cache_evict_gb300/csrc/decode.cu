@@ -1829,7 +1829,7 @@ static cudaError_t launch_pdl(void (*kernel)(Args...), dim3 grid, dim3 block, si
     return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
-cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st, cudaEvent_t ev_int2_start,
+cudaError_t launch_decode(const DecodeParams& pin, cudaStream_t st, cudaEvent_t ev_int2_start,
                           cudaEvent_t ev_int2_stop) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1838,6 +1838,23 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t st, cudaEvent_t ev
     if (at.sms == 0) {
         e = cudaDeviceGetAttribute(&at.sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
+    }
+    DecodeParams p = pin;
+    {   // Fewer history pages (at most) than two waves of minimum items on
+        // the INT2 grid (a batch of one or two long sequences): items of one
+        // wave instead, so that no block takes a second item while others
+        // idle.  Longer items only lower the item count the workspace was
+        // sized for.
+        const int per_sm = (p.NT == 1 || !(p.codebook || p.boost)) ? 3 : 2;  // as int2_blocks_per_sm
+        const int64_t blocks = (int64_t)per_sm * at.sms;
+        const int64_t line = (int64_t)p.B * p.hk * p.max_pages;
+        if (p.pps == kShortItemPages && line < 2 * kShortItemPages * blocks) {
+            const int pps = (int)std::min<int64_t>(256, ((line + blocks - 1) / blocks + 3) & ~3ll);
+            if (pps > p.pps) {
+                p.pps = pps;
+                p.tail_pg = 2 * kShortItemPages;
+            }
+        }
     }
     if (!at.setp) {
         e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
