@@ -72,7 +72,8 @@ __device__ __forceinline__ void prep_body(const DecodeParams& p) {
         if (lane == 0) {
             p.item_start[0] = 0;
             p.item_start2[0] = 0;
-            *p.counter = 0;
+            p.counter[0] = 0;
+            p.counter[kBfCounter] = 0;
         }
         for (int base = 0; base < p.B; base += 32) {
             const int b = base + lane;
@@ -1510,10 +1511,26 @@ __global__ void __launch_bounds__(kBfThreads, 3) bf16_kernel(DecodeParams p) {
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
     };
+    // Block i takes item i first; the items after the first gridDim.x come
+    // from a work counter (blocks start as the INT2 grid retires, so a fixed
+    // stride would leave the late ones the same share).  s_it[buf] is the
+    // item staged into buffer buf next, each claimed an item ahead so that the
+    // atomic's latency hides behind an item's work.
+    __shared__ int s_it[2];
+    int32_t* ctr = p.counter + kBfCounter;
+    int pend = 0;  // thread 0: the item after the next one
+    if (threadIdx.x == 0) {
+        s_it[0] = blockIdx.x;
+        s_it[1] = gridDim.x + atomicAdd(ctr, 1);
+        pend = gridDim.x + atomicAdd(ctr, 1);
+    }
+    __syncthreads();
     int buf = 0;
-    stage(blockIdx.x, 0);
-    for (int it = blockIdx.x; it < total; it += gridDim.x, buf ^= 1) {
-        stage(it + gridDim.x, buf ^ 1);
+    int it = s_it[0];
+    stage(it, 0);
+    for (; it < total; buf ^= 1) {
+        const int nxt = s_it[buf ^ 1];
+        stage(nxt, buf ^ 1);
         asm volatile("cp.async.wait_group 1;" ::: "memory");
         __syncthreads();  // this item's rows and query rows have landed
         const int bk = it / p.bf_items, item = it % p.bf_items;
@@ -1553,7 +1570,12 @@ __global__ void __launch_bounds__(kBfThreads, 3) bf16_kernel(DecodeParams p) {
                 part[(size_t)p.G * kD + p.G + h] = L;
             }
         }
-        __syncthreads();  // states read before this buffer is refilled
+        if (threadIdx.x == 0) {  // the item staged into this buffer after nxt
+            s_it[buf] = pend;
+            pend = gridDim.x + atomicAdd(ctr, 1);
+        }
+        __syncthreads();  // states read before this buffer is refilled; s_it[buf] visible
+        it = nxt;
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
     if (threadIdx.x == 0) pdl_wait();

@@ -65,6 +65,7 @@ __global__ void __launch_bounds__(32 * kEvictWarps) evict_kernel(EvictParams p) 
     constexpr int kEvictTerms = kD / kEvictWarps;
     __shared__ df part[kEvictWarps][kD];
     pdl_trigger();  // the decode's query preparation does not read what this kernel writes
+    pdl_wait();     // launched early (programmatic serialization): the previous kernel's results first
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int vec = blockIdx.x;
     const int i = vec / (p.hk * 2);
@@ -317,12 +318,24 @@ __global__ void __launch_bounds__(32 * kEvictWarps) evict_kernel(EvictParams p) 
     }
 }
 
+// Launched with programmatic stream serialization: the blocks may be
+// scheduled while the previous kernel's last blocks finish, and wait
+// (griddepcontrol.wait) for its completion before reading anything.
 cudaError_t launch_evict(const EvictParams& p, cudaStream_t st) {
     const int vecs = p.n_tok * p.hk * 2;
     if (vecs == 0) return cudaSuccess;
-    if (vecs < 512) evict_kernel<8><<<vecs, 256, 0, st>>>(p);
-    else evict_kernel<4><<<vecs, 128, 0, st>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(vecs);
+    cfg.blockDim = dim3(vecs < 512 ? 256 : 128);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = vecs < 512 ? cudaLaunchKernelEx(&cfg, evict_kernel<8>, p)
+                                     : cudaLaunchKernelEx(&cfg, evict_kernel<4>, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace oscar

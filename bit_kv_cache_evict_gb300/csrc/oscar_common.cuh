@@ -15,6 +15,7 @@ constexpr int kD = 128;           // head_dim
 constexpr int kGroup = 32;        // quantisation group
 constexpr int kNumGroups = kD / kGroup;
 constexpr int kPage = 64;         // tokens per page
+constexpr int kBfCounter = 32;      // index of the BF16 item queue's counter
 constexpr int kShortItemPages = 16; // pages per short split-K item (the queue's tail)
 constexpr int kBlock = OSCAR_BLOCK_BYTES;
 constexpr int kKCodes = 0;        // byte offsets inside a (page, kv) block
@@ -357,7 +358,7 @@ struct DecodeParams {
     float* out;
     int32_t* status;
     // workspace sections
-    int32_t* counter;     // [1]
+    int32_t* counter;     // [64]: [0] INT2 item queue, [kBfCounter] BF16 item queue (separate 128-byte lines)
     int32_t* item_start;  // [B + 1] long items before sequence b (prefix sums)
     int32_t* item_start2; // [B + 1] short tail items before sequence b
     uint32_t* qfrag;      // [B*Hk][NT][8][32][2] fp16 q' fragments (times 2^e_h)
