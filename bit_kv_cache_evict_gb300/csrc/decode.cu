@@ -51,13 +51,16 @@ constexpr int kPrepSmem = kD * kD * 4 + kPrepUnits * kD * 4 + kPrepUnits * 4;
 __device__ __forceinline__ void prep_body(const DecodeParams& p);
 
 // Launched as a programmatic dependent of the eviction (it reads neither the
-// pool nor the BF16 segment), so the two overlap; it waits for the
-// eviction's completion before it exits, so that everything launched after
-// it sees the evicted tokens.
-__global__ void __launch_bounds__(kPrepThreads) prep_kernel(DecodeParams p) {
+// pool nor the BF16 segment), so the two overlap.  One block waits for the
+// eviction's completion before it exits, which keeps this grid from
+// completing earlier, so that everything launched after it sees the evicted
+// tokens; the other blocks leave as soon as their work is done (their SM
+// slots go to the rest of the grid and to the INT2 kernel's blocks).
+// 64 registers, so that a block fits on an SM beside the eviction's blocks.
+__global__ void __launch_bounds__(kPrepThreads, 4) prep_kernel(DecodeParams p) {
     pdl_trigger();
     prep_body(p);
-    if (threadIdx.x == 0) pdl_wait();
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) pdl_wait();
 }
 
 __device__ __forceinline__ void prep_body(const DecodeParams& p) {
@@ -1484,8 +1487,9 @@ __device__ void bf16_tile(int nvalid, uint8_t* rows, const __nv_bfloat16* qsm, f
 // block) items with two buffers per warp, so that the next item's rows (and
 // its query rows, staged by warp 0) are in flight while the current item is
 // attended.  Launched as a programmatic dependent of int2_kernel, whose
-// results it does not read; it waits for int2_kernel's completion before it
-// exits, so that the merge after it sees both.
+// results it does not read; its block 0 waits for int2_kernel's completion
+// before it exits (the others leave when their items are done), so this grid
+// completes after int2_kernel and the merge after it sees both.
 __global__ void __launch_bounds__(kBfThreads, 3) bf16_kernel(DecodeParams p) {
     extern __shared__ __align__(128) uint8_t bsm[];
     pdl_trigger();
@@ -1578,7 +1582,7 @@ __global__ void __launch_bounds__(kBfThreads, 3) bf16_kernel(DecodeParams p) {
         it = nxt;
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
-    if (threadIdx.x == 0) pdl_wait();
+    if (blockIdx.x == 0 && threadIdx.x == 0) pdl_wait();  // this grid completes after int2_kernel
 }
 
 // ---------------------------------------------------------------------------
@@ -1812,6 +1816,19 @@ static Int2Attr& attr_for_device(int dev) {
     return attrs[dev & 63];
 }
 
+// Dynamic shared memory of a kernel, and the largest L1 / shared carveout:
+// an SM changes its split only when idle, so every kernel of the chain asks
+// for the same split and a programmatically launched kernel can start on SMs
+// where its predecessor still runs.
+template <typename... Args>
+static cudaError_t set_smem(void (*kernel)(Args...), int bytes) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
+    return e;
+}
+
 template <int NT, bool LM = false, bool BOOST = false>
 static cudaError_t launch_int2(const DecodeParams& p, cudaStream_t st, int sms, bool& attr_set) {
     using SM = Int2Smem<NT, int2_stages<NT, LM, BOOST>()>;
@@ -1819,8 +1836,7 @@ static cudaError_t launch_int2(const DecodeParams& p, cudaStream_t st, int sms, 
     // the blocks of one SM share its 228 KB (1 KB of it reserved per block)
     static_assert(int2_blocks_per_sm<NT, LM, BOOST>() * (smem + 1024) <= 228 * 1024, "blocks per SM must fit");
     if (!attr_set) {
-        cudaError_t e =
-            cudaFuncSetAttribute(int2_kernel<NT, LM, BOOST>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaError_t e = set_smem(int2_kernel<NT, LM, BOOST>, smem);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -1879,7 +1895,7 @@ cudaError_t launch_decode(const DecodeParams& pin, cudaStream_t st, cudaEvent_t 
         }
     }
     if (!at.setp) {
-        e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
+        e = set_smem(prep_kernel, kPrepSmem);
         if (e != cudaSuccess) return e;
         at.setp = true;
     }
@@ -1896,7 +1912,7 @@ cudaError_t launch_decode(const DecodeParams& pin, cudaStream_t st, cudaEvent_t 
     if (e != cudaSuccess) return e;
     if (ev_int2_stop && (e = cudaEventRecord(ev_int2_stop, st)) != cudaSuccess) return e;
     if (!at.setb) {
-        e = cudaFuncSetAttribute(bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kBfSmem);
+        e = set_smem(bf16_kernel, kBfSmem);
         if (e != cudaSuccess) return e;
         at.setb = true;
     }
@@ -1904,7 +1920,7 @@ cudaError_t launch_decode(const DecodeParams& pin, cudaStream_t st, cudaEvent_t 
     e = launch_pdl(bf16_kernel, dim3(min(bf_total, 3 * at.sms)), dim3(kBfThreads), kBfSmem, st, p);
     if (e != cudaSuccess) return e;
     if (!at.setm) {
-        e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMergeSmem);
+        e = set_smem(merge_kernel, kMergeSmem);
         if (e != cudaSuccess) return e;
         at.setm = true;
     }

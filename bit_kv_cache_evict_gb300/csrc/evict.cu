@@ -320,10 +320,28 @@ __global__ void __launch_bounds__(32 * kEvictWarps) evict_kernel(EvictParams p) 
 
 // Launched with programmatic stream serialization: the blocks may be
 // scheduled while the previous kernel's last blocks finish, and wait
-// (griddepcontrol.wait) for its completion before reading anything.
+// (griddepcontrol.wait) for its completion before reading anything.  The
+// kernel asks for the largest shared-memory carveout although it uses 8 KB:
+// an SM can change its L1 / shared split only when idle, so with a small
+// split the decode's kernels (up to 213 KB per SM), launched early by the
+// programmatic dependency, could not start on an SM until its eviction
+// blocks had drained.
 cudaError_t launch_evict(const EvictParams& p, cudaStream_t st) {
     const int vecs = p.n_tok * p.hk * 2;
     if (vecs == 0) return cudaSuccess;
+    static bool carveout_set[64] = {};
+    int dev = 0;
+    cudaError_t ce = cudaGetDevice(&dev);
+    if (ce != cudaSuccess) return ce;
+    if (!carveout_set[dev & 63]) {
+        ce = cudaFuncSetAttribute(evict_kernel<8>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  (int)cudaSharedmemCarveoutMaxShared);
+        if (ce == cudaSuccess)
+            ce = cudaFuncSetAttribute(evict_kernel<4>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                      (int)cudaSharedmemCarveoutMaxShared);
+        if (ce != cudaSuccess) return ce;
+        carveout_set[dev & 63] = true;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(vecs);
     cfg.blockDim = dim3(vecs < 512 ? 256 : 128);
