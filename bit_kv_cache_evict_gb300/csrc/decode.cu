@@ -56,8 +56,9 @@ __device__ __forceinline__ void prep_body(const DecodeParams& p);
 // completing earlier, so that everything launched after it sees the evicted
 // tokens; the other blocks leave as soon as their work is done (their SM
 // slots go to the rest of the grid and to the INT2 kernel's blocks).
-// 64 registers, so that a block fits on an SM beside the eviction's blocks.
-__global__ void __launch_bounds__(kPrepThreads, 4) prep_kernel(DecodeParams p) {
+// 40 registers, so that two blocks fit on an SM beside the eviction's blocks
+// (the grid is one wave there).
+__global__ void __launch_bounds__(kPrepThreads, 6) prep_kernel(DecodeParams p) {
     pdl_trigger();
     prep_body(p);
     if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) pdl_wait();
