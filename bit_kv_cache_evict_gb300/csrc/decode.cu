@@ -1594,27 +1594,36 @@ __global__ void __launch_bounds__(kBfThreads, 3) bf16_kernel(DecodeParams p) {
 // e.g. one long sequence): the row's split-K partials are dealt round-robin
 // to its warps, each warp merges its share (log-sum-exp in base 2), and the
 // row's first warp combines the shares.  U_V is copied row-major into shared
-// memory with cp.async meanwhile; the un-rotation o = w . U_V^T then reads
-// U_V in a lane-rotated order (lane l takes index (j + l) mod 128 at step j)
-// so that every shared-memory access is conflict-free.
+// memory with cp.async meanwhile (rows padded to kURow floats).  The
+// un-rotation o = w . U_V^T of the block's rows (at most eight) runs on
+// tensor cores, shared by the eight warps: warp w computes outputs
+// 16w .. 16w+15 of every row as D(16 x 8) += W(16 x 16) . U_V^T(16 x 8)
+// over the 128 inputs, rows 8-15 of W zero, W and U_V each split into fp16
+// high and rounded-remainder parts (22 significant bits) and the three
+// products hi.hi + hi.lo + lo.hi accumulated in fp32 (the lo.lo term is
+// below 2^-22 of the product).  U_V is read once per block instead of once
+// per row.
 constexpr int kMergeWarps = 8;
 constexpr int kMergeThreads = 32 * kMergeWarps;
 constexpr int kMergeRow = kD + 4;  // floats per warp row (y[128], M, L; a multiple of 4 for float4 access)
-constexpr int kMergeSmem = (kD * kD + kMergeWarps * kMergeRow) * 4;
+constexpr int kURow = kD + 8;      // floats per staged U_V row: fragment loads of 8 rows hit distinct banks
+constexpr int kMergeSmem = (kD * kURow + 2 * kMergeWarps * kMergeRow) * 4;
 constexpr int kMergeBatch = 12;   // split-K partials per batch of loads
 constexpr int kMaxBfItems = 5;    // BF16 segment blocks per row: ceil(320 / 64)
 
 __global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(DecodeParams p) {
     extern __shared__ __align__(16) float msm[];
-    float* Us = msm;                  // [a][j] = U_V[a][j]
-    float* Ws = msm + kD * kD;        // [warp][kMergeRow]: a warp's share (y, M, L), then the row's w
+    float* Us = msm;                  // [a][kURow] = U_V[a][j]
+    float* Ws = msm + kD * kURow;     // [warp][kMergeRow]: a warp's share (y, M, L), then the row's w
+    float* Ys = Ws + kMergeWarps * kMergeRow;  // [row][kMergeRow]: the block's un-rotated rows
     const int kv = blockIdx.y;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     {
         const uint8_t* src = reinterpret_cast<const uint8_t*>(p.U + ((size_t)kv * 2 + 1) * kD * kD);
         uint8_t* dst = reinterpret_cast<uint8_t*>(Us);
-        for (int i = threadIdx.x; i < kD * kD / 4; i += kMergeThreads)
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst + 16 * i)), "l"(src + 16 * i)
+        for (int i = threadIdx.x; i < kD * kD / 4; i += kMergeThreads)  // 16-byte chunk i: row i / 32, chunk i % 32
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst + (i >> 5) * kURow * 4 + 16 * (i & 31))),
+                         "l"(src + 16 * i)
                          : "memory");
         asm volatile("cp.async.commit_group;" ::: "memory");
     }
@@ -1730,10 +1739,10 @@ __global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(DecodeParams p)
         __syncthreads();  // shares read before the rows' w overwrite them
     }
     const bool lead = active && sub == 0;
-    if (lead) {
+    if (sub == 0) {  // the row's w (zero for rows past the batch)
         const float inv = (L > 0.f) ? 1.f / L : 0.f;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) y[k] *= inv;
+        for (int k = 0; k < 4; ++k) y[k] = active ? y[k] * inv : 0.f;
         {
             const float t0 = y[0] + y[1], t1 = y[0] - y[1], t2 = y[2] + y[3], t3 = y[2] - y[3];
             y[0] = t0 + t2;
@@ -1756,23 +1765,47 @@ __global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(DecodeParams p)
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
     __syncthreads();
-    if (!lead) return;
-    // o[a] = sum_j w[j] U_V[a][j] for a = lane + 32 c, four j per load (the
-    // lanes start at rotated float4 columns, so each quarter-warp's 16-byte
-    // reads fall on distinct banks); two partial sums per output
-    const float* w = Ws + (size_t)warp * kMergeRow;
-    float acc[4][2] = {};
-#pragma unroll 4
-    for (int j4 = 0; j4 < kD / 4; ++j4) {
-        const int jj = 4 * ((j4 + lane) & (kD / 4 - 1));
-        const float4 wv = *reinterpret_cast<const float4*>(w + jj);
+    {   // un-rotation on tensor cores: A row gID = block row gID (its w in Ws[gID * wpr]), B = U_V^T
+        const int gID = lane >> 2, tq = lane & 3;
+        const float* wrow = Ws + (size_t)(gID * wpr) * kMergeRow;
+        const bool rowok = gID < rpb;
+        float d[2][4] = {};
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const float4 u = *reinterpret_cast<const float4*>(Us + (lane + 32 * c) * kD + jj);
-            float& a = acc[c][j4 & 1];
-            a = fmaf(wv.w, u.w, fmaf(wv.z, u.z, fmaf(wv.y, u.y, fmaf(wv.x, u.x, a))));
+        for (int ks = 0; ks < kD / 16; ++ks) {
+            const int k0 = 16 * ks + 2 * tq;
+            float2 w0 = make_float2(0.f, 0.f), w1 = w0;
+            if (rowok) {
+                w0 = *reinterpret_cast<const float2*>(wrow + k0);
+                w1 = *reinterpret_cast<const float2*>(wrow + k0 + 8);
+            }
+            uint32_t ah0, ah2, al0, al2;
+            {
+                const float v[4] = {w0.x, w0.y, w1.x, w1.y};
+                split_f16(v, ah0, ah2, al0, al2);
+            }
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                const int a = 16 * warp + 8 * t + gID;  // output (column n = gID of n-tile 2 warp + t)
+                const float2 u0 = *reinterpret_cast<const float2*>(Us + (size_t)a * kURow + k0);
+                const float2 u1 = *reinterpret_cast<const float2*>(Us + (size_t)a * kURow + k0 + 8);
+                uint32_t bh0, bh1, bl0, bl1;
+                const float v[4] = {u0.x, u0.y, u1.x, u1.y};
+                split_f16(v, bh0, bh1, bl0, bl1);
+                mma_f16_16816(d[t], ah0, 0u, ah2, 0u, bh0, bh1);
+                mma_f16_16816(d[t], ah0, 0u, ah2, 0u, bl0, bl1);
+                mma_f16_16816(d[t], al0, 0u, al2, 0u, bh0, bh1);
+            }
+        }
+        if (rowok) {  // D rows 0-7 = block rows: outputs 16 warp + 8 t + 2 tq, + 1
+#pragma unroll
+            for (int t = 0; t < 2; ++t)
+                *reinterpret_cast<float2*>(Ys + (size_t)gID * kMergeRow + 16 * warp + 8 * t + 2 * tq) =
+                    make_float2(d[t][0], d[t][1]);
         }
     }
+    __syncthreads();
+    if (!lead) return;
+    const float* yrow = Ys + (size_t)(warp / wpr) * kMergeRow;
     // BF16 segment: log-sum-exp merge of its item partials (unrotated domain)
     float mb = -INFINITY;
 #pragma unroll
@@ -1799,7 +1832,7 @@ __global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(DecodeParams p)
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
         const int a2 = lane + 32 * c;
-        o[a2] = (wi * (acc[c][0] + acc[c][1]) + wb * ob[c]) * inv;
+        o[a2] = (wi * yrow[a2] + wb * ob[c]) * inv;
     }
 }
 
