@@ -1853,11 +1853,13 @@ static Int2Attr& attr_for_device(int dev) {
 // Dynamic shared memory of a kernel, and the largest L1 / shared carveout:
 // an SM changes its split only when idle, so every kernel of the chain asks
 // for the same split and a programmatically launched kernel can start on SMs
-// where its predecessor still runs.
+// where its predecessor still runs.  (Not for the eight-head Lloyd-Max INT2
+// kernel: its register spills go through L1, which the largest split leaves
+// at 28 KB; it took 9 % longer with it.)
 template <typename... Args>
-static cudaError_t set_smem(void (*kernel)(Args...), int bytes) {
+static cudaError_t set_smem(void (*kernel)(Args...), int bytes, bool max_carveout = true) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e == cudaSuccess)
+    if (e == cudaSuccess && max_carveout)
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  (int)cudaSharedmemCarveoutMaxShared);
     return e;
@@ -1870,7 +1872,7 @@ static cudaError_t launch_int2(const DecodeParams& p, cudaStream_t st, int sms, 
     // the blocks of one SM share its 228 KB (1 KB of it reserved per block)
     static_assert(int2_blocks_per_sm<NT, LM, BOOST>() * (smem + 1024) <= 228 * 1024, "blocks per SM must fit");
     if (!attr_set) {
-        cudaError_t e = set_smem(int2_kernel<NT, LM, BOOST>, smem);
+        cudaError_t e = set_smem(int2_kernel<NT, LM, BOOST>, smem, !(NT == 2 && LM));
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
