@@ -1360,7 +1360,10 @@ __device__ __forceinline__ void bf16_stage_rows(const DecodeParams& p, int b, in
 
 // One warp's 16-token tile from staged rows and the staged query rows of
 // its KV group (qsm: [G][kD] bf16); leaves the warp's state (o, m, l) per
-// head in rows.
+// head in rows.  MMA row h holds head h (rows G..15 are zero): S = Q.K^T,
+// then O += P.V twice into the same accumulators, with A = the bf16 high
+// part of P (its low 16 bits cleared, exact) and A = the rounded remainder,
+// so P keeps ~16 bits and each head's output is one accumulator row.
 template <int G>
 __device__ void bf16_tile(int nvalid, uint8_t* rows, const __nv_bfloat16* qsm, float qscale) {
     const int lane = threadIdx.x & 31, gID = lane >> 2, tq = lane & 3;
@@ -1372,19 +1375,14 @@ __device__ void bf16_tile(int nvalid, uint8_t* rows, const __nv_bfloat16* qsm, f
         }
         return;
     }
-    // A = query rows: row r < 2G holds head r/2, the rest are zero
-    constexpr bool kHigh = (G == 8);                  // rows gID + 8 in use
-    const bool row_lo_on = gID < 2 * G;
-    const __nv_bfloat16* qa = qsm + (row_lo_on ? (gID >> 1) : 0) * kD;
-    const __nv_bfloat16* qb = qsm + (kHigh ? ((gID + 8) >> 1) : 0) * kD;
-    uint32_t qf[8][4];
+    const bool row_on = gID < G;
+    const __nv_bfloat16* qa = qsm + (row_on ? gID : 0) * kD;
+    uint32_t qf[8][2];  // A fragments (rows gID: a0, a2; rows gID + 8 are zero)
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
         const int d0 = 16 * ks + 2 * tq;
-        qf[ks][0] = row_lo_on ? *reinterpret_cast<const uint32_t*>(qa + d0) : 0u;
-        qf[ks][2] = row_lo_on ? *reinterpret_cast<const uint32_t*>(qa + d0 + 8) : 0u;
-        qf[ks][1] = kHigh ? *reinterpret_cast<const uint32_t*>(qb + d0) : 0u;
-        qf[ks][3] = kHigh ? *reinterpret_cast<const uint32_t*>(qb + d0 + 8) : 0u;
+        qf[ks][0] = row_on ? *reinterpret_cast<const uint32_t*>(qa + d0) : 0u;
+        qf[ks][1] = row_on ? *reinterpret_cast<const uint32_t*>(qa + d0 + 8) : 0u;
     }
 
     // S = Q.K^T for tokens 8nt .. 8nt+7 (B via ldmatrix: matrix i/8 = dims
@@ -1399,47 +1397,43 @@ __device__ void bf16_tile(int nvalid, uint8_t* rows, const __nv_bfloat16* qsm, f
         for (int ks = 0; ks < 8; ks += 2) {
             uint32_t kb[4];
             ldsm_x4(kb, rb + 32 * ks);
-            mma_bf16_16816(sacc[nt], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], kb[0], kb[1]);
-            mma_bf16_16816(sacc[nt], qf[ks + 1][0], qf[ks + 1][1], qf[ks + 1][2], qf[ks + 1][3], kb[2], kb[3]);
+            mma_bf16_16816(sacc[nt], qf[ks][0], 0u, qf[ks][1], 0u, kb[0], kb[1]);
+            mma_bf16_16816(sacc[nt], qf[ks + 1][0], 0u, qf[ks + 1][1], 0u, kb[2], kb[3]);
         }
     }
-    // scale to base 2, mask, row max / exp / sum (rows gID: e 0,1; gID+8: e 2,3)
-    float ma = -INFINITY, mb = -INFINITY;
+    // scale to base 2, mask, row max / exp / sum (row gID: e 0, 1)
+    float ma = -INFINITY;
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int tok = 8 * nt + 2 * tq + (e & 1);
+        for (int e = 0; e < 2; ++e) {
+            const int tok = 8 * nt + 2 * tq + e;
             sacc[nt][e] = (tok < nvalid) ? sacc[nt][e] * qscale : -INFINITY;
-            if (e < 2) ma = fmaxf(ma, sacc[nt][e]);
-            else mb = fmaxf(mb, sacc[nt][e]);
+            ma = fmaxf(ma, sacc[nt][e]);
         }
     ma = fmaxf(ma, __shfl_xor_sync(kFull, ma, 1));
     ma = fmaxf(ma, __shfl_xor_sync(kFull, ma, 2));
-    mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, 1));
-    mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, 2));
-    float la = 0.f, lb = 0.f;
+    float la = 0.f;
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            sacc[nt][e] = ex2(sacc[nt][e] - (e < 2 ? ma : mb));
-            if (e < 2) la += sacc[nt][e];
-            else lb += sacc[nt][e];
+        for (int e = 0; e < 2; ++e) {
+            sacc[nt][e] = ex2(sacc[nt][e] - ma);
+            la += sacc[nt][e];
         }
     la += __shfl_xor_sync(kFull, la, 1);
     la += __shfl_xor_sync(kFull, la, 2);
-    lb += __shfl_xor_sync(kFull, lb, 1);
-    lb += __shfl_xor_sync(kFull, lb, 2);
 
-    // P as the A operand of O = P.V (k = the 16 tokens): even rows take the
-    // bf16 high part, odd rows the rounded remainder
-    const SplitSel take_lo = split_sel(gID & 1);
-    uint32_t pa[4];
-    pa[0] = row_lo_on ? split_pair(make_float2(sacc[0][0], sacc[0][1]), take_lo) : 0u;
-    pa[2] = row_lo_on ? split_pair(make_float2(sacc[1][0], sacc[1][1]), take_lo) : 0u;
-    pa[1] = kHigh ? split_pair(make_float2(sacc[0][2], sacc[0][3]), take_lo) : 0u;
-    pa[3] = kHigh ? split_pair(make_float2(sacc[1][2], sacc[1][3]), take_lo) : 0u;
+    // P as the A operand of O = P.V (k = the 16 tokens), high and low parts
+    uint32_t ph[2], pl[2];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        const float w0 = sacc[nt][0], w1 = sacc[nt][1];
+        const float h0 = __uint_as_float(__float_as_uint(w0) & 0xffff0000u);
+        const float h1 = __uint_as_float(__float_as_uint(w1) & 0xffff0000u);
+        ph[nt] = row_on ? pack_bf16x2_rn(h0, h1) : 0u;
+        pl[nt] = row_on ? pack_bf16x2_rn(w0 - h0, w1 - h1) : 0u;
+    }
 
     // O = P.V over dims 8j .. 8j+7 (B via ldmatrix.trans: matrix i/8 = tokens
     // 8((i/8)&1) + i%8, dims 16jp + 8(i/16))
@@ -1451,35 +1445,19 @@ __device__ void bf16_tile(int nvalid, uint8_t* rows, const __nv_bfloat16* qsm, f
         ldsm_x4_trans(vf, vb + 32 * jp);
 #pragma unroll
         for (int e = 0; e < 4; ++e) o[2 * jp][e] = o[2 * jp + 1][e] = 0.f;
-        mma_bf16_16816(o[2 * jp], pa[0], pa[1], pa[2], pa[3], vf[0], vf[1]);
-        mma_bf16_16816(o[2 * jp + 1], pa[0], pa[1], pa[2], pa[3], vf[2], vf[3]);
+        mma_bf16_16816(o[2 * jp], ph[0], 0u, ph[1], 0u, vf[0], vf[1]);
+        mma_bf16_16816(o[2 * jp], pl[0], 0u, pl[1], 0u, vf[0], vf[1]);
+        mma_bf16_16816(o[2 * jp + 1], ph[0], 0u, ph[1], 0u, vf[2], vf[3]);
+        mma_bf16_16816(o[2 * jp + 1], pl[0], 0u, pl[1], 0u, vf[2], vf[3]);
     }
     __syncwarp();  // all row reads done: the tile now holds the warp's state
-    // O_h = row 2h + row 2h + 1 (lanes gID and gID ^ 1)
+    if (row_on) {  // head gID: accumulator row gID
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) o[j][e] += __shfl_xor_sync(kFull, o[j][e], 4);
-    if ((gID & 1) == 0) {
-        const int h = gID >> 1;
-        if (h < G) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-                *reinterpret_cast<float2*>(st + h * (kD + 2) + 8 * j + 2 * tq) = make_float2(o[j][0], o[j][1]);
-            if (tq == 0) {
-                st[h * (kD + 2) + kD] = ma;
-                st[h * (kD + 2) + kD + 1] = la;
-            }
-        }
-        if (kHigh) {
-            const int h2 = h + 4;
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-                *reinterpret_cast<float2*>(st + h2 * (kD + 2) + 8 * j + 2 * tq) = make_float2(o[j][2], o[j][3]);
-            if (tq == 0) {
-                st[h2 * (kD + 2) + kD] = mb;
-                st[h2 * (kD + 2) + kD + 1] = lb;
-            }
+        for (int j = 0; j < 16; ++j)
+            *reinterpret_cast<float2*>(st + gID * (kD + 2) + 8 * j + 2 * tq) = make_float2(o[j][0], o[j][1]);
+        if (tq == 0) {
+            st[gID * (kD + 2) + kD] = ma;
+            st[gID * (kD + 2) + kD + 1] = la;
         }
     }
 }
@@ -1627,11 +1605,24 @@ __global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(DecodeParams p)
                          : "memory");
         asm volatile("cp.async.commit_group;" ::: "memory");
     }
-    pdl_wait();  // partials of int2_kernel and bf16_kernel
     const int wpr = p.merge_wpr, rpb = kMergeWarps / wpr;
     const int r = blockIdx.x * rpb + warp / wpr, sub = warp % wpr;
     const bool active = r < p.B * p.G;
     const int b = active ? r / p.G : 0, hh = active ? r % p.G : 0;
+    // the (sequence, KV head)'s partials: n_long long items, then n_short
+    // short ones.  The plan comes from prep_kernel, which completed before
+    // int2_kernel passed its wait, i.e. before this grid could start: read it
+    // before the wait, so that only the partials' loads follow it.
+    int splits = 0, first = 0, first2 = 0, n_long = 0;
+    if (active) {
+        const int s0 = __ldg(p.item_start + b), t0 = __ldg(p.item_start2 + b);
+        n_long = (__ldg(p.item_start + b + 1) - s0) / p.hk;
+        const int n_short = (__ldg(p.item_start2 + b + 1) - t0) / p.hk;
+        splits = n_long + n_short;
+        first = s0 + kv * n_long;
+        first2 = __ldg(p.item_start + p.B) + t0 + kv * n_short - n_long;
+    }
+    pdl_wait();  // partials of int2_kernel and bf16_kernel
     const int r5 = bitrev5(lane);
     // lane handles Hadamard indices j = 4 lane + k, stored at bitrev7(j)
     float M = -INFINITY, L = 0.f, y[4] = {0.f, 0.f, 0.f, 0.f};
@@ -1657,13 +1648,6 @@ __global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(DecodeParams p)
         }
     }
     if (active) {
-        // the (sequence, KV head)'s partials: n_long long items, then n_short short ones
-        const int s0 = __ldg(p.item_start + b), t0 = __ldg(p.item_start2 + b);
-        const int n_long = (__ldg(p.item_start + b + 1) - s0) / p.hk;
-        const int n_short = (__ldg(p.item_start2 + b + 1) - t0) / p.hk;
-        const int splits = n_long + n_short;
-        const int first = s0 + kv * n_long;
-        const int first2 = __ldg(p.item_start + p.B) + t0 + kv * n_short - n_long;
         // this warp's splits sub, sub + wpr, ..., merged by online log-sum-exp
         // in batches whose loads (statistics and this lane's four values of
         // each split) are all issued before any is used
