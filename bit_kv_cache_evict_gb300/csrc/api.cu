@@ -90,7 +90,7 @@ static WsLayout ws_layout(const oscar_shape* s, int batch, int max_pages) {
     w.qsum = off;
     off = round_up(off + (size_t)batch * hk * w.NT * 4 * 4 * 4, 256);
     w.qkinv = off;
-    off = round_up(off + (size_t)batch * hk * 4, 256);
+    off = round_up(off + (size_t)batch * hk * 16, 256);
     w.qrot = off;
     off = round_up(off + (size_t)batch * hk * w.NT * 4 * kD * 4, 256);
     w.part = off;

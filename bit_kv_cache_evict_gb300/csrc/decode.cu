@@ -214,7 +214,7 @@ __device__ __forceinline__ void prep_body(const DecodeParams& p) {
         const int ex = mx > 0.f ? (int)((__float_as_uint(mx) >> 23) & 0xffu) - 127 : 0;
         const int e = min(126, max(-126, kQTopExp - ex));
         const float up = __uint_as_float((uint32_t)(127 + e) << 23);
-        if (u == u0 && lane == 0) p.qkinv[bk] = __uint_as_float((uint32_t)(127 - e) << 23);
+        if (u == u0 && lane < 4) p.qkinv[(size_t)bk * 4 + lane] = lane == 0 ? __uint_as_float((uint32_t)(127 - e) << 23) : 0.f;
         uint32_t* frag = p.qfrag + ((size_t)bk * p.NT + nt) * 8 * 32 * 2;
         float* qsum = p.qsum + ((size_t)bk * p.NT * 4 + hl) * 4;
         const int ks = lane >> 2, tq = lane & 3;
@@ -299,6 +299,11 @@ template <int NT, bool LM, bool BOOST>
 __host__ __device__ constexpr int int2_blocks_per_sm() { return (NT == 1 || !(LM || BOOST)) ? 3 : 2; }
 template <int NT, bool LM, bool BOOST>
 __host__ __device__ constexpr int int2_stages() { return (NT == 2 && int2_blocks_per_sm<NT, LM, BOOST>() == 3) ? kStages - 1 : kStages; }
+// Whether an instantiation prefetches each item's q' data into shared
+// memory (the uniform four-head kernel; the others load it at the item's
+// first page).
+template <int NT, bool LM, bool BOOST>
+__host__ __device__ constexpr bool int2_q_prefetch() { return NT == 1 && !LM && !BOOST; }
 
 template <int NT, int NS = kStages>
 struct Int2Smem {
@@ -323,6 +328,15 @@ struct Int2Smem {
     // channel boost: q' [kD] float4 (four heads) there instead
     static constexpr int kBytesLM = kBytes + NT * 8 * 32 * 8;
     static_assert(NT * 8 * 32 * 8 >= kD * NT * 16, "room for the boost's q'");
+    // The uniform four-head kernel instead has two item buffers, filled by
+    // the producer with bulk copies when it starts an item: q' fragments
+    // [8][32] uint2, the group sums [4] float4, 2^-e (a 16-byte record);
+    // then their "full" and "empty" barriers.
+    static constexpr int kQbFrag = 0, kQbSum = 8 * 32 * 8, kQbKinv = kQbSum + 4 * 16, kQbBytes = kQbKinv + 16;
+    static constexpr int kQb = kQf;                      // [2][kQbBytes]
+    static constexpr int kQbBars = kQb + 2 * kQbBytes;   // qfull[2], qempty[2]
+    static constexpr int kBytesQP = kQbBars + 4 * 8;
+    static_assert(kQb % 16 == 0 && kQbBytes % 16 == 0, "bulk-copy destinations 16-byte aligned");
 };
 
 __device__ __forceinline__ int find_seq(const int32_t* item_start, int B, int item) {
@@ -1010,6 +1024,9 @@ __global__ void __launch_bounds__(kInt2Threads, (int2_blocks_per_sm<NT, LM, BOOS
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::kBars);
     uint64_t* empty = full + NS;
     uint64_t* merge_bar = empty + NS;  // consumer-warp rendezvous at item ends
+    constexpr bool QP = int2_q_prefetch<NT, LM, BOOST>();
+    uint64_t* qfull = reinterpret_cast<uint64_t*>(smem + SM::kQbBars);  // QP only: item buffers' barriers
+    uint64_t* qempty = qfull + 2;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
@@ -1017,6 +1034,12 @@ __global__ void __launch_bounds__(kInt2Threads, (int2_blocks_per_sm<NT, LM, BOOS
             mbar_init(&empty[s], 1);
         }
         mbar_init(merge_bar, kConsumerWarps);
+        if constexpr (QP) {
+            for (int s = 0; s < 2; ++s) {
+                mbar_init(&qfull[s], 1);
+                mbar_init(&qempty[s], kConsumerWarps);
+            }
+        }
         fence_mbar_init();
     }
     __syncthreads();
@@ -1028,6 +1051,7 @@ __global__ void __launch_bounds__(kInt2Threads, (int2_blocks_per_sm<NT, LM, BOOS
         const int total_long = __ldg(p.item_start + p.B);
         const int total = total_long + __ldg(p.item_start2 + p.B);
         uint32_t n = 0;      // slots issued so far (stage n % NS, warp n % 4)
+        uint32_t pitem = 0;  // items started (QP: item k's q' data goes to buffer k % 2)
         bool ok = true;
         // one slot: wait for the stage, then publish its info (and copy)
         auto post = [&](int item, int b, int kv, int pid, int valid, int flags) -> bool {
@@ -1083,6 +1107,26 @@ __global__ void __launch_bounds__(kInt2Threads, (int2_blocks_per_sm<NT, LM, BOOS
             const int pg0 = is_long ? split * p.pps : sp.long_pages + split * kShortItemPages;
             const int npg = is_long ? min(p.pps, sp.long_pages - pg0) : min(kShortItemPages, seq_pages - pg0);
             const int nslots = (npg + kConsumerWarps - 1) / kConsumerWarps * kConsumerWarps;
+            if constexpr (QP) {  // the item's q' data into its buffer, once item k - 2 has left it
+                const uint32_t qs = pitem & 1u;
+                if (pitem >= 2) {
+                    const bool w = mbar_wait_bounded(&qempty[qs], ((pitem >> 1) - 1) & 1u, kWaitPolls);
+                    if (!__all_sync(kFull, w)) {
+                        ok = false;
+                        break;
+                    }
+                }
+                if (lane == 0) {
+                    const size_t bk = (size_t)b * p.hk + kv;
+                    uint8_t* qb = smem + SM::kQb + qs * SM::kQbBytes;
+                    mbar_arrive_expect_tx(&qfull[qs], SM::kQbBytes);
+                    bulk_g2s(qb + SM::kQbFrag, p.qfrag + bk * 8 * 32 * 2, 8 * 32 * 8, &qfull[qs]);
+                    bulk_g2s(qb + SM::kQbSum, p.qsum + bk * 4 * 4, 4 * 16, &qfull[qs]);
+                    bulk_g2s(qb + SM::kQbKinv, p.qkinv + bk * 4, 16, &qfull[qs]);
+                }
+                __syncwarp();
+                ++pitem;
+            }
             for (int c = 0; c < nslots && ok; c += 32) {
                 // page ids of the next 32 slots, one per lane
                 int pid = -1;
@@ -1105,6 +1149,9 @@ __global__ void __launch_bounds__(kInt2Threads, (int2_blocks_per_sm<NT, LM, BOOS
             const uint32_t first = n > (uint32_t)NS ? n - NS : 0;
             for (uint32_t k = first; k < n; ++k)
                 (void)mbar_wait_bounded(&full[k % NS], (k / NS) & 1u, kWaitPolls);
+            if constexpr (QP)
+                for (uint32_t k = pitem > 2 ? pitem - 2 : 0; k < pitem; ++k)
+                    (void)mbar_wait_bounded(&qfull[k & 1u], (k >> 1) & 1u, kWaitPolls);
         }
         return;
     }
@@ -1129,6 +1176,8 @@ __global__ void __launch_bounds__(kInt2Threads, (int2_blocks_per_sm<NT, LM, BOOS
     float4* qbS = reinterpret_cast<float4*>(smem + SM::kQf + NT * 8 * 32 * 8);  // boost: q' of the four heads
     float4 qsv[NT];
     float kq = 1.f;  // the item's 2^-e (prep's power of two of q'), folded into the K scales
+    uint32_t citem = 0, cur_qs = 0;  // QP: items started by this warp, the current item's buffer
+    const uint2* qcur = qfS;         // the current item's q' fragments
     float m_run[NT], l_run[NT], zacc[NT][4], acc_o[NT][8][4];
     Codebook cbk{1.f, 1.f, 0.f, 0.f};  // Lloyd-Max levels of the current item's KV head
 
@@ -1144,10 +1193,30 @@ __global__ void __launch_bounds__(kInt2Threads, (int2_blocks_per_sm<NT, LM, BOOS
         const int item = sraw.x, flags = sraw.w >> 8, valid = sraw.w & 0xff;
         const uint8_t* blk = stages + s * kBlock;
 
-        if (flags & kFlagFirst) {
+        if (QP && (flags & kFlagFirst)) {  // the producer prefetched the item's q' data
+            cur_qs = citem & 1u;
+            const bool wq = mbar_wait_bounded(&qfull[cur_qs], (citem >> 1) & 1u, kWaitPolls);
+            if (!__all_sync(kFull, wq)) {
+                if (lane == 0) report(p.status, OSCAR_STATUS_TIMEOUT);
+                return;
+            }
+            ++citem;
+            const uint8_t* qb = smem + SM::kQb + cur_qs * SM::kQbBytes;
+            qcur = reinterpret_cast<const uint2*>(qb + SM::kQbFrag);
+            kq = *reinterpret_cast<const float*>(qb + SM::kQbKinv);
+            qsv[0] = reinterpret_cast<const float4*>(qb + SM::kQbSum)[tq];
+            m_run[0] = -INFINITY;
+            l_run[0] = 0.f;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) zacc[0][g] = 0.f;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc_o[0][mt][e] = 0.f;
+        } else if (flags & kFlagFirst) {
             const int bk = sraw.y * p.hk + sraw.z;
             if (LM) cbk = codebook_of(p.codebook, sraw.z);
-            kq = p.qkinv[bk];
+            kq = p.qkinv[(size_t)bk * 4];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 const uint32_t* fr = p.qfrag + ((size_t)bk * NT + nt) * 8 * 32 * 2;
@@ -1209,15 +1278,16 @@ __global__ void __launch_bounds__(kInt2Threads, (int2_blocks_per_sm<NT, LM, BOOS
                                                      p.gshift, qbS, brec, cbk);
             } else {
                 if (valid == kPage)
-                    attend_page<NT, true, LM, BOOST>(blk, valid, wbuf, qfS, qsv, kq, m_run, l_run, zacc, acc_o,
+                    attend_page<NT, true, LM, BOOST>(blk, valid, wbuf, qcur, qsv, kq, m_run, l_run, zacc, acc_o,
                                                      take_lo, p.gshift, cbk, qbS, brec);
                 else
-                    attend_page<NT, false, LM, BOOST>(blk, valid, wbuf, qfS, qsv, kq, m_run, l_run, zacc, acc_o,
+                    attend_page<NT, false, LM, BOOST>(blk, valid, wbuf, qcur, qsv, kq, m_run, l_run, zacc, acc_o,
                                                       take_lo, p.gshift, cbk, qbS, brec);
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
+        if (QP && (flags & kFlagLast) && lane == 0) mbar_arrive(&qempty[cur_qs]);  // done with the item's q' data
 
         if (flags & kFlagLast) {
             // this warp's partial state -> its scratch (no longer needed)
@@ -1852,7 +1922,7 @@ static cudaError_t set_smem(void (*kernel)(Args...), int bytes, bool max_carveou
 template <int NT, bool LM = false, bool BOOST = false>
 static cudaError_t launch_int2(const DecodeParams& p, cudaStream_t st, int sms, bool& attr_set) {
     using SM = Int2Smem<NT, int2_stages<NT, LM, BOOST>()>;
-    constexpr int smem = (LM || BOOST) ? SM::kBytesLM : SM::kBytes;
+    constexpr int smem = int2_q_prefetch<NT, LM, BOOST>() ? SM::kBytesQP : ((LM || BOOST) ? SM::kBytesLM : SM::kBytes);
     // the blocks of one SM share its 228 KB (1 KB of it reserved per block)
     static_assert(int2_blocks_per_sm<NT, LM, BOOST>() * (smem + 1024) <= 228 * 1024, "blocks per SM must fit");
     if (!attr_set) {

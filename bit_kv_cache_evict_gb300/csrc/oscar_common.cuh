@@ -363,7 +363,7 @@ struct DecodeParams {
     int32_t* item_start2; // [B + 1] short tail items before sequence b
     uint32_t* qfrag;      // [B*Hk][NT][8][32][2] fp16 q' fragments (times 2^e_h)
     float* qsum;          // [B*Hk][NT*4][4] group sums of q' (times 2^e_h)
-    float* qkinv;         // [B*Hk] 2^-e of the (sequence, KV head)'s q' fragments
+    float* qkinv;         // [B*Hk][4] 2^-e of the (sequence, KV head)'s q' fragments (16-byte records, [0] used)
     float* qrot;          // [B*Hk][4][kD] q' in stored order (fp32), written when boost is set
     float* part;          // [max_items][part_stride]
     float* bf_part;       // [B*Hk][bf_items][part_stride]
