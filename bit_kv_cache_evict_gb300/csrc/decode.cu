@@ -272,9 +272,12 @@ __device__ __forceinline__ void prep_body(const DecodeParams& p) {
 // logits of its four 16-token tiles, updates its softmax state once, and
 // runs the P.V products; it then releases the stage on an "empty"
 // mbarrier.  At an item's end the four warps merge their partial states in
-// shared memory and write one partial per item.  Every wait is bounded; on a
-// timeout the block reports OSCAR_STATUS_TIMEOUT, lets its copies land and
-// exits.
+// shared memory and write one partial per item.  In the uniform four-head
+// kernel the producer also copies each item's q' data (fragments, group
+// sums, 2^-e) into one of two item buffers when it starts the item, so that
+// the consumers find it in shared memory at the item's first page.  Every
+// wait is bounded; on a timeout the block reports OSCAR_STATUS_TIMEOUT, lets
+// its copies land and exits.
 constexpr int kConsumerWarps = 4;
 constexpr int kStages = 2 * kConsumerWarps;
 // Poll budget of every bounded mbarrier wait: a try_wait suspends about 4 us
